@@ -1,0 +1,372 @@
+"""Pins for the float64 oracle: checks against values printed on the pages,
+closed forms, invariants, a library routine and brute force.
+
+Every pin is a function ``pin_xxx(orc)`` taking the oracle module (or a mutant
+of it) and raising ``AssertionError`` on a mismatch.  ``tests/test_oracle.py``
+runs them on the real oracle; ``tests/test_oracle_mutants.py`` runs them on
+copies of the oracle with planted mistakes and expects each mutant to fail at
+least one pin.
+"""
+
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        return json.load(f)
+
+
+def _printed_tol(g):
+    # A value printed with n decimals is within 0.5e-n of the exact one.
+    return 0.5 * 10.0 ** (-g["printed_decimals"]) + 1e-12
+
+
+def _example_as_attention(g):
+    """The four-key example as a one-query, d=1 attention with scale 1:
+    q = [1], k_j = score_j, v_j = value_j, so s_j = q . k_j = score_j."""
+    q = np.array([[1.0]])
+    k = np.array(g["scores"], dtype=np.float64)[:, None]
+    v = np.array(g["values"], dtype=np.float64)[:, None]
+    return q, k, v
+
+
+# --------------------------------------------------------------------------
+# Printed values (FA-2 page, split worked example and its gradient)
+# --------------------------------------------------------------------------
+
+def pin_split_example_block_states(orc):
+    g = _golden("split_example.json")
+    s = np.array([g["scores"]])
+    v = np.array(g["values"])[:, None]
+    states = orc.split_states_f64(s, v, [tuple(b) for b in g["blocks"]])
+    tol = _printed_tol(g)
+    for (m, l, u), want in zip(states, g["block_states"]):
+        assert abs(m[0] - want["m"]) <= tol, (m, want)
+        assert abs(l[0] - want["l"]) <= tol, (l, want)
+        assert abs(u[0, 0] - want["u"]) <= tol, (u, want)
+
+
+def pin_split_example_merge(orc):
+    g = _golden("split_example.json")
+    s = np.array([g["scores"]])
+    v = np.array(g["values"])[:, None]
+    states = orc.split_states_f64(s, v, [tuple(b) for b in g["blocks"]])
+    o, _ = orc.merge_states_f64(states)
+    tol = _printed_tol(g)
+    assert abs(o[0, 0] - g["merged_output"]) <= tol, o
+    wrong = orc.normalise_then_average_f64(states)
+    assert abs(wrong[0, 0] - g["normalise_then_average_output"]) <= tol, wrong
+    assert abs(wrong[0, 0] - o[0, 0]) > 1.0
+
+
+def pin_split_example_full_attention(orc):
+    g = _golden("split_example.json")
+    q, k, v = _example_as_attention(g)
+    o, lse = orc.attention_f64(q, k, v, 1.0, causal=False)
+    assert abs(o[0, 0] - g["merged_output"]) <= _printed_tol(g), o
+    # The merge of the two block states must give the same LSE as the whole row.
+    s = np.array([g["scores"]])
+    _, lse_m = orc.merge_states_f64(
+        orc.split_states_f64(s, v, [tuple(b) for b in g["blocks"]]))
+    assert abs(lse[0] - lse_m[0]) <= 1e-12, (lse, lse_m)
+
+
+def pin_split_example_gradient(orc):
+    """Central differences of the oracle's output with respect to each score
+    reproduce the printed gradient (FA-2 page, split gradient section)."""
+    g = _golden("split_gradient.json")
+    q, k, v = _example_as_attention(g)
+    h = 1e-5
+    grad = []
+    for j in range(k.shape[0]):
+        kp = k.copy()
+        km = k.copy()
+        kp[j, 0] += h
+        km[j, 0] -= h
+        yp = orc.attention_f64(q, kp, v, 1.0)[0][0, 0]
+        ym = orc.attention_f64(q, km, v, 1.0)[0][0, 0]
+        grad.append((yp - ym) / (2 * h))
+    tol = _printed_tol(g) + 1e-8
+    for got, want in zip(grad, g["d_output_d_scores"]):
+        assert abs(got - want) <= tol, (grad, g["d_output_d_scores"])
+    assert abs(sum(grad)) <= 1e-8
+
+
+# --------------------------------------------------------------------------
+# Split / online-softmax algebra (FA-3 page section 二; FA-2 page split section)
+# --------------------------------------------------------------------------
+
+def _tile_split_bounds(nk, block, num_splits):
+    """Contiguous ranges of whole blocks, ceil(T/S) blocks per split; trailing
+    splits may be empty (the empty-tail rule of the FA-2 split section)."""
+    t = -(-nk // block)
+    per = -(-t // num_splits)
+    out = []
+    for s in range(num_splits):
+        a = min(s * per * block, nk)
+        b = min((s + 1) * per * block, nk)
+        out.append((a, max(a, b)))
+    return out
+
+
+def pin_split_invariance(orc):
+    rng = np.random.default_rng(7)
+    for nk in (1, 4, 5, 13, 64, 130):
+        q = rng.standard_normal((9, 8))
+        k = rng.standard_normal((nk, 8))
+        v = rng.standard_normal((nk, 5))
+        for causal in (False, True):
+            o_ref, lse_ref = orc.attention_f64(q, k, v, 0.3, causal)
+            s = orc.scores_f64(q, k, 0.3, causal)
+            for block in (1, 2, 4, 16):
+                for ns in (1, 2, 3, 4, 16, 64):
+                    bounds = _tile_split_bounds(nk, block, ns)
+                    o, lse = orc.merge_states_f64(
+                        orc.split_states_f64(s, v, bounds, block=block))
+                    assert np.allclose(o, o_ref, rtol=0, atol=1e-12)
+                    assert np.allclose(lse, lse_ref, rtol=0, atol=1e-12)
+            # Unaligned split points, including empty ranges in the middle.
+            cuts = sorted(rng.integers(0, nk + 1, size=3).tolist())
+            bounds = [(0, cuts[0]), (cuts[0], cuts[1]), (cuts[1], cuts[1]),
+                      (cuts[1], cuts[2]), (cuts[2], nk)]
+            o, lse = orc.merge_states_f64(orc.split_states_f64(s, v, bounds))
+            assert np.allclose(o, o_ref, rtol=0, atol=1e-12)
+            assert np.allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def pin_empty_split_state(orc):
+    s = np.array([[0.5, 1.5, -2.0]])
+    v = np.array([[1.0], [2.0], [3.0]])
+    (m, l, u), = orc.split_states_f64(s, v, [(3, 3)])
+    assert m[0] == -np.inf and l[0] == 0.0 and u[0, 0] == 0.0
+    # A range whose scores are all masked is empty in the same way, with no NaN.
+    sm = np.array([[0.5, -np.inf, -np.inf]])
+    (m, l, u), = orc.split_states_f64(sm, v, [(1, 3)], block=1)
+    assert m[0] == -np.inf and l[0] == 0.0 and u[0, 0] == 0.0
+    o, lse = orc.merge_states_f64(orc.split_states_f64(sm, v, [(0, 1), (1, 3)]))
+    assert o[0, 0] == 1.0 and lse[0] == 0.5
+
+
+def pin_online_recurrence(orc):
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal((6, 4))
+    k = rng.standard_normal((23, 4))
+    v = rng.standard_normal((23, 3))
+    for causal in (False, True):
+        s = orc.scores_f64(q, k, 0.7, causal)
+        o_ref, lse_ref = orc.attention_f64(q, k, v, 0.7, causal)
+        for edges in ([0, 23], [0, 1, 2, 23], [0, 5, 5, 12, 23], list(range(24))):
+            m, l, u = orc.online_softmax_state_f64(s, v, edges)
+            assert np.allclose(u / l[:, None], o_ref, rtol=0, atol=1e-12)
+            assert np.allclose(m + np.log(l), lse_ref, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Closed forms and invariants
+# --------------------------------------------------------------------------
+
+def pin_single_key(orc):
+    rng = np.random.default_rng(3)
+    q = rng.standard_normal((2, 3, 5, 16))
+    k = rng.standard_normal((2, 3, 1, 16))
+    v = rng.standard_normal((2, 3, 1, 8))
+    for causal in (False, True):
+        o, lse = orc.attention_f64(q, k, v, 0.25, causal)
+        assert np.allclose(o, np.broadcast_to(v, o.shape), rtol=0, atol=1e-14)
+        s = 0.25 * np.einsum("bhid,bhjd->bhi", q, k)
+        assert np.allclose(lse, s, rtol=0, atol=1e-13)
+
+
+def pin_zero_query(orc):
+    rng = np.random.default_rng(4)
+    k = rng.standard_normal((1, 2, 37, 8))
+    v = rng.standard_normal((1, 2, 37, 4))
+    q = np.zeros((1, 2, 6, 8))
+    o, lse = orc.attention_f64(q, k, v, 0.5, causal=False)
+    assert np.allclose(o, v.mean(axis=2, keepdims=True).repeat(6, axis=2), atol=1e-14)
+    assert np.allclose(lse, math.log(37), atol=1e-14)
+    # Causal with Q = 0: row i averages the first i+1 values, LSE = ln(i+1).
+    o, lse = orc.attention_f64(q, k, v, 0.5, causal=True)
+    for i in range(6):
+        assert np.allclose(o[:, :, i], v[:, :, : i + 1].mean(axis=2), atol=1e-14)
+        assert np.allclose(lse[:, :, i], math.log(i + 1), atol=1e-14)
+
+
+def pin_causal_first_row(orc):
+    rng = np.random.default_rng(5)
+    q = rng.standard_normal((9, 8))
+    k = rng.standard_normal((12, 8))
+    v = rng.standard_normal((12, 8))
+    o, lse = orc.attention_f64(q, k, v, 0.4, causal=True)
+    assert np.allclose(o[0], v[0], atol=1e-14)
+    assert abs(lse[0] - 0.4 * float(q[0] @ k[0])) < 1e-13
+
+
+def pin_rows_sum_to_one(orc):
+    rng = np.random.default_rng(6)
+    q = rng.standard_normal((17, 8))
+    k = rng.standard_normal((29, 8))
+    for causal in (False, True):
+        s = orc.scores_f64(q, k, 0.9, causal)
+        _, lse = orc.attention_f64(q, k, np.eye(29), 0.9, causal)
+        p = np.exp(s - lse[:, None])
+        assert np.allclose(p.sum(axis=1), 1.0, atol=1e-13)
+        # With V = I the output is P itself.
+        o, _ = orc.attention_f64(q, k, np.eye(29), 0.9, causal)
+        assert np.allclose(o, p, atol=1e-13)
+        if causal:
+            assert np.all(np.triu(o, 1)[:, :17] == 0.0)
+
+
+def pin_shift_invariance(orc):
+    """S + c 1^T leaves O unchanged and moves LSE by c (follows from the FA-3
+    page's recurrence: every term carries the same factor exp(c)).  Realised
+    as K' = K + 1 w^T, which shifts row i by scale * q_i . w."""
+    rng = np.random.default_rng(8)
+    q = rng.standard_normal((10, 8))
+    k = rng.standard_normal((21, 8))
+    v = rng.standard_normal((21, 6))
+    w = 3.0 * rng.standard_normal(8)
+    for causal in (False, True):
+        o1, lse1 = orc.attention_f64(q, k, v, 0.6, causal)
+        o2, lse2 = orc.attention_f64(q, k + w[None, :], v, 0.6, causal)
+        assert np.allclose(o1, o2, atol=1e-12)
+        assert np.allclose(lse2 - lse1, 0.6 * (q @ w), atol=1e-12)
+
+
+def pin_huge_scores(orc):
+    """Huge scores must not overflow (FA-2 page, section 正确性与部署边界: test
+    huge scores and tiny denominators separately).  Scores near 1e3 shifted by
+    -1e3 give the same O and an LSE lower by exactly 1e3."""
+    rng = np.random.default_rng(9)
+    s_small = rng.standard_normal((4, 11))
+    v = rng.standard_normal((11, 3))
+    q = np.concatenate([s_small, np.ones((4, 1))], axis=1)
+    k_small = np.concatenate([np.eye(11), np.zeros((11, 1))], axis=1)
+    k_big = np.concatenate([np.eye(11), np.full((11, 1), 1000.0)], axis=1)
+    o1, lse1 = orc.attention_f64(q, k_small, v, 1.0)
+    o2, lse2 = orc.attention_f64(q, k_big, v, 1.0)
+    assert np.all(np.isfinite(o2)) and np.all(np.isfinite(lse2))
+    assert np.allclose(o1, o2, atol=1e-12)
+    assert np.allclose(lse2 - lse1, 1000.0, atol=1e-9)
+    # Tiny denominators: one key far above the rest makes l close to 1 and the
+    # others' weights ~1e-40; the output is then that key's value.
+    s = np.array([[0.0, -92.0, -95.0]])
+    (m, l, u), = orc.split_states_f64(s, np.array([[1.0], [2.0], [3.0]]), [(0, 3)])
+    assert m[0] == 0.0 and abs(l[0] - 1.0) < 1e-39
+    o, _ = orc.attention_f64(np.array([[1.0]]), np.array([[0.0], [-92.0], [-95.0]]),
+                             np.array([[1.0], [2.0], [3.0]]), 1.0)
+    assert abs(o[0, 0] - 1.0) < 1e-38
+
+
+def pin_key_permutation(orc):
+    rng = np.random.default_rng(10)
+    q = rng.standard_normal((7, 8))
+    k = rng.standard_normal((19, 8))
+    v = rng.standard_normal((19, 4))
+    perm = rng.permutation(19)
+    o1, lse1 = orc.attention_f64(q, k, v, 0.5)
+    o2, lse2 = orc.attention_f64(q, k[perm], v[perm], 0.5)
+    assert np.allclose(o1, o2, atol=1e-13) and np.allclose(lse1, lse2, atol=1e-13)
+
+
+def pin_row_subset(orc):
+    rng = np.random.default_rng(12)
+    q = rng.standard_normal((40, 8))
+    k = rng.standard_normal((33, 8))
+    v = rng.standard_normal((33, 5))
+    rows = np.array([0, 3, 17, 32, 39])
+    for causal in (False, True):
+        o, lse = orc.attention_f64(q, k, v, 0.35, causal, row_block=7)
+        o_r, lse_r = orc.attention_rows_f64(q, k, v, 0.35, causal, rows)
+        assert np.array_equal(o_r, o[rows]) or np.allclose(o_r, o[rows], atol=1e-14)
+        assert np.allclose(lse_r, lse[rows], atol=1e-14)
+
+
+# --------------------------------------------------------------------------
+# Library routine and brute force
+# --------------------------------------------------------------------------
+
+def pin_torch_sdpa_float64(orc):
+    """The FA-2 page (section 5.1) names torch SDPA as the error reference; its
+    CPU float64 kernel is an independent implementation of the same op."""
+    import torch
+
+    rng = np.random.default_rng(13)
+    for (nq, nk, d, dv) in ((33, 33, 16, 16), (20, 47, 8, 12), (47, 20, 8, 8)):
+        q = rng.standard_normal((2, 3, nq, d))
+        k = rng.standard_normal((2, 3, nk, d))
+        v = rng.standard_normal((2, 3, nk, dv))
+        for causal in (False, True):
+            mask = None
+            if causal:
+                mask = torch.ones(nq, nk, dtype=torch.bool).tril()
+            ref = torch.nn.functional.scaled_dot_product_attention(
+                torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v),
+                attn_mask=mask, scale=0.45)
+            o, _ = orc.attention_f64(q, k, v, 0.45, causal)
+            assert np.allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+            sref = torch.from_numpy(q) @ torch.from_numpy(k).transpose(-1, -2) * 0.45
+            if causal:
+                sref = sref.masked_fill(~mask, float("-inf"))
+            _, lse = orc.attention_f64(q, k, v, 0.45, causal)
+            assert np.allclose(lse, torch.logsumexp(sref, dim=-1).numpy(), atol=1e-12)
+
+
+def _brute(q, k, v, scale, causal):
+    nq, nk = len(q), len(k)
+    o, lse = [], []
+    for i in range(nq):
+        s = []
+        for j in range(nk):
+            if causal and j > i:
+                continue
+            s.append((j, scale * math.fsum(a * b for a, b in zip(q[i], k[j]))))
+        m = max(x for _, x in s)
+        e = [(j, math.exp(x - m)) for j, x in s]
+        den = math.fsum(w for _, w in e)
+        o.append([math.fsum(w * v[j][c] for j, w in e) / den for c in range(len(v[0]))])
+        lse.append(m + math.log(den))
+    return o, lse
+
+
+def pin_brute_force(orc):
+    rng = np.random.default_rng(14)
+    for (nq, nk, d, dv) in ((1, 1, 1, 1), (3, 5, 2, 3), (8, 8, 4, 4), (6, 2, 3, 2), (5, 7, 4, 1)):
+        q = rng.standard_normal((nq, d))
+        k = rng.standard_normal((nk, d))
+        v = rng.standard_normal((nk, dv))
+        for causal in (False, True):
+            o, lse = orc.attention_f64(q, k, v, 0.8, causal)
+            ob, lb = _brute(q.tolist(), k.tolist(), v.tolist(), 0.8, causal)
+            assert np.allclose(o, np.array(ob), rtol=0, atol=1e-14)
+            assert np.allclose(lse, np.array(lb), rtol=0, atol=1e-14)
+
+
+ALL_PINS = [
+    pin_split_example_block_states,
+    pin_split_example_merge,
+    pin_split_example_full_attention,
+    pin_split_example_gradient,
+    pin_split_invariance,
+    pin_empty_split_state,
+    pin_online_recurrence,
+    pin_single_key,
+    pin_zero_query,
+    pin_causal_first_row,
+    pin_rows_sum_to_one,
+    pin_shift_invariance,
+    pin_huge_scores,
+    pin_key_permutation,
+    pin_row_subset,
+    pin_torch_sdpa_float64,
+    pin_brute_force,
+]

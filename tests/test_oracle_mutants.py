@@ -1,0 +1,67 @@
+"""Planted mistakes in the oracle must each fail at least one pin.
+
+Each mutant is a copy of ``oracle/attention.py`` with one textual change (a
+dropped term, a wrong sign or index, a transposed operand, a shifted mask), run
+on the CPU.  A mutant that passes every pin would mean the pins cannot tell
+that mistake from the correct oracle.
+"""
+
+import os
+import types
+
+import warnings
+
+import pytest
+
+from oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "oracle", "attention.py")
+
+MUTANTS = [
+    ("dropped scale", "s = float(scale) * (q[rows] @ k.T)", "s = (q[rows] @ k.T)"),
+    ("keys used as queries", "s = float(scale) * (q[rows] @ k.T)",
+     "s = float(scale) * (k[rows % k.shape[0]] @ k.T)"),
+    ("mask includes diagonal", "cols[None, :] > rows[:, None]", "cols[None, :] >= rows[:, None]"),
+    ("mask flipped", "cols[None, :] > rows[:, None]", "cols[None, :] < rows[:, None]"),
+    ("lse sign", "lse = np.where(empty, NEG_INF, m_ref + np.log(l))",
+     "lse = np.where(empty, NEG_INF, m_ref - np.log(l))"),
+    ("lse drops max", "lse = np.where(empty, NEG_INF, m_ref + np.log(l))",
+     "lse = np.where(empty, NEG_INF, np.log(l))"),
+    ("min instead of max", "m = s.max(axis=1)", "m = s.min(axis=1)"),
+    ("no normalisation", "o = np.where(empty[:, None], 0.0, o / l[:, None])",
+     "o = np.where(empty[:, None], 0.0, o)"),
+    ("values reversed", "o = p @ v\n", "o = p @ v[::-1]\n"),
+    ("dropped l rescale", "l = corr * l + p.sum(axis=1)", "l = l + p.sum(axis=1)"),
+    ("dropped O rescale", "o = corr[:, None] * o + p @ v[a:b]", "o = o + p @ v[a:b]"),
+    ("rescale sign", "corr = np.exp(m - ref)", "corr = np.exp(ref - m)"),
+    ("block off by one", "x = s[:, a:b]", "x = s[:, a:b + 1]"),
+    ("merge weight sign", "w = np.exp(ms - ref[None, :])", "w = np.exp(ref[None, :] - ms)"),
+    ("merge drops l weight", "big_l = (w * ls).sum(axis=0)", "big_l = ls.sum(axis=0)"),
+    ("merge lse drops max", "lse = np.where(big_l > 0, ref + np.log(big_l), NEG_INF)",
+     "lse = np.where(big_l > 0, np.log(big_l), NEG_INF)"),
+    ("wrong merge is right", "outs = [st[2] / st[1][:, None] for st in states if np.all(st[1] > 0)]\n    return np.mean(np.stack(outs), axis=0)",
+     "return merge_states_f64(states)[0]"),
+]
+
+
+def _load_mutant(find, repl):
+    with open(SRC, encoding="utf-8") as f:
+        src = f.read()
+    assert src.count(find) == 1, f"mutation anchor not unique: {find!r}"
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(src.replace(find, repl), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name,find,repl", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, find, repl):
+    mod = _load_mutant(find, repl)
+    caught = []
+    warnings.simplefilter("ignore", RuntimeWarning)
+    for pin in ALL_PINS:
+        try:
+            pin(mod)
+        except Exception as e:  # AssertionError, or a crash from a broken shape
+            caught.append((pin.__name__, type(e).__name__))
+    assert caught, f"mutant '{name}' passed every pin"
