@@ -1,0 +1,167 @@
+"""GB300 (sm_103a) exact attention forward: Python binding of ``libfa_gb300.so``.
+
+The functions below carry the names of the C ABI in ``include/fa.h`` and only
+marshal arguments: every step of the computation runs in the library's CUDA
+kernels. PyTorch supplies device memory and the current CUDA stream. There is
+no fallback: if the library is missing or a call fails, an exception says so.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
+
+FA_OK = 0
+STATUS_NAMES = {
+    0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_ALIGN", 3: "FA_ERR_SHAPE", 4: "FA_ERR_HEADDIM",
+    5: "FA_ERR_SPLITS", 6: "FA_ERR_WORKSPACE", 7: "FA_ERR_CUDA", 8: "FA_ERR_TIMEOUT",
+    9: "FA_ERR_SCALE",
+}
+FA_MAX_SPLITS = 256
+
+_lib = None
+
+
+class FAError(RuntimeError):
+    """A library call returned a status other than FA_OK."""
+
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {fa_status_string(status)}")
+
+
+def load_library() -> ctypes.CDLL:
+    """Load the in-tree CUDA library (build it with ``exact_attention_80_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with `python -m exact_attention_80_gb300.build`")
+    try:  # make torch's CUDA runtime the one the library binds to
+        import torch  # noqa: F401
+    except ImportError:
+        pass
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd.restype = i
+    lib.fa_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
+    lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_splitkv.restype = i
+    lib.fa_combine.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
+    lib.fa_combine.restype = i
+    lib.fa_fwd_grid_ctas.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_grid_ctas.restype = ctypes.c_longlong
+    lib.fa_device_status.argtypes = [vp, i]
+    lib.fa_device_status.restype = i
+    lib.fa_status_string.argtypes = [i]
+    lib.fa_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def fa_status_string(status: int) -> str:
+    return load_library().fa_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != FA_OK:
+        raise FAError(status, what)
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _bhnd(q, k, v):
+    import torch
+
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+        if t.dim() != 4 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    return int(B), int(H), int(Nq), int(k.shape[2]), int(d)
+
+
+def default_scale(d: int) -> float:
+    """1/sqrt(d) rounded once to float32 (the value the kernel receives)."""
+    return float(ctypes.c_float(d ** -0.5).value)
+
+
+def fa_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None, stream=None):
+    """Fused forward into caller-owned ``o`` (bf16 [B,H,Nq,d]) and ``lse`` (fp32 [B,H,Nq])."""
+    B, H, Nq, Nk, d = _bhnd(q, k, v)
+    scale = default_scale(d) if scale is None else float(scale)
+    st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                               scale, int(bool(causal)), _stream_handle(stream))
+    _check(st, "fa_fwd")
+
+
+def fa_splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int) -> int:
+    return int(load_library().fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits))
+
+
+def fa_fwd_splitkv(q, k, v, workspace, num_splits: int, causal: bool = False,
+                   scale: float | None = None, stream=None):
+    """Split-KV partial states into ``workspace`` (see include/fa.h for the layout)."""
+    B, H, Nq, Nk, d = _bhnd(q, k, v)
+    scale = default_scale(d) if scale is None else float(scale)
+    st = load_library().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(workspace), B, H, Nq, Nk,
+                                       d, scale, int(bool(causal)), int(num_splits),
+                                       _stream_handle(stream))
+    _check(st, "fa_fwd_splitkv")
+
+
+def fa_combine(workspace, o, lse, B: int, H: int, Nq: int, d: int, num_splits: int,
+               stream=None):
+    """Merge partial states from ``workspace`` into ``o`` and ``lse``."""
+    st = load_library().fa_combine(_ptr(workspace), _ptr(o), _ptr(lse), int(B), int(H), int(Nq),
+                                   int(d), int(num_splits), _stream_handle(stream))
+    _check(st, "fa_combine")
+
+
+def fa_fwd_grid_ctas(B: int, H: int, Nq: int, d: int, num_splits: int = 1) -> int:
+    return int(load_library().fa_fwd_grid_ctas(B, H, Nq, d, num_splits))
+
+
+def fa_device_status(clear: bool = True, stream=None) -> int:
+    """Synchronises the stream and returns the device status (FA_OK or FA_ERR_TIMEOUT)."""
+    return int(load_library().fa_device_status(_stream_handle(stream), int(bool(clear))))
+
+
+def attention(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int = 1,
+              stream=None):
+    """Allocate outputs and run the forward; ``num_splits > 1`` takes the split-KV +
+    combine path. Returns ``(o, lse)``."""
+    import torch
+
+    B, H, Nq, Nk, d = _bhnd(q, k, v)
+    o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    if num_splits == 1:
+        fa_fwd(q, k, v, o, lse, causal, scale, stream)
+    else:
+        nbytes = fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+        if nbytes == 0:
+            raise FAError(5, "fa_splitkv_workspace_bytes")
+        ws = torch.empty(nbytes // 4, dtype=torch.float32, device=q.device)
+        fa_fwd_splitkv(q, k, v, ws, num_splits, causal, scale, stream)
+        fa_combine(ws, o, lse, B, H, Nq, d, num_splits, stream)
+    return o, lse

@@ -1,0 +1,250 @@
+// fa_api.cu — the C ABI declared in include/fa.h: argument validation, TMA
+// tensor-map encoding, work partition and kernel dispatch. Host code only,
+// apart from the device status word defined here.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+#include "fa_internal.h"
+
+namespace fa {
+
+// Error word raised by kernels whose bounded waits give up (bits: fa_internal.h).
+__device__ unsigned g_fa_device_status = 0u;
+
+cudaError_t device_status_ptr(unsigned** ptr) {
+    static unsigned* cache[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && cache[dev]) {
+        *ptr = cache[dev];
+        return cudaSuccess;
+    }
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_fa_device_status);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) cache[dev] = static_cast<unsigned*>(p);
+    *ptr = static_cast<unsigned*>(p);
+    return cudaSuccess;
+}
+
+FwdConfig fwd_config(int d) {
+    FwdConfig c = {};
+    switch (d) {
+        case 64:
+            c = {FwdLayout<64>::Q_TILES, FwdLayout<64>::BN, FwdLayout<64>::STAGES,
+                 FwdLayout<64>::THREADS, FwdLayout<64>::ALLOC_BYTES};
+            break;
+        case 128:
+            c = {FwdLayout<128>::Q_TILES, FwdLayout<128>::BN, FwdLayout<128>::STAGES,
+                 FwdLayout<128>::THREADS, FwdLayout<128>::ALLOC_BYTES};
+            break;
+        case 256:
+            c = {FwdLayout<256>::Q_TILES, FwdLayout<256>::BN, FwdLayout<256>::STAGES,
+                 FwdLayout<256>::THREADS, FwdLayout<256>::ALLOC_BYTES};
+            break;
+        default:
+            break;
+    }
+    return c;
+}
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool valid_d(int d) { return d == 64 || d == 128 || d == 256; }
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 [BH][N][d] viewed as a 3-D tensor (d, N, BH); box = 64 columns x rows,
+// 128-byte swizzle; rows past N read as zeros.
+bool encode_rows_map(CUtensorMap* map, const void* base, int d, int N, int BH, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUresult r =
+        enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+fa_status check_common(const void* q, const void* k, const void* v, int B, int H, int Nq, int Nk,
+                       int d, float scale) {
+    if (!q || !k || !v) return FA_ERR_NULL;
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_SHAPE;
+    const long long bh = static_cast<long long>(B) * H;
+    if (bh > 0x7fffffffll) return FA_ERR_SHAPE;
+    if (!valid_d(d)) return FA_ERR_HEADDIM;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_SCALE;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return FA_ERR_ALIGN;
+    return FA_OK;
+}
+
+long long grid_ctas(int B, int H, int Nq, int d, int num_splits) {
+    const FwdConfig c = fwd_config(d);
+    const long long rows_per_cta = 128ll * c.q_tiles;
+    const long long units = (Nq + rows_per_cta - 1) / rows_per_cta;
+    return static_cast<long long>(B) * H * units * num_splits;
+}
+
+fa_status launch_forward(const void* q, const void* k, const void* v, void* o, float* lse,
+                         float* ws, int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                         int num_splits, int split_mode, cudaStream_t stream) {
+    const FwdConfig c = fwd_config(d);
+    const long long ctas = grid_ctas(B, H, Nq, d, num_splits);
+    if (ctas < 1 || ctas > 0x7fffffffll) return FA_ERR_SHAPE;
+
+    FwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int BH = B * H;
+    if (!encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
+        !encode_rows_map(&p.tm_k, k, d, Nk, BH, c.bn) ||
+        !encode_rows_map(&p.tm_v, v, d, Nk, BH, c.bn))
+        return FA_ERR_CUDA;
+    p.o = o;
+    p.lse = lse;
+    if (split_mode) {
+        const size_t rows = static_cast<size_t>(BH) * Nq;
+        p.ws_o = ws;
+        p.ws_m = ws + static_cast<size_t>(num_splits) * rows * d;
+        p.ws_l = p.ws_m + static_cast<size_t>(num_splits) * rows;
+    }
+    p.BH = BH;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.causal = causal ? 1 : 0;
+    p.num_splits = num_splits;
+    p.split_mode = split_mode;
+    p.n_units = static_cast<int>(ctas / (static_cast<long long>(BH) * num_splits));
+    const int kv_tiles = (Nk + c.bn - 1) / c.bn;
+    p.kv_tiles_per_split = (kv_tiles + num_splits - 1) / num_splits;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_limit = kDefaultWaitLimit;
+    if (device_status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
+
+    cudaError_t e = cudaErrorInvalidValue;
+    const unsigned grid = static_cast<unsigned>(ctas);
+    switch (d) {
+        case 64: e = launch_fwd_d64(p, grid, stream); break;
+        case 128: e = launch_fwd_d128(p, grid, stream); break;
+        case 256: e = launch_fwd_d256(p, grid, stream); break;
+        default: break;
+    }
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream) {
+    fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
+    if (s != FA_OK) return s;
+    if (!o || !lse) return FA_ERR_NULL;
+    if (!fa::aligned(o, 16) || !fa::aligned(lse, 4)) return FA_ERR_ALIGN;
+    return fa::launch_forward(q, k, v, o, lse, nullptr, B, H, Nq, Nk, d, scale, causal, 1, 0,
+                              stream);
+}
+
+size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
+    if (B < 1 || H < 1 || Nq < 1 || !fa::valid_d(d) || num_splits < 1 ||
+        num_splits > FA_MAX_SPLITS)
+        return 0;
+    const size_t rows = static_cast<size_t>(B) * H * Nq;
+    return static_cast<size_t>(num_splits) * rows * (static_cast<size_t>(d) + 2) * sizeof(float);
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* workspace, int B,
+                         int H, int Nq, int Nk, int d, float scale, int causal, int num_splits,
+                         cudaStream_t stream) {
+    fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
+    if (s != FA_OK) return s;
+    if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_SPLITS;
+    if (!workspace || !fa::aligned(workspace, 16)) return FA_ERR_WORKSPACE;
+    return fa::launch_forward(q, k, v, nullptr, nullptr, static_cast<float*>(workspace), B, H, Nq,
+                              Nk, d, scale, causal, num_splits, 1, stream);
+}
+
+fa_status fa_combine(const void* workspace, void* o, float* lse, int B, int H, int Nq, int d,
+                     int num_splits, cudaStream_t stream) {
+    if (!o || !lse) return FA_ERR_NULL;
+    if (B < 1 || H < 1 || Nq < 1) return FA_ERR_SHAPE;
+    if (static_cast<long long>(B) * H > 0x7fffffffll) return FA_ERR_SHAPE;
+    if (!fa::valid_d(d)) return FA_ERR_HEADDIM;
+    if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_SPLITS;
+    if (!workspace || !fa::aligned(workspace, 16)) return FA_ERR_WORKSPACE;
+    if (!fa::aligned(o, 16) || !fa::aligned(lse, 4)) return FA_ERR_ALIGN;
+    const long long rows = static_cast<long long>(B) * H * Nq;
+    const float* ws = static_cast<const float*>(workspace);
+    const float* ws_m = ws + static_cast<size_t>(num_splits) * rows * d;
+    const float* ws_l = ws_m + static_cast<size_t>(num_splits) * rows;
+    const cudaError_t e = fa::launch_combine(ws, ws_m, ws_l, o, lse, rows, num_splits, d, stream);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+long long fa_fwd_grid_ctas(int B, int H, int Nq, int d, int num_splits) {
+    if (B < 1 || H < 1 || Nq < 1 || !fa::valid_d(d) || num_splits < 1 ||
+        num_splits > FA_MAX_SPLITS)
+        return -1;
+    return fa::grid_ctas(B, H, Nq, d, num_splits);
+}
+
+fa_status fa_device_status(cudaStream_t stream, int clear) {
+    unsigned* ptr = nullptr;
+    if (fa::device_status_ptr(&ptr) != cudaSuccess) return FA_ERR_CUDA;
+    unsigned host = 0;
+    if (cudaMemcpyAsync(&host, ptr, sizeof(host), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (clear && host) {
+        const unsigned zero = 0;
+        if (cudaMemcpyAsync(ptr, &zero, sizeof(zero), cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return FA_ERR_CUDA;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+    }
+    return host ? FA_ERR_TIMEOUT : FA_OK;
+}
+
+const char* fa_status_string(fa_status status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_NULL: return "FA_ERR_NULL: a required pointer is NULL";
+        case FA_ERR_ALIGN: return "FA_ERR_ALIGN: a pointer is not 16-byte (lse: 4-byte) aligned";
+        case FA_ERR_SHAPE: return "FA_ERR_SHAPE: B, H, Nq or Nk out of range";
+        case FA_ERR_HEADDIM: return "FA_ERR_HEADDIM: head dim must be 64, 128 or 256";
+        case FA_ERR_SPLITS: return "FA_ERR_SPLITS: num_splits must be in [1, FA_MAX_SPLITS]";
+        case FA_ERR_WORKSPACE: return "FA_ERR_WORKSPACE: workspace NULL or not 16-byte aligned";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA runtime or driver call failed";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+        case FA_ERR_SCALE: return "FA_ERR_SCALE: scale must be finite and > 0";
+    }
+    return "unknown fa_status";
+}
+
+}  // extern "C"

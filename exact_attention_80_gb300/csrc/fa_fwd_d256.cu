@@ -1,0 +1,9 @@
+// Forward kernel instantiation for head dim 256 (one translation unit per head
+// dim so the three compile in parallel).
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+cudaError_t launch_fwd_d256(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+    return launch_fwd<256>(p, grid, stream);
+}
+}  // namespace fa

@@ -1,0 +1,68 @@
+// fa_internal.h — parameters and launchers shared by the host API (fa_api.cu)
+// and the kernel translation units. Not part of the public ABI.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+namespace fa {
+
+// Bits of the device status word (one per kind of bounded wait that gave up).
+enum : unsigned {
+    kStatusWaitQ = 1u << 0,
+    kStatusWaitKvFull = 1u << 1,
+    kStatusWaitKvEmpty = 1u << 2,
+    kStatusWaitS = 1u << 3,
+    kStatusWaitP = 1u << 4,
+    kStatusWaitO = 1u << 5,
+    kStatusWaitDrain = 1u << 6,
+};
+
+// Default bound of one wait, in SM clock cycles (~1 s at 2 GHz). Legitimate
+// waits in these kernels last microseconds.
+constexpr long long kDefaultWaitLimit = 1ll << 31;
+
+struct FwdParams {
+    CUtensorMap tm_q;  // bf16 [B*H][Nq][d], box {64, 128, 1}, 128B swizzle
+    CUtensorMap tm_k;  // bf16 [B*H][Nk][d], box {64, BN, 1}
+    CUtensorMap tm_v;  // same as tm_k
+    void* o;           // bf16 [B*H][Nq][d]      (plain mode)
+    float* lse;        // fp32 [B*H][Nq]         (plain mode)
+    float* ws_o;       // fp32 [S][B*H][Nq][d]   (split mode)
+    float* ws_m;       // fp32 [S][B*H][Nq]
+    float* ws_l;       // fp32 [S][B*H][Nq]
+    int BH, Nq, Nk;
+    int causal;
+    int num_splits;          // 1 in plain mode
+    int split_mode;          // 0: write O/LSE, 1: write partial (O, m, l)
+    int n_units;             // query units of (tiles per CTA * 128) rows per head
+    int kv_tiles_per_split;  // ceil(ceil(Nk/BN) / num_splits)
+    float scale_log2;        // scale * log2(e)
+    long long wait_limit;    // cycles
+    unsigned* status;        // device status word
+};
+
+struct FwdConfig {
+    int q_tiles;  // 128-row query tiles per CTA
+    int bn;       // keys per KV tile
+    int stages;   // K/V ring slots
+    int threads;
+    size_t smem;  // dynamic shared memory bytes
+};
+
+FwdConfig fwd_config(int d);
+
+cudaError_t launch_fwd_d64(const FwdParams& p, unsigned grid, cudaStream_t stream);
+cudaError_t launch_fwd_d128(const FwdParams& p, unsigned grid, cudaStream_t stream);
+cudaError_t launch_fwd_d256(const FwdParams& p, unsigned grid, cudaStream_t stream);
+
+cudaError_t launch_combine(const float* ws_o, const float* ws_m, const float* ws_l, void* o,
+                           float* lse, long long rows, int num_splits, int d,
+                           cudaStream_t stream);
+
+// Address of the device status word on the current device (cached per device).
+cudaError_t device_status_ptr(unsigned** ptr);
+
+}  // namespace fa

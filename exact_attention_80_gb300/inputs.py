@@ -1,0 +1,75 @@
+"""Seeded synthetic inputs, the one module both the CUDA path's callers and the
+float64 oracle's callers use. It holds no attention arithmetic: it only draws
+numbers and rounds them to bf16.
+
+Recipe (the workloads of the five benchmark configurations):
+
+* Q, K, V are drawn i.i.d. N(0, 1) in float32 from ``torch.Generator`` seeded
+  with ``seed``, in the order Q, K, V, then rounded to bf16 (round to nearest
+  even, torch's conversion). The same bf16 bits go to the GPU and, upcast
+  exactly, to the oracle.
+* ``outlier_frac`` > 0 (the large-head-dim configuration): for each (b, h),
+  ``floor(outlier_frac * Nk)`` distinct key rows, chosen by a seeded
+  permutation (drawn after V, same generator), are multiplied by
+  ``outlier_scale`` in float32 before the bf16 rounding. A factor of 8 is a
+  power of two, so it commutes with the rounding.
+"""
+
+from __future__ import annotations
+
+import math
+
+import torch
+
+CONFIG_SEED_BASE = 1000
+
+
+def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int, seed: int,
+             outlier_frac: float = 0.0, outlier_scale: float = 8.0):
+    """Return bf16 CPU tensors ``(q [B,H,Nq,d], k [B,H,Nk,d], v [B,H,Nk,d])``."""
+    g = torch.Generator().manual_seed(int(seed))
+    q = torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32)
+    k = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
+    v = torch.randn((B, H, Nk, d), generator=g, dtype=torch.float32)
+    if outlier_frac > 0.0:
+        count = int(math.floor(outlier_frac * Nk))
+        for b in range(B):
+            for h in range(H):
+                rows = torch.randperm(Nk, generator=g)[:count]
+                k[b, h, rows] *= outlier_scale
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+def to_f64(t):
+    """Exact upcast of a (bf16) torch tensor to a float64 numpy array."""
+    return t.to(torch.float64).numpy()
+
+
+def f32(x: float) -> float:
+    """Round a Python float to the nearest float32 (the value a kernel receives)."""
+    return float(torch.tensor(x, dtype=torch.float32).item())
+
+
+# The five benchmark workloads (shape, mask, scale, seed).
+CONFIGS = {
+    "c1": dict(B=1, H=1, Nq=128, Nk=128, d=64, causal=False, seed=CONFIG_SEED_BASE + 0),
+    "c2": dict(B=8, H=32, Nq=2048, Nk=2048, d=128, causal=False, seed=CONFIG_SEED_BASE + 1),
+    "c2_causal": dict(B=8, H=32, Nq=2048, Nk=2048, d=128, causal=True, seed=CONFIG_SEED_BASE + 1),
+    "c3": dict(B=1, H=8, Nq=8192, Nk=8192, d=128, causal=False, seed=CONFIG_SEED_BASE + 2),
+    "c3_causal": dict(B=1, H=8, Nq=8192, Nk=8192, d=128, causal=True, seed=CONFIG_SEED_BASE + 2),
+    "c4": dict(B=8, H=16, Nq=8191, Nk=8191, d=256, causal=True, seed=CONFIG_SEED_BASE + 3,
+               outlier_frac=0.01),
+    "c5": dict(B=1, H=8, Nq=128, Nk=131072, d=128, causal=False, seed=CONFIG_SEED_BASE + 4),
+}
+
+
+def config_inputs(name: str):
+    c = CONFIGS[name]
+    return make_qkv(c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["seed"],
+                    outlier_frac=c.get("outlier_frac", 0.0))
+
+
+def metric_flops(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool) -> float:
+    """The benchmark's FLOP count: 4*B*H*Nq*Nk*d, halved for a causal mask."""
+    f = 4.0 * B * H * Nq * Nk * d
+    return f / 2 if causal else f

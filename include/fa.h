@@ -1,0 +1,140 @@
+/*
+ * fa.h — exact scaled-dot-product attention forward on GB300 (sm_103a).
+ *
+ * What is computed (per batch b and head h, rows i of Q, keys j of K/V):
+ *     S = scale * Q K^T            (optionally causal: key j visible to query i iff j <= i)
+ *     O = softmax_row(S) V          (exact softmax, no approximation of the definition)
+ *     LSE_i = ln sum_j exp(S_ij)    (natural log, in units of the scaled score)
+ * The result is the plain definition of attention; the kernels reach it tile by
+ * tile with the two-level online softmax ("Inside FlashAttention-3：面向 Hopper
+ * 架构的 IO-Aware 精确注意力机制深度解析", section 二 "核心算法：Two-Level 在线
+ * Softmax 的再回顾": running max m, running sum l, accumulator rescaled by
+ * exp(m_old - m_new); and "AI 大模型之 FlashAttention_02", section "warp之间怎样
+ * 减少通信": the division by l is deferred to the final write).
+ *
+ * Conventions shared by every entry point
+ *  - Layout: Q, K, V, O are row-major contiguous bf16 tensors [B][H][N][d]
+ *    (N = Nq for Q and O, Nk for K and V); LSE is fp32 [B][H][Nq].
+ *  - Every pointer is a DEVICE pointer owned by the caller. The library
+ *    allocates nothing, frees nothing and never synchronises (except
+ *    fa_device_status, which says so).
+ *  - Calls are asynchronous on `stream`; the return value covers argument
+ *    validation and the launch only. Device-side failures surface at the
+ *    caller's next synchronisation, or as FA_ERR_TIMEOUT from fa_device_status.
+ *  - d must be 64, 128 or 256. Any other head dim is an error, never a silent
+ *    fallback (the FlashAttention_02 page, sections 4.4 and 8, warns that
+ *    frameworks silently switch backends for unsupported head dims).
+ *  - `causal` != 0 selects the top-left aligned causal mask (key j visible to
+ *    query i iff j <= i). The FlashAttention_02 page, section "正确性与部署边界",
+ *    leaves square/non-square alignment to the implementation's documentation:
+ *    this is it.
+ *  - `scale` must be finite and > 0; it is used exactly as given (float32).
+ *  - q, k, v, o and the workspace must be 16-byte aligned; lse 4-byte aligned.
+ *  - The output buffers must not overlap the inputs.
+ */
+#ifndef FA_GB300_FA_H
+#define FA_GB300_FA_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_NULL = 1,       /* a required pointer is NULL */
+    FA_ERR_ALIGN = 2,      /* a pointer is not aligned as stated above */
+    FA_ERR_SHAPE = 3,      /* B, H, Nq or Nk < 1, or a size overflows 32/64-bit indexing */
+    FA_ERR_HEADDIM = 4,    /* d is not 64, 128 or 256 */
+    FA_ERR_SPLITS = 5,     /* num_splits < 1 or > FA_MAX_SPLITS */
+    FA_ERR_WORKSPACE = 6,  /* workspace pointer NULL or misaligned */
+    FA_ERR_CUDA = 7,       /* a CUDA runtime or driver call failed (no device, launch, tensor-map encode) */
+    FA_ERR_TIMEOUT = 8,    /* a kernel gave up on a bounded wait (reported by fa_device_status) */
+    FA_ERR_SCALE = 9       /* scale is not finite or not > 0 */
+} fa_status;
+
+#define FA_MAX_SPLITS 256
+
+/*
+ * fa_fwd — fused attention forward, one launch.
+ *   q    [B][H][Nq][d] bf16 (read)        k, v [B][H][Nk][d] bf16 (read)
+ *   o    [B][H][Nq][d] bf16 (written)     lse  [B][H][Nq] fp32 (written)
+ * Work partition: each CTA owns query tiles of one (b, h) and sweeps all keys
+ * it needs ("AI 大模型之 FlashAttention_02", section "从头级并行转向序列级并行":
+ * query tiles of one head go to different CTAs, no cross-CTA reduction).
+ * Causal tiles that lie wholly above the diagonal are skipped.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                 cudaStream_t stream);
+
+/*
+ * fa_splitkv_workspace_bytes — size in bytes of the workspace fa_fwd_splitkv
+ * writes and fa_combine reads, for the given shape and split count (0 when an
+ * argument is out of range). Workspace layout, fp32, in this order:
+ *   O_part [S][B][H][Nq][d]   unnormalised partial outputs  (u of each split)
+ *   m      [S][B][H][Nq]      partial row max, natural-log units of the scaled score
+ *   l      [S][B][H][Nq]      partial row sum, relative to that split's m
+ * ("AI 大模型之 FlashAttention_02", section "工程实操 沿键切分的归约与沿查询切分的
+ * 区别", subsection "接口与实现约束": a split scheme must state its split axis,
+ * each group's output responsibility, the partial-statistics layout and the
+ * merge operator; this comment and fa_combine's are that statement.)
+ */
+size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
+
+/*
+ * fa_fwd_splitkv — split-KV forward: writes partial states, no final output.
+ * Split axis: keys. With T = ceil(Nk / BN) key tiles (BN = 128 for d <= 128,
+ * 64 for d = 256) and P = ceil(T / num_splits), split s owns key tiles
+ * [s*P, min((s+1)*P, T)). Trailing splits may be empty; an empty split (or a
+ * row whose keys in that split are all masked) writes m = -inf, l = 0, O = 0
+ * (same section, subsection "扩展验证组合": the empty-tail rule; the true key
+ * count Nk masks the last tile). Same q/k/v/shape rules as fa_fwd; `workspace`
+ * must hold fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits) bytes.
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* workspace,
+                         int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                         int num_splits, cudaStream_t stream);
+
+/*
+ * fa_combine — merge operator for the split partial states ("AI 大模型之
+ * FlashAttention_02", section "工程实操 沿键切分的归约与沿查询切分的区别",
+ * subsection "逐步计算与预期结果", steps 2-3): per row
+ *     M = max_s m_s,  w_s = exp(m_s - M),  L = sum_s w_s l_s,
+ *     O = (sum_s w_s O_s) / L  -> bf16,   LSE = M + ln L.
+ * (Normalising each split first and averaging is the wrong merge the page
+ * warns against; it is not what this computes.) Reads the workspace written
+ * by fa_fwd_splitkv with the same B, H, Nq, d, num_splits; writes o and lse
+ * exactly as fa_fwd does.
+ */
+fa_status fa_combine(const void* workspace, void* o, float* lse,
+                     int B, int H, int Nq, int d, int num_splits, cudaStream_t stream);
+
+/*
+ * fa_fwd_grid_ctas — number of CTAs fa_fwd (num_splits = 1) or
+ * fa_fwd_splitkv would launch for this shape: B * H * ceil(Nq / BM) * num_splits,
+ * BM = 256 query rows per CTA for d <= 128 (two 128-row tiles) and 128 for
+ * d = 256 ("AI 大模型之 FlashAttention_02", section "从头级并行转向序列级并行" and
+ * the printed CTA counts of section "本册配套实验验证记录"). Returns -1 when an
+ * argument is out of range. Host-only; launches nothing.
+ */
+long long fa_fwd_grid_ctas(int B, int H, int Nq, int d, int num_splits);
+
+/*
+ * fa_device_status — SYNCHRONISES `stream`, then reads the library's device
+ * error word: FA_OK, or FA_ERR_TIMEOUT if any kernel since the last clear gave
+ * up on a bounded wait (it then exits cleanly and leaves its outputs
+ * undefined). `clear` != 0 resets the word. FA_ERR_CUDA if the read fails.
+ */
+fa_status fa_device_status(cudaStream_t stream, int clear);
+
+/* fa_status_string — static, human-readable name of a status code. */
+const char* fa_status_string(fa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_FA_H */

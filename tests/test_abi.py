@@ -1,0 +1,139 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every symbol that
+include/fa.h declares, and rejects bad arguments with the documented status
+before any CUDA work. No kernel is launched here."""
+
+import ctypes
+import json
+import math
+import os
+import re
+
+import pytest
+
+import exact_attention_80_gb300 as fa
+from exact_attention_80_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+P = ctypes.c_void_p
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(fa.LIB_PATH):
+        fa_build.build()
+    return fa.load_library()
+
+
+def declared_functions():
+    with open(HEADER, encoding="utf-8") as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for want in ("fa_fwd", "fa_fwd_splitkv", "fa_combine", "fa_splitkv_workspace_bytes",
+                 "fa_status_string", "fa_fwd_grid_ctas", "fa_device_status"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/fa.h but not exported"
+
+
+def test_status_strings(lib):
+    for code, name in fa.STATUS_NAMES.items():
+        assert fa.fa_status_string(code).startswith(name)
+
+
+def _fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, Nq=8, Nk=8, d=64,
+         scale=0.125, causal=0):
+    return lib.fa_fwd(P(q), P(k), P(v), P(o), P(lse), B, H, Nq, Nk, d, scale, causal, P(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(k=0), 1), (dict(v=0), 1), (dict(o=0), 1), (dict(lse=0), 1),
+    (dict(B=0), 3), (dict(H=0), 3), (dict(Nq=0), 3), (dict(Nk=0), 3), (dict(Nk=-5), 3),
+    (dict(B=1 << 16, H=1 << 16), 3),
+    (dict(d=32), 4), (dict(d=96), 4), (dict(d=512), 4), (dict(d=0), 4),
+    (dict(scale=0.0), 9), (dict(scale=-0.1), 9), (dict(scale=float("nan")), 9),
+    (dict(scale=float("inf")), 9),
+    (dict(q=FAKE + 8), 2), (dict(k=FAKE + 4), 2), (dict(v=FAKE + 2), 2), (dict(o=FAKE + 8), 2),
+    (dict(lse=FAKE + 2), 2),
+])
+def test_fwd_rejects(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+
+
+def _split(lib, ws=FAKE, S=4, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, B=1, H=1, Nq=8, Nk=8, d=64, scale=0.125, causal=0)
+    a.update(kw)
+    return lib.fa_fwd_splitkv(P(a["q"]), P(a["k"]), P(a["v"]), P(ws), a["B"], a["H"], a["Nq"],
+                              a["Nk"], a["d"], a["scale"], a["causal"], S, P(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=0), 6), (dict(ws=FAKE + 4), 6), (dict(S=0), 5), (dict(S=257), 5),
+    (dict(d=80), 4), (dict(q=0), 1), (dict(Nq=0), 3), (dict(scale=0.0), 9),
+])
+def test_splitkv_rejects(lib, kw, code):
+    assert _split(lib, **kw) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, FAKE, FAKE, 1, 1, 8, 64, 2), 6), ((FAKE, 0, FAKE, 1, 1, 8, 64, 2), 1),
+    ((FAKE, FAKE, 0, 1, 1, 8, 64, 2), 1), ((FAKE, FAKE, FAKE, 0, 1, 8, 64, 2), 3),
+    ((FAKE, FAKE, FAKE, 1, 1, 8, 48, 2), 4), ((FAKE, FAKE, FAKE, 1, 1, 8, 64, 0), 5),
+    ((FAKE + 8, FAKE, FAKE, 1, 1, 8, 64, 2), 6), ((FAKE, FAKE + 8, FAKE, 1, 1, 8, 64, 2), 2),
+])
+def test_combine_rejects(lib, args, code):
+    ws, o, lse, B, H, Nq, d, S = args
+    assert lib.fa_combine(P(ws), P(o), P(lse), B, H, Nq, d, S, P(0)) == code
+
+
+def test_workspace_bytes(lib):
+    for (B, H, Nq, d, S) in ((1, 8, 128, 128, 64), (2, 3, 77, 64, 1), (8, 16, 8191, 256, 3)):
+        assert fa.fa_splitkv_workspace_bytes(B, H, Nq, d, S) == S * B * H * Nq * (d + 2) * 4
+    assert fa.fa_splitkv_workspace_bytes(1, 1, 1, 100, 1) == 0
+    assert fa.fa_splitkv_workspace_bytes(1, 1, 1, 64, 0) == 0
+    assert fa.fa_splitkv_workspace_bytes(0, 1, 1, 64, 1) == 0
+
+
+def test_cta_counts_match_printed_schedule(lib):
+    """The FA-2 page's printed CTA counts (batch*heads*ceil(seq/tile)) and the
+    library's grid: 256-row CTAs for d<=128, 128-row CTAs for d=256."""
+    with open(os.path.join(ROOT, "tests", "golden", "cta_schedule.json"), encoding="utf-8") as f:
+        g = json.load(f)
+    for b, h, n, tile, ctas in g["rows"]:
+        assert b * h * math.ceil(n / tile) == ctas
+    by_tile = {(r[0], r[1], r[2], r[3]): r[4] for r in g["rows"]}
+    assert fa.fa_fwd_grid_ctas(1, 8, 8192, 128) == by_tile[(1, 8, 8192, 256)]
+    assert fa.fa_fwd_grid_ctas(1, 8, 8192, 64) == by_tile[(1, 8, 8192, 256)]
+    assert fa.fa_fwd_grid_ctas(1, 8, 8192, 256) == by_tile[(1, 8, 8192, 128)]
+    # Splits multiply the grid; one CTA per head when a head has one query unit.
+    assert fa.fa_fwd_grid_ctas(1, 8, 128, 128, 64) == 8 * 64
+    assert fa.fa_fwd_grid_ctas(1, 8, 8192, 128, 1) > g["heads_only_ctas"]["ctas"]
+    assert fa.fa_fwd_grid_ctas(1, 8, 128, 100, 1) == -1
+
+
+def test_valid_call_without_gpu_reports_cuda_error(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("would launch on fake pointers; only meaningful without a GPU")
+    assert _fwd(lib) == 7
+    assert lib.fa_device_status(P(0), 1) == 7
+
+
+def test_python_binding_rejects_bad_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        fa.fa_fwd(q, q, q, q, q)
+    qb = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        fa.fa_fwd(qb, qb, qb, qb, qb)  # CPU tensors are refused before any call

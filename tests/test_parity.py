@@ -1,0 +1,298 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle on
+the same seeded bf16 inputs.
+
+Acceptance (bf16 inputs, fp32 accumulation): on O, max-abs error <= 2e-2 and
+relative L2 error <= 5e-3; on LSE, max-abs error <= 1e-3.  Small shapes are
+compared element by element; the full benchmark shapes are compared on sampled
+rows that the oracle computes one at a time.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+import exact_attention_80_gb300 as fa  # noqa: E402
+import oracle  # noqa: E402
+from exact_attention_80_gb300.inputs import CONFIGS, config_inputs, f32, make_qkv, to_f64  # noqa: E402
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 2e-2
+REL_L2 = 5e-3
+LSE_ABS = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    fa.load_library()
+    fa.fa_device_status(clear=True)
+
+
+def check(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
+    o = o_gpu.float().cpu().numpy().astype(np.float64)
+    lse = lse_gpu.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(o)), f"{what}: non-finite O"
+    err = np.abs(o - o_ref)
+    max_abs = float(err.max())
+    rel = float(np.linalg.norm((o - o_ref).ravel()) / max(np.linalg.norm(o_ref.ravel()), 1e-30))
+    lse_err = float(np.abs(lse - lse_ref).max())
+    assert max_abs <= MAX_ABS, f"{what}: max-abs {max_abs:.3e}"
+    assert rel <= REL_L2, f"{what}: rel-L2 {rel:.3e}"
+    assert lse_err <= LSE_ABS, f"{what}: LSE err {lse_err:.3e}"
+    return max_abs, rel, lse_err
+
+
+def run_gpu(q, k, v, causal, scale, num_splits=1):
+    o, lse = fa.attention(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale,
+                          num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(clear=True) == fa.FA_OK
+    return o, lse
+
+
+SMALL = [
+    # B, H, Nq, Nk, d, causal
+    (1, 1, 128, 128, 64, False),
+    (2, 3, 300, 333, 64, False),
+    (2, 3, 300, 333, 64, True),
+    (1, 2, 257, 511, 128, False),
+    (1, 2, 257, 511, 128, True),
+    (2, 2, 384, 384, 128, True),
+    (1, 2, 200, 190, 256, False),
+    (1, 2, 200, 190, 256, True),
+    (1, 1, 1, 1, 128, False),
+    (1, 1, 1, 1000, 128, False),
+    (1, 1, 1000, 1, 64, False),
+    (1, 1, 300, 100, 128, True),   # Nq > Nk: rows past Nk see every key
+    (1, 1, 100, 300, 128, True),   # Nq < Nk: top-left alignment
+    (1, 1, 513, 129, 256, True),
+    (3, 1, 640, 640, 64, True),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,d,causal", SMALL)
+def test_small_shapes_elementwise(B, H, Nq, Nk, d, causal):
+    seed = 7 + Nq + 3 * Nk + d
+    q, k, v = make_qkv(B, H, Nq, Nk, d, seed)
+    scale = f32(1.0 / math.sqrt(d))
+    o, lse = run_gpu(q, k, v, causal, scale)
+    o_ref, lse_ref = oracle.attention_f64(to_f64(q), to_f64(k), to_f64(v), scale, causal)
+    check(o, lse, o_ref, lse_ref, f"{(B, H, Nq, Nk, d, causal)}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_outlier_keys_and_other_scales(d):
+    q, k, v = make_qkv(2, 2, 191, 191, d, 99, outlier_frac=0.01)
+    for scale in (f32(0.5 / math.sqrt(d)), f32(2.0 / math.sqrt(d))):
+        for causal in (False, True):
+            o, lse = run_gpu(q, k, v, causal, scale)
+            o_ref, lse_ref = oracle.attention_f64(to_f64(q), to_f64(k), to_f64(v), scale, causal)
+            check(o, lse, o_ref, lse_ref, f"d={d} scale={scale} causal={causal}")
+
+
+def test_worked_example_on_gpu():
+    """The FA-2 page's four-key example as a real kernel call: d=64, scale 1,
+    q = e0, K rows = score_j * e0, V rows = value_j * e0 (all exact in bf16)."""
+    scores = [1.0, 2.0, 4.0, 0.0]
+    values = [2.0, 5.0, 1.0, 9.0]
+    q = torch.zeros(1, 1, 1, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    v = torch.zeros(1, 1, 4, 64, dtype=torch.bfloat16)
+    q[0, 0, 0, 0] = 1.0
+    for j in range(4):
+        k[0, 0, j, 0] = scores[j]
+        v[0, 0, j, 0] = values[j]
+    for splits in (1, 2, 3, 4):
+        o, lse = run_gpu(q, k, v, False, 1.0, num_splits=splits)
+        assert abs(o[0, 0, 0, 0].item() - 1.612955) <= MAX_ABS
+        assert torch.all(o[0, 0, 0, 1:] == 0)
+        want_lse = math.log(sum(math.exp(s) for s in scores))
+        assert abs(lse[0, 0, 0].item() - want_lse) <= LSE_ABS
+
+
+def _split_bounds(Nk, bn, S):
+    T = -(-Nk // bn)
+    per = -(-T // S)
+    out = []
+    for s in range(S):
+        a = min(s * per, T)
+        b = min(a + per, T)
+        out.append((min(a * bn, Nk), min(b * bn, Nk)))
+    return out
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_split_partials_match_oracle_states(d):
+    """Each split's (m, l, O) workspace entries against the oracle's partial
+    state over the same key range (documented split rule in include/fa.h)."""
+    B, H, Nq, Nk, S = 1, 2, 130, 1100, 4
+    bn = 64 if d == 256 else 128
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 5 + d)
+    scale = f32(1.0 / math.sqrt(d))
+    for causal in (False, True):
+        nbytes = fa.fa_splitkv_workspace_bytes(B, H, Nq, d, S)
+        ws = torch.full((nbytes // 4,), float("nan"), dtype=torch.float32, device="cuda")
+        fa.fa_fwd_splitkv(q.cuda(), k.cuda(), v.cuda(), ws, S, causal, scale)
+        torch.cuda.synchronize()
+        rows = B * H * Nq
+        w = ws.cpu().numpy().astype(np.float64)
+        wo = w[: S * rows * d].reshape(S, B * H, Nq, d)
+        wm = w[S * rows * d: S * rows * (d + 1)].reshape(S, B * H, Nq)
+        wl = w[S * rows * (d + 1):].reshape(S, B * H, Nq)
+        bounds = _split_bounds(Nk, bn, S)
+        qf, kf, vf = to_f64(q), to_f64(k), to_f64(v)
+        for h in range(B * H):
+            s_full = oracle.scores_f64(qf.reshape(-1, Nq, d)[h], kf.reshape(-1, Nk, d)[h], scale,
+                                       causal)
+            states = oracle.split_states_f64(s_full, vf.reshape(-1, Nk, d)[h], bounds)
+            for sidx, (m_ref, l_ref, u_ref) in enumerate(states):
+                fin = np.isfinite(m_ref)
+                assert np.array_equal(np.isfinite(wm[sidx, h]), fin)
+                assert np.all(wl[sidx, h][~fin] == 0) and np.all(wo[sidx, h][~fin] == 0)
+                if fin.any():
+                    assert np.abs(wm[sidx, h][fin] - m_ref[fin]).max() <= 1e-4
+                    assert np.abs(wl[sidx, h][fin] / l_ref[fin] - 1).max() <= 1e-3
+                    o_n = wo[sidx, h][fin] / wl[sidx, h][fin][:, None]
+                    o_r = u_ref[fin] / l_ref[fin][:, None]
+                    assert np.abs(o_n - o_r).max() <= MAX_ABS
+
+
+def test_combine_of_printed_block_states():
+    """fa_combine fed the two printed block states (m, l, u) of the FA-2 page's
+    split example as a 2-split workspace must give 1.612955."""
+    d, S = 64, 2
+    ws = torch.zeros(S * (d + 2), dtype=torch.float32)
+    for s, (m, l, u) in enumerate([(2.0, 1.367879, 5.735759), (4.0, 1.018316, 1.164841)]):
+        ws[s * d] = u
+        ws[S * d + s] = m
+        ws[S * d + S + s] = l
+    o = torch.empty(1, 1, 1, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(1, 1, 1, dtype=torch.float32, device="cuda")
+    fa.fa_combine(ws.cuda(), o, lse, 1, 1, 1, d, S)
+    torch.cuda.synchronize()
+    assert abs(o[0, 0, 0, 0].item() - 1.612955) <= 1e-2
+    assert abs(lse.item() - (4.0 + math.log(1.367879 * math.exp(-2.0) + 1.018316))) <= 1e-4
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_combine_of_oracle_partials(d):
+    """fa_combine alone, fed oracle-made partial states (with empty splits)."""
+    rng = np.random.default_rng(d)
+    BH, Nq, Nk = 3, 45, 200
+    q = rng.standard_normal((BH, Nq, d))
+    k = rng.standard_normal((BH, Nk, d))
+    v = rng.standard_normal((BH, Nk, d))
+    bounds = [(0, 50), (50, 50), (50, 120), (120, 200), (200, 200)]
+    S = len(bounds)
+    ws = np.zeros((S * BH * Nq * (d + 2),), dtype=np.float32)
+    wo = ws[: S * BH * Nq * d].reshape(S, BH, Nq, d)
+    wm = ws[S * BH * Nq * d: S * BH * Nq * (d + 1)].reshape(S, BH, Nq)
+    wl = ws[S * BH * Nq * (d + 1):].reshape(S, BH, Nq)
+    o_ref = np.zeros((BH, Nq, d))
+    lse_ref = np.zeros((BH, Nq))
+    for h in range(BH):
+        s_full = oracle.scores_f64(q[h], k[h], 0.1, False)
+        states = oracle.split_states_f64(s_full, v[h], bounds)
+        for s, (m, l, u) in enumerate(states):
+            wm[s, h], wl[s, h], wo[s, h] = m, l, u
+        o_ref[h], lse_ref[h] = oracle.merge_states_f64(states)
+    o = torch.empty(1, BH, Nq, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(1, BH, Nq, dtype=torch.float32, device="cuda")
+    fa.fa_combine(torch.from_numpy(ws).cuda(), o, lse, 1, BH, Nq, d, S)
+    torch.cuda.synchronize()
+    check(o[0], lse[0], o_ref, lse_ref, "combine")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_split_invariance(causal):
+    """Output semantics do not change with the split count (FA-2 page, split
+    section: 1, 2, 3, 4 splits including empty tails), plus 16 and 64."""
+    B, H, Nq, Nk, d = 1, 2, 256, 4000, 128
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 4242)
+    scale = f32(1.0 / math.sqrt(d))
+    o_ref, lse_ref = oracle.attention_f64(to_f64(q), to_f64(k), to_f64(v), scale, causal)
+    outs = []
+    for S in (1, 2, 3, 4, 16, 64):
+        o, lse = run_gpu(q, k, v, causal, scale, num_splits=S)
+        check(o, lse, o_ref, lse_ref, f"splits={S}")
+        outs.append(o.float())
+    for x in outs[1:]:
+        assert (x - outs[0]).abs().max().item() <= MAX_ABS
+
+
+def test_guard_bands_untouched():
+    """Writes stay inside O and LSE: sentinel-filled bands after both survive."""
+    B, H, Nq, Nk, d = 1, 3, 130, 200, 128
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 31)
+    pad = 4096
+    o_buf = torch.full((B * H * Nq * d + pad,), 7.0, dtype=torch.bfloat16, device="cuda")
+    l_buf = torch.full((B * H * Nq + pad,), 7.0, dtype=torch.float32, device="cuda")
+    o = o_buf[: B * H * Nq * d].view(B, H, Nq, d)
+    lse = l_buf[: B * H * Nq].view(B, H, Nq)
+    for causal in (False, True):
+        fa.fa_fwd(q.cuda(), k.cuda(), v.cuda(), o, lse, causal=causal)
+        torch.cuda.synchronize()
+        assert torch.all(o_buf[B * H * Nq * d:] == 7.0)
+        assert torch.all(l_buf[B * H * Nq:] == 7.0)
+
+
+def test_deterministic():
+    q, k, v = make_qkv(2, 2, 700, 900, 128, 77)
+    a = run_gpu(q, k, v, True, None)
+    b = run_gpu(q, k, v, True, None)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_shift_invariance_on_gpu():
+    """K' = K + 1 w^T shifts every score of row i by scale*q_i.w: O unchanged,
+    LSE moved; compared against the oracle on the rounded K'."""
+    B, H, Nq, Nk, d = 1, 2, 200, 300, 64
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 55)
+    w = torch.linspace(-2, 2, d)
+    k2 = (k.float() + w).to(torch.bfloat16)
+    scale = f32(1.0 / math.sqrt(d))
+    o1, _ = run_gpu(q, k, v, False, scale)
+    o2, lse2 = run_gpu(q, k2, v, False, scale)
+    o_ref, lse_ref = oracle.attention_f64(to_f64(q), to_f64(k2), to_f64(v), scale, False)
+    check(o2, lse2, o_ref, lse_ref, "shifted")
+    assert (o1.float() - o2.float()).abs().max().item() <= 2 * MAX_ABS
+
+
+# ---------------------------------------------------------------- full sizes
+
+def sampled_check(name, num_splits=1, n_samples=48):
+    c = CONFIGS[name]
+    q, k, v = config_inputs(name)
+    scale = f32(1.0 / math.sqrt(c["d"]))
+    o, lse = run_gpu(q, k, v, c["causal"], scale, num_splits=num_splits)
+    B, H, Nq, Nk, d = c["B"], c["H"], c["Nq"], c["Nk"], c["d"]
+    rng = np.random.default_rng(c["seed"])
+    picks = [(0, 0, 0), (B - 1, H - 1, Nq - 1), (B - 1, 0, Nq - 1)]
+    picks += [(int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(Nq)))
+              for _ in range(n_samples - len(picks))]
+    o_cpu, lse_cpu = o.float().cpu(), lse.cpu()
+    got_o, got_l, ref_o, ref_l = [], [], [], []
+    for b, h, i in picks:
+        ro, rl = oracle.attention_rows_f64(to_f64(q[b, h]), to_f64(k[b, h]), to_f64(v[b, h]),
+                                           scale, c["causal"], [i])
+        ref_o.append(ro[0])
+        ref_l.append(rl[0])
+        got_o.append(o_cpu[b, h, i])
+        got_l.append(lse_cpu[b, h, i])
+    check(torch.stack(got_o), torch.stack(got_l), np.stack(ref_o), np.array(ref_l), name)
+    assert torch.isfinite(o_cpu).all() and torch.isfinite(lse_cpu).all()
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c2_causal", "c3", "c3_causal", "c4"])
+def test_full_size_config_sampled(name):
+    sampled_check(name)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 4, 16, 64])
+def test_full_size_splitkv_sampled(splits):
+    sampled_check("c5", num_splits=splits, n_samples=24)
