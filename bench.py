@@ -1,0 +1,512 @@
+#!/usr/bin/env python
+"""Benchmark of the fused exact attention forward on GB300.
+
+One step = one pass of the hot path over one batch: ``fa_fwd`` on the headline
+workload (B=8, H=32, Nq=Nk=2048, d=128, non-causal, bf16; seeded synthetic
+N(0,1) inputs). Prints ONE JSON line (rank 0) with TFLOPS (4*B*H*Nq*Nk*d per
+step, halved for causal), the roofline of the kernel against the measured
+dense bf16 peak, the same metric end to end from pinned host buffers, SM
+clocks sampled during the timed region, the float64 CPU oracle timed on a
+bounded sample, and timings of the other workloads (causal, long sequence,
+d=256, split-KV + combine sweep).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under ``torchrun`` each rank runs the same per-GPU workload (weak scaling, no
+data exchange: heads are independent); timing takes the max over ranks.
+``--impl reference`` times the float64 oracle on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+CSRC = os.path.join(ROOT, "exact_attention_80_gb300", "csrc")
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ------------------------------------------------------------------ distributed helpers
+
+def dist_env():
+    """(rank, world_size, local_rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def dist_barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def dist_max(value: float, world: int, device=None) -> float:
+    """Max of a float over ranks (the slowest rank sets the job time)."""
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_sum(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def shard_seed(base_seed: int, rank: int) -> int:
+    """Each rank draws its own batch (weak scaling); rank 0 keeps the base seed."""
+    return base_seed + 7919 * rank
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason sampler around the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, period_ms: int = 100):
+        self.gpu_index = gpu_index
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", f"-lms={self.period_ms}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.6)  # nvidia-smi start-up
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(2 * self.period_ms / 1000.0)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peaks():
+    try:
+        with open(PEAKS_FILE, encoding="utf-8") as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, only if it was taken
+    on the current kernel sources (else None)."""
+    try:
+        with open(TRAFFIC_FILE, encoding="utf-8") as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in rec.get("entries", []):
+        if (e.get("kernel") == kernel and e.get("workload") == workload
+                and e.get("source_hash") == kernel_source_hash()):
+            return float(e["dram_bytes_per_launch"])
+    return None
+
+
+def cpu_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_sample(cfg: dict, budget_s: float, seed: int, max_heads: int | None = None):
+    """Time the float64 oracle over whole (b, h) heads of the workload until the
+    budget is spent. Returns (tflops, heads, seconds)."""
+    import oracle
+    from exact_attention_80_gb300.inputs import f32, make_qkv, metric_flops, to_f64
+
+    d = cfg["d"]
+    q, k, v = make_qkv(1, 1, cfg["Nq"], cfg["Nk"], d, seed)
+    qf, kf, vf = to_f64(q)[0, 0], to_f64(k)[0, 0], to_f64(v)[0, 0]
+    scale = f32(1.0 / math.sqrt(d))
+    heads, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attention_f64(qf, kf, vf, scale, cfg["causal"])
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or (max_heads is not None and heads >= max_heads):
+            break
+    flops = heads * metric_flops(1, 1, cfg["Nq"], cfg["Nk"], d, cfg["causal"])
+    return flops / el / 1e12, heads, el
+
+
+# ------------------------------------------------------------------ our arm
+
+def time_launches(fn, steps: int, stream):
+    """CUDA events bracketing every step on `stream`; returns per-step ms."""
+    import torch
+
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    evs[0].record(stream)
+    for i in range(steps):
+        fn()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
+
+
+def extra_workloads(device, stream, reps: int = 20):
+    """TFLOPS of the other benchmark workloads (seeded device-side N(0,1) bf16)."""
+    import torch
+
+    import exact_attention_80_gb300 as fa
+    from exact_attention_80_gb300.inputs import CONFIGS, metric_flops
+
+    out = {}
+    gen = torch.Generator(device=device)
+    for name in ("c1", "c2_causal", "c3", "c3_causal", "c4", "c5"):
+        c = CONFIGS[name]
+        B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
+        gen.manual_seed(c["seed"])
+        q = torch.randn((B, H, Nq, d), generator=gen, device=device).to(torch.bfloat16)
+        k = torch.randn((B, H, Nk, d), generator=gen, device=device).to(torch.bfloat16)
+        v = torch.randn((B, H, Nk, d), generator=gen, device=device).to(torch.bfloat16)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Nq), device=device)
+        flops = metric_flops(B, H, Nq, Nk, d, causal)
+        if name != "c5":
+            fn = lambda: fa.fa_fwd(q, k, v, o, lse, causal, stream=stream)  # noqa: E731
+            for _ in range(3):
+                fn()
+            ms = statistics.median(time_launches(fn, reps, stream))
+            out[name] = {"tflops": round(flops / ms / 1e9, 1), "us": round(ms * 1e3, 1)}
+        else:
+            sweep = {}
+            for S in (1, 2, 3, 4, 16, 64):
+                ws = torch.empty(fa.fa_splitkv_workspace_bytes(B, H, Nq, d, S) // 4,
+                                 device=device)
+                f_split = lambda: fa.fa_fwd_splitkv(q, k, v, ws, S, causal, stream=stream)  # noqa
+                f_comb = lambda: fa.fa_combine(ws, o, lse, B, H, Nq, d, S, stream=stream)  # noqa
+                for _ in range(3):
+                    f_split()
+                    f_comb()
+                ms_s = statistics.median(time_launches(f_split, reps, stream))
+                ms_c = statistics.median(time_launches(f_comb, reps, stream))
+                kv_bytes = 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2
+                part = S * B * H * Nq * (d + 2) * 4
+                comb_bytes = part + B * H * Nq * (d * 2 + 4)
+                sweep[str(S)] = {
+                    "tflops": round(flops / (ms_s + ms_c) / 1e9, 1),
+                    "split_us": round(ms_s * 1e3, 1), "combine_us": round(ms_c * 1e3, 1),
+                    "split_gbs": round((kv_bytes + part) / ms_s / 1e6, 1),
+                    "combine_gbs": round(comb_bytes / ms_c / 1e6, 1)}
+            out[name] = sweep
+        del q, k, v, o, lse
+    return out
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    import exact_attention_80_gb300 as fa
+    import oracle
+    from exact_attention_80_gb300.inputs import CONFIGS, f32, make_qkv, metric_flops, to_f64
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist_init("nccl")
+    fa.load_library()
+    stream = torch.cuda.current_stream(device)
+
+    wl = args.workload
+    c = CONFIGS[wl]
+    B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
+    seed = shard_seed(c["seed"], rank)
+    q_h, k_h, v_h = make_qkv(B, H, Nq, Nk, d, seed)
+    scale = f32(1.0 / math.sqrt(d))
+    q, k, v = q_h.to(device), k_h.to(device), v_h.to(device)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=device)
+    flops = metric_flops(B, H, Nq, Nk, d, causal)
+    in_bytes = 3 * q.numel() * 2 if Nq == Nk else (q.numel() + 2 * k.numel()) * 2
+
+    step = lambda: fa.fa_fwd(q, k, v, o, lse, causal, scale, stream=stream)  # noqa: E731
+
+    # ---- timed region (device-resident inputs)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    dist_barrier(world, device)
+    torch.cuda.synchronize()
+    per_step = time_launches(step, args.steps, stream)
+    torch.cuda.synchronize()
+    dist_barrier(world, device)
+    if sampler:
+        sampler.stop()
+    total_ms = dist_max(sum(per_step), world, device)
+    status = fa.fa_device_status(clear=True, stream=stream)
+    if status != fa.FA_OK:
+        raise RuntimeError(f"device status {fa.fa_status_string(status)}")
+    ms_per_step = total_ms / args.steps
+    value = dist_sum(flops, world, device) * args.steps / (total_ms / 1e3) / 1e12
+    avg_launch_ms = statistics.mean(per_step)
+
+    # ---- numeric check outside the timed window (sampled rows vs the oracle)
+    rng = np.random.default_rng(seed)
+    worst = 0.0
+    o_cpu, lse_cpu = o.float().cpu(), lse.cpu()
+    for _ in range(8):
+        b, h, i = int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(Nq))
+        ro, rl = oracle.attention_rows_f64(to_f64(q_h[b, h]), to_f64(k_h[b, h]),
+                                           to_f64(v_h[b, h]), scale, causal, [i])
+        worst = max(worst, float(np.abs(o_cpu[b, h, i].numpy() - ro[0]).max()))
+        if abs(float(lse_cpu[b, h, i]) - rl[0]) > 1e-3:
+            raise RuntimeError("bench parity check failed on LSE")
+    if worst > 2e-2:
+        raise RuntimeError(f"bench parity check failed: max-abs {worst:.3e}")
+
+    # ---- end to end through the public API from pinned host buffers
+    qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
+    op = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        q.copy_(qp, non_blocking=True)
+        k.copy_(kp, non_blocking=True)
+        v.copy_(vp, non_blocking=True)
+        fa.fa_fwd(q, k, v, o, lse, causal, scale, stream=stream)
+        op.copy_(o, non_blocking=True)
+        lp.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps, 50))
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    dist_barrier(world, device)
+    e2e_ms = dist_max(sum(time_launches(e2e_step, e2e_steps, stream)), world, device) / e2e_steps
+    e2e_value = dist_sum(flops, world, device) / (e2e_ms / 1e3) / 1e12
+    h2d = (qp.numel() + kp.numel() + vp.numel()) * 2
+    d2h = op.numel() * 2 + lp.numel() * 4
+
+    extras = extra_workloads(device, stream) if (rank == 0 and not args.no_extras) else None
+    dist_barrier(world, device)
+
+    if rank != 0:
+        return None
+    peak_tf, _, peak_kind = measured_peaks()
+    achieved = flops / (avg_launch_ms / 1e3) / 1e12
+    clocks = sampler.summary() if sampler else None
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        tf, heads, secs = oracle_sample(c, args.cpu_budget, seed)
+        cpu = {"value": round(tf, 6), "unit": "TFLOPS", "cores": cpu_threads(), "kind": "oracle",
+               "sample": f"{heads} of the {B * H} (b,h) heads of {wl}, float64 NumPy, "
+                         f"{secs:.1f} s"}
+    line = {
+        "metric": "attention fwd TFLOPS (bf16, 4*B*H*Nq*Nk*d, halved for causal)",
+        "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16)",
+        "config": {"workload": f"{wl}: B={B} H={H} Nq={Nq} Nk={Nk} d={d} "
+                               f"{'causal' if causal else 'non-causal'}",
+                   "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": causal,
+                   "seed": seed, "per_rank_batch": B,
+                   "l2": f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB of Q/K/V per rank "
+                         f"vs {L2_BYTES / 2**20:.0f} MiB L2); no flush",
+                   "parallelism": f"replicas x{world} (independent heads, no exchange)"},
+        "roofline": {"bound": "tensor", "kernel": f"fa_fwd_kernel<{d}>",
+                     "achieved": round(achieved, 1), "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak_tf, 4),
+                     "peak_kind": f"{peak_kind} bf16 burst (kernel timed alone)",
+                     "traffic": recorded_traffic(f"fa_fwd_kernel<{d}>", wl),
+                     "flops_per_launch": flops},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+        "parity_sampled_max_abs": worst,
+        "other_workloads": extras,
+    }
+    return line
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The float64 oracle as the reference arm, on the host cores, rank 0 only.
+    Each step is a bounded sample of the workload: a block of 256 query rows of
+    one (b, h) head against all of its keys."""
+    import oracle
+    from exact_attention_80_gb300.inputs import CONFIGS, f32, make_qkv, to_f64
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    wl = args.workload
+    c = CONFIGS[wl]
+    B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
+    q, k, v = make_qkv(1, 1, Nq, Nk, d, c["seed"])
+    qf, kf, vf = to_f64(q)[0, 0], to_f64(k)[0, 0], to_f64(v)[0, 0]
+    scale = f32(1.0 / math.sqrt(d))
+    rows_per_step = min(256, Nq)
+    n_blocks = -(-Nq // rows_per_step)
+
+    def step(i):
+        r0 = (i % n_blocks) * rows_per_step
+        rows = list(range(r0, min(r0 + rows_per_step, Nq)))
+        oracle.attention_rows_f64(qf, kf, vf, scale, causal, rows)
+        return len(rows)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    rows_done = sum(step(i) for i in range(args.steps))
+    secs = time.perf_counter() - t0
+    flops = 4.0 * rows_done * Nk * d / (2 if causal else 1)
+    value = flops / secs / 1e12
+    return {
+        "impl": "reference",
+        "metric": "attention fwd TFLOPS (bf16, 4*B*H*Nq*Nk*d, halved for causal)",
+        "value": round(value, 6), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16, upcast to float64)",
+        "config": {"workload": f"{wl}: B={B} H={H} Nq={Nq} Nk={Nk} d={d} "
+                               f"{'causal' if causal else 'non-causal'}",
+                   "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": causal},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cpu_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step = {rows_per_step} query rows of one (b,h) head "
+                                   f"of {wl} against all {Nk} keys (float64 NumPy oracle)"},
+        "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of float64 oracle work for cpu_baseline")
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+    if args.impl == "ours" and int(os.environ.get("WORLD_SIZE", "1")) > 1:
+        import torch.distributed as dist
+
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
