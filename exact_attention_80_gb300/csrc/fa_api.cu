@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -56,6 +57,20 @@ FwdConfig fwd_config(int d) {
 }
 
 namespace {
+
+cudaError_t sm_count(int* out) {
+    static int cache[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
+        *out = cache[dev];
+        return cudaSuccess;
+    }
+    e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) cache[dev] = *out;
+    return e;
+}
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool valid_d(int d) { return d == 64 || d == 128 || d == 256; }
@@ -142,6 +157,11 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     p.n_units = static_cast<int>(ctas / (static_cast<long long>(BH) * num_splits));
     const int kv_tiles = (Nk + c.bn - 1) / c.bn;
     p.kv_tiles_per_split = (kv_tiles + num_splits - 1) / num_splits;
+    // Heads per scheduling group: about one wave of CTAs (one CTA per SM).
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess) return FA_ERR_CUDA;
+    const long long ctas_per_head = static_cast<long long>(p.n_units) * num_splits;
+    p.head_group = static_cast<int>(std::max<long long>(1, std::min<long long>(BH, sms / ctas_per_head)));
     p.scale_log2 = scale * 1.4426950408889634f;
     p.wait_limit = kDefaultWaitLimit;
     if (device_status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;

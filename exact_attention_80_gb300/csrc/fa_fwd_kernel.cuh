@@ -35,6 +35,10 @@
 namespace fa {
 
 constexpr int kBM = 128;  // query rows per tile = TMEM lanes
+// How far (base-2 units) a row's max may rise above the exponent reference
+// before the reference moves and O, l are rescaled: p <= 2^8 = 256 is exact
+// in bf16's exponent range and far from fp32 overflow.
+constexpr float kRescaleSlack = 8.0f;
 
 template <int D>
 struct FwdCfg;
@@ -69,8 +73,10 @@ struct FwdLayout {
     static constexpr int BAR_KVFULL = 1;
     static constexpr int BAR_KVEMPTY = BAR_KVFULL + STAGES;
     static constexpr int BAR_SFULL = BAR_KVEMPTY + STAGES;
-    static constexpr int BAR_PFULL = BAR_SFULL + Q_TILES;
-    static constexpr int BAR_OFULL = BAR_PFULL + Q_TILES;
+    static constexpr int P_CHUNKS = BN / 64;  // P is written to TMEM in 64-key chunks
+    static constexpr int HANDOFFS = 1;  // ... and handed to the MMA in this many parts (one measured best)
+    static constexpr int BAR_PFULL = BAR_SFULL + Q_TILES;  // [tile][handoff]
+    static constexpr int BAR_OFULL = BAR_PFULL + Q_TILES * HANDOFFS;
     static constexpr int BAR_DRAIN = BAR_OFULL + Q_TILES;
     static constexpr int NUM_BARS = BAR_DRAIN + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] tmem base, [1] abort
@@ -87,6 +93,19 @@ struct FwdLayout {
     static_assert(ALLOC_BYTES <= 232448, "shared memory over the 227 KB per-CTA limit");
     static_assert(ALLOC_BYTES > 232448 / 2, "two CTAs per SM would contend for TMEM");
     static_assert(BN % 32 == 0 && D % 64 == 0, "tile shape");
+
+    // Register split (two query tiles): the kernel is compiled for LAUNCH_REGS
+    // per thread; the control warpgroup gives registers back and the two
+    // softmax warpgroups take them. setmaxnreg.inc waits until the pool has the
+    // registers, so the split must add up to exactly the launch allocation;
+    // the host refuses to launch if the compiled count differs.
+    static constexpr bool REG_SPLIT = (Q_TILES == 2);
+    static constexpr int LAUNCH_REGS = 168;
+    static constexpr int CTRL_REGS = 72;
+    static constexpr int SOFTMAX_REGS = 216;
+    static_assert(!REG_SPLIT || 128 * CTRL_REGS + 256 * SOFTMAX_REGS == THREADS * LAUNCH_REGS,
+                  "register split must equal the launch allocation");
+    static_assert(65536 / THREADS >= LAUNCH_REGS || !REG_SPLIT, "launch registers");
 };
 
 // Work owned by one CTA.
@@ -104,13 +123,20 @@ struct Work {
 template <int D>
 __device__ __forceinline__ void compute_work(const FwdParams& p, Work<FwdCfg<D>::Q_TILES>& w) {
     using L = FwdLayout<D>;
+    // CTA order: key splits fastest; then heads in groups of p.head_group
+    // (sized so one group is about one wave of CTAs), and within a group the
+    // query units heaviest first (last rows first under a causal mask) across
+    // the group's heads. CTAs running together share a few heads' K/V in L2,
+    // and long causal units start before short ones.
     long long lin = blockIdx.x;
     w.split = static_cast<int>(lin % p.num_splits);
     lin /= p.num_splits;
-    w.bh = static_cast<int>(lin % p.BH);
-    lin /= p.BH;
-    // Heaviest units (last query rows under a causal mask) are dispatched first.
-    const int unit = p.n_units - 1 - static_cast<int>(lin);
+    const long long per_group = static_cast<long long>(p.head_group) * p.n_units;
+    const int group = static_cast<int>(lin / per_group);
+    const int r = static_cast<int>(lin % per_group);
+    const int heads_here = min(p.head_group, p.BH - group * p.head_group);
+    const int unit = p.n_units - 1 - r / heads_here;
+    w.bh = group * p.head_group + r % heads_here;
     w.q0 = unit * L::Q_TILES * kBM;
     const int total_tiles = (p.Nk + L::BN - 1) / L::BN;
     const int t0 = min(w.split * p.kv_tiles_per_split, total_tiles);
@@ -183,7 +209,7 @@ __global__ void __launch_bounds__(FwdLayout<D>::THREADS, 1)
         }
         for (int t = 0; t < QT; ++t) {
             mbar_init(bar(L::BAR_SFULL + t), 1);
-            mbar_init(bar(L::BAR_PFULL + t), kBM);
+            for (int h = 0; h < L::HANDOFFS; ++h) mbar_init(bar(L::BAR_PFULL + t * L::HANDOFFS + h), kBM);
             mbar_init(bar(L::BAR_OFULL + t), 1);
         }
         mbar_init(bar(L::BAR_DRAIN), 1);
@@ -204,7 +230,11 @@ __global__ void __launch_bounds__(FwdLayout<D>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = misc[0];
 
-    if (warp == 0) {
+    if (warp < 4) {
+      // Control warpgroup. setmaxnreg sits inside each role's branch so that
+      // the register allocator sees one limit per code path.
+      if constexpr (L::REG_SPLIT) setmaxnreg_dec<L::CTRL_REGS>();
+      if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0 && w.nmax > 0) {
             int nvalid = 0;
@@ -272,10 +302,11 @@ __global__ void __launch_bounds__(FwdLayout<D>::THREADS, 1)
                     umma_ss(tmem + L::S_COL(t), a, b, IDESC_S, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int t, int slot, bool accumulate) {
+            auto issue_pv = [&](int t, int slot, int part, bool accumulate) {
                 const uint32_t vb = sbase + L::SLOT_OFF + slot * L::SLOT_BYTES;
+                constexpr int KK = BN / 16 / L::HANDOFFS;  // MMAs (16 keys each) per hand-off
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
+                for (int kk = part * KK; kk < part * KK + KK; ++kk) {
                     // V is MN-major: 16 keys = two 8-row swizzle atoms (2048 bytes);
                     // 64-column chunks of d are BN*128 bytes apart.
                     const uint64_t b = make_sdesc_sw128(vb + kk * 2048, BN * 128, 1024);
@@ -317,11 +348,17 @@ __global__ void __launch_bounds__(FwdLayout<D>::THREADS, 1)
 #pragma unroll
                     for (int t = 0; t < QT; ++t) {
                         if (ok && j < w.n[t]) {
-                            ok = wait_phase(bar(L::BAR_PFULL + t), j & 1, p, abort_flag,
-                                            kStatusWaitP);
+                            // O_t += P_t V_j chunk by chunk, each as soon as the
+                            // softmax has written that chunk of P_t.
+#pragma unroll
+                            for (int h = 0; h < L::HANDOFFS; ++h) {
+                                ok = wait_phase(bar(L::BAR_PFULL + t * L::HANDOFFS + h), j & 1, p,
+                                                abort_flag, kStatusWaitP);
+                                if (!ok) break;
+                                tc_fence_after();
+                                issue_pv(t, slot_v, h, j > 0);
+                            }
                             if (!ok) break;
-                            tc_fence_after();
-                            issue_pv(t, slot_v, j > 0);
                             if (j + 1 < w.n[t]) {
                                 issue_s(t, slot_k);
                                 umma_commit(bar(L::BAR_SFULL + t));
@@ -341,8 +378,10 @@ __global__ void __launch_bounds__(FwdLayout<D>::THREADS, 1)
                 wait_phase(bar(L::BAR_DRAIN), 0, p, abort_flag, kStatusWaitDrain, false);
             }
         }
-    } else if (warp >= 4) {
+      }
+    } else {
         // ------------------------------------------------------------ softmax
+        if constexpr (L::REG_SPLIT) setmaxnreg_inc<L::SOFTMAX_REGS>();
         const int t = (warp - 4) >> 2;
         const int quarter = warp & 3;  // TMEM lane quarter this warp may access
         const int r = quarter * 32 + lane;
@@ -356,8 +395,9 @@ __global__ void __launch_bounds__(FwdLayout<D>::THREADS, 1)
         for (int i = 1; i < QT; ++i)
             if (t == i) n = w.n[i];
 
-        float m = -INFINITY;  // running max of scale*log2e*s (base-2 units)
-        float l = 0.f;        // running sum relative to m
+        float m = -INFINITY;       // exponent reference (base-2 units of scale*log2e*s)
+        float m_true = -INFINITY;  // true running row max, same units
+        float l = 0.f;             // running sum relative to m
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             ok = wait_phase(bar(L::BAR_SFULL + t), j & 1, p, abort_flag, kStatusWaitS);
@@ -388,45 +428,72 @@ __global__ void __launch_bounds__(FwdLayout<D>::THREADS, 1)
             }
             __syncwarp();
 
-            float mx = s[0];
+            // Row max: four independent three-input max chains.
+            float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-            for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
-            const float m_new = fmaxf(m, mx * sl2);
+            for (int c = 0; c < BN; c += 8) {
+                a0 = max3f(a0, s[c + 0], s[c + 1]);
+                a1 = max3f(a1, s[c + 2], s[c + 3]);
+                a2 = max3f(a2, s[c + 4], s[c + 5]);
+                a3 = max3f(a3, s[c + 6], s[c + 7]);
+            }
+            const float m_tile = max3f(a0, a1, fmaxf(a2, a3)) * sl2;  // base-2 units
+            m_true = fmaxf(m_true, m_tile);
+            // The exponent reference m only moves when this tile's max exceeds it
+            // by more than kRescaleSlack; otherwise every p = 2^(x - m) <= 2^slack
+            // and the old reference is kept, so O and l need no rescale. The
+            // result is the same: O/l and m + log2(l) do not depend on which
+            // reference is used, only rounding does.
+            const bool move = m_tile > m + kRescaleSlack;
+            const float m_new = move ? m_tile : m;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // all masked so far
-            const float alpha = (m == m_use) ? 1.f : ex2(m - m_use);
+            const float alpha = move ? ex2(m - m_use) : 1.f;
             const float neg = -m_use;
 
-            float sum = 0.f;
-#pragma unroll
-            for (int cc = 0; cc < BN / 64; ++cc) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float e0 = ex2(fmaf(s[cc * 64 + 2 * i], sl2, neg));
-                    const float e1 = ex2(fmaf(s[cc * 64 + 2 * i + 1], sl2, neg));
-                    sum += e0 + e1;
-                    pk[i] = pack_bf16x2(e0, e1);
-                }
-                tmem_st32(tS + cc * 32, pk);  // P over the first BN/2 columns of S
-            }
-            l = l * alpha + sum;
-
-            // Rescale the accumulator. PV_{j-1} has completed: the commit that
-            // signalled S_j was issued after it.
+            // Rescale the accumulator before any of this tile's PV MMAs run.
+            // PV_{j-1} has completed: the commit that signalled S_j came after it.
             if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                const uint64_t ax2 = f2pack(alpha, alpha);
 #pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
                     tmem_ld32(tO + cc * 32, o);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    for (int i = 0; i < 16; ++i) {
+                        float x0, x1;
+                        f2unpack(fmul2(f2pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), ax2),
+                                 x0, x1);
+                        o[2 * i] = __float_as_uint(x0);
+                        o[2 * i + 1] = __float_as_uint(x1);
+                    }
                     tmem_st32(tO + cc * 32, o);
                 }
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(L::BAR_PFULL + t));
+
+            float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums
+#pragma unroll
+            for (int cc = 0; cc < L::P_CHUNKS; ++cc) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float e0 = ex2(fmaf(s[cc * 64 + 2 * i], sl2, neg));
+                    const float e1 = ex2(fmaf(s[cc * 64 + 2 * i + 1], sl2, neg));
+                    part[(2 * i) & 7] += e0;
+                    part[(2 * i + 1) & 7] += e1;
+                    pk[i] = pack_bf16x2(e0, e1);
+                }
+                tmem_st32(tS + cc * 32, pk);  // P chunk over S's columns [32cc, 32cc+32)
+                constexpr int PER_HANDOFF = L::P_CHUNKS / L::HANDOFFS;
+                if ((cc + 1) % PER_HANDOFF == 0) {
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(bar(L::BAR_PFULL + t * L::HANDOFFS + cc / PER_HANDOFF));
+                }
+            }
+            const float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
+                              ((part[4] + part[5]) + (part[6] + part[7]));
+            l = l * alpha + sum;
             m = m_new;
         }
 
@@ -470,6 +537,10 @@ __global__ void __launch_bounds__(FwdLayout<D>::THREADS, 1)
                 const size_t part_idx =
                     (static_cast<size_t>(w.split) * p.BH + w.bh) * p.Nq + q_row;
                 float* orow = p.ws_o + part_idx * D;
+                // Partial states are stated relative to the split's true row max:
+                // move l and O from the lazy reference m to m_true.
+                const float rebase = (l > 0.f && m != m_true) ? ex2(m - m_true) : 1.f;
+                const uint64_t rb2 = f2pack(rebase, rebase);
 #pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
@@ -480,6 +551,16 @@ __global__ void __launch_bounds__(FwdLayout<D>::THREADS, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = 0u;
                     }
+                    if (rebase != 1.f) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            float x0, x1;
+                            f2unpack(fmul2(f2pack(__uint_as_float(o[2 * i]),
+                                                  __uint_as_float(o[2 * i + 1])), rb2), x0, x1);
+                            o[2 * i] = __float_as_uint(x0);
+                            o[2 * i + 1] = __float_as_uint(x1);
+                        }
+                    }
                     if (row_ok) {
                         uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
@@ -488,8 +569,8 @@ __global__ void __launch_bounds__(FwdLayout<D>::THREADS, 1)
                     }
                 }
                 if (row_ok) {
-                    p.ws_m[part_idx] = (l > 0.f) ? m * 0.69314718055994530942f : -INFINITY;
-                    p.ws_l[part_idx] = l;
+                    p.ws_m[part_idx] = (l > 0.f) ? m_true * 0.69314718055994530942f : -INFINITY;
+                    p.ws_l[part_idx] = l * rebase;
                 }
             }
         }
@@ -510,6 +591,13 @@ cudaError_t launch_fwd(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+        if constexpr (L::REG_SPLIT) {
+            // The setmaxnreg split is sized for exactly LAUNCH_REGS per thread.
+            cudaFuncAttributes a;
+            e = cudaFuncGetAttributes(&a, fa_fwd_kernel<D>);
+            if (e != cudaSuccess) return e;
+            if (a.numRegs != L::LAUNCH_REGS) return cudaErrorInvalidKernelImage;
+        }
         e = cudaFuncSetAttribute(fa_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(L::ALLOC_BYTES));
         if (e != cudaSuccess) return e;

@@ -39,6 +39,7 @@ struct FwdParams {
     int split_mode;          // 0: write O/LSE, 1: write partial (O, m, l)
     int n_units;             // query units of (tiles per CTA * 128) rows per head
     int kv_tiles_per_split;  // ceil(ceil(Nk/BN) / num_splits)
+    int head_group;          // heads per scheduling group (CTA order)
     float scale_log2;        // scale * log2(e)
     long long wait_limit;    // cycles
     unsigned* status;        // device status word
