@@ -18,7 +18,7 @@ FA_OK = 0
 STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_ALIGN", 3: "FA_ERR_SHAPE", 4: "FA_ERR_HEADDIM",
     5: "FA_ERR_SPLITS", 6: "FA_ERR_WORKSPACE", 7: "FA_ERR_CUDA", 8: "FA_ERR_TIMEOUT",
-    9: "FA_ERR_SCALE",
+    9: "FA_ERR_SCALE", 10: "FA_ERR_SCRATCH",
 }
 FA_MAX_SPLITS = 256
 
@@ -165,3 +165,22 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, num_spl
         fa_fwd_splitkv(q, k, v, ws, num_splits, causal, scale, stream)
         fa_combine(ws, o, lse, B, H, Nq, d, num_splits, stream)
     return o, lse
+
+
+def fa_fwd_splitkv_static(q, k, v, o, lse, num_splits: int, causal: bool = False,
+                          scale: float | None = None, stream=None):
+    """Split-KV forward + merge into caller-owned ``o``/``lse`` with no workspace
+    argument: the partial states live in the library's static device buffer
+    (``FA_STATIC_SCRATCH_BYTES``), so nothing is allocated. For callers that may
+    not allocate device memory; calls that overlap on the GPU share that buffer
+    and race (see include/fa.h)."""
+    B, H, Nq, Nk, d = _bhnd(q, k, v)
+    scale = default_scale(d) if scale is None else float(scale)
+    lib = load_library()
+    fn = lib.fa_fwd_splitkv_static
+    vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    fn.restype = i
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, scale,
+            int(bool(causal)), int(num_splits), _stream_handle(stream))
+    _check(st, "fa_fwd_splitkv_static")

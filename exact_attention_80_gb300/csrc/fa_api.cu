@@ -263,6 +263,8 @@ const char* fa_status_string(fa_status status) {
         case FA_ERR_CUDA: return "FA_ERR_CUDA: a CUDA runtime or driver call failed";
         case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT: a kernel gave up on a bounded wait";
         case FA_ERR_SCALE: return "FA_ERR_SCALE: scale must be finite and > 0";
+        case FA_ERR_SCRATCH:
+            return "FA_ERR_SCRATCH: partial states exceed the library's static scratch buffer";
     }
     return "unknown fa_status";
 }

@@ -52,7 +52,8 @@ typedef enum {
     FA_ERR_WORKSPACE = 6,  /* workspace pointer NULL or misaligned */
     FA_ERR_CUDA = 7,       /* a CUDA runtime or driver call failed (no device, launch, tensor-map encode) */
     FA_ERR_TIMEOUT = 8,    /* a kernel gave up on a bounded wait (reported by fa_device_status) */
-    FA_ERR_SCALE = 9       /* scale is not finite or not > 0 */
+    FA_ERR_SCALE = 9,      /* scale is not finite or not > 0 */
+    FA_ERR_SCRATCH = 10    /* fa_fwd_splitkv_static: partial states exceed FA_STATIC_SCRATCH_BYTES */
 } fa_status;
 
 #define FA_MAX_SPLITS 256
@@ -129,6 +130,39 @@ long long fa_fwd_grid_ctas(int B, int H, int Nq, int d, int num_splits);
  * undefined). `clear` != 0 resets the word. FA_ERR_CUDA if the read fails.
  */
 fa_status fa_device_status(cudaStream_t stream, int clear);
+
+/*
+ * fa_fwd_splitkv_static — split-KV forward plus merge that allocates nothing
+ * and takes no workspace argument. The pages have no counterpart to this
+ * entry point; it exists for callers that cannot call cudaMalloc: a host
+ * program or framework that owns every byte of device memory through its own
+ * allocator and budget (so a library allocation would go unaccounted or fail),
+ * or a serving loop where an allocation could block on device-wide
+ * synchronisation at the wrong moment.
+ *
+ * It computes exactly what fa_fwd_splitkv followed by fa_combine computes
+ * (same kernels, same split rule, same o/lse output contract as fa_fwd), but
+ * keeps the partial states in one statically sized device buffer of
+ * FA_STATIC_SCRATCH_BYTES that the library defines. Every GPU that loads the
+ * library holds that buffer until the process exits.
+ *   - The partial states, fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits)
+ *     bytes, must fit in FA_STATIC_SCRATCH_BYTES; larger problems return
+ *     FA_ERR_SCRATCH before any CUDA call (use fewer splits, or fa_fwd_splitkv
+ *     with your own workspace).
+ *   - The first call on a device looks up that device's address of the buffer
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - All calls on a device share the one buffer and it keeps the last call's
+ *     contents. Nothing in it needs to start at zero: the split kernel writes
+ *     every entry the merge reads. Calls whose work overlaps on the GPU (other
+ *     streams, other host threads) race on the buffer and give wrong results;
+ *     order them on one stream or with events.
+ * Arguments and the other status codes are those of fa_fwd plus num_splits.
+ */
+#define FA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+fa_status fa_fwd_splitkv_static(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                                int num_splits, cudaStream_t stream);
 
 /* fa_status_string — static, human-readable name of a status code. */
 const char* fa_status_string(fa_status status);
