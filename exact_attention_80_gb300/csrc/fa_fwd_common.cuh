@@ -1,0 +1,180 @@
+// fa_fwd_common.cuh — pieces shared by the forward kernels: work partition,
+// bounded mbarrier waits, K/V ring positions and the per-row epilogue.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "fa_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+constexpr int kBM = 128;  // query rows per tile = TMEM lanes
+// How far (base-2 units) a row's max may rise above the exponent reference
+// before the reference moves and O, l are rescaled: p <= 2^8 = 256 is exact
+// in bf16's exponent range and far from fp32 overflow.
+constexpr float kRescaleSlack = 8.0f;
+
+// Ring position (slot, phase parity) of a sequence of K/V entries.
+template <int ST>
+struct RingPos {
+    int slot = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void advance() {
+        if (++slot == ST) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+};
+
+// Work owned by one CTA.
+template <int Q_TILES>
+struct Work {
+    int bh;        // batch * H + head
+    int q0;        // first query row of the unit
+    int split;     // key split index (0 in plain mode)
+    int kv_tile0;  // first key tile of the split
+    int kv_end;    // exclusive key bound of the split (for masking)
+    int n[Q_TILES];  // key tiles each query tile visits
+    int nmax;
+};
+
+template <int QT, int BN>
+__device__ __forceinline__ void compute_work(const FwdParams& p, Work<QT>& w) {
+    // CTA order: key splits fastest; then heads in groups of p.head_group
+    // (sized so one group is about one wave of CTAs), and within a group the
+    // query units heaviest first (last rows first under a causal mask) across
+    // the group's heads. CTAs running together share a few heads' K/V in L2,
+    // and long causal units start before short ones.
+    long long lin = blockIdx.x;
+    w.split = static_cast<int>(lin % p.num_splits);
+    lin /= p.num_splits;
+    const long long per_group = static_cast<long long>(p.head_group) * p.n_units;
+    const int group = static_cast<int>(lin / per_group);
+    const int r = static_cast<int>(lin % per_group);
+    const int heads_here = min(p.head_group, p.BH - group * p.head_group);
+    const int unit = p.n_units - 1 - r / heads_here;
+    w.bh = group * p.head_group + r % heads_here;
+    w.q0 = unit * QT * kBM;
+    const int total_tiles = (p.Nk + BN - 1) / BN;
+    const int t0 = min(w.split * p.kv_tiles_per_split, total_tiles);
+    const int t1 = min(t0 + p.kv_tiles_per_split, total_tiles);
+    w.kv_tile0 = t0;
+    w.kv_end = min(p.Nk, t1 * BN);
+    w.nmax = 0;
+#pragma unroll
+    for (int t = 0; t < QT; ++t) {
+        const int row0 = w.q0 + t * kBM;
+        int n = 0;
+        if (row0 < p.Nq) {
+            int end = t1;
+            if (p.causal) {
+                const int last_row = min(row0 + kBM - 1, p.Nq - 1);
+                end = min(end, last_row / BN + 1);
+            }
+            n = max(0, end - t0);
+        }
+        w.n[t] = n;
+        w.nmax = max(w.nmax, n);
+    }
+}
+
+// Bounded wait on an mbarrier phase. Returns false if this CTA is aborting
+// (honor_abort) or the wait ran past the limit (then raises the abort).
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const FwdParams& p,
+                                           volatile uint32_t* abort_flag, unsigned what,
+                                           bool honor_abort = true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long start = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (honor_abort && *abort_flag) return false;
+        if (clock64() - start > p.wait_limit) {
+            *abort_flag = 1u;
+            atomicOr(p.status, what);
+            return false;
+        }
+    }
+}
+
+// Writes one query row's result from its TMEM accumulator row (lane address
+// tO, D fp32 columns; ignored when n == 0): normalised O (bf16) and LSE in
+// plain mode, or the unnormalised partial state (O, m, l) in split mode.
+// Deferred normalisation: one division per row, at the write.
+template <int D>
+__device__ __forceinline__ void write_row(const FwdParams& p, int bh, int split, int q_row, int n,
+                                          float m, float m_true, float l, uint32_t tO) {
+    const bool row_ok = q_row < p.Nq;
+    const size_t row_idx = static_cast<size_t>(bh) * p.Nq + q_row;
+    if (!p.split_mode) {
+        // Deferred normalisation: one division per row, at the write.
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + row_idx * D;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            if (n > 0) {
+                tmem_ld32(tO + cc * 32, o);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
+                                    __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (row_ok) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+        }
+        if (row_ok)
+            p.lse[row_idx] = (l > 0.f) ? (m + lg2(l)) * 0.69314718055994530942f : -INFINITY;
+    } else {
+        const size_t part_idx =
+            (static_cast<size_t>(split) * p.BH + bh) * p.Nq + q_row;
+        float* orow = p.ws_o + part_idx * D;
+        // Partial states are stated relative to the split's true row max:
+        // move l and O from the lazy reference m to m_true.
+        const float rebase = (l > 0.f && m != m_true) ? ex2(m - m_true) : 1.f;
+        const uint64_t rb2 = f2pack(rebase, rebase);
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t o[32];
+            if (n > 0) {
+                tmem_ld32(tO + cc * 32, o);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+            if (rebase != 1.f) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float x0, x1;
+                    f2unpack(fmul2(f2pack(__uint_as_float(o[2 * i]),
+                                          __uint_as_float(o[2 * i + 1])), rb2), x0, x1);
+                    o[2 * i] = __float_as_uint(x0);
+                    o[2 * i + 1] = __float_as_uint(x1);
+                }
+            }
+            if (row_ok) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+            }
+        }
+        if (row_ok) {
+            p.ws_m[part_idx] = (l > 0.f) ? m_true * 0.69314718055994530942f : -INFINITY;
+            p.ws_l[part_idx] = l * rebase;
+        }
+    }
+}
+
+}  // namespace fa
