@@ -201,6 +201,11 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
+def kernel_name(d: int) -> str:
+    """The forward kernel the library launches for head dim d."""
+    return f"fa_fwd_tp_kernel<{d}>" if d == 256 else f"fa_fwd_sp_kernel<{d}>"
+
+
 def cpu_threads() -> int:
     try:
         from threadpoolctl import threadpool_info
@@ -414,11 +419,11 @@ def run_ours(args):
                    "l2": f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB of Q/K/V per rank "
                          f"vs {L2_BYTES / 2**20:.0f} MiB L2); no flush",
                    "parallelism": f"replicas x{world} (independent heads, no exchange)"},
-        "roofline": {"bound": "tensor", "kernel": f"fa_fwd_kernel<{d}>",
+        "roofline": {"bound": "tensor", "kernel": kernel_name(d),
                      "achieved": round(achieved, 1), "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tf, 4),
                      "peak_kind": f"{peak_kind} bf16 burst (kernel timed alone)",
-                     "traffic": recorded_traffic(f"fa_fwd_kernel<{d}>", wl),
+                     "traffic": recorded_traffic(kernel_name(d), wl),
                      "flops_per_launch": flops},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
