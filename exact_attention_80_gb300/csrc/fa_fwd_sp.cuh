@@ -411,16 +411,26 @@ __global__ void __launch_bounds__(LayoutSP<D>::THREADS, 1)
             const float alpha = move ? ex2(m - m_use) : 1.f;
             const float neg = -m_use;
 
+            // x = s*scale*log2e - m as packed fp32 pairs (one FFMA2 per two keys),
+            // p = 2^x on the MUFU, row sums as four packed partial pairs.
             uint32_t pk[BN / 2];  // P as packed bf16 pairs
-            float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums
+            const uint64_t sl2x2 = f2pack(sl2, sl2);
+            const uint64_t negx2 = f2pack(neg, neg);
+            uint64_t part2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int i = 0; i < BN / 2; ++i) {
-                const float e0 = ex2(fmaf(s[2 * i], sl2, neg));
-                const float e1 = ex2(fmaf(s[2 * i + 1], sl2, neg));
-                part[(2 * i) & 7] += e0;
-                part[(2 * i + 1) & 7] += e1;
+                float x0, x1;
+                f2unpack(ffma2(f2pack(s[2 * i], s[2 * i + 1]), sl2x2, negx2), x0, x1);
+                const float e0 = ex2(x0);
+                const float e1 = ex2(x1);
+                part2[i & 3] = fadd2(part2[i & 3], f2pack(e0, e1));
                 pk[i] = pack_bf16x2(e0, e1);
             }
+            float part[8];
+            f2unpack(part2[0], part[0], part[1]);
+            f2unpack(part2[1], part[2], part[3]);
+            f2unpack(part2[2], part[4], part[5]);
+            f2unpack(part2[3], part[6], part[7]);
 
             if (j > 0) {
                 // PV_t(j-1) must be done before P_t is overwritten and before O_t

@@ -422,16 +422,22 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
                 }
             }
 
-            float part[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // partial row sums
+            // x = s*scale*log2e - m as packed fp32 pairs (one FFMA2 per two keys),
+            // p = 2^x on the MUFU, row sums as four packed partial pairs.
+            const uint64_t sl2x2 = f2pack(sl2, sl2);
+            const uint64_t negx2 = f2pack(neg, neg);
+            uint64_t part2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int cc = 0; cc < BN / 64; ++cc) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float e0 = ex2(fmaf(s[cc * 64 + 2 * i], sl2, neg));
-                    const float e1 = ex2(fmaf(s[cc * 64 + 2 * i + 1], sl2, neg));
-                    part[(2 * i) & 7] += e0;
-                    part[(2 * i + 1) & 7] += e1;
+                    float x0, x1;
+                    f2unpack(ffma2(f2pack(s[cc * 64 + 2 * i], s[cc * 64 + 2 * i + 1]), sl2x2, negx2),
+                             x0, x1);
+                    const float e0 = ex2(x0);
+                    const float e1 = ex2(x1);
+                    part2[i & 3] = fadd2(part2[i & 3], f2pack(e0, e1));
                     pk[i] = pack_bf16x2(e0, e1);
                 }
                 tmem_st32(tS + cc * 32, pk);  // P over the buffer's columns [32cc, 32cc+32)
@@ -439,6 +445,11 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(L::BAR_PFULL + 2 * t + b));
+            float part[8];
+            f2unpack(part2[0], part[0], part[1]);
+            f2unpack(part2[1], part[2], part[3]);
+            f2unpack(part2[2], part[4], part[5]);
+            f2unpack(part2[3], part[6], part[7]);
             const float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
                               ((part[4] + part[5]) + (part[6] + part[7]));
             l = l * alpha + sum;
