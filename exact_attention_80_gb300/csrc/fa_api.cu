@@ -128,7 +128,8 @@ long long grid_ctas(int B, int H, int Nq, int d, int num_splits) {
 
 fa_status launch_forward(const void* q, const void* k, const void* v, void* o, float* lse,
                          float* ws, int B, int H, int Nq, int Nk, int d, float scale, int causal,
-                         int num_splits, int split_mode, cudaStream_t stream) {
+                         int num_splits, int split_mode, cudaStream_t stream,
+                         long long wait_limit = kDefaultWaitLimit, int withhold_q = 0) {
     const FwdConfig c = fwd_config(d);
     const long long ctas = grid_ctas(B, H, Nq, d, num_splits);
     if (ctas < 1 || ctas > 0x7fffffffll) return FA_ERR_SHAPE;
@@ -163,7 +164,8 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     const long long ctas_per_head = static_cast<long long>(p.n_units) * num_splits;
     p.head_group = static_cast<int>(std::max<long long>(1, std::min<long long>(BH, sms / ctas_per_head)));
     p.scale_log2 = scale * 1.4426950408889634f;
-    p.wait_limit = kDefaultWaitLimit;
+    p.wait_limit = wait_limit;
+    p.test_withhold_q = withhold_q;
     if (device_status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
 
     cudaError_t e = cudaErrorInvalidValue;
@@ -226,6 +228,19 @@ fa_status fa_combine(const void* workspace, void* o, float* lse, int B, int H, i
     const float* ws_l = ws_m + static_cast<size_t>(num_splits) * rows;
     const cudaError_t e = fa::launch_combine(ws, ws_m, ws_l, o, lse, rows, num_splits, d, stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_test_fwd_withheld_q(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int Nq, int Nk, int d, long long wait_limit_cycles,
+                                 cudaStream_t stream) {
+    fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, 1.0f);
+    if (s != FA_OK) return s;
+    if (!o || !lse) return FA_ERR_NULL;
+    if (!fa::aligned(o, 16) || !fa::aligned(lse, 4)) return FA_ERR_ALIGN;
+    if (wait_limit_cycles < (1ll << 16) || wait_limit_cycles > fa::kDefaultWaitLimit)
+        return FA_ERR_SHAPE;
+    return fa::launch_forward(q, k, v, o, lse, nullptr, B, H, Nq, Nk, d, 1.0f, 0, 1, 0, stream,
+                              wait_limit_cycles, 1);
 }
 
 long long fa_fwd_grid_ctas(int B, int H, int Nq, int d, int num_splits) {

@@ -165,10 +165,12 @@ __global__ void __launch_bounds__(LayoutSP<D>::THREADS, 1)
             int nvalid = 0;
 #pragma unroll
             for (int t = 0; t < QT; ++t) nvalid += (w.n[t] > 0) ? 1 : 0;
-            mbar_arrive_expect_tx(bar(L::BAR_QFULL), nvalid * L::Q_TILE_BYTES);
+            // (The failure-detection test hook withholds the Q tiles so that the
+            // issuer's bounded wait runs out; nothing else changes.)
+            if (!p.test_withhold_q) mbar_arrive_expect_tx(bar(L::BAR_QFULL), nvalid * L::Q_TILE_BYTES);
 #pragma unroll
             for (int t = 0; t < QT; ++t) {
-                if (w.n[t] > 0) {
+                if (w.n[t] > 0 && !p.test_withhold_q) {
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128),

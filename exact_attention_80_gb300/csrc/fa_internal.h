@@ -42,6 +42,7 @@ struct FwdParams {
     int head_group;          // heads per scheduling group (CTA order)
     float scale_log2;        // scale * log2(e)
     long long wait_limit;    // cycles
+    int test_withhold_q;     // failure-detection test hook: 1 = never load Q
     unsigned* status;        // device status word
 };
 

@@ -164,6 +164,21 @@ fa_status fa_fwd_splitkv_static(const void* q, const void* k, const void* v, voi
                                 int B, int H, int Nq, int Nk, int d, float scale, int causal,
                                 int num_splits, cudaStream_t stream);
 
+/*
+ * fa_test_fwd_withheld_q — failure-detection test hook (not for production
+ * use). Launches the fa_fwd kernel (scale 1, non-causal) with its Q tile loads
+ * withheld and every mbarrier wait bounded by `wait_limit_cycles` SM cycles
+ * (2^16 .. 2^31). The MMA issuer's wait for Q then runs out before any MMA is
+ * issued; the kernel raises its abort flag, the other roles leave at their
+ * next wait, in-flight K/V copies are waited for, TMEM is freed and the kernel
+ * exits without touching o or lse. A following fa_device_status returns
+ * FA_ERR_TIMEOUT, and the CUDA context stays usable. No fault, trap or hang is
+ * involved: only a wait that nothing will satisfy, with a bound.
+ */
+fa_status fa_test_fwd_withheld_q(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 int B, int H, int Nq, int Nk, int d, long long wait_limit_cycles,
+                                 cudaStream_t stream);
+
 /* fa_status_string — static, human-readable name of a status code. */
 const char* fa_status_string(fa_status status);
 
