@@ -203,7 +203,7 @@ def recorded_traffic(kernel: str, workload: str):
 
 def kernel_name(d: int) -> str:
     """The forward kernel the library launches for head dim d."""
-    return f"fa_fwd_tp_kernel<{d}>" if d == 256 else f"fa_fwd_sp_kernel<{d}>"
+    return f"fa_fwd_tp_kernel<{d}>" if d == 256 else f"fa_fwd_tm_kernel<{d}>"
 
 
 def cpu_threads() -> int:

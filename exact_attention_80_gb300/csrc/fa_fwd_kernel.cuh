@@ -1,27 +1,28 @@
 // fa_fwd_kernel.cuh — selects the forward kernel design per head dim and
 // launches it.
-//   d = 64, 128: fa_fwd_sp.cuh — two 128-row query tiles per CTA, BN = 128,
-//                P staged in shared memory, S freed as soon as it is read.
+//   d = 64, 128: fa_fwd_tm.cuh — two 128-row query tiles per CTA, BN = 128,
+//                P handed to the PV MMA in TMEM over its S columns, the two
+//                tiles alternating on the tensor core.
 //   d = 256:     fa_fwd_tp.cuh — one query tile per CTA (O takes half of TMEM),
 //                BN = 64, S double-buffered in TMEM with P packed over it.
 #pragma once
 
 #include <type_traits>
 
-#include "fa_fwd_sp.cuh"
+#include "fa_fwd_tm.cuh"
 #include "fa_fwd_tp.cuh"
 
 namespace fa {
 
 template <int D>
-using FwdLayout = std::conditional_t<D == 256, LayoutTP<D>, LayoutSP<D>>;
+using FwdLayout = std::conditional_t<D == 256, LayoutTP<D>, LayoutTM<D>>;
 
 template <int D>
 cudaError_t launch_fwd(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     using L = FwdLayout<D>;
     constexpr auto kernel = [] {
         if constexpr (D == 256) return fa_fwd_tp_kernel<D>;
-        else return fa_fwd_sp_kernel<D>;
+        else return fa_fwd_tm_kernel<D>;
     }();
     static bool attr_set[64] = {};
     int dev = 0;

@@ -1,0 +1,470 @@
+// fa_fwd_tm.cuh — fused exact attention forward, two query tiles per CTA with
+// P handed to the tensor core in TMEM.
+//
+// One CTA owns two query tiles of 128 rows of one (batch, head) and sweeps the
+// keys those rows need in key tiles of BN = 128. Roles, by warp:
+//   warp 0      TMA producer: Q tiles once, then K and V tiles into a ring of
+//               STAGES shared-memory slots, in the order the issuer consumes
+//               them: K_0, then per step j: V_j, K_{j+1}.
+//   warp 1      tcgen05 issuer, owns the TMEM allocation. Step j, per tile t
+//               as its P arrives: O_t += P_t(j) V_j (A = P_t from TMEM), then
+//               at once S_t(j+1) = Q_t K_{j+1}^T into the same TMEM columns.
+//   warps 2-3   idle.
+//   warps 4..   one 128-thread softmax group per query tile: thread = row =
+//               TMEM lane. Reads S_t(j), computes P_t(j) and writes it as
+//               packed bf16 pairs over the first half of S_t's columns;
+//               rescales its own row of O_t when the exponent reference moves;
+//               deferred 1/l and LSE at the end.
+// The two tiles alternate on the tensor core: while one tile's softmax runs,
+// the MMAs of the other tile (its PV, then its next S) run, so the tensor and
+// vector work of the two tiles overlap (the FlashAttention-T page, section
+// "工程落地：参数、监控与未来演进", "Wavefront 调度"). Keeping P in TMEM
+// spares the shared-memory store path and the async-proxy fence a P staged in
+// shared memory needs; with O row-major each thread rescales its own row, so
+// the softmax groups need no barrier of their own.
+//
+// tcgen05.mma operations of one thread run in issue order, so S_t(j+1),
+// issued after O_t += P_t(j) V_j, overwrites P_t(j) only after that MMA has
+// read it; the S_t(j+1) commit also covers the PV, so a softmax that sees
+// S_t(j+1) may rescale O_t.
+//
+// The recurrence is the FA-3 page's (section 二): per key tile x_j,
+//   m_j = max(m_{j-1}, rowmax x_j), l_j = e^{m_{j-1}-m_j} l_{j-1} + rowsum e^{x_j-m_j},
+//   O_j = e^{m_{j-1}-m_j} O_{j-1} + e^{x_j-m_j} V_j,
+// evaluated in base 2 with log2(e) folded into the scale (x = scale*log2e*s).
+//
+// Every mbarrier wait is bounded: past `wait_limit` cycles the waiting role
+// sets a shared abort flag and a bit in the device status word, the others
+// leave at their next wait, in-flight TMA copies and MMAs are waited for
+// (again bounded), TMEM is freed and the CTA exits.
+#pragma once
+
+#include "fa_fwd_common.cuh"
+
+namespace fa {
+
+template <int D>
+struct TmCfg;
+template <>
+struct TmCfg<64> {
+    static constexpr int STAGES = 8;
+};
+template <>
+struct TmCfg<128> {
+    static constexpr int STAGES = 5;
+};
+
+template <int D>
+struct LayoutTM {
+    static constexpr int Q_TILES = 2;
+    static constexpr int BN = 128;
+    static constexpr int STAGES = TmCfg<D>::STAGES;
+    static constexpr int THREADS = (4 + 4 * Q_TILES) * 32;
+    static constexpr int CHUNKS = D / 64;  // 64-element (128-byte) column chunks
+
+    // shared memory (offsets from a 1024-aligned base)
+    static constexpr uint32_t Q_TILE_BYTES = kBM * D * 2;
+    static constexpr uint32_t SLOT_BYTES = BN * D * 2;
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t SLOT_OFF = Q_OFF + Q_TILES * Q_TILE_BYTES;
+    static constexpr uint32_t BAR_OFF = SLOT_OFF + STAGES * SLOT_BYTES;
+    static constexpr int BAR_QFULL = 0;
+    static constexpr int BAR_KVFULL = 1;
+    static constexpr int BAR_KVEMPTY = BAR_KVFULL + STAGES;
+    static constexpr int BAR_SFULL = BAR_KVEMPTY + STAGES;  // [tile] S_t(j) (and PV_t(j-1)) done
+    static constexpr int BAR_PFULL = BAR_SFULL + Q_TILES;   // [tile] P_t(j) in TMEM (128 arrivals)
+    static constexpr int BAR_OFULL = BAR_PFULL + Q_TILES;   // [tile] last PV_t finished
+    static constexpr int BAR_DRAIN = BAR_OFULL + Q_TILES;
+    static constexpr int NUM_BARS = BAR_DRAIN + 1;
+    static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] tmem base, [1] abort
+    static constexpr uint32_t BYTES = MISC_OFF + 16;
+    static constexpr size_t ALLOC_BYTES = BYTES + 1024;  // slack for 1024 alignment
+
+    // tensor memory columns (32-bit each; 512 allocated): S_t (P_t packed over
+    // its first BN/2 columns), then O_t.
+    static constexpr uint32_t TMEM_COLS = 512;
+    __host__ __device__ static constexpr uint32_t S_COL(int t) { return t * BN; }
+    __host__ __device__ static constexpr uint32_t O_COL(int t) { return 256 + t * D; }
+
+    static_assert(Q_TILES * BN <= 256, "S region overflows its half of TMEM");
+    static_assert(256 + Q_TILES * D <= 512, "O region overflows TMEM");
+    static_assert(ALLOC_BYTES <= 232448, "shared memory over the 227 KB per-CTA limit");
+    static_assert(ALLOC_BYTES > 232448 / 2, "two CTAs per SM would contend for TMEM");
+    static_assert(D % 64 == 0 && STAGES >= 3, "tile shape");
+
+    // Register split: control warpgroup 72, softmax warpgroups 216; the sum is
+    // the launch allocation (THREADS x LAUNCH_REGS), checked on the host.
+    static constexpr bool REG_SPLIT = true;
+    static constexpr int LAUNCH_REGS = 168;
+    static constexpr int CTRL_REGS = 72;
+    static constexpr int SOFTMAX_REGS = 216;
+    static_assert(128 * CTRL_REGS + 256 * SOFTMAX_REGS == THREADS * LAUNCH_REGS,
+                  "register split must equal the launch allocation");
+};
+
+template <int D>
+__global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
+    fa_fwd_tm_kernel(const __grid_constant__ FwdParams p) {
+    using L = LayoutTM<D>;
+    constexpr int QT = L::Q_TILES;
+    constexpr int BN = L::BN;
+    constexpr int ST = L::STAGES;
+
+    extern __shared__ uint8_t smem_raw[];
+    // Swizzle atoms need 1024-byte alignment in the shared window itself.
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(smem);
+    uint32_t* misc = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+    volatile uint32_t* abort_flag = misc + 1;
+    auto bar = [&](int i) -> uint32_t { return sbase + L::BAR_OFF + 8u * i; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    Work<QT> w;
+    compute_work<QT, BN>(p, w);
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::BAR_QFULL), 1);
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(bar(L::BAR_KVFULL + s), 1);
+            mbar_init(bar(L::BAR_KVEMPTY + s), 1);
+        }
+        for (int t = 0; t < QT; ++t) {
+            mbar_init(bar(L::BAR_SFULL + t), 1);
+            mbar_init(bar(L::BAR_PFULL + t), kBM);
+            mbar_init(bar(L::BAR_OFULL + t), 1);
+        }
+        mbar_init(bar(L::BAR_DRAIN), 1);
+        *abort_flag = 0u;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+    }
+    if (warp == 1) {
+        tmem_alloc(sbase + L::MISC_OFF, L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+
+    if (warp < 4) {
+      // Control warpgroup. setmaxnreg sits inside each role's branch so that
+      // the register allocator sees one limit per code path.
+      if constexpr (L::REG_SPLIT) setmaxnreg_dec<L::CTRL_REGS>();
+      if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        // The whole warp runs the loop (uniform values); one elected lane issues.
+        if (w.nmax > 0) {
+            const bool leader = elect_one();
+            int nvalid = 0;
+#pragma unroll
+            for (int t = 0; t < QT; ++t) nvalid += (w.n[t] > 0) ? 1 : 0;
+            // (The failure-detection test hook withholds the Q tiles so that the
+            // issuer's bounded wait runs out; nothing else changes.)
+            if (leader && !p.test_withhold_q) mbar_arrive_expect_tx(bar(L::BAR_QFULL), nvalid * L::Q_TILE_BYTES);
+#pragma unroll
+            for (int t = 0; t < QT; ++t) {
+                if (leader && w.n[t] > 0 && !p.test_withhold_q) {
+#pragma unroll
+                    for (int c = 0; c < L::CHUNKS; ++c)
+                        tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128),
+                                    &p.tm_q, bar(L::BAR_QFULL), 64 * c, w.q0 + t * kBM, w.bh);
+                }
+            }
+            // Entry e of the sequence: K_0; then for step j: V_j, K_{j+1} (if any).
+            const int total = 2 * w.nmax;
+            RingPos<ST> pos;
+            int issued = 0;
+            bool ok = true;
+            for (int e = 0; e < total; ++e) {
+                const bool is_v = (e & 1) != 0;  // K_j at e = 2j, V_j at e = 2j + 1
+                const int kv = e >> 1;
+                if (e >= ST) {
+                    ok = wait_phase(bar(L::BAR_KVEMPTY + pos.slot), pos.phase ^ 1u, p, abort_flag,
+                                    kStatusWaitKvEmpty);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                }
+                if (leader) {
+                    mbar_arrive_expect_tx(bar(L::BAR_KVFULL + pos.slot), L::SLOT_BYTES);
+                    const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
+                    const int row = (w.kv_tile0 + kv) * BN;
+#pragma unroll
+                    for (int c = 0; c < L::CHUNKS; ++c)
+                        tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
+                                    bar(L::BAR_KVFULL + pos.slot), 64 * c, row, w.bh);
+                }
+                issued = e + 1;
+                pos.advance();
+            }
+            if (ok) {
+                // Producer tail: wait until the issuer has released the last use
+                // of every slot, so no tcgen05.commit arrival is still in flight
+                // towards this CTA's shared memory when it exits.
+                for (int e = max(0, total - ST); e < total && ok; ++e) {
+                    ok = wait_phase(bar(L::BAR_KVEMPTY + e % ST), (e / ST) & 1, p, abort_flag,
+                                    kStatusWaitKvEmpty);
+                    ok = __all_sync(0xffffffffu, ok);
+                }
+            }
+            if (!ok) {
+                // Let every copy already issued land before the CTA goes away.
+                wait_phase(bar(L::BAR_QFULL), 0, p, abort_flag, kStatusWaitDrain, false);
+                for (int e = max(0, issued - ST); e < issued; ++e)
+                    wait_phase(bar(L::BAR_KVFULL + e % ST), (e / ST) & 1, p, abort_flag,
+                               kStatusWaitDrain, false);
+            }
+        }
+      } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        // The whole warp runs the loop, so descriptors and TMEM addresses stay in
+        // warp-uniform registers; one elected lane issues each tcgen05 op.
+        if (w.nmax > 0) {
+            const bool leader = elect_one();
+            auto wait_all = [&](uint32_t b, uint32_t parity, unsigned what) {
+                return __all_sync(0xffffffffu, wait_phase(b, parity, p, abort_flag, what));
+            };
+            constexpr uint32_t IDESC_S = make_idesc_bf16(kBM, BN, false, false);
+            constexpr uint32_t IDESC_O = make_idesc_bf16(kBM, D, false, true);
+            // Descriptors are built once; an operand at byte offset `off` from a
+            // base adds off >> 4 to the low word (the 14-bit start field never
+            // carries: shared addresses stay below 2^18).
+            const uint64_t kmaj0 = make_sdesc_sw128(sbase, 16, 1024);          // Q, K: K-major
+            const uint64_t vmn0 = make_sdesc_sw128(sbase, BN * 128, 1024);     // V: MN-major
+            const uint32_t kmaj_lo = static_cast<uint32_t>(kmaj0);
+            const uint32_t kmaj_hi = static_cast<uint32_t>(kmaj0 >> 32);
+            const uint32_t vmn_lo = static_cast<uint32_t>(vmn0);
+            const uint32_t vmn_hi = static_cast<uint32_t>(vmn0 >> 32);
+            auto desc = [](uint32_t lo, uint32_t hi, uint32_t off) -> uint64_t {
+                return (static_cast<uint64_t>(hi) << 32) | (lo + (off >> 4));
+            };
+            auto issue_s = [&](int t, int slot) {
+                const uint32_t qa = L::Q_OFF + t * L::Q_TILE_BYTES;
+                const uint32_t kb = L::SLOT_OFF + slot * L::SLOT_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t in_row = (kk & 3) * 32;  // 16 bf16 = 32 bytes of a 128-byte row
+                    if (leader)
+                        umma_ss(tmem + L::S_COL(t), desc(kmaj_lo, kmaj_hi, qa + (kk >> 2) * (kBM * 128) + in_row),
+                                desc(kmaj_lo, kmaj_hi, kb + (kk >> 2) * (BN * 128) + in_row), IDESC_S,
+                                kk > 0 ? 1u : 0u);
+                }
+            };
+            // O_t += P_t V: A = P_t packed two bf16 per TMEM column (16 keys = 8
+            // columns), B = V MN-major (16 keys = two 8-row swizzle atoms,
+            // 2048 bytes; 64-column chunks of d BN*128 bytes apart).
+            auto issue_pv = [&](int t, int slot, bool accumulate) {
+                const uint32_t vb = L::SLOT_OFF + slot * L::SLOT_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk)
+                    if (leader)
+                        umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8,
+                                desc(vmn_lo, vmn_hi, vb + kk * 2048), IDESC_O,
+                                (accumulate || kk > 0) ? 1u : 0u);
+            };
+
+            RingPos<ST> pos;
+            bool ok = wait_all(bar(L::BAR_QFULL), 0, kStatusWaitQ);
+            if (ok) ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll
+                for (int t = 0; t < QT; ++t) {
+                    if (w.n[t] > 0) {
+                        issue_s(t, pos.slot);
+                        if (leader) umma_commit(bar(L::BAR_SFULL + t));
+                    }
+                }
+                if (leader) umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
+                pos.advance();
+            }
+            for (int j = 0; j < w.nmax && ok; ++j) {
+                const int slot_v = pos.slot;
+                ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
+                if (!ok) break;
+                pos.advance();
+                const bool k_next = (j + 1 < w.nmax);
+                const int slot_k = pos.slot;
+                if (k_next) {
+                    ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
+                    if (!ok) break;
+                    pos.advance();
+                }
+#pragma unroll
+                for (int t = 0; t < QT; ++t) {
+                    if (ok && j < w.n[t]) {
+                        ok = wait_all(bar(L::BAR_PFULL + t), j & 1, kStatusWaitP);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(t, slot_v, j > 0);
+                        if (j + 1 < w.n[t]) {
+                            issue_s(t, slot_k);
+                            if (leader) umma_commit(bar(L::BAR_SFULL + t));
+                        } else {
+                            if (leader) umma_commit(bar(L::BAR_OFULL + t));
+                        }
+                    }
+                }
+                if (!ok) break;
+                if (leader) umma_commit(bar(L::BAR_KVEMPTY + slot_v));
+                if (k_next && leader) umma_commit(bar(L::BAR_KVEMPTY + slot_k));
+            }
+            // Always wait for every MMA this thread issued before the CTA can
+            // reach its teardown: on an abort no softmax waits for O_full, and
+            // TMEM must not be released under an MMA in flight.
+            if (leader) umma_commit(bar(L::BAR_DRAIN));
+            wait_phase(bar(L::BAR_DRAIN), 0, p, abort_flag, kStatusWaitDrain, false);
+        }
+      }
+    } else {
+        // ------------------------------------------------------------ softmax
+        if constexpr (L::REG_SPLIT) setmaxnreg_inc<L::SOFTMAX_REGS>();
+        const int t = (warp - 4) >> 2;
+        const int quarter = warp & 3;  // TMEM lane quarter this warp may access
+        const int r = quarter * 32 + lane;
+        const int q_row = w.q0 + t * kBM + r;
+        const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tS = tmem + lane_field + L::S_COL(t);
+        const uint32_t tO = tmem + lane_field + L::O_COL(t);
+        const float sl2 = p.scale_log2;
+        int n = w.n[0];
+#pragma unroll
+        for (int i = 1; i < QT; ++i)
+            if (t == i) n = w.n[i];
+
+        float m = -INFINITY;       // exponent reference (base-2 units of scale*log2e*s)
+        float m_true = -INFINITY;  // true running row max, same units
+        float l = 0.f;             // running sum relative to m
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            ok = wait_phase(bar(L::BAR_SFULL + t), j & 1, p, abort_flag, kStatusWaitS);
+            // tcgen05.ld/st are warp-collective: the whole warp leaves together.
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+
+            float s[BN];
+#pragma unroll
+            for (int cc = 0; cc < BN / 32; ++cc) {
+                uint32_t raw[32];
+                tmem_ld32(tS + cc * 32, raw);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(raw[i]);
+            }
+            tmem_wait_ld();
+
+            // Mask: keys past the split / sequence end, and (causal) keys after
+            // this row. TMA zero-fills keys >= Nk, so they must become -inf.
+            const int kv0 = (w.kv_tile0 + j) * BN;
+            int valid = w.kv_end - kv0;
+            if (p.causal) valid = min(valid, q_row - kv0 + 1);
+            if (valid < BN) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c)
+                    if (c >= valid) s[c] = -INFINITY;
+            }
+            __syncwarp();
+
+            // Row max: four independent three-input max chains.
+            float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < BN; c += 8) {
+                a0 = max3f(a0, s[c + 0], s[c + 1]);
+                a1 = max3f(a1, s[c + 2], s[c + 3]);
+                a2 = max3f(a2, s[c + 4], s[c + 5]);
+                a3 = max3f(a3, s[c + 6], s[c + 7]);
+            }
+            const float m_tile = max3f(a0, a1, fmaxf(a2, a3)) * sl2;  // base-2 units
+            m_true = fmaxf(m_true, m_tile);
+            // The exponent reference m only moves when this tile's max exceeds it
+            // by more than kRescaleSlack; otherwise every p = 2^(x - m) <= 2^slack
+            // and the old reference is kept, so O and l need no rescale. The
+            // result is the same: O/l and m + log2(l) do not depend on which
+            // reference is used, only rounding does.
+            const bool move = m_tile > m + kRescaleSlack;
+            const float m_new = move ? m_tile : m;
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // all masked so far
+            const float alpha = move ? ex2(m - m_use) : 1.f;
+            const float neg = -m_use;
+
+            // x = s*scale*log2e - m as packed fp32 pairs (one FFMA2 per two keys),
+            // p = 2^x on the MUFU, row sums as four packed partial pairs; P goes
+            // over S_t's first BN/2 columns as packed bf16 pairs, 32 columns
+            // (64 keys) at a time.
+            const uint64_t sl2x2 = f2pack(sl2, sl2);
+            const uint64_t negx2 = f2pack(neg, neg);
+            uint64_t part2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+            for (int h = 0; h < BN / 64; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int c = h * 64 + 2 * i;
+                    float x0, x1;
+                    f2unpack(ffma2(f2pack(s[c], s[c + 1]), sl2x2, negx2), x0, x1);
+                    const float e0 = ex2(x0);
+                    const float e1 = ex2(x1);
+                    part2[i & 3] = fadd2(part2[i & 3], f2pack(e0, e1));
+                    pk[i] = pack_bf16x2(e0, e1);
+                }
+                tmem_st32(tS + h * 32, pk);
+            }
+
+            // O_t(j-1) is complete (the S_t(j) commit covers PV_t(j-1)); rescale
+            // the rows whose reference moved. tcgen05.ld/st are warp-collective,
+            // so the warp takes this branch together (alpha = 1 rows multiply by 1).
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                const uint64_t ax2 = f2pack(alpha, alpha);
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + cc * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float x0, x1;
+                        f2unpack(fmul2(f2pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), ax2),
+                                 x0, x1);
+                        o[2 * i] = __float_as_uint(x0);
+                        o[2 * i + 1] = __float_as_uint(x1);
+                    }
+                    tmem_st32(tO + cc * 32, o);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(L::BAR_PFULL + t));
+
+            float part[8];
+            f2unpack(part2[0], part[0], part[1]);
+            f2unpack(part2[1], part[2], part[3]);
+            f2unpack(part2[2], part[4], part[5]);
+            f2unpack(part2[3], part[6], part[7]);
+            const float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
+                              ((part[4] + part[5]) + (part[6] + part[7]));
+            l = l * alpha + sum;
+            m = m_new;
+        }
+
+        if (ok && n > 0) {
+            ok = wait_phase(bar(L::BAR_OFULL + t), 0, p, abort_flag, kStatusWaitO);
+            ok = __all_sync(0xffffffffu, ok);
+            if (ok) tc_fence_after();
+        }
+        if (ok) write_row<D>(p, w.bh, w.split, q_row, n, m, m_true, l, tO);
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
+}  // namespace fa

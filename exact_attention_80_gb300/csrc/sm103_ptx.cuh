@@ -60,22 +60,17 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-// Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(int id, int count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-// Named barrier that also ORs a predicate over the participating threads.
-__device__ __forceinline__ bool named_bar_or(int id, int count, bool pred) {
-    uint32_t r;
+// One lane of a converged warp (the lowest active lane): the warp runs a loop
+// with uniform values and only the elected lane issues tcgen05 / TMA work, so
+// the operands stay in warp-uniform registers.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
     asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %3, 0;\n\t"
-        "bar.red.or.pred q, %1, %2, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}"
-        : "=r"(r)
-        : "r"(id), "r"(count), "r"(pred ? 1u : 0u)
-        : "memory");
-    return r != 0;
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
 }
 
 // ---------------------------------------------------------------- TMA
