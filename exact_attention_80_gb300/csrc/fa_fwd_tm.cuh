@@ -43,15 +43,17 @@
 
 namespace fa {
 
+// Per head dim: K/V ring depth and the setmaxnreg split (control warpgroup /
+// softmax warpgroups), each the spill-free choice for that instantiation.
 template <int D>
 struct TmCfg;
 template <>
 struct TmCfg<64> {
-    static constexpr int STAGES = 8;
+    static constexpr int STAGES = 8, CTRL_REGS = 72, SOFTMAX_REGS = 216;
 };
 template <>
 struct TmCfg<128> {
-    static constexpr int STAGES = 5;
+    static constexpr int STAGES = 5, CTRL_REGS = 88, SOFTMAX_REGS = 208;
 };
 
 template <int D>
@@ -92,12 +94,12 @@ struct LayoutTM {
     static_assert(ALLOC_BYTES > 232448 / 2, "two CTAs per SM would contend for TMEM");
     static_assert(D % 64 == 0 && STAGES >= 3, "tile shape");
 
-    // Register split: control warpgroup 72, softmax warpgroups 216; the sum is
-    // the launch allocation (THREADS x LAUNCH_REGS), checked on the host.
+    // Register split: the sum is the launch allocation (THREADS x LAUNCH_REGS),
+    // checked on the host.
     static constexpr bool REG_SPLIT = true;
     static constexpr int LAUNCH_REGS = 168;
-    static constexpr int CTRL_REGS = 72;
-    static constexpr int SOFTMAX_REGS = 216;
+    static constexpr int CTRL_REGS = TmCfg<D>::CTRL_REGS;
+    static constexpr int SOFTMAX_REGS = TmCfg<D>::SOFTMAX_REGS;
     static_assert(128 * CTRL_REGS + 256 * SOFTMAX_REGS == THREADS * LAUNCH_REGS,
                   "register split must equal the launch allocation");
 };
@@ -269,7 +271,20 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
                                 (accumulate || kk > 0) ? 1u : 0u);
             };
 
+            // K/V entries in consumption order: K_0, then per step j: V_j, K_{j+1}.
             RingPos<ST> pos;
+            int slot_v = 0, slot_k = 0;  // slots of V_j and K_{j+1} for the current step
+            auto wait_kv = [&](int j) -> bool {  // V_j, then K_{j+1} if any step needs it
+                slot_v = pos.slot;
+                if (!wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull)) return false;
+                pos.advance();
+                if (j + 1 < w.nmax) {
+                    slot_k = pos.slot;
+                    if (!wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull)) return false;
+                    pos.advance();
+                }
+                return true;
+            };
             bool ok = wait_all(bar(L::BAR_QFULL), 0, kStatusWaitQ);
             if (ok) ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
             if (ok) {
@@ -283,37 +298,55 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
                 }
                 if (leader) umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
                 pos.advance();
+                ok = wait_kv(0);
             }
+            // Per step: tile 0's PV and next S; tile 1's PV; tile 1's next S. The
+            // next step's K/V waits go where the MMA queue holds the most work:
+            // between tile 1's PV and S for d = 128 (PV of N = 128), after tile
+            // 0's batch for d = 64 (a shorter PV). Each group of waits and
+            // commits then sits behind queued MMAs, so the tensor core does not
+            // idle while the issuing thread synchronises.
+            constexpr bool kKvWaitMid1 = (D >= 128);
             for (int j = 0; j < w.nmax && ok; ++j) {
-                const int slot_v = pos.slot;
-                ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
-                if (!ok) break;
-                pos.advance();
+                const int sv = slot_v, sk = slot_k;
                 const bool k_next = (j + 1 < w.nmax);
-                const int slot_k = pos.slot;
-                if (k_next) {
-                    ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
+                if (j < w.n[0]) {
+                    ok = wait_all(bar(L::BAR_PFULL + 0), j & 1, kStatusWaitP);
                     if (!ok) break;
-                    pos.advance();
-                }
-#pragma unroll
-                for (int t = 0; t < QT; ++t) {
-                    if (ok && j < w.n[t]) {
-                        ok = wait_all(bar(L::BAR_PFULL + t), j & 1, kStatusWaitP);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(t, slot_v, j > 0);
-                        if (j + 1 < w.n[t]) {
-                            issue_s(t, slot_k);
-                            if (leader) umma_commit(bar(L::BAR_SFULL + t));
-                        } else {
-                            if (leader) umma_commit(bar(L::BAR_OFULL + t));
-                        }
+                    tc_fence_after();
+                    issue_pv(0, sv, j > 0);
+                    if (j + 1 < w.n[0]) {
+                        issue_s(0, sk);
+                        if (leader) umma_commit(bar(L::BAR_SFULL + 0));
+                    } else {
+                        if (leader) umma_commit(bar(L::BAR_OFULL + 0));
                     }
                 }
-                if (!ok) break;
-                if (leader) umma_commit(bar(L::BAR_KVEMPTY + slot_v));
-                if (k_next && leader) umma_commit(bar(L::BAR_KVEMPTY + slot_k));
+                if (!kKvWaitMid1 && k_next) {
+                    ok = wait_kv(j + 1);
+                    if (!ok) break;
+                }
+                const bool act1 = j < w.n[1];
+                if (act1) {
+                    ok = wait_all(bar(L::BAR_PFULL + 1), j & 1, kStatusWaitP);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(1, sv, j > 0);
+                }
+                if (leader) umma_commit(bar(L::BAR_KVEMPTY + sv));  // V_j: both PVs issued
+                if (kKvWaitMid1 && k_next) {
+                    ok = wait_kv(j + 1);
+                    if (!ok) break;
+                }
+                if (act1) {
+                    if (j + 1 < w.n[1]) {
+                        issue_s(1, sk);
+                        if (leader) umma_commit(bar(L::BAR_SFULL + 1));
+                    } else {
+                        if (leader) umma_commit(bar(L::BAR_OFULL + 1));
+                    }
+                }
+                if (k_next && leader) umma_commit(bar(L::BAR_KVEMPTY + sk));  // K_{j+1}: both Ss issued
             }
             // Always wait for every MMA this thread issued before the CTA can
             // reach its teardown: on an abort no softmax waits for O_full, and
