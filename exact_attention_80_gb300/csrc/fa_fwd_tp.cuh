@@ -6,7 +6,8 @@
 //   warp 0      TMA producer: Q tiles once, then K and V tiles into a ring of
 //               STAGES shared-memory slots (full/empty mbarriers), in the order
 //               the issuer consumes them: K_0, then per step j: K_{j+1}, V_j.
-//   warp 1      tcgen05 issuer (one thread), owns the TMEM allocation. Step j:
+//   warp 1      tcgen05 issuer (a warp-uniform loop, one elected lane
+//               issues), owns the TMEM allocation. Step j:
 //               S_t(j+1) = Q_t K_{j+1}^T for every tile, then O_t += P_t(j) V_j
 //               as each tile's P arrives. S is double-buffered per tile in
 //               TMEM, so the next S is computed while the softmax works on
@@ -167,16 +168,18 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
       if constexpr (L::REG_SPLIT) setmaxnreg_dec<L::CTRL_REGS>();
       if (warp == 0) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && w.nmax > 0) {
+        // The whole warp runs the loop (uniform values); one elected lane issues.
+        if (w.nmax > 0) {
+            const bool leader = elect_one();
             int nvalid = 0;
 #pragma unroll
             for (int t = 0; t < QT; ++t) nvalid += (w.n[t] > 0) ? 1 : 0;
             // (The failure-detection test hook withholds the Q tiles so that the
             // issuer's bounded wait runs out; nothing else changes.)
-            if (!p.test_withhold_q) mbar_arrive_expect_tx(bar(L::BAR_QFULL), nvalid * L::Q_TILE_BYTES);
+            if (leader && !p.test_withhold_q) mbar_arrive_expect_tx(bar(L::BAR_QFULL), nvalid * L::Q_TILE_BYTES);
 #pragma unroll
             for (int t = 0; t < QT; ++t) {
-                if (w.n[t] > 0 && !p.test_withhold_q) {
+                if (leader && w.n[t] > 0 && !p.test_withhold_q) {
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128),
@@ -204,15 +207,18 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
                 if (e >= ST) {
                     ok = wait_phase(bar(L::BAR_KVEMPTY + pos.slot), pos.phase ^ 1u, p, abort_flag,
                                     kStatusWaitKvEmpty);
+                    ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                 }
-                mbar_arrive_expect_tx(bar(L::BAR_KVFULL + pos.slot), L::SLOT_BYTES);
-                const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
-                const int row = (w.kv_tile0 + tile) * BN;
+                if (leader) {
+                    mbar_arrive_expect_tx(bar(L::BAR_KVFULL + pos.slot), L::SLOT_BYTES);
+                    const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
+                    const int row = (w.kv_tile0 + tile) * BN;
 #pragma unroll
-                for (int c = 0; c < L::CHUNKS; ++c)
-                    tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
-                                bar(L::BAR_KVFULL + pos.slot), 64 * c, row, w.bh);
+                    for (int c = 0; c < L::CHUNKS; ++c)
+                        tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
+                                    bar(L::BAR_KVFULL + pos.slot), 64 * c, row, w.bh);
+                }
                 issued = e + 1;
                 pos.advance();
             }
@@ -220,9 +226,11 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
                 // Producer tail: wait until the issuer has released the last use
                 // of every slot, so no tcgen05.commit arrival is still in flight
                 // towards this CTA's shared memory when it exits.
-                for (int e = max(0, total - ST); e < total && ok; ++e)
+                for (int e = max(0, total - ST); e < total && ok; ++e) {
                     ok = wait_phase(bar(L::BAR_KVEMPTY + e % ST), (e / ST) & 1, p, abort_flag,
                                     kStatusWaitKvEmpty);
+                    ok = __all_sync(0xffffffffu, ok);
+                }
             }
             if (!ok) {
                 // Let every copy already issued land before the CTA goes away.
@@ -234,7 +242,13 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
         }
       } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && w.nmax > 0) {
+        // The whole warp runs the loop, so descriptors and TMEM addresses stay in
+        // warp-uniform registers; one elected lane issues each tcgen05 op.
+        if (w.nmax > 0) {
+            const bool leader = elect_one();
+            auto wait_all = [&](uint32_t b, uint32_t parity, unsigned what) {
+                return __all_sync(0xffffffffu, wait_phase(b, parity, p, abort_flag, what));
+            };
             constexpr uint32_t IDESC_S = make_idesc_bf16(kBM, BN, false, false);
             constexpr uint32_t IDESC_O = make_idesc_bf16(kBM, D, false, true);
             auto issue_s = [&](int t, int b, int slot) {
@@ -245,7 +259,7 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
                     const uint32_t in_row = (kk & 3) * 32;  // 16 bf16 = 32 bytes of a 128-byte row
                     const uint64_t a = make_sdesc_sw128(qa + (kk >> 2) * (kBM * 128) + in_row, 16, 1024);
                     const uint64_t bd = make_sdesc_sw128(kb + (kk >> 2) * (BN * 128) + in_row, 16, 1024);
-                    umma_ss(tmem + L::S_COL(t, b), a, bd, IDESC_S, kk > 0 ? 1u : 0u);
+                    if (leader) umma_ss(tmem + L::S_COL(t, b), a, bd, IDESC_S, kk > 0 ? 1u : 0u);
                 }
             };
             auto issue_pv = [&](int t, int b, int slot, bool accumulate) {
@@ -255,33 +269,32 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
                     // V is MN-major: 16 keys = two 8-row swizzle atoms (2048 bytes);
                     // 64-column chunks of d are BN*128 bytes apart.
                     const uint64_t bd = make_sdesc_sw128(vb + kk * 2048, BN * 128, 1024);
-                    umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t, b) + kk * 8, bd, IDESC_O,
-                            (accumulate || kk > 0) ? 1u : 0u);
+                    if (leader)
+                        umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t, b) + kk * 8, bd, IDESC_O,
+                                (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
 
             RingPos<ST> pos;
-            bool ok = wait_phase(bar(L::BAR_QFULL), 0, p, abort_flag, kStatusWaitQ);
-            if (ok) ok = wait_phase(bar(L::BAR_KVFULL + pos.slot), pos.phase, p, abort_flag,
-                                    kStatusWaitKvFull);
+            bool ok = wait_all(bar(L::BAR_QFULL), 0, kStatusWaitQ);
+            if (ok) ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
             if (ok) {
                 tc_fence_after();
 #pragma unroll
                 for (int t = 0; t < QT; ++t) {
                     if (w.n[t] > 0) {
                         issue_s(t, 0, pos.slot);
-                        umma_commit(bar(L::BAR_SFULL + 2 * t + 0));
+                        if (leader) umma_commit(bar(L::BAR_SFULL + 2 * t + 0));
                     }
                 }
-                umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
+                if (leader) umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
                 pos.advance();
             }
             for (int j = 0; j < w.nmax && ok; ++j) {
                 // S_t(j+1) into the other S buffer. It overwrites P_t(j-1),
                 // whose PV was issued in the previous step (MMAs run in order).
                 if (j + 1 < w.nmax) {
-                    ok = wait_phase(bar(L::BAR_KVFULL + pos.slot), pos.phase, p, abort_flag,
-                                    kStatusWaitKvFull);
+                    ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
                     if (!ok) break;
                     tc_fence_after();
                     const int b = (j + 1) & 1;
@@ -289,36 +302,34 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
                     for (int t = 0; t < QT; ++t) {
                         if (j + 1 < w.n[t]) {
                             issue_s(t, b, pos.slot);
-                            umma_commit(bar(L::BAR_SFULL + 2 * t + b));
+                            if (leader) umma_commit(bar(L::BAR_SFULL + 2 * t + b));
                         }
                     }
-                    umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
+                    if (leader) umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
                     pos.advance();
                 }
                 // O_t += P_t(j) V_j as each tile's P arrives.
-                ok = wait_phase(bar(L::BAR_KVFULL + pos.slot), pos.phase, p, abort_flag,
-                                kStatusWaitKvFull);
+                ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
                 if (!ok) break;
 #pragma unroll
                 for (int t = 0; t < QT; ++t) {
                     if (ok && j < w.n[t]) {
-                        ok = wait_phase(bar(L::BAR_PFULL + 2 * t + (j & 1)), (j >> 1) & 1, p,
-                                        abort_flag, kStatusWaitP);
+                        ok = wait_all(bar(L::BAR_PFULL + 2 * t + (j & 1)), (j >> 1) & 1, kStatusWaitP);
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(t, j & 1, pos.slot, j > 0);
-                        umma_commit(bar(L::BAR_PVDONE + t));
-                        if (j + 1 == w.n[t]) umma_commit(bar(L::BAR_OFULL + t));
+                        if (leader) umma_commit(bar(L::BAR_PVDONE + t));
+                        if (leader && j + 1 == w.n[t]) umma_commit(bar(L::BAR_OFULL + t));
                     }
                 }
                 if (!ok) break;
-                umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
+                if (leader) umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
                 pos.advance();
             }
             // Always wait for every MMA this thread issued before the CTA can
             // reach its teardown: on an abort no softmax waits for O_full, and
             // TMEM must not be released under an MMA in flight.
-            umma_commit(bar(L::BAR_DRAIN));
+            if (leader) umma_commit(bar(L::BAR_DRAIN));
             wait_phase(bar(L::BAR_DRAIN), 0, p, abort_flag, kStatusWaitDrain, false);
         }
       }
