@@ -74,7 +74,7 @@ struct LayoutTM {
     static constexpr int BAR_KVFULL = 1;
     static constexpr int BAR_KVEMPTY = BAR_KVFULL + STAGES;
     static constexpr int BAR_SFULL = BAR_KVEMPTY + STAGES;  // [tile] S_t(j) (and PV_t(j-1)) done
-    static constexpr int BAR_PFULL = BAR_SFULL + Q_TILES;   // [tile] P_t(j) in TMEM (128 arrivals)
+    static constexpr int BAR_PFULL = BAR_SFULL + Q_TILES;   // [tile] P_t(j) in TMEM (one arrival per warp)
     static constexpr int BAR_OFULL = BAR_PFULL + Q_TILES;   // [tile] last PV_t finished
     static constexpr int BAR_DRAIN = BAR_OFULL + Q_TILES;
     static constexpr int NUM_BARS = BAR_DRAIN + 1;
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
         }
         for (int t = 0; t < QT; ++t) {
             mbar_init(bar(L::BAR_SFULL + t), 1);
-            mbar_init(bar(L::BAR_PFULL + t), kBM);
+            mbar_init(bar(L::BAR_PFULL + t), 4);  // one arrival per warp of the group
             mbar_init(bar(L::BAR_OFULL + t), 1);
         }
         mbar_init(bar(L::BAR_DRAIN), 1);
@@ -333,7 +333,6 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
                     tc_fence_after();
                     issue_pv(1, sv, j > 0);
                 }
-                if (leader) umma_commit(bar(L::BAR_KVEMPTY + sv));  // V_j: both PVs issued
                 if (kKvWaitMid1 && k_next) {
                     ok = wait_kv(j + 1);
                     if (!ok) break;
@@ -346,7 +345,10 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
                         if (leader) umma_commit(bar(L::BAR_OFULL + 1));
                     }
                 }
-                if (k_next && leader) umma_commit(bar(L::BAR_KVEMPTY + sk));  // K_{j+1}: both Ss issued
+                // V_j and K_{j+1} are released together after the step's last MMA,
+                // so no commit sits between tile 1's PV and the next K/V waits.
+                if (leader) umma_commit(bar(L::BAR_KVEMPTY + sv));
+                if (k_next && leader) umma_commit(bar(L::BAR_KVEMPTY + sk));
             }
             // Always wait for every MMA this thread issued before the CTA can
             // reach its teardown: on an abort no softmax waits for O_full, and
@@ -472,7 +474,8 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(L::BAR_PFULL + t));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::BAR_PFULL + t));
 
             float part[8];
             f2unpack(part2[0], part[0], part[1]);
