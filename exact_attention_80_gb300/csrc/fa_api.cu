@@ -141,6 +141,7 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
         !encode_rows_map(&p.tm_k, k, d, Nk, BH, c.bn) ||
         !encode_rows_map(&p.tm_v, v, d, Nk, BH, c.bn))
         return FA_ERR_CUDA;
+    if (!split_mode && !encode_rows_map(&p.tm_o, o, d, Nq, BH, 128)) return FA_ERR_CUDA;
     p.o = o;
     p.lse = lse;
     if (split_mode) {

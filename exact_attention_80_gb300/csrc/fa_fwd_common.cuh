@@ -40,14 +40,15 @@ struct Work {
     int nmax;
 };
 
+// Unit `lin` (blockIdx.x for a one-unit CTA; a persistent CTA walks lin =
+// blockIdx.x + k * gridDim.x).
 template <int QT, int BN>
-__device__ __forceinline__ void compute_work(const FwdParams& p, Work<QT>& w) {
+__device__ __forceinline__ void compute_work(const FwdParams& p, long long lin, Work<QT>& w) {
     // CTA order: key splits fastest; then heads in groups of p.head_group
     // (sized so one group is about one wave of CTAs), and within a group the
     // query units heaviest first (last rows first under a causal mask) across
     // the group's heads. CTAs running together share a few heads' K/V in L2,
     // and long causal units start before short ones.
-    long long lin = blockIdx.x;
     w.split = static_cast<int>(lin % p.num_splits);
     lin /= p.num_splits;
     const long long per_group = static_cast<long long>(p.head_group) * p.n_units;
@@ -98,83 +99,92 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
     }
 }
 
-// Writes one query row's result from its TMEM accumulator row (lane address
-// tO, D fp32 columns; ignored when n == 0): normalised O (bf16) and LSE in
-// plain mode, or the unnormalised partial state (O, m, l) in split mode.
-// Deferred normalisation: one division per row, at the write.
+// One query row's output, written 32 fp32 columns at a time from the final
+// accumulator row: normalised O (bf16) and LSE in plain mode, or the
+// unnormalised partial state (O, m, l) in split mode. Deferred normalisation:
+// one division per row, at the write.
 template <int D>
-__device__ __forceinline__ void write_row(const FwdParams& p, int bh, int split, int q_row, int n,
-                                          float m, float m_true, float l, uint32_t tO) {
-    const bool row_ok = q_row < p.Nq;
-    const size_t row_idx = static_cast<size_t>(bh) * p.Nq + q_row;
-    if (!p.split_mode) {
-        // Deferred normalisation: one division per row, at the write.
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + row_idx * D;
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            if (n > 0) {
-                tmem_ld32(tO + cc * 32, o);
-                tmem_wait_ld();
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = 0u;
-            }
+struct RowOut {
+    bool row_ok;
+    bool split;
+    float f;  // plain: 1/l; split: move from the lazy reference m to m_true
+    size_t row_idx, part_idx;
+    float m, m_true, l;
+
+    __device__ __forceinline__ RowOut(const FwdParams& p, int bh, int split_idx, int q_row, float m_,
+                                      float m_true_, float l_)
+        : row_ok(q_row < p.Nq), split(p.split_mode != 0), m(m_), m_true(m_true_), l(l_) {
+        row_idx = static_cast<size_t>(bh) * p.Nq + q_row;
+        part_idx = (static_cast<size_t>(split_idx) * p.BH + bh) * p.Nq + q_row;
+        if (!split) f = (l > 0.f) ? 1.f / l : 0.f;
+        else f = (l > 0.f && m != m_true) ? ex2(m - m_true) : 1.f;
+    }
+    // Columns [32 cc, 32 cc + 32) of the row, fp32 bits (zero when the row saw
+    // no key); `o` is scaled in place.
+    __device__ __forceinline__ void chunk(const FwdParams& p, int cc, uint32_t (&o)[32]) const {
+        if (!split) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i)
-                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l,
-                                    __uint_as_float(o[2 * i + 1]) * inv_l);
+                pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * f, __uint_as_float(o[2 * i + 1]) * f);
             if (row_ok) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + row_idx * D + cc * 32);
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
             }
-        }
-        if (row_ok)
-            p.lse[row_idx] = (l > 0.f) ? (m + lg2(l)) * 0.69314718055994530942f : -INFINITY;
-    } else {
-        const size_t part_idx =
-            (static_cast<size_t>(split) * p.BH + bh) * p.Nq + q_row;
-        float* orow = p.ws_o + part_idx * D;
-        // Partial states are stated relative to the split's true row max:
-        // move l and O from the lazy reference m to m_true.
-        const float rebase = (l > 0.f && m != m_true) ? ex2(m - m_true) : 1.f;
-        const uint64_t rb2 = f2pack(rebase, rebase);
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-            uint32_t o[32];
-            if (n > 0) {
-                tmem_ld32(tO + cc * 32, o);
-                tmem_wait_ld();
-            } else {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] = 0u;
-            }
-            if (rebase != 1.f) {
+        } else {
+            if (f != 1.f) {
+                const uint64_t f2 = f2pack(f, f);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float x0, x1;
-                    f2unpack(fmul2(f2pack(__uint_as_float(o[2 * i]),
-                                          __uint_as_float(o[2 * i + 1])), rb2), x0, x1);
+                    f2unpack(fmul2(f2pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), f2),
+                             x0, x1);
                     o[2 * i] = __float_as_uint(x0);
                     o[2 * i + 1] = __float_as_uint(x1);
                 }
             }
             if (row_ok) {
-                uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+                uint4* dst = reinterpret_cast<uint4*>(p.ws_o + part_idx * D + cc * 32);
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
                     dst[i] = make_uint4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
             }
         }
-        if (row_ok) {
-            p.ws_m[part_idx] = (l > 0.f) ? m_true * 0.69314718055994530942f : -INFINITY;
-            p.ws_l[part_idx] = l * rebase;
+    }
+    // The row's scalars: LSE (plain) or the partial m, l (split).
+    __device__ __forceinline__ void finish(const FwdParams& p) const {
+        if (!row_ok) return;
+        constexpr float kLn2 = 0.69314718055994530942f;
+        if (!split) {
+            p.lse[row_idx] = (l > 0.f) ? (m + lg2(l)) * kLn2 : -INFINITY;
+        } else {
+            p.ws_m[part_idx] = (l > 0.f) ? m_true * kLn2 : -INFINITY;
+            p.ws_l[part_idx] = l * f;
         }
     }
+};
+
+// Writes one query row's result from its TMEM accumulator row (lane address
+// tO, D fp32 columns; not read when n == 0), a chunk at a time.
+template <int D>
+__device__ __forceinline__ void write_row(const FwdParams& p, int bh, int split, int q_row, int n,
+                                          float m, float m_true, float l, uint32_t tO) {
+    const RowOut<D> out(p, bh, split, q_row, m, m_true, l);
+#pragma unroll 1
+    for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        if (n > 0) {
+            tmem_ld32(tO + cc * 32, o);
+            tmem_wait_ld();
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
+        out.chunk(p, cc, o);
+    }
+    out.finish(p);
 }
 
 }  // namespace fa

@@ -70,13 +70,14 @@ struct LayoutTM {
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t SLOT_OFF = Q_OFF + Q_TILES * Q_TILE_BYTES;
     static constexpr uint32_t BAR_OFF = SLOT_OFF + STAGES * SLOT_BYTES;
-    static constexpr int BAR_QFULL = 0;
-    static constexpr int BAR_KVFULL = 1;
+    static constexpr int BAR_QFULL = 0;                       // [tile] Q_t landed
+    static constexpr int BAR_KVFULL = BAR_QFULL + Q_TILES;
     static constexpr int BAR_KVEMPTY = BAR_KVFULL + STAGES;
     static constexpr int BAR_SFULL = BAR_KVEMPTY + STAGES;  // [tile] S_t(j) (and PV_t(j-1)) done
     static constexpr int BAR_PFULL = BAR_SFULL + Q_TILES;   // [tile] P_t(j) in TMEM (one arrival per warp)
     static constexpr int BAR_OFULL = BAR_PFULL + Q_TILES;   // [tile] last PV_t finished
-    static constexpr int BAR_DRAIN = BAR_OFULL + Q_TILES;
+    static constexpr int BAR_OSTAGED = BAR_OFULL + Q_TILES; // [tile] bf16 O_t staged (one arrival per warp)
+    static constexpr int BAR_DRAIN = BAR_OSTAGED + Q_TILES;
     static constexpr int NUM_BARS = BAR_DRAIN + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] tmem base, [1] abort
     static constexpr uint32_t BYTES = MISC_OFF + 16;
@@ -124,15 +125,16 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
     const int lane = threadIdx.x & 31;
 
     Work<QT> w;
-    compute_work<QT, BN>(p, w);
+    compute_work<QT, BN>(p, blockIdx.x, w);
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(L::BAR_QFULL), 1);
         for (int s = 0; s < ST; ++s) {
             mbar_init(bar(L::BAR_KVFULL + s), 1);
             mbar_init(bar(L::BAR_KVEMPTY + s), 1);
         }
         for (int t = 0; t < QT; ++t) {
+            mbar_init(bar(L::BAR_QFULL + t), 1);
+            mbar_init(bar(L::BAR_OSTAGED + t), 4);
             mbar_init(bar(L::BAR_SFULL + t), 1);
             mbar_init(bar(L::BAR_PFULL + t), 4);  // one arrival per warp of the group
             mbar_init(bar(L::BAR_OFULL + t), 1);
@@ -164,21 +166,20 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
         // The whole warp runs the loop (uniform values); one elected lane issues.
         if (w.nmax > 0) {
             const bool leader = elect_one();
-            int nvalid = 0;
-#pragma unroll
-            for (int t = 0; t < QT; ++t) nvalid += (w.n[t] > 0) ? 1 : 0;
-            // (The failure-detection test hook withholds the Q tiles so that the
-            // issuer's bounded wait runs out; nothing else changes.)
-            if (leader && !p.test_withhold_q) mbar_arrive_expect_tx(bar(L::BAR_QFULL), nvalid * L::Q_TILE_BYTES);
-#pragma unroll
-            for (int t = 0; t < QT; ++t) {
+            // Q_t of each tile with work, on its own barrier. (The failure-
+            // detection test hook withholds the Q tiles so that the issuer's
+            // bounded wait runs out; nothing else changes.)
+            auto load_q = [&](int t) {
                 if (leader && w.n[t] > 0 && !p.test_withhold_q) {
+                    mbar_arrive_expect_tx(bar(L::BAR_QFULL + t), L::Q_TILE_BYTES);
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128),
-                                    &p.tm_q, bar(L::BAR_QFULL), 64 * c, w.q0 + t * kBM, w.bh);
+                                    &p.tm_q, bar(L::BAR_QFULL + t), 64 * c, w.q0 + t * kBM, w.bh);
                 }
-            }
+            };
+            // Q_0, K_0, then Q_1: the first S can start after two tiles' bytes.
+            load_q(0);
             // Entry e of the sequence: K_0; then for step j: V_j, K_{j+1} (if any).
             const int total = 2 * w.nmax;
             RingPos<ST> pos;
@@ -204,6 +205,7 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
                 }
                 issued = e + 1;
                 pos.advance();
+                if (e == 0) load_q(1);
             }
             if (ok) {
                 // Producer tail: wait until the issuer has released the last use
@@ -217,7 +219,10 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             }
             if (!ok) {
                 // Let every copy already issued land before the CTA goes away.
-                wait_phase(bar(L::BAR_QFULL), 0, p, abort_flag, kStatusWaitDrain, false);
+#pragma unroll
+                for (int t = 0; t < QT; ++t)
+                    if (w.n[t] > 0 && !p.test_withhold_q && issued > 0)
+                        wait_phase(bar(L::BAR_QFULL + t), 0, p, abort_flag, kStatusWaitDrain, false);
                 for (int e = max(0, issued - ST); e < issued; ++e)
                     wait_phase(bar(L::BAR_KVFULL + e % ST), (e / ST) & 1, p, abort_flag,
                                kStatusWaitDrain, false);
@@ -285,17 +290,20 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
                 }
                 return true;
             };
-            bool ok = wait_all(bar(L::BAR_QFULL), 0, kStatusWaitQ);
-            if (ok) ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
+            bool ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
             if (ok) {
-                tc_fence_after();
 #pragma unroll
                 for (int t = 0; t < QT; ++t) {
-                    if (w.n[t] > 0) {
+                    if (ok && w.n[t] > 0) {
+                        ok = wait_all(bar(L::BAR_QFULL + t), 0, kStatusWaitQ);
+                        if (!ok) break;
+                        tc_fence_after();
                         issue_s(t, pos.slot);
                         if (leader) umma_commit(bar(L::BAR_SFULL + t));
                     }
                 }
+            }
+            if (ok) {
                 if (leader) umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
                 pos.advance();
                 ok = wait_kv(0);
@@ -493,7 +501,50 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) tc_fence_after();
         }
-        if (ok) write_row<D>(p, w.bh, w.split, q_row, n, m, m_true, l, tO);
+        if (ok && !p.split_mode && n > 0) {
+            // Plain mode: stage bf16 O_t in Q_t's shared memory (free once the
+            // tile's last PV has finished: every S_t MMA came before it), in the
+            // 128-byte-swizzled layout of a Q_t load, then one thread writes the
+            // tile with TMA stores (rows past Nq are clipped) instead of 128
+            // threads writing 16-byte pieces of separate rows.
+            const RowOut<D> out(p, w.bh, w.split, q_row, m, m_true, l);
+            const uint32_t q_tile = sbase + L::Q_OFF + t * L::Q_TILE_BYTES;
+            const uint32_t swz = static_cast<uint32_t>(r & 7);
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(tO + cc * 32, o);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * out.f, __uint_as_float(o[2 * i + 1]) * out.f);
+                // 32 columns = four 16-byte units of the row's line in 64-column chunk cc/2.
+                const uint32_t line = q_tile + (cc >> 1) * (kBM * 128) + r * 128;
+#pragma unroll
+                for (int uu = 0; uu < 4; ++uu) {
+                    const uint32_t u = static_cast<uint32_t>((cc & 1) * 4 + uu);
+                    st_shared_v4(line + ((u ^ swz) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2], pk[4 * uu + 3]);
+                }
+            }
+            out.finish(p);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::BAR_OSTAGED + t));
+            if (quarter == 0) {
+                bool staged = wait_phase(bar(L::BAR_OSTAGED + t), 0, p, abort_flag, kStatusWaitO);
+                staged = __all_sync(0xffffffffu, staged);
+                if (staged && lane == 0) {
+#pragma unroll
+                    for (int c = 0; c < L::CHUNKS; ++c)
+                        tma_store_3d(&p.tm_o, q_tile + c * (kBM * 128), 64 * c, w.q0 + t * kBM, w.bh);
+                    bulk_commit_group();
+                    bulk_wait_group_read0();  // shared memory read before the CTA exits
+                }
+            }
+        } else if (ok) {
+            write_row<D>(p, w.bh, w.split, q_row, n, m, m_true, l, tO);
+        }
     }
 
     __syncwarp();

@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
     const int lane = threadIdx.x & 31;
 
     Work<QT> w;
-    compute_work<QT, BN>(p, w);
+    compute_work<QT, BN>(p, blockIdx.x, w);
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::BAR_QFULL), 1);
