@@ -187,4 +187,54 @@ __device__ __forceinline__ void write_row(const FwdParams& p, int bh, int split,
     out.finish(p);
 }
 
+// Plain-mode epilogue of one 128-row query tile, run by the tile's 128
+// softmax threads (thread r = row r = TMEM lane r): O_t / l as bf16 is staged in
+// the tile's own Q shared memory (`q_tile`, free once the tile's last PV has
+// finished, as every S MMA reading Q came before it) in the 128-byte-swizzled
+// layout a Q load through the same kind of tensor map produces, and the
+// group's first warp writes the tile with TMA tensor stores (rows past Nq are
+// clipped). `staged` is an mbarrier expecting one arrival per warp. Returns
+// false if the bounded wait for the staging ran out.
+template <int D>
+__device__ __forceinline__ bool store_tile_tma(const FwdParams& p, int bh, int q_row0, int r, int q_row,
+                                               float m, float m_true, float l, uint32_t tO,
+                                               uint32_t q_tile, uint32_t staged,
+                                               volatile uint32_t* abort_flag) {
+    const int lane = r & 31;
+    const RowOut<D> out(p, bh, 0, q_row, m, m_true, l);
+    const uint32_t swz = static_cast<uint32_t>(r & 7);
+#pragma unroll 1
+    for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t o[32];
+        tmem_ld32(tO + cc * 32, o);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * out.f, __uint_as_float(o[2 * i + 1]) * out.f);
+        // 32 columns = four 16-byte units of the row's line in 64-column chunk cc/2.
+        const uint32_t line = q_tile + (cc >> 1) * (kBM * 128) + r * 128;
+#pragma unroll
+        for (int uu = 0; uu < 4; ++uu) {
+            const uint32_t u = static_cast<uint32_t>((cc & 1) * 4 + uu);
+            st_shared_v4(line + ((u ^ swz) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2], pk[4 * uu + 3]);
+        }
+    }
+    out.finish(p);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(staged);
+    bool ok = true;
+    if (r < 32) {
+        ok = __all_sync(0xffffffffu, wait_phase(staged, 0, p, abort_flag, kStatusWaitO));
+        if (ok && lane == 0) {
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c) tma_store_3d(&p.tm_o, q_tile + c * (kBM * 128), 64 * c, q_row0, bh);
+            bulk_commit_group();
+            bulk_wait_group_read0();  // shared memory read before the CTA exits
+        }
+    }
+    return ok;
+}
+
 }  // namespace fa

@@ -502,46 +502,9 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             if (ok) tc_fence_after();
         }
         if (ok && !p.split_mode && n > 0) {
-            // Plain mode: stage bf16 O_t in Q_t's shared memory (free once the
-            // tile's last PV has finished: every S_t MMA came before it), in the
-            // 128-byte-swizzled layout of a Q_t load, then one thread writes the
-            // tile with TMA stores (rows past Nq are clipped) instead of 128
-            // threads writing 16-byte pieces of separate rows.
-            const RowOut<D> out(p, w.bh, w.split, q_row, m, m_true, l);
-            const uint32_t q_tile = sbase + L::Q_OFF + t * L::Q_TILE_BYTES;
-            const uint32_t swz = static_cast<uint32_t>(r & 7);
-#pragma unroll 1
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(tO + cc * 32, o);
-                tmem_wait_ld();
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * out.f, __uint_as_float(o[2 * i + 1]) * out.f);
-                // 32 columns = four 16-byte units of the row's line in 64-column chunk cc/2.
-                const uint32_t line = q_tile + (cc >> 1) * (kBM * 128) + r * 128;
-#pragma unroll
-                for (int uu = 0; uu < 4; ++uu) {
-                    const uint32_t u = static_cast<uint32_t>((cc & 1) * 4 + uu);
-                    st_shared_v4(line + ((u ^ swz) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2], pk[4 * uu + 3]);
-                }
-            }
-            out.finish(p);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::BAR_OSTAGED + t));
-            if (quarter == 0) {
-                bool staged = wait_phase(bar(L::BAR_OSTAGED + t), 0, p, abort_flag, kStatusWaitO);
-                staged = __all_sync(0xffffffffu, staged);
-                if (staged && lane == 0) {
-#pragma unroll
-                    for (int c = 0; c < L::CHUNKS; ++c)
-                        tma_store_3d(&p.tm_o, q_tile + c * (kBM * 128), 64 * c, w.q0 + t * kBM, w.bh);
-                    bulk_commit_group();
-                    bulk_wait_group_read0();  // shared memory read before the CTA exits
-                }
-            }
+            // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA.
+            store_tile_tma<D>(p, w.bh, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
+                              sbase + L::Q_OFF + t * L::Q_TILE_BYTES, bar(L::BAR_OSTAGED + t), abort_flag);
         } else if (ok) {
             write_row<D>(p, w.bh, w.split, q_row, n, m, m_true, l, tO);
         }

@@ -75,7 +75,8 @@ struct LayoutTP {
     static constexpr int BAR_PFULL = BAR_SFULL + 2 * Q_TILES;  // [tile][S buffer]
     static constexpr int BAR_PVDONE = BAR_PFULL + 2 * Q_TILES; // [tile]
     static constexpr int BAR_OFULL = BAR_PVDONE + Q_TILES;     // [tile]
-    static constexpr int BAR_DRAIN = BAR_OFULL + Q_TILES;
+    static constexpr int BAR_OSTAGED = BAR_OFULL + Q_TILES;    // [tile] bf16 O_t staged (one arrival per warp)
+    static constexpr int BAR_DRAIN = BAR_OSTAGED + Q_TILES;
     static constexpr int NUM_BARS = BAR_DRAIN + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] tmem base, [1] abort
     static constexpr uint32_t BYTES = MISC_OFF + 16;
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             mbar_init(bar(L::BAR_PFULL + 2 * t + 1), kBM);
             mbar_init(bar(L::BAR_PVDONE + t), 1);
             mbar_init(bar(L::BAR_OFULL + t), 1);
+            mbar_init(bar(L::BAR_OSTAGED + t), 4);
         }
         mbar_init(bar(L::BAR_DRAIN), 1);
         *abort_flag = 0u;
@@ -474,7 +476,13 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) tc_fence_after();
         }
-        if (ok) write_row<D>(p, w.bh, w.split, q_row, n, m, m_true, l, tO);
+        if (ok && !p.split_mode && n > 0) {
+            // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA.
+            store_tile_tma<D>(p, w.bh, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
+                              sbase + L::Q_OFF + t * L::Q_TILE_BYTES, bar(L::BAR_OSTAGED + t), abort_flag);
+        } else if (ok) {
+            write_row<D>(p, w.bh, w.split, q_row, n, m, m_true, l, tO);
+        }
     }
 
     __syncwarp();
