@@ -6,10 +6,14 @@ Conventions (shared with the CUDA library only by documentation, never by code):
 
 * Tensors are ``[..., N, d]``; the leading dimensions are independent heads.
 * ``scale`` is the float32 value the caller hands the GPU, upcast exactly.
-* ``causal`` is top-left aligned: key ``j`` is visible to query ``i`` iff
-  ``j <= i``.  (The FA-2 page, section "正确性与部署边界", leaves the alignment
-  for non-square shapes to the implementation's documentation; top-left is the
-  reading used here and in the library.)
+* ``causal`` selects the mask: ``False``/``0`` none; ``True``/``1``/
+  ``"top_left"``: key ``j`` is visible to query ``i`` iff ``j <= i``;
+  ``2``/``"bottom_right"``: iff ``j <= i + (Nk - Nq)``, so the last query row
+  sees every key.  (The FA-2 page, section "正确性与部署边界", leaves the
+  alignment for non-square shapes to the implementation's documentation; both
+  readings are offered and coincide when Nq = Nk.)
+* A row that sees no key (bottom-right with Nq > Nk) has no softmax; it is
+  reported as O = 0, LSE = -inf, the same convention as an empty split.
 * LSE is the natural logarithm of the row's softmax denominator, in units of the
   scaled score: ``LSE_i = m_i + ln(l_i)``.
 """
@@ -30,13 +34,26 @@ def _as_heads(x):
     return a.reshape((-1,) + a.shape[-2:]), lead
 
 
+def causal_offset(causal, nq, nk):
+    """Offset ``c`` of the causal mask: key ``j`` is visible to query ``i`` iff
+    ``j <= i + c``; ``None`` when there is no mask (see the module docstring)."""
+    if causal is None or causal is False or (not isinstance(causal, str) and causal == 0):
+        return None
+    if causal is True or causal == 1 or causal == "top_left":
+        return 0
+    if causal == 2 or causal == "bottom_right":
+        return nk - nq
+    raise ValueError(f"unknown causal mode {causal!r}")
+
+
 def scores_f64(q, k, scale, causal, rows=None):
     """Scaled, masked score matrix S = scale * Q K^T for one head.
 
     FA-2 page, section 3.1: the method computes the same dense attention as the
     naive one, so S is the full dot-product matrix.  ``q`` is ``[Nq, d]``,
     ``k`` is ``[Nk, d]``; ``rows`` (optional) selects query rows by their global
-    index, which also positions the causal mask.  Masked entries are -inf.
+    index, which also positions the causal mask (``q`` is the whole head, so
+    Nq is its length).  Masked entries are -inf.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -44,9 +61,10 @@ def scores_f64(q, k, scale, causal, rows=None):
         rows = np.arange(q.shape[0])
     rows = np.asarray(rows)
     s = float(scale) * (q[rows] @ k.T)
-    if causal:
+    off = causal_offset(causal, q.shape[0], k.shape[0])
+    if off is not None:
         cols = np.arange(k.shape[0])
-        s = np.where(cols[None, :] > rows[:, None], NEG_INF, s)
+        s = np.where(cols[None, :] > rows[:, None] + off, NEG_INF, s)
     return s
 
 
@@ -55,7 +73,8 @@ def _softmax_rows(s, v):
 
     m = max_j s_ij;  P = exp(s - m);  l = sum_j P;  O = (P V) / l;  LSE = m + ln l.
     A row with no visible key has no softmax; it is reported as O = 0,
-    LSE = -inf (never produced by top-left causal attention with Nk >= 1).
+    LSE = -inf (never produced by top-left causal attention with Nk >= 1; the
+    first Nq - Nk rows under bottom-right alignment when Nq > Nk).
     """
     m = s.max(axis=1)
     empty = ~np.isfinite(m)

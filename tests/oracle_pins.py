@@ -305,10 +305,13 @@ def pin_torch_sdpa_float64(orc):
         q = rng.standard_normal((2, 3, nq, d))
         k = rng.standard_normal((2, 3, nk, d))
         v = rng.standard_normal((2, 3, nk, dv))
-        for causal in (False, True):
+        modes = [False, True] + (["bottom_right"] if nq <= nk else [])
+        for causal in modes:
             mask = None
-            if causal:
+            if causal is True:
                 mask = torch.ones(nq, nk, dtype=torch.bool).tril()
+            elif causal == "bottom_right":
+                mask = torch.ones(nq, nk, dtype=torch.bool).tril(diagonal=nk - nq)
             ref = torch.nn.functional.scaled_dot_product_attention(
                 torch.from_numpy(q), torch.from_numpy(k), torch.from_numpy(v),
                 attn_mask=mask, scale=0.45)
@@ -321,15 +324,21 @@ def pin_torch_sdpa_float64(orc):
             assert np.allclose(lse, torch.logsumexp(sref, dim=-1).numpy(), atol=1e-12)
 
 
-def _brute(q, k, v, scale, causal):
+def _brute(q, k, v, scale, causal, offset=0):
+    """Per-element loops; with ``causal`` key j is visible to query i iff
+    j <= i + offset.  A row with no visible key gives O = 0, LSE = -inf."""
     nq, nk = len(q), len(k)
     o, lse = [], []
     for i in range(nq):
         s = []
         for j in range(nk):
-            if causal and j > i:
+            if causal and j > i + offset:
                 continue
             s.append((j, scale * math.fsum(a * b for a, b in zip(q[i], k[j]))))
+        if not s:
+            o.append([0.0] * len(v[0]))
+            lse.append(-math.inf)
+            continue
         m = max(x for _, x in s)
         e = [(j, math.exp(x - m)) for j, x in s]
         den = math.fsum(w for _, w in e)
@@ -351,6 +360,51 @@ def pin_brute_force(orc):
             assert np.allclose(lse, np.array(lb), rtol=0, atol=1e-14)
 
 
+def pin_brute_force_bottom_right(orc):
+    """Bottom-right alignment against per-element loops with offset Nk - Nq,
+    including Nq > Nk (rows that see no key)."""
+    rng = np.random.default_rng(15)
+    for (nq, nk, d, dv) in ((3, 5, 2, 3), (5, 3, 2, 2), (1, 6, 3, 2), (7, 7, 2, 2), (6, 1, 2, 3)):
+        q = rng.standard_normal((nq, d))
+        k = rng.standard_normal((nk, d))
+        v = rng.standard_normal((nk, dv))
+        o, lse = orc.attention_f64(q, k, v, 0.8, "bottom_right")
+        ob, lb = _brute(q.tolist(), k.tolist(), v.tolist(), 0.8, True, nk - nq)
+        assert np.allclose(o, np.array(ob), rtol=0, atol=1e-14)
+        lb = np.array(lb)
+        assert np.array_equal(np.isinf(lse), np.isinf(lb))
+        assert np.allclose(lse[np.isfinite(lb)], lb[np.isfinite(lb)], rtol=0, atol=1e-14)
+
+
+def pin_bottom_right_rows(orc):
+    """Closed forms of the bottom-right mask (key j visible to query i iff
+    j <= i + Nk - Nq): for Nq = Nk it is the top-left mask; the last query row
+    sees every key; with Nq > Nk the first Nq - Nk rows see nothing (O = 0,
+    LSE = -inf) and the next one sees key 0 only (O = V_0, LSE = its score)."""
+    rng = np.random.default_rng(16)
+    q = rng.standard_normal((13, 6))
+    k = rng.standard_normal((13, 6))
+    v = rng.standard_normal((13, 4))
+    a = orc.attention_f64(q, k, v, 0.5, "bottom_right")
+    b = orc.attention_f64(q, k, v, 0.5, True)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    # Nq < Nk: last row = non-causal last row; first row = attention over keys 0..Nk-Nq.
+    q5 = q[:5]
+    o, lse = orc.attention_f64(q5, k, v, 0.5, 2)
+    o_nc, lse_nc = orc.attention_f64(q5, k, v, 0.5, False)
+    assert np.allclose(o[4], o_nc[4], atol=1e-15) and np.isclose(lse[4], lse_nc[4], atol=1e-15)
+    o0, lse0 = orc.attention_f64(q5[:1], k[:9], v[:9], 0.5, False)
+    assert np.allclose(o[0], o0[0], atol=1e-15) and np.isclose(lse[0], lse0[0], atol=1e-15)
+    # Nq > Nk: rows 0..Nq-Nk-1 see nothing, row Nq-Nk sees key 0 only.
+    k3, v3 = k[:3], v[:3]
+    o, lse = orc.attention_f64(q[:7], k3, v3, 0.5, "bottom_right")
+    assert np.array_equal(o[:4], np.zeros((4, 4))) and np.all(lse[:4] == -np.inf)
+    assert np.allclose(o[4], v3[0], atol=1e-15)
+    assert np.isclose(lse[4], 0.5 * float(q[4] @ k3[0]), atol=1e-15)
+    o_nc, lse_nc = orc.attention_f64(q[:7], k3, v3, 0.5, False)
+    assert np.allclose(o[6], o_nc[6], atol=1e-15)
+
+
 ALL_PINS = [
     pin_split_example_block_states,
     pin_split_example_merge,
@@ -369,4 +423,6 @@ ALL_PINS = [
     pin_row_subset,
     pin_torch_sdpa_float64,
     pin_brute_force,
+    pin_brute_force_bottom_right,
+    pin_bottom_right_rows,
 ]

@@ -22,8 +22,10 @@ MUTANTS = [
     ("dropped scale", "s = float(scale) * (q[rows] @ k.T)", "s = (q[rows] @ k.T)"),
     ("keys used as queries", "s = float(scale) * (q[rows] @ k.T)",
      "s = float(scale) * (k[rows % k.shape[0]] @ k.T)"),
-    ("mask includes diagonal", "cols[None, :] > rows[:, None]", "cols[None, :] >= rows[:, None]"),
-    ("mask flipped", "cols[None, :] > rows[:, None]", "cols[None, :] < rows[:, None]"),
+    ("mask includes diagonal", "cols[None, :] > rows[:, None] + off", "cols[None, :] >= rows[:, None] + off"),
+    ("mask flipped", "cols[None, :] > rows[:, None] + off", "cols[None, :] < rows[:, None] + off"),
+    ("bottom-right offset sign", "return nk - nq", "return nq - nk"),
+    ("bottom-right as top-left", "return nk - nq", "return 0"),
     ("lse sign", "lse = np.where(empty, NEG_INF, m_ref + np.log(l))",
      "lse = np.where(empty, NEG_INF, m_ref - np.log(l))"),
     ("lse drops max", "lse = np.where(empty, NEG_INF, m_ref + np.log(l))",
