@@ -18,8 +18,12 @@ FA_OK = 0
 STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_ALIGN", 3: "FA_ERR_SHAPE", 4: "FA_ERR_HEADDIM",
     5: "FA_ERR_SPLITS", 6: "FA_ERR_WORKSPACE", 7: "FA_ERR_CUDA", 8: "FA_ERR_TIMEOUT",
-    9: "FA_ERR_SCALE", 10: "FA_ERR_SCRATCH",
+    9: "FA_ERR_SCALE", 10: "FA_ERR_SCRATCH", 11: "FA_ERR_CAUSAL",
 }
+# Causal mask modes (include/fa.h): key j visible to query i iff j <= i (top-left)
+# or j <= i + Nk - Nq (bottom-right).
+CAUSAL_NONE, CAUSAL_TOP_LEFT, CAUSAL_BOTTOM_RIGHT = 0, 1, 2
+_CAUSAL_NAMES = {"none": 0, "top_left": 1, "bottom_right": 2}
 FA_MAX_SPLITS = 256
 
 _lib = None
@@ -100,17 +104,30 @@ def _bhnd(q, k, v):
     return int(B), int(H), int(Nq), int(k.shape[2]), int(d)
 
 
+def causal_code(causal) -> int:
+    """The C-ABI causal value: ``False``/``True`` (top-left), 0/1/2, or one of
+    ``"none"``, ``"top_left"``, ``"bottom_right"``. Other values pass through as
+    given, for the library to reject (FA_ERR_CAUSAL)."""
+    if isinstance(causal, str):
+        if causal not in _CAUSAL_NAMES:
+            raise ValueError(f"unknown causal mode {causal!r}")
+        return _CAUSAL_NAMES[causal]
+    if isinstance(causal, bool):
+        return CAUSAL_TOP_LEFT if causal else CAUSAL_NONE
+    return int(causal)
+
+
 def default_scale(d: int) -> float:
     """1/sqrt(d) rounded once to float32 (the value the kernel receives)."""
     return float(ctypes.c_float(d ** -0.5).value)
 
 
-def fa_fwd(q, k, v, o, lse, causal: bool = False, scale: float | None = None, stream=None):
+def fa_fwd(q, k, v, o, lse, causal=False, scale: float | None = None, stream=None):
     """Fused forward into caller-owned ``o`` (bf16 [B,H,Nq,d]) and ``lse`` (fp32 [B,H,Nq])."""
     B, H, Nq, Nk, d = _bhnd(q, k, v)
     scale = default_scale(d) if scale is None else float(scale)
     st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
-                               scale, int(bool(causal)), _stream_handle(stream))
+                               scale, causal_code(causal), _stream_handle(stream))
     _check(st, "fa_fwd")
 
 
@@ -118,13 +135,13 @@ def fa_splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int)
     return int(load_library().fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits))
 
 
-def fa_fwd_splitkv(q, k, v, workspace, num_splits: int, causal: bool = False,
+def fa_fwd_splitkv(q, k, v, workspace, num_splits: int, causal=False,
                    scale: float | None = None, stream=None):
     """Split-KV partial states into ``workspace`` (see include/fa.h for the layout)."""
     B, H, Nq, Nk, d = _bhnd(q, k, v)
     scale = default_scale(d) if scale is None else float(scale)
     st = load_library().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(workspace), B, H, Nq, Nk,
-                                       d, scale, int(bool(causal)), int(num_splits),
+                                       d, scale, causal_code(causal), int(num_splits),
                                        _stream_handle(stream))
     _check(st, "fa_fwd_splitkv")
 
@@ -146,7 +163,7 @@ def fa_device_status(clear: bool = True, stream=None) -> int:
     return int(load_library().fa_device_status(_stream_handle(stream), int(bool(clear))))
 
 
-def attention(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int = 1,
+def attention(q, k, v, causal=False, scale: float | None = None, num_splits: int = 1,
               stream=None):
     """Allocate outputs and run the forward; ``num_splits > 1`` takes the split-KV +
     combine path. Returns ``(o, lse)``."""
@@ -167,7 +184,7 @@ def attention(q, k, v, causal: bool = False, scale: float | None = None, num_spl
     return o, lse
 
 
-def fa_fwd_splitkv_static(q, k, v, o, lse, num_splits: int, causal: bool = False,
+def fa_fwd_splitkv_static(q, k, v, o, lse, num_splits: int, causal=False,
                           scale: float | None = None, stream=None):
     """Split-KV forward + merge into caller-owned ``o``/``lse`` with no workspace
     argument: the partial states live in the library's static device buffer
@@ -182,5 +199,5 @@ def fa_fwd_splitkv_static(q, k, v, o, lse, num_splits: int, causal: bool = False
     fn.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
     fn.restype = i
     st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, scale,
-            int(bool(causal)), int(num_splits), _stream_handle(stream))
+            causal_code(causal), int(num_splits), _stream_handle(stream))
     _check(st, "fa_fwd_splitkv_static")

@@ -107,6 +107,10 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int d, int N, int BH, i
     return r == CUDA_SUCCESS;
 }
 
+bool valid_causal(int causal) {
+    return causal == FA_CAUSAL_NONE || causal == FA_CAUSAL_TOP_LEFT || causal == FA_CAUSAL_BOTTOM_RIGHT;
+}
+
 fa_status check_common(const void* q, const void* k, const void* v, int B, int H, int Nq, int Nk,
                        int d, float scale) {
     if (!q || !k || !v) return FA_ERR_NULL;
@@ -154,6 +158,9 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     p.Nq = Nq;
     p.Nk = Nk;
     p.causal = causal ? 1 : 0;
+    // Key j is visible to query row i iff j <= i + causal_off (top-left: 0;
+    // bottom-right: Nk - Nq).
+    p.causal_off = (causal == FA_CAUSAL_BOTTOM_RIGHT) ? Nk - Nq : 0;
     p.num_splits = num_splits;
     p.split_mode = split_mode;
     p.n_units = static_cast<int>(ctas / (static_cast<long long>(BH) * num_splits));
@@ -189,6 +196,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream) {
     fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
     if (s != FA_OK) return s;
+    if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
     if (!o || !lse) return FA_ERR_NULL;
     if (!fa::aligned(o, 16) || !fa::aligned(lse, 4)) return FA_ERR_ALIGN;
     return fa::launch_forward(q, k, v, o, lse, nullptr, B, H, Nq, Nk, d, scale, causal, 1, 0,
@@ -208,6 +216,7 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* work
                          cudaStream_t stream) {
     fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
     if (s != FA_OK) return s;
+    if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
     if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_SPLITS;
     if (!workspace || !fa::aligned(workspace, 16)) return FA_ERR_WORKSPACE;
     return fa::launch_forward(q, k, v, nullptr, nullptr, static_cast<float*>(workspace), B, H, Nq,
@@ -281,6 +290,8 @@ const char* fa_status_string(fa_status status) {
         case FA_ERR_SCALE: return "FA_ERR_SCALE: scale must be finite and > 0";
         case FA_ERR_SCRATCH:
             return "FA_ERR_SCRATCH: partial states exceed the library's static scratch buffer";
+        case FA_ERR_CAUSAL:
+            return "FA_ERR_CAUSAL: causal must be FA_CAUSAL_NONE, _TOP_LEFT or _BOTTOM_RIGHT";
     }
     return "unknown fa_status";
 }

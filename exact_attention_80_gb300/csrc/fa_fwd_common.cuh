@@ -71,8 +71,9 @@ __device__ __forceinline__ void compute_work(const FwdParams& p, long long lin, 
         if (row0 < p.Nq) {
             int end = t1;
             if (p.causal) {
-                const int last_row = min(row0 + kBM - 1, p.Nq - 1);
-                end = min(end, last_row / BN + 1);
+                // Keys up to the tile's last row + causal_off; none if that is < 0.
+                const int last_key = min(row0 + kBM - 1, p.Nq - 1) + p.causal_off;
+                end = min(end, last_key < 0 ? 0 : last_key / BN + 1);
             }
             n = max(0, end - t0);
         }

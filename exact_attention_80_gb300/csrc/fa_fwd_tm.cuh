@@ -403,10 +403,11 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             tmem_wait_ld();
 
             // Mask: keys past the split / sequence end, and (causal) keys after
-            // this row. TMA zero-fills keys >= Nk, so they must become -inf.
+            // this row + causal_off. TMA zero-fills keys >= Nk, so they must
+            // become -inf.
             const int kv0 = (w.kv_tile0 + j) * BN;
             int valid = w.kv_end - kv0;
-            if (p.causal) valid = min(valid, q_row - kv0 + 1);
+            if (p.causal) valid = min(valid, q_row + p.causal_off - kv0 + 1);
             if (valid < BN) {
 #pragma unroll
                 for (int c = 0; c < BN; ++c)

@@ -36,6 +36,7 @@ struct FwdParams {
     float* ws_l;       // fp32 [S][B*H][Nq]
     int BH, Nq, Nk;
     int causal;
+    int causal_off;          // causal: key j visible to query row i iff j <= i + causal_off
     int num_splits;          // 1 in plain mode
     int split_mode;          // 0: write O/LSE, 1: write partial (O, m, l)
     int n_units;             // query units of (tiles per CTA * 128) rows per head

@@ -2,7 +2,7 @@
  * fa.h — exact scaled-dot-product attention forward on GB300 (sm_103a).
  *
  * What is computed (per batch b and head h, rows i of Q, keys j of K/V):
- *     S = scale * Q K^T            (optionally causal: key j visible to query i iff j <= i)
+ *     S = scale * Q K^T            (optionally causal: key j visible to query i iff j <= i + c)
  *     O = softmax_row(S) V          (exact softmax, no approximation of the definition)
  *     LSE_i = ln sum_j exp(S_ij)    (natural log, in units of the scaled score)
  * The result is the plain definition of attention; the kernels reach it tile by
@@ -24,10 +24,16 @@
  *  - d must be 64, 128 or 256. Any other head dim is an error, never a silent
  *    fallback (the FlashAttention_02 page, sections 4.4 and 8, warns that
  *    frameworks silently switch backends for unsupported head dims).
- *  - `causal` != 0 selects the top-left aligned causal mask (key j visible to
- *    query i iff j <= i). The FlashAttention_02 page, section "正确性与部署边界",
- *    leaves square/non-square alignment to the implementation's documentation:
- *    this is it.
+ *  - `causal` selects the mask: FA_CAUSAL_NONE (0); FA_CAUSAL_TOP_LEFT (1),
+ *    key j visible to query i iff j <= i; FA_CAUSAL_BOTTOM_RIGHT (2), iff
+ *    j <= i + (Nk - Nq), so the last query row sees every key (the usual
+ *    alignment when Nq new queries attend to a cache of Nk keys). Any other
+ *    value is FA_ERR_CAUSAL. The two alignments coincide when Nq = Nk. The
+ *    FlashAttention_02 page, section "正确性与部署边界", leaves square/non-square
+ *    alignment to the implementation's documentation: this is it.
+ *  - A query row that sees no key (bottom-right with Nq > Nk: its first Nq - Nk
+ *    rows) gets O = 0 and LSE = -inf; in split mode its partial state is
+ *    m = -inf, l = 0, O = 0, like an empty split.
  *  - `scale` must be finite and > 0; it is used exactly as given (float32).
  *  - q, k, v, o and the workspace must be 16-byte aligned; lse 4-byte aligned.
  *  - The output buffers must not overlap the inputs.
@@ -53,8 +59,13 @@ typedef enum {
     FA_ERR_CUDA = 7,       /* a CUDA runtime or driver call failed (no device, launch, tensor-map encode) */
     FA_ERR_TIMEOUT = 8,    /* a kernel gave up on a bounded wait (reported by fa_device_status) */
     FA_ERR_SCALE = 9,      /* scale is not finite or not > 0 */
-    FA_ERR_SCRATCH = 10    /* fa_fwd_splitkv_static: partial states exceed FA_STATIC_SCRATCH_BYTES */
+    FA_ERR_SCRATCH = 10,   /* fa_fwd_splitkv_static: partial states exceed FA_STATIC_SCRATCH_BYTES */
+    FA_ERR_CAUSAL = 11     /* causal is not FA_CAUSAL_NONE, _TOP_LEFT or _BOTTOM_RIGHT */
 } fa_status;
+
+#define FA_CAUSAL_NONE 0
+#define FA_CAUSAL_TOP_LEFT 1
+#define FA_CAUSAL_BOTTOM_RIGHT 2
 
 #define FA_MAX_SPLITS 256
 

@@ -65,6 +65,7 @@ def _fwd(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, B=1, H=1, Nq=8, Nk=8, d=
     (dict(scale=float("inf")), 9),
     (dict(q=FAKE + 8), 2), (dict(k=FAKE + 4), 2), (dict(v=FAKE + 2), 2), (dict(o=FAKE + 8), 2),
     (dict(lse=FAKE + 2), 2),
+    (dict(causal=3), 11), (dict(causal=-1), 11),
 ])
 def test_fwd_rejects(lib, kw, code):
     assert _fwd(lib, **kw) == code
@@ -79,7 +80,7 @@ def _split(lib, ws=FAKE, S=4, **kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(ws=0), 6), (dict(ws=FAKE + 4), 6), (dict(S=0), 5), (dict(S=257), 5),
-    (dict(d=80), 4), (dict(q=0), 1), (dict(Nq=0), 3), (dict(scale=0.0), 9),
+    (dict(d=80), 4), (dict(q=0), 1), (dict(Nq=0), 3), (dict(scale=0.0), 9), (dict(causal=7), 11),
 ])
 def test_splitkv_rejects(lib, kw, code):
     assert _split(lib, **kw) == code

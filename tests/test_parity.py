@@ -40,7 +40,11 @@ def check(o_gpu, lse_gpu, o_ref, lse_ref, what=""):
     err = np.abs(o - o_ref)
     max_abs = float(err.max())
     rel = float(np.linalg.norm((o - o_ref).ravel()) / max(np.linalg.norm(o_ref.ravel()), 1e-30))
-    lse_err = float(np.abs(lse - lse_ref).max())
+    # Rows that see no key (bottom-right mask with Nq > Nk) have LSE = -inf on
+    # both sides; the finite rows are compared.
+    empty = ~np.isfinite(lse_ref)
+    assert np.array_equal(np.isneginf(lse), empty), f"{what}: -inf LSE rows differ"
+    lse_err = float(np.abs(lse[~empty] - lse_ref[~empty]).max()) if (~empty).any() else 0.0
     assert max_abs <= MAX_ABS, f"{what}: max-abs {max_abs:.3e}"
     assert rel <= REL_L2, f"{what}: rel-L2 {rel:.3e}"
     assert lse_err <= LSE_ABS, f"{what}: LSE err {lse_err:.3e}"
@@ -72,6 +76,15 @@ SMALL = [
     (1, 1, 100, 300, 128, True),   # Nq < Nk: top-left alignment
     (1, 1, 513, 129, 256, True),
     (3, 1, 640, 640, 64, True),
+    # bottom-right alignment: key j visible to query i iff j <= i + Nk - Nq
+    (1, 1, 300, 100, 128, "bottom_right"),  # Nq > Nk: the first 200 rows see no key
+    (1, 1, 100, 300, 128, "bottom_right"),
+    (2, 3, 257, 511, 64, "bottom_right"),
+    (1, 2, 200, 190, 256, "bottom_right"),
+    (1, 2, 190, 200, 256, "bottom_right"),
+    (1, 1, 1, 1000, 128, "bottom_right"),  # one new query over a 1000-key cache
+    (1, 1, 513, 129, 64, "bottom_right"),
+    (3, 1, 640, 640, 64, "bottom_right"),  # Nq = Nk: same as top-left
 ]
 
 
@@ -208,7 +221,7 @@ def test_combine_of_oracle_partials(d):
     check(o[0], lse[0], o_ref, lse_ref, "combine")
 
 
-@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("causal", [False, True, "bottom_right"])
 def test_split_invariance(causal):
     """Output semantics do not change with the split count (FA-2 page, split
     section: 1, 2, 3, 4 splits including empty tails), plus 16 and 64."""
@@ -223,6 +236,20 @@ def test_split_invariance(causal):
         outs.append(o.float())
     for x in outs[1:]:
         assert (x - outs[0]).abs().max().item() <= MAX_ABS
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_bottom_right_rows_without_keys_split(d):
+    """Bottom-right with Nq > Nk through split-KV + combine: rows that see no key
+    in any split come out as O = 0, LSE = -inf; the others match the oracle."""
+    B, H, Nq, Nk = 1, 2, 300, 170
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 515 + d)
+    scale = f32(1.0 / math.sqrt(d))
+    o_ref, lse_ref = oracle.attention_f64(to_f64(q), to_f64(k), to_f64(v), scale, "bottom_right")
+    assert np.all(lse_ref[..., : Nq - Nk] == -np.inf)
+    for S in (1, 2, 3):
+        o, lse = run_gpu(q, k, v, "bottom_right", scale, num_splits=S)
+        check(o, lse, o_ref, lse_ref, f"d={d} splits={S}")
 
 
 def test_guard_bands_untouched():
