@@ -263,8 +263,13 @@ def extra_workloads(device, stream, reps: int = 20):
 
     out = {}
     gen = torch.Generator(device=device)
-    for name in ("c1", "c2_causal", "c3", "c3_causal", "c4", "c5"):
-        c = CONFIGS[name]
+    # Chunked prefill against a key cache: 4096 new queries over 8192 keys with the
+    # bottom-right causal mask (FLOPs from the visible pairs).
+    configs = dict(CONFIGS)
+    configs["prefill_bottom_right"] = dict(B=1, H=32, Nq=4096, Nk=8192, d=128,
+                                           causal="bottom_right", seed=1006)
+    for name in ("c1", "c2_causal", "c3", "c3_causal", "c4", "prefill_bottom_right", "c5"):
+        c = configs[name]
         B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
         gen.manual_seed(c["seed"])
         q = torch.randn((B, H, Nq, d), generator=gen, device=device).to(torch.bfloat16)

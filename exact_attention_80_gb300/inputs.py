@@ -69,7 +69,12 @@ def config_inputs(name: str):
                     outlier_frac=c.get("outlier_frac", 0.0))
 
 
-def metric_flops(B: int, H: int, Nq: int, Nk: int, d: int, causal: bool) -> float:
-    """The benchmark's FLOP count: 4*B*H*Nq*Nk*d, halved for a causal mask."""
+def metric_flops(B: int, H: int, Nq: int, Nk: int, d: int, causal) -> float:
+    """The benchmark's FLOP count: 4*B*H*Nq*Nk*d, halved for a (top-left)
+    causal mask. For the bottom-right mask, whose shapes are not square, it is
+    4*B*H*d times the number of visible (query, key) pairs."""
+    if causal == "bottom_right" or causal == 2:
+        pairs = sum(max(0, min(Nk, i + Nk - Nq + 1)) for i in range(Nq))
+        return 4.0 * B * H * d * pairs
     f = 4.0 * B * H * Nq * Nk * d
     return f / 2 if causal else f

@@ -13,6 +13,9 @@ Pages this oracle follows (cited by title and section):
   (the FA-3 page), section 二 "核心算法：Two-Level 在线 Softmax 的再回顾" — the
   running-max / running-sum / rescaled-accumulator recurrence; section 十
   "总结" — the method does not change the mathematical definition of attention.
+* The FA-3 page, section 7.2 "cuDNN 集成" — variable-length sequences as
+  ragged tensors (``attention_varlen_f64``: one attention problem per packed
+  sequence).
 * "AI 大模型之 FlashAttention_02" (the FA-2 page), section 3.1 and 4.1 — exact
   softmax attention, O(S²d); section "工程实操 沿键切分的归约与沿查询切分的区别" —
   split partial states (m, l, u) and the merge that rescales by exp(m_b − M).
@@ -23,6 +26,7 @@ the pages, closed forms, invariants, a library routine and brute force.
 
 from .attention import (  # noqa: F401
     attention_f64,
+    attention_varlen_f64,
     attention_rows_f64,
     scores_f64,
     online_softmax_state_f64,

@@ -125,6 +125,38 @@ def attention_rows_f64(q, k, v, scale, causal, rows):
     return _softmax_rows(s, np.asarray(v, dtype=np.float64))
 
 
+def attention_varlen_f64(q, k, v, cu_q, cu_k, scale, causal=False):
+    """Exact attention over a batch of variable-length sequences.
+
+    The FA-3 page (section 7.2, cuDNN integration) names variable-length
+    sequences held as ragged tensors.  Layout: the sequences are packed along
+    the token axis, token-major: ``q`` ``[total_q, H, d]``, ``k`` ``[total_k, H,
+    d]``, ``v`` ``[total_k, H, dv]``; sequence b owns query tokens
+    ``cu_q[b] .. cu_q[b+1]-1`` and key tokens ``cu_k[b] .. cu_k[b+1]-1``.  Each
+    sequence is its own attention problem (its queries see only its keys; the
+    causal mask is positioned by its own lengths).  Returns ``(O [total_q, H,
+    dv], LSE [H, total_q])``.  A sequence with keys but no queries contributes
+    nothing; queries with no key give O = 0, LSE = -inf.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    total_q, heads = q.shape[0], q.shape[1]
+    dv = v.shape[2]
+    o = np.zeros((total_q, heads, dv))
+    lse = np.full((heads, total_q), NEG_INF)
+    for b in range(len(cu_q) - 1):
+        q0, q1 = int(cu_q[b]), int(cu_q[b + 1])
+        k0, k1 = int(cu_k[b]), int(cu_k[b + 1])
+        if q1 <= q0 or k1 <= k0:
+            continue  # no queries, or no keys (O = 0, LSE = -inf already)
+        ob, lb = attention_f64(q[q0:q1].transpose(1, 0, 2), k[k0:k1].transpose(1, 0, 2),
+                               v[k0:k1].transpose(1, 0, 2), scale, causal)
+        o[q0:q1] = ob.transpose(1, 0, 2)
+        lse[:, q0:q1] = lb
+    return o, lse
+
+
 def online_softmax_state_f64(s, v, edges):
     """Two-level online softmax over key blocks, as a recurrence.
 

@@ -405,6 +405,77 @@ def pin_bottom_right_rows(orc):
     assert np.allclose(o[6], o_nc[6], atol=1e-15)
 
 
+def pin_varlen_equal_lengths(orc):
+    """Packed sequences of equal length are a dense batch: the varlen oracle on
+    token-major packing equals the batched oracle on [B, H, N, d]."""
+    rng = np.random.default_rng(17)
+    B, H, N, M, d = 3, 2, 9, 11, 4
+    q = rng.standard_normal((B, H, N, d))
+    k = rng.standard_normal((B, H, M, d))
+    v = rng.standard_normal((B, H, M, 5))
+    pack = lambda x: x.transpose(0, 2, 1, 3).reshape(-1, x.shape[1], x.shape[3])  # noqa: E731
+    cu_q = np.arange(B + 1) * N
+    cu_k = np.arange(B + 1) * M
+    for causal in (False, True, "bottom_right"):
+        o, lse = orc.attention_varlen_f64(pack(q), pack(k), pack(v), cu_q, cu_k, 0.6, causal)
+        o_d, lse_d = orc.attention_f64(q, k, v, 0.6, causal)
+        assert np.allclose(o, pack(o_d), rtol=0, atol=1e-15)
+        assert np.allclose(lse, lse_d.transpose(1, 0, 2).reshape(H, -1), rtol=0, atol=1e-15)
+
+
+def pin_varlen_brute_force(orc):
+    """Ragged lengths (including a sequence with no query and one with no key)
+    against per-element loops run sequence by sequence, head by head."""
+    rng = np.random.default_rng(18)
+    lq = [3, 0, 1, 5, 2]
+    lk = [4, 2, 6, 3, 0]
+    H, d, dv = 2, 3, 2
+    cu_q = np.concatenate([[0], np.cumsum(lq)])
+    cu_k = np.concatenate([[0], np.cumsum(lk)])
+    q = rng.standard_normal((cu_q[-1], H, d))
+    k = rng.standard_normal((cu_k[-1], H, d))
+    v = rng.standard_normal((cu_k[-1], H, dv))
+    for causal, off_of in ((False, None), (True, lambda a, b: 0), ("bottom_right", lambda a, b: b - a)):
+        o, lse = orc.attention_varlen_f64(q, k, v, cu_q, cu_k, 0.7, causal)
+        for b in range(len(lq)):
+            for h in range(H):
+                qs = q[cu_q[b]:cu_q[b + 1], h].tolist()
+                ks = k[cu_k[b]:cu_k[b + 1], h].tolist()
+                vs = v[cu_k[b]:cu_k[b + 1], h].tolist()
+                if not qs:
+                    continue
+                if not ks:
+                    assert np.all(o[cu_q[b]:cu_q[b + 1], h] == 0)
+                    assert np.all(lse[h, cu_q[b]:cu_q[b + 1]] == -np.inf)
+                    continue
+                off = 0 if off_of is None else off_of(len(qs), len(ks))
+                ob, lb = _brute(qs, ks, vs, 0.7, off_of is not None, off)
+                assert np.allclose(o[cu_q[b]:cu_q[b + 1], h], np.array(ob), rtol=0, atol=1e-14)
+                lb = np.array(lb)
+                got = lse[h, cu_q[b]:cu_q[b + 1]]
+                assert np.array_equal(np.isinf(got), np.isinf(lb))
+                assert np.allclose(got[np.isfinite(lb)], lb[np.isfinite(lb)], rtol=0, atol=1e-14)
+
+
+def pin_varlen_independence(orc):
+    """Sequences do not see each other: changing one sequence's keys and values
+    leaves every other sequence's output unchanged, bit for bit."""
+    rng = np.random.default_rng(19)
+    cu_q = np.array([0, 4, 9, 12])
+    cu_k = np.array([0, 6, 8, 15])
+    q = rng.standard_normal((12, 2, 3))
+    k = rng.standard_normal((15, 2, 3))
+    v = rng.standard_normal((15, 2, 4))
+    o1, l1 = orc.attention_varlen_f64(q, k, v, cu_q, cu_k, 0.5, True)
+    k2, v2 = k.copy(), v.copy()
+    k2[6:8] += 3.0
+    v2[6:8] -= 1.0
+    o2, l2 = orc.attention_varlen_f64(q, k2, v2, cu_q, cu_k, 0.5, True)
+    keep = np.r_[0:4, 9:12]
+    assert np.array_equal(o1[keep], o2[keep]) and np.array_equal(l1[:, keep], l2[:, keep])
+    assert not np.allclose(o1[4:9], o2[4:9])
+
+
 ALL_PINS = [
     pin_split_example_block_states,
     pin_split_example_merge,
@@ -425,4 +496,7 @@ ALL_PINS = [
     pin_brute_force,
     pin_brute_force_bottom_right,
     pin_bottom_right_rows,
+    pin_varlen_equal_lengths,
+    pin_varlen_brute_force,
+    pin_varlen_independence,
 ]

@@ -26,6 +26,8 @@ MUTANTS = [
     ("mask flipped", "cols[None, :] > rows[:, None] + off", "cols[None, :] < rows[:, None] + off"),
     ("bottom-right offset sign", "return nk - nq", "return nq - nk"),
     ("bottom-right as top-left", "return nk - nq", "return 0"),
+    ("varlen keys of the next sequence", "k[k0:k1].transpose(1, 0, 2),", "k[k0:k1 + 1].transpose(1, 0, 2),"),
+    ("varlen values shifted", "v[k0:k1].transpose(1, 0, 2), scale, causal)", "v[k0 + 1:k1 + 1].transpose(1, 0, 2), scale, causal)"),
     ("lse sign", "lse = np.where(empty, NEG_INF, m_ref + np.log(l))",
      "lse = np.where(empty, NEG_INF, m_ref - np.log(l))"),
     ("lse drops max", "lse = np.where(empty, NEG_INF, m_ref + np.log(l))",
