@@ -21,6 +21,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import itertools
 import json
 import math
 import os
@@ -306,7 +307,37 @@ def extra_workloads(device, stream, reps: int = 20):
                     "combine_gbs": round(comb_bytes / ms_c / 1e6, 1)}
             out[name] = sweep
         del q, k, v, o, lse
+    out["varlen_causal"] = varlen_workload(device, stream, reps)
     return out
+
+
+def varlen_workload(device, stream, reps):
+    """Ragged batch: 16 packed sequences with seeded lengths in [512, 4096],
+    H=32, d=128, top-left causal; FLOPs 4*H*d times the visible pairs."""
+    import random
+
+    import torch
+
+    import exact_attention_80_gb300 as fa
+
+    rnd = random.Random(1007)
+    lens = [rnd.randint(512, 4096) for _ in range(16)]
+    H, d = 32, 128
+    total = sum(lens)
+    gen = torch.Generator(device=device).manual_seed(1007)
+    q = torch.randn((total, H, d), generator=gen, device=device).to(torch.bfloat16)
+    k = torch.randn((total, H, d), generator=gen, device=device).to(torch.bfloat16)
+    v = torch.randn((total, H, d), generator=gen, device=device).to(torch.bfloat16)
+    cu = torch.tensor([0] + list(itertools.accumulate(lens)), dtype=torch.int32, device=device)
+    o = torch.empty_like(q)
+    lse = torch.empty((H, total), device=device)
+    fn = lambda: fa.fa_fwd_varlen(q, k, v, o, lse, cu, cu, max(lens), True, stream=stream)  # noqa: E731
+    for _ in range(3):
+        fn()
+    ms = statistics.median(time_launches(fn, reps, stream))
+    flops = 4.0 * H * d * sum(n * (n + 1) / 2 for n in lens)
+    return {"tflops": round(flops / ms / 1e9, 1), "us": round(ms * 1e3, 1), "sequences": len(lens),
+            "tokens": total}
 
 
 def run_ours(args):

@@ -15,10 +15,11 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfa_gb300.so")
 
 FA_OK = 0
+FA_ERR_SEQLENS = 12
 STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_ALIGN", 3: "FA_ERR_SHAPE", 4: "FA_ERR_HEADDIM",
     5: "FA_ERR_SPLITS", 6: "FA_ERR_WORKSPACE", 7: "FA_ERR_CUDA", 8: "FA_ERR_TIMEOUT",
-    9: "FA_ERR_SCALE", 10: "FA_ERR_SCRATCH", 11: "FA_ERR_CAUSAL",
+    9: "FA_ERR_SCALE", 10: "FA_ERR_SCRATCH", 11: "FA_ERR_CAUSAL", 12: "FA_ERR_SEQLENS",
 }
 # Causal mask modes (include/fa.h): key j visible to query i iff j <= i (top-left)
 # or j <= i + Nk - Nq (bottom-right).
@@ -59,6 +60,8 @@ def load_library() -> ctypes.CDLL:
     lib.fa_fwd_splitkv.restype = i
     lib.fa_combine.argtypes = [vp, vp, vp, i, i, i, i, i, vp]
     lib.fa_combine.restype = i
+    lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_varlen.restype = i
     lib.fa_fwd_grid_ctas.argtypes = [i, i, i, i, i]
     lib.fa_fwd_grid_ctas.restype = ctypes.c_longlong
     lib.fa_device_status.argtypes = [vp, i]
@@ -129,6 +132,46 @@ def fa_fwd(q, k, v, o, lse, causal=False, scale: float | None = None, stream=Non
     st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
                                scale, causal_code(causal), _stream_handle(stream))
     _check(st, "fa_fwd")
+
+
+def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal=False,
+                  scale: float | None = None, stream=None):
+    """Forward over packed variable-length sequences: ``q``/``o`` bf16
+    [total_q, H, d], ``k``/``v`` bf16 [total_k, H, d], ``lse`` fp32 [H, total_q],
+    ``cu_seqlens_*`` int32 [B+1] on the device (include/fa.h, fa_fwd_varlen)."""
+    import torch
+
+    for t in (q, k, v, o):
+        if t.dtype != torch.bfloat16 or t.dim() != 3 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("q, k, v, o must be contiguous CUDA bf16 [tokens, H, d]")
+    for t in (cu_seqlens_q, cu_seqlens_k):
+        if t.dtype != torch.int32 or t.dim() != 1 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("cu_seqlens must be contiguous CUDA int32 [B+1]")
+    if lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
+        raise ValueError("lse must be contiguous CUDA fp32 [H, total_q]")
+    total_q, H, d = (int(x) for x in q.shape)
+    total_k = int(k.shape[0])
+    B = int(cu_seqlens_q.shape[0]) - 1
+    if int(cu_seqlens_k.shape[0]) != B + 1 or B < 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B+1 >= 2 entries")
+    scale = default_scale(d) if scale is None else float(scale)
+    st = load_library().fa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                                      _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), B, H, total_q,
+                                      total_k, int(max_seqlen_q), d, scale, causal_code(causal),
+                                      _stream_handle(stream))
+    _check(st, "fa_fwd_varlen")
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal=False,
+                     scale: float | None = None, stream=None):
+    """Allocate ``o`` [total_q, H, d] and ``lse`` [H, total_q] and run
+    :func:`fa_fwd_varlen`. Returns ``(o, lse)``."""
+    import torch
+
+    o = torch.empty_like(q)
+    lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, causal, scale, stream)
+    return o, lse
 
 
 def fa_splitkv_workspace_bytes(B: int, H: int, Nq: int, d: int, num_splits: int) -> int:

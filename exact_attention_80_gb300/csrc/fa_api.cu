@@ -91,13 +91,16 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // bf16 [BH][N][d] viewed as a 3-D tensor (d, N, BH); box = 64 columns x rows,
 // 128-byte swizzle; rows past N read as zeros.
-bool encode_rows_map(CUtensorMap* map, const void* base, int d, int N, int BH, int box_rows) {
+// 3-D bf16 map (d, rows, heads) with the given row and head strides in bytes,
+// box {64, box_rows, 1}, 128-byte swizzle.
+bool encode_map(CUtensorMap* map, const void* base, int d, long long rows, long long heads,
+                unsigned long long row_stride, unsigned long long head_stride, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                                static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                                static_cast<cuuint64_t>(heads)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride),
+                                   static_cast<cuuint64_t>(head_stride)};
     const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r =
@@ -105,6 +108,19 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int d, int N, int BH, i
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+// Dense [BH][N][d]: rows d*2 bytes apart, heads N*d*2.
+bool encode_rows_map(CUtensorMap* map, const void* base, int d, int N, int BH, int box_rows) {
+    return encode_map(map, base, d, N, BH, static_cast<unsigned long long>(d) * 2,
+                      static_cast<unsigned long long>(N) * d * 2, box_rows);
+}
+
+// Token-major packed [total][H][d] (variable-length batches): tokens H*d*2 bytes
+// apart, heads d*2.
+bool encode_tokens_map(CUtensorMap* map, const void* base, int d, int total, int H, int box_rows) {
+    return encode_map(map, base, d, total, H, static_cast<unsigned long long>(H) * d * 2,
+                      static_cast<unsigned long long>(d) * 2, box_rows);
 }
 
 bool valid_causal(int causal) {
@@ -130,10 +146,20 @@ long long grid_ctas(int B, int H, int Nq, int d, int num_splits) {
     return static_cast<long long>(B) * H * units * num_splits;
 }
 
+// Variable-length batch description (device cu arrays; see include/fa.h).
+struct Varlen {
+    const int* cu_q;
+    const int* cu_k;
+    int total_q, total_k;
+};
+
+// Dense: Q [B][H][Nq][d], K/V [B][H][Nk][d]. Varlen (vl != nullptr): token-major
+// packed sequences, Nq = max_seqlen_q, Nk = total_k, one work row per (b, h).
 fa_status launch_forward(const void* q, const void* k, const void* v, void* o, float* lse,
                          float* ws, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                          int num_splits, int split_mode, cudaStream_t stream,
-                         long long wait_limit = kDefaultWaitLimit, int withhold_q = 0) {
+                         long long wait_limit = kDefaultWaitLimit, int withhold_q = 0,
+                         const Varlen* vl = nullptr) {
     const FwdConfig c = fwd_config(d);
     const long long ctas = grid_ctas(B, H, Nq, d, num_splits);
     if (ctas < 1 || ctas > 0x7fffffffll) return FA_ERR_SHAPE;
@@ -141,11 +167,23 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
     const int BH = B * H;
-    if (!encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
-        !encode_rows_map(&p.tm_k, k, d, Nk, BH, c.bn) ||
-        !encode_rows_map(&p.tm_v, v, d, Nk, BH, c.bn))
-        return FA_ERR_CUDA;
-    if (!split_mode && !encode_rows_map(&p.tm_o, o, d, Nq, BH, 128)) return FA_ERR_CUDA;
+    if (vl) {
+        if (!encode_tokens_map(&p.tm_q, q, d, vl->total_q, H, 128) ||
+            !encode_tokens_map(&p.tm_k, k, d, vl->total_k, H, c.bn) ||
+            !encode_tokens_map(&p.tm_v, v, d, vl->total_k, H, c.bn))
+            return FA_ERR_CUDA;
+        p.varlen = 1;
+        p.H = H;
+        p.total_q = vl->total_q;
+        p.cu_q = vl->cu_q;
+        p.cu_k = vl->cu_k;
+    } else {
+        if (!encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
+            !encode_rows_map(&p.tm_k, k, d, Nk, BH, c.bn) ||
+            !encode_rows_map(&p.tm_v, v, d, Nk, BH, c.bn))
+            return FA_ERR_CUDA;
+        if (!split_mode && !encode_rows_map(&p.tm_o, o, d, Nq, BH, 128)) return FA_ERR_CUDA;
+    }
     p.o = o;
     p.lse = lse;
     if (split_mode) {
@@ -158,13 +196,14 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     p.Nq = Nq;
     p.Nk = Nk;
     p.causal = causal ? 1 : 0;
-    // Key j is visible to query row i iff j <= i + causal_off (top-left: 0;
-    // bottom-right: Nk - Nq).
-    p.causal_off = (causal == FA_CAUSAL_BOTTOM_RIGHT) ? Nk - Nq : 0;
+    // Bottom-right: key j visible to query row i iff j <= i + Nk - Nq of the
+    // sequence (the kernels take the offset per sequence).
+    p.causal_br = (causal == FA_CAUSAL_BOTTOM_RIGHT) ? 1 : 0;
     p.num_splits = num_splits;
     p.split_mode = split_mode;
     p.n_units = static_cast<int>(ctas / (static_cast<long long>(BH) * num_splits));
     const int kv_tiles = (Nk + c.bn - 1) / c.bn;
+    // (Varlen: one split; every sequence's key tiles fit in ceil(total_k / BN).)
     p.kv_tiles_per_split = (kv_tiles + num_splits - 1) / num_splits;
     // Heads per scheduling group: about one wave of CTAs (one CTA per SM).
     int sms = 0;
@@ -209,6 +248,26 @@ size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
         return 0;
     const size_t rows = static_cast<size_t>(B) * H * Nq;
     return static_cast<size_t>(num_splits) * rows * (static_cast<size_t>(d) + 2) * sizeof(float);
+}
+
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                        int total_q, int total_k, int max_seqlen_q, int d, float scale,
+                        int causal, cudaStream_t stream) {
+    fa_status s = fa::check_common(q, k, v, B, H, total_q, total_k, d, scale);
+    if (s != FA_OK) return s;
+    if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
+    if (!o || !lse || !cu_seqlens_q || !cu_seqlens_k) return FA_ERR_NULL;
+    if (!fa::aligned(o, 16) || !fa::aligned(lse, 4) || !fa::aligned(cu_seqlens_q, 4) ||
+        !fa::aligned(cu_seqlens_k, 4))
+        return FA_ERR_ALIGN;
+    if (max_seqlen_q < 1 || max_seqlen_q > total_q) return FA_ERR_SHAPE;
+    if (static_cast<long long>(total_q) * H * d > 0x7fffffffffffll ||
+        static_cast<long long>(total_k) * H * d > 0x7fffffffffffll)
+        return FA_ERR_SHAPE;
+    const fa::Varlen vl = {cu_seqlens_q, cu_seqlens_k, total_q, total_k};
+    return fa::launch_forward(q, k, v, o, lse, nullptr, B, H, max_seqlen_q, total_k, d, scale,
+                              causal, 1, 0, stream, fa::kDefaultWaitLimit, 0, &vl);
 }
 
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* workspace, int B,
@@ -273,7 +332,10 @@ fa_status fa_device_status(cudaStream_t stream, int clear) {
             return FA_ERR_CUDA;
         if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
     }
-    return host ? FA_ERR_TIMEOUT : FA_OK;
+    // Bounded waits that gave up take precedence; otherwise a rejected
+    // variable-length partition.
+    if (host & ~fa::kStatusBadSeqlens) return FA_ERR_TIMEOUT;
+    return host ? FA_ERR_SEQLENS : FA_OK;
 }
 
 const char* fa_status_string(fa_status status) {
@@ -292,6 +354,8 @@ const char* fa_status_string(fa_status status) {
             return "FA_ERR_SCRATCH: partial states exceed the library's static scratch buffer";
         case FA_ERR_CAUSAL:
             return "FA_ERR_CAUSAL: causal must be FA_CAUSAL_NONE, _TOP_LEFT or _BOTTOM_RIGHT";
+        case FA_ERR_SEQLENS:
+            return "FA_ERR_SEQLENS: cu_seqlens are not a valid partition (see fa_fwd_varlen)";
     }
     return "unknown fa_status";
 }

@@ -28,14 +28,29 @@ struct RingPos {
     }
 };
 
+// Where a query row's output goes: O row (in units of d elements) =
+// o_base + q * o_stride, LSE index = lse_base + q, for row q of the sequence;
+// split partials at (split * BH + bh) * Nq + q. Rows q >= len_q are not written.
+struct RowMap {
+    long long o_base;
+    long long lse_base;
+    int o_stride;
+    int len_q;
+};
+
 // Work owned by one CTA.
 template <int Q_TILES>
 struct Work {
-    int bh;        // batch * H + head
-    int q0;        // first query row of the unit
+    int bh;        // batch * H + head (work row)
+    int zq;        // head coordinate of the Q/K/V/O tensor maps (bh, or h for varlen)
+    int qbase;     // token of the sequence's first query row (0 unless varlen)
+    int kbase;     // token of the sequence's first key (0 unless varlen)
+    int q0;        // first query row of the unit, within the sequence
     int split;     // key split index (0 in plain mode)
-    int kv_tile0;  // first key tile of the split
-    int kv_end;    // exclusive key bound of the split (for masking)
+    int kv_tile0;  // first key tile of the split, within the sequence
+    int kv_end;    // exclusive key bound of the split (for masking), within the sequence
+    int causal_off;  // causal: key j visible to query row i iff j <= i + causal_off
+    RowMap rm;
     int n[Q_TILES];  // key tiles each query tile visits
     int nmax;
 };
@@ -58,21 +73,54 @@ __device__ __forceinline__ void compute_work(const FwdParams& p, long long lin, 
     const int unit = p.n_units - 1 - r / heads_here;
     w.bh = group * p.head_group + r % heads_here;
     w.q0 = unit * QT * kBM;
-    const int total_tiles = (p.Nk + BN - 1) / BN;
+    // The sequence's rows and keys: the whole head (dense), or the packed
+    // sequence b of a variable-length batch.
+    int len_q = p.Nq, len_k = p.Nk;
+    w.zq = w.bh;
+    w.qbase = 0;
+    w.kbase = 0;
+    w.rm.o_base = static_cast<long long>(w.bh) * p.Nq;
+    w.rm.lse_base = w.rm.o_base;
+    w.rm.o_stride = 1;
+    if (p.varlen) {
+        const int b = w.bh / p.H;
+        const int h = w.bh - b * p.H;
+        const int cq0 = p.cu_q[b], cq1 = p.cu_q[b + 1], ck0 = p.cu_k[b], ck1 = p.cu_k[b + 1];
+        const bool valid = 0 <= cq0 && cq0 <= cq1 && cq1 <= p.total_q && cq1 - cq0 <= p.Nq &&
+                           0 <= ck0 && ck0 <= ck1 && ck1 <= p.Nk;
+        if (!valid) {
+            // Nothing is read or written for a sequence whose offsets are broken.
+            if (threadIdx.x == 0) atomicOr(p.status, kStatusBadSeqlens);
+            len_q = 0;
+            len_k = 0;
+        } else {
+            len_q = cq1 - cq0;
+            len_k = ck1 - ck0;
+        }
+        w.zq = h;
+        w.qbase = valid ? cq0 : 0;
+        w.kbase = valid ? ck0 : 0;
+        w.rm.o_base = static_cast<long long>(w.qbase) * p.H + h;
+        w.rm.lse_base = static_cast<long long>(h) * p.total_q + w.qbase;
+        w.rm.o_stride = p.H;
+    }
+    w.rm.len_q = len_q;
+    w.causal_off = p.causal_br ? len_k - len_q : 0;
+    const int total_tiles = (len_k + BN - 1) / BN;
     const int t0 = min(w.split * p.kv_tiles_per_split, total_tiles);
     const int t1 = min(t0 + p.kv_tiles_per_split, total_tiles);
     w.kv_tile0 = t0;
-    w.kv_end = min(p.Nk, t1 * BN);
+    w.kv_end = min(len_k, t1 * BN);
     w.nmax = 0;
 #pragma unroll
     for (int t = 0; t < QT; ++t) {
         const int row0 = w.q0 + t * kBM;
         int n = 0;
-        if (row0 < p.Nq) {
+        if (row0 < len_q) {
             int end = t1;
             if (p.causal) {
                 // Keys up to the tile's last row + causal_off; none if that is < 0.
-                const int last_key = min(row0 + kBM - 1, p.Nq - 1) + p.causal_off;
+                const int last_key = min(row0 + kBM - 1, len_q - 1) + w.causal_off;
                 end = min(end, last_key < 0 ? 0 : last_key / BN + 1);
             }
             n = max(0, end - t0);
@@ -109,13 +157,14 @@ struct RowOut {
     bool row_ok;
     bool split;
     float f;  // plain: 1/l; split: move from the lazy reference m to m_true
-    size_t row_idx, part_idx;
+    size_t row_idx, lse_idx, part_idx;
     float m, m_true, l;
 
-    __device__ __forceinline__ RowOut(const FwdParams& p, int bh, int split_idx, int q_row, float m_,
-                                      float m_true_, float l_)
-        : row_ok(q_row < p.Nq), split(p.split_mode != 0), m(m_), m_true(m_true_), l(l_) {
-        row_idx = static_cast<size_t>(bh) * p.Nq + q_row;
+    __device__ __forceinline__ RowOut(const FwdParams& p, const RowMap& rm, int bh, int split_idx,
+                                      int q_row, float m_, float m_true_, float l_)
+        : row_ok(q_row < rm.len_q), split(p.split_mode != 0), m(m_), m_true(m_true_), l(l_) {
+        row_idx = static_cast<size_t>(rm.o_base + static_cast<long long>(q_row) * rm.o_stride);
+        lse_idx = static_cast<size_t>(rm.lse_base + q_row);
         part_idx = (static_cast<size_t>(split_idx) * p.BH + bh) * p.Nq + q_row;
         if (!split) f = (l > 0.f) ? 1.f / l : 0.f;
         else f = (l > 0.f && m != m_true) ? ex2(m - m_true) : 1.f;
@@ -159,7 +208,7 @@ struct RowOut {
         if (!row_ok) return;
         constexpr float kLn2 = 0.69314718055994530942f;
         if (!split) {
-            p.lse[row_idx] = (l > 0.f) ? (m + lg2(l)) * kLn2 : -INFINITY;
+            p.lse[lse_idx] = (l > 0.f) ? (m + lg2(l)) * kLn2 : -INFINITY;
         } else {
             p.ws_m[part_idx] = (l > 0.f) ? m_true * kLn2 : -INFINITY;
             p.ws_l[part_idx] = l * f;
@@ -170,9 +219,10 @@ struct RowOut {
 // Writes one query row's result from its TMEM accumulator row (lane address
 // tO, D fp32 columns; not read when n == 0), a chunk at a time.
 template <int D>
-__device__ __forceinline__ void write_row(const FwdParams& p, int bh, int split, int q_row, int n,
-                                          float m, float m_true, float l, uint32_t tO) {
-    const RowOut<D> out(p, bh, split, q_row, m, m_true, l);
+__device__ __forceinline__ void write_row(const FwdParams& p, const RowMap& rm, int bh, int split,
+                                          int q_row, int n, float m, float m_true, float l,
+                                          uint32_t tO) {
+    const RowOut<D> out(p, rm, bh, split, q_row, m, m_true, l);
 #pragma unroll 1
     for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -194,15 +244,17 @@ __device__ __forceinline__ void write_row(const FwdParams& p, int bh, int split,
 // finished, as every S MMA reading Q came before it) in the 128-byte-swizzled
 // layout a Q load through the same kind of tensor map produces, and the
 // group's first warp writes the tile with TMA tensor stores (rows past Nq are
-// clipped). `staged` is an mbarrier expecting one arrival per warp. Returns
-// false if the bounded wait for the staging ran out.
+// clipped). `bh` is the head coordinate of the O tensor map. `staged` is an
+// mbarrier expecting one arrival per warp. Returns false if the bounded wait
+// for the staging ran out. Dense layouts only: a packed variable-length
+// sequence's tile would spill into the next sequence's rows.
 template <int D>
-__device__ __forceinline__ bool store_tile_tma(const FwdParams& p, int bh, int q_row0, int r, int q_row,
-                                               float m, float m_true, float l, uint32_t tO,
-                                               uint32_t q_tile, uint32_t staged,
+__device__ __forceinline__ bool store_tile_tma(const FwdParams& p, const RowMap& rm, int bh, int q_row0,
+                                               int r, int q_row, float m, float m_true, float l,
+                                               uint32_t tO, uint32_t q_tile, uint32_t staged,
                                                volatile uint32_t* abort_flag) {
     const int lane = r & 31;
-    const RowOut<D> out(p, bh, 0, q_row, m, m_true, l);
+    const RowOut<D> out(p, rm, bh, 0, q_row, m, m_true, l);
     const uint32_t swz = static_cast<uint32_t>(r & 7);
 #pragma unroll 1
     for (int cc = 0; cc < D / 32; ++cc) {

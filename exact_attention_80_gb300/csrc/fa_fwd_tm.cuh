@@ -124,8 +124,6 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    Work<QT> w;
-    compute_work<QT, BN>(p, blockIdx.x, w);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < ST; ++s) {
@@ -161,6 +159,10 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
       // Control warpgroup. setmaxnreg sits inside each role's branch so that
       // the register allocator sees one limit per code path.
       if constexpr (L::REG_SPLIT) setmaxnreg_dec<L::CTRL_REGS>();
+      // The work record is derived inside each role, after its register limit
+      // is set, so that no role carries fields it does not use.
+      Work<QT> w;
+      compute_work<QT, BN>(p, blockIdx.x, w);
       if (warp == 0) {
         // ------------------------------------------------------------ producer
         // The whole warp runs the loop (uniform values); one elected lane issues.
@@ -175,7 +177,7 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128),
-                                    &p.tm_q, bar(L::BAR_QFULL + t), 64 * c, w.q0 + t * kBM, w.bh);
+                                    &p.tm_q, bar(L::BAR_QFULL + t), 64 * c, w.qbase + w.q0 + t * kBM, w.zq);
                 }
             };
             // Q_0, K_0, then Q_1: the first S can start after two tiles' bytes.
@@ -197,11 +199,11 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
                 if (leader) {
                     mbar_arrive_expect_tx(bar(L::BAR_KVFULL + pos.slot), L::SLOT_BYTES);
                     const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
-                    const int row = (w.kv_tile0 + kv) * BN;
+                    const int row = w.kbase + (w.kv_tile0 + kv) * BN;
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
-                                    bar(L::BAR_KVFULL + pos.slot), 64 * c, row, w.bh);
+                                    bar(L::BAR_KVFULL + pos.slot), 64 * c, row, w.zq);
                 }
                 issued = e + 1;
                 pos.advance();
@@ -368,6 +370,8 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
     } else {
         // ------------------------------------------------------------ softmax
         if constexpr (L::REG_SPLIT) setmaxnreg_inc<L::SOFTMAX_REGS>();
+        Work<QT> w;
+        compute_work<QT, BN>(p, blockIdx.x, w);
         const int t = (warp - 4) >> 2;
         const int quarter = warp & 3;  // TMEM lane quarter this warp may access
         const int r = quarter * 32 + lane;
@@ -403,11 +407,11 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             tmem_wait_ld();
 
             // Mask: keys past the split / sequence end, and (causal) keys after
-            // this row + causal_off. TMA zero-fills keys >= Nk, so they must
-            // become -inf.
+            // this row + causal_off. Keys past the sequence end are zero fill
+            // (or the next packed sequence's tokens), so they must become -inf.
             const int kv0 = (w.kv_tile0 + j) * BN;
             int valid = w.kv_end - kv0;
-            if (p.causal) valid = min(valid, q_row + p.causal_off - kv0 + 1);
+            if (p.causal) valid = min(valid, q_row + w.causal_off - kv0 + 1);
             if (valid < BN) {
 #pragma unroll
                 for (int c = 0; c < BN; ++c)
@@ -502,12 +506,12 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) tc_fence_after();
         }
-        if (ok && !p.split_mode && n > 0) {
+        if (ok && !p.split_mode && !p.varlen && n > 0) {
             // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA.
-            store_tile_tma<D>(p, w.bh, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
+            store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
                               sbase + L::Q_OFF + t * L::Q_TILE_BYTES, bar(L::BAR_OSTAGED + t), abort_flag);
         } else if (ok) {
-            write_row<D>(p, w.bh, w.split, q_row, n, m, m_true, l, tO);
+            write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m, m_true, l, tO);
         }
     }
 

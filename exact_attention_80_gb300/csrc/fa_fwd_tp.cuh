@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128),
-                                    &p.tm_q, bar(L::BAR_QFULL), 64 * c, w.q0 + t * kBM, w.bh);
+                                    &p.tm_q, bar(L::BAR_QFULL), 64 * c, w.qbase + w.q0 + t * kBM, w.zq);
                 }
             }
             // Entry e of the sequence: K_0; then for step j: K_{j+1} (if any), V_j.
@@ -215,11 +215,11 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
                 if (leader) {
                     mbar_arrive_expect_tx(bar(L::BAR_KVFULL + pos.slot), L::SLOT_BYTES);
                     const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
-                    const int row = (w.kv_tile0 + tile) * BN;
+                    const int row = w.kbase + (w.kv_tile0 + tile) * BN;
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
-                                    bar(L::BAR_KVFULL + pos.slot), 64 * c, row, w.bh);
+                                    bar(L::BAR_KVFULL + pos.slot), 64 * c, row, w.zq);
                 }
                 issued = e + 1;
                 pos.advance();
@@ -375,11 +375,11 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             tmem_wait_ld();
 
             // Mask: keys past the split / sequence end, and (causal) keys after
-            // this row + causal_off. TMA zero-fills keys >= Nk, so they must
-            // become -inf.
+            // this row + causal_off. Keys past the sequence end are zero fill
+            // (or the next packed sequence's tokens), so they must become -inf.
             const int kv0 = (w.kv_tile0 + j) * BN;
             int valid = w.kv_end - kv0;
-            if (p.causal) valid = min(valid, q_row + p.causal_off - kv0 + 1);
+            if (p.causal) valid = min(valid, q_row + w.causal_off - kv0 + 1);
             if (valid < BN) {
 #pragma unroll
                 for (int c = 0; c < BN; ++c)
@@ -477,12 +477,12 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) tc_fence_after();
         }
-        if (ok && !p.split_mode && n > 0) {
+        if (ok && !p.split_mode && !p.varlen && n > 0) {
             // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA.
-            store_tile_tma<D>(p, w.bh, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
+            store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
                               sbase + L::Q_OFF + t * L::Q_TILE_BYTES, bar(L::BAR_OSTAGED + t), abort_flag);
         } else if (ok) {
-            write_row<D>(p, w.bh, w.split, q_row, n, m, m_true, l, tO);
+            write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m, m_true, l, tO);
         }
     }
 

@@ -18,6 +18,9 @@ enum : unsigned {
     kStatusWaitP = 1u << 4,
     kStatusWaitO = 1u << 5,
     kStatusWaitDrain = 1u << 6,
+    // Not a wait: variable-length offsets that are not a valid partition
+    // (decreasing, past the token count, or longer than max_seqlen_q).
+    kStatusBadSeqlens = 1u << 7,
 };
 
 // Default bound of one wait, in SM clock cycles (~1 s at 2 GHz). Legitimate
@@ -35,8 +38,17 @@ struct FwdParams {
     float* ws_m;       // fp32 [S][B*H][Nq]
     float* ws_l;       // fp32 [S][B*H][Nq]
     int BH, Nq, Nk;
-    int causal;
-    int causal_off;          // causal: key j visible to query row i iff j <= i + causal_off
+    int causal;              // 1: causal mask
+    int causal_br;           // 1: bottom-right alignment (key j visible to query i iff
+                             //    j <= i + Nk - Nq of the sequence), 0: top-left
+    // Variable-length batches (varlen = 1): Q, K, V, O token-major [total][H][d]
+    // with sequence b at tokens cu_q[b] .. cu_q[b+1]-1 (keys: cu_k); LSE
+    // [H][total_q]. BH = B * H work rows; Nq = max_seqlen_q; Nk = total_k.
+    int varlen;
+    int H;
+    int total_q;
+    const int* cu_q;         // device int32 [B + 1]
+    const int* cu_k;
     int num_splits;          // 1 in plain mode
     int split_mode;          // 0: write O/LSE, 1: write partial (O, m, l)
     int n_units;             // query units of (tiles per CTA * 128) rows per head

@@ -17,6 +17,7 @@ Recipe (the workloads of the five benchmark configurations):
 
 from __future__ import annotations
 
+import itertools
 import math
 
 import torch
@@ -38,6 +39,20 @@ def make_qkv(B: int, H: int, Nq: int, Nk: int, d: int, seed: int,
                 rows = torch.randperm(Nk, generator=g)[:count]
                 k[b, h, rows] *= outlier_scale
     return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+def make_varlen(lq, lk, H: int, d: int, seed: int):
+    """Packed variable-length inputs: bf16 CPU tensors ``q [sum lq, H, d]``,
+    ``k``/``v [sum lk, H, d]`` (token-major, drawn N(0, 1) in the order Q, K, V
+    like :func:`make_qkv`) and int32 prefix offsets ``cu_q``, ``cu_k`` [B+1]."""
+    g = torch.Generator().manual_seed(int(seed))
+    tq, tk = int(sum(lq)), int(sum(lk))
+    q = torch.randn((tq, H, d), generator=g, dtype=torch.float32)
+    k = torch.randn((tk, H, d), generator=g, dtype=torch.float32)
+    v = torch.randn((tk, H, d), generator=g, dtype=torch.float32)
+    cu_q = torch.tensor([0] + list(itertools.accumulate(lq)), dtype=torch.int32)
+    cu_k = torch.tensor([0] + list(itertools.accumulate(lk)), dtype=torch.int32)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16), cu_q, cu_k
 
 
 def to_f64(t):

@@ -60,7 +60,8 @@ typedef enum {
     FA_ERR_TIMEOUT = 8,    /* a kernel gave up on a bounded wait (reported by fa_device_status) */
     FA_ERR_SCALE = 9,      /* scale is not finite or not > 0 */
     FA_ERR_SCRATCH = 10,   /* fa_fwd_splitkv_static: partial states exceed FA_STATIC_SCRATCH_BYTES */
-    FA_ERR_CAUSAL = 11     /* causal is not FA_CAUSAL_NONE, _TOP_LEFT or _BOTTOM_RIGHT */
+    FA_ERR_CAUSAL = 11,    /* causal is not FA_CAUSAL_NONE, _TOP_LEFT or _BOTTOM_RIGHT */
+    FA_ERR_SEQLENS = 12    /* fa_fwd_varlen: cu_seqlens not a valid partition (from fa_device_status) */
 } fa_status;
 
 #define FA_CAUSAL_NONE 0
@@ -125,6 +126,35 @@ fa_status fa_combine(const void* workspace, void* o, float* lse,
                      int B, int H, int Nq, int d, int num_splits, cudaStream_t stream);
 
 /*
+ * fa_fwd_varlen — fused forward over a batch of variable-length sequences held
+ * as one ragged, token-major packed tensor (the FA-3 page, "Inside
+ * FlashAttention-3：面向 Hopper 架构的 IO-Aware 精确注意力机制深度解析", section
+ * 7.2 "cuDNN 集成": variable-length sequences through ragged tensors).
+ *
+ *   q, o:  bf16 [total_q][H][d]      k, v: bf16 [total_k][H][d]
+ *   lse:   fp32 [H][total_q]
+ *   cu_seqlens_q, cu_seqlens_k: DEVICE int32 [B + 1]; sequence b owns query
+ *   tokens cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and key tokens
+ *   cu_seqlens_k[b] .. cu_seqlens_k[b+1]-1. Required: cu[0] >= 0,
+ *   nondecreasing, cu_seqlens_q[B] <= total_q, cu_seqlens_k[B] <= total_k, and
+ *   every query length <= max_seqlen_q.
+ *
+ * Each sequence is its own attention problem: its queries see only its keys,
+ * and the causal mask (top-left or bottom-right) is placed by its own lengths.
+ * Sequences may be empty; queries with no key get O = 0, LSE = -inf. Tokens
+ * past cu_seqlens_q[B] are not written. Offsets that break the requirements
+ * are found on the device: that sequence is neither read nor written and
+ * fa_device_status later reports FA_ERR_SEQLENS. Host checks: pointers
+ * (cu arrays 4-byte aligned), 1 <= max_seqlen_q <= total_q, causal, d, scale.
+ * Launches ceil(max_seqlen_q / 256) (d <= 128; 128 for d = 256) query units per
+ * (sequence, head); units past a sequence's end exit at once.
+ */
+fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse,
+                        const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int H,
+                        int total_q, int total_k, int max_seqlen_q, int d, float scale,
+                        int causal, cudaStream_t stream);
+
+/*
  * fa_fwd_grid_ctas — number of CTAs fa_fwd (num_splits = 1) or
  * fa_fwd_splitkv would launch for this shape: B * H * ceil(Nq / BM) * num_splits,
  * BM = 256 query rows per CTA for d <= 128 (two 128-row tiles) and 128 for
@@ -136,9 +166,10 @@ long long fa_fwd_grid_ctas(int B, int H, int Nq, int d, int num_splits);
 
 /*
  * fa_device_status — SYNCHRONISES `stream`, then reads the library's device
- * error word: FA_OK, or FA_ERR_TIMEOUT if any kernel since the last clear gave
- * up on a bounded wait (it then exits cleanly and leaves its outputs
- * undefined). `clear` != 0 resets the word. FA_ERR_CUDA if the read fails.
+ * error word: FA_OK; FA_ERR_TIMEOUT if any kernel since the last clear gave up
+ * on a bounded wait (it then exits cleanly and leaves its outputs undefined);
+ * else FA_ERR_SEQLENS if fa_fwd_varlen met offsets that are not a valid
+ * partition. `clear` != 0 resets the word. FA_ERR_CUDA if the read fails.
  */
 fa_status fa_device_status(cudaStream_t stream, int clear);
 

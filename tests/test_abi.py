@@ -37,7 +37,7 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     for want in ("fa_fwd", "fa_fwd_splitkv", "fa_combine", "fa_splitkv_workspace_bytes",
-                 "fa_status_string", "fa_fwd_grid_ctas", "fa_device_status"):
+                 "fa_status_string", "fa_fwd_grid_ctas", "fa_device_status", "fa_fwd_varlen"):
         assert want in names
 
 
@@ -95,6 +95,22 @@ def test_splitkv_rejects(lib, kw, code):
 def test_combine_rejects(lib, args, code):
     ws, o, lse, B, H, Nq, d, S = args
     assert lib.fa_combine(P(ws), P(o), P(lse), B, H, Nq, d, S, P(0)) == code
+
+
+def _varlen(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, cq=FAKE, ck=FAKE, B=2, H=1, tq=64,
+            tk=64, maxq=32, d=64, scale=0.125, causal=0):
+    return lib.fa_fwd_varlen(P(q), P(k), P(v), P(o), P(lse), P(cq), P(ck), B, H, tq, tk, maxq, d,
+                             scale, causal, P(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(cq=0), 1), (dict(ck=0), 1), (dict(o=0), 1), (dict(q=0), 1),
+    (dict(cq=FAKE + 2), 2), (dict(ck=FAKE + 1), 2), (dict(o=FAKE + 8), 2),
+    (dict(maxq=0), 3), (dict(maxq=65), 3), (dict(tq=0), 3), (dict(B=0), 3),
+    (dict(d=96), 4), (dict(scale=0.0), 9), (dict(causal=4), 11),
+])
+def test_varlen_rejects(lib, kw, code):
+    assert _varlen(lib, **kw) == code
 
 
 def test_workspace_bytes(lib):
