@@ -100,7 +100,7 @@ size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
 /*
  * fa_fwd_splitkv — split-KV forward: writes partial states, no final output.
  * Split axis: keys. With T = ceil(Nk / BN) key tiles (BN = 128 keys for
- * d <= 128, 64 for d = 256) and P = ceil(T / num_splits), split s owns key tiles
+ * d <= 128, 96 for d = 256) and P = ceil(T / num_splits), split s owns key tiles
  * [s*P, min((s+1)*P, T)). Trailing splits may be empty; an empty split (or a
  * row whose keys in that split are all masked) writes m = -inf, l = 0, O = 0
  * (same section, subsection "扩展验证组合": the empty-tail rule; the true key

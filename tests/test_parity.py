@@ -144,7 +144,7 @@ def test_split_partials_match_oracle_states(d):
     """Each split's (m, l, O) workspace entries against the oracle's partial
     state over the same key range (documented split rule in include/fa.h)."""
     B, H, Nq, Nk, S = 1, 2, 130, 1100, 4
-    bn = 64 if d == 256 else 128  # keys per KV tile (include/fa.h, fa_fwd_splitkv)
+    bn = 96 if d == 256 else 128  # keys per KV tile (include/fa.h, fa_fwd_splitkv)
     q, k, v = make_qkv(B, H, Nq, Nk, d, 5 + d)
     scale = f32(1.0 / math.sqrt(d))
     for causal in (False, True):
