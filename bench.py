@@ -242,11 +242,19 @@ def oracle_sample(cfg: dict, budget_s: float, seed: int, max_heads: int | None =
 
 # ------------------------------------------------------------------ our arm
 
-def time_launches(fn, steps: int, stream):
-    """CUDA events bracketing every step on `stream`; returns per-step ms."""
+def time_launches(fn, steps: int, stream, queue_ahead: bool = False):
+    """CUDA events bracketing every step on `stream`; returns per-step ms.
+
+    With ``queue_ahead`` the stream first runs a device-side sleep long enough
+    for the host to enqueue every step, so kernels shorter than the host's
+    launch time run back to back and the events time the device work, not the
+    gaps between launches."""
     import torch
 
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    if queue_ahead:
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(200_000 * steps)  # ~0.1 ms of SM cycles per step
     evs[0].record(stream)
     for i in range(steps):
         fn()
@@ -283,11 +291,14 @@ def extra_workloads(device, stream, reps: int = 20):
             fn = lambda: fa.fa_fwd(q, k, v, o, lse, causal, stream=stream)  # noqa: E731
             for _ in range(3):
                 fn()
-            ms = statistics.median(time_launches(fn, reps, stream))
+            ms = statistics.median(time_launches(fn, reps, stream, queue_ahead=True))
             out[name] = {"tflops": round(flops / ms / 1e9, 1), "us": round(ms * 1e3, 1)}
         else:
             sweep = {}
-            for S in (1, 2, 3, 4, 16, 64):
+            # The printed split counts, plus the one that gives one CTA per SM.
+            sms = torch.cuda.get_device_properties(device).multi_processor_count
+            fill = max(1, min(fa.FA_MAX_SPLITS, sms // fa.fa_fwd_grid_ctas(B, H, Nq, d, 1)))
+            for S in sorted({1, 2, 3, 4, 16, 64, fill}):
                 ws = torch.empty(fa.fa_splitkv_workspace_bytes(B, H, Nq, d, S) // 4,
                                  device=device)
                 f_split = lambda: fa.fa_fwd_splitkv(q, k, v, ws, S, causal, stream=stream)  # noqa
@@ -295,8 +306,8 @@ def extra_workloads(device, stream, reps: int = 20):
                 for _ in range(3):
                     f_split()
                     f_comb()
-                ms_s = statistics.median(time_launches(f_split, reps, stream))
-                ms_c = statistics.median(time_launches(f_comb, reps, stream))
+                ms_s = statistics.median(time_launches(f_split, reps, stream, queue_ahead=True))
+                ms_c = statistics.median(time_launches(f_comb, reps, stream, queue_ahead=True))
                 kv_bytes = 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2
                 part = S * B * H * Nq * (d + 2) * 4
                 comb_bytes = part + B * H * Nq * (d * 2 + 4)
@@ -334,7 +345,7 @@ def varlen_workload(device, stream, reps):
     fn = lambda: fa.fa_fwd_varlen(q, k, v, o, lse, cu, cu, max(lens), True, stream=stream)  # noqa: E731
     for _ in range(3):
         fn()
-    ms = statistics.median(time_launches(fn, reps, stream))
+    ms = statistics.median(time_launches(fn, reps, stream, queue_ahead=True))
     flops = 4.0 * H * d * sum(n * (n + 1) / 2 for n in lens)
     return {"tflops": round(flops / ms / 1e9, 1), "us": round(ms * 1e3, 1), "sequences": len(lens),
             "tokens": total}

@@ -1,18 +1,23 @@
-// fa_combine.cu — merge of split-KV partial states, one warp per query row.
+// fa_combine.cu — merge of split-KV partial states.
 //
 // Merge operator ("AI 大模型之 FlashAttention_02", section "工程实操 沿键切分的
 // 归约与沿查询切分的区别", steps 2-3): with M = max_s m_s and w_s = exp(m_s - M),
 //   L = sum_s w_s l_s,   O = (sum_s w_s O_s) / L,   LSE = M + ln L.
 // Splits with m_s = -inf (empty, or every key masked) get weight 0.
-// HBM-bound: each row reads num_splits * (d + 2) floats and writes d bf16 + 1
-// float; a warp reads one split's d floats as one contiguous 4*d-byte segment.
+//
+// HBM-bound, and short: at decode shapes the whole workspace is a few MB, so
+// the kernel is one round of loads if every load is in flight at once. W warps
+// share a row (W = 1, 2, 4 or 8, from the split count); warp w takes splits
+// w, w + W, ... in batches of up to 16 partial rows, whose loads all go out
+// before the weights are known. Each lane owns d/32 consecutive columns, so a
+// warp reads a split's row as one contiguous 4d-byte segment. With W > 1 the
+// warps' sums meet in shared memory; every warp computes the same M, so no
+// rescaling is needed there.
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
 
 namespace fa {
-
-constexpr int kCombineWarps = 8;
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -26,88 +31,190 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kCombineWarps * 32)
+struct CombineShape {
+    static constexpr int PER = D / 32;                     // columns per lane: 2, 4, 8
+    static constexpr int BATCH = PER >= 8 ? 8 : 16;        // partial rows in flight per warp
+    static constexpr int MAX_WARPS = 8;                    // warps per row, at most
+};
+
+// One lane's PER consecutive floats of a partial row.
+template <int PER>
+__device__ __forceinline__ void load_cols(float* x, const float* src) {
+    if constexpr (PER == 2) {
+        const float2 a = *reinterpret_cast<const float2*>(src);
+        x[0] = a.x;
+        x[1] = a.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < PER; i += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(src + i);
+            x[i] = a.x;
+            x[i + 1] = a.y;
+            x[i + 2] = a.z;
+            x[i + 3] = a.w;
+        }
+    }
+}
+
+// Block: rows_per_block rows x W warps; warp = r * W + wi.
+template <int D>
+__global__ void __launch_bounds__(256)
     fa_combine_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_m,
                       const float* __restrict__ ws_l, __nv_bfloat16* __restrict__ o,
-                      float* __restrict__ lse, long long rows, int num_splits) {
-    constexpr int PER = D / 32;  // output elements per lane: 2, 4 or 8
-    const long long row = static_cast<long long>(blockIdx.x) * kCombineWarps + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (row >= rows) return;
+                      float* __restrict__ lse, long long rows, int num_splits, int W) {
+    using Sh = CombineShape<D>;
+    constexpr int PER = Sh::PER, BATCH = Sh::BATCH;
+    __shared__ float part[Sh::MAX_WARPS][D];
+    __shared__ float part_l[Sh::MAX_WARPS];
 
-    float big_m = -INFINITY;
-    for (int s = lane; s < num_splits; s += 32) big_m = fmaxf(big_m, ws_m[s * rows + row]);
-    big_m = warp_max(big_m);
-    const float ref = (big_m == -INFINITY) ? 0.f : big_m;
+    const int S = num_splits;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rows_per_block = (blockDim.x >> 5) / W;
+    const int r = warp / W, wi = warp % W;
+    const long long row = static_cast<long long>(blockIdx.x) * rows_per_block + r;
+    const bool live = row < rows;
+    // Splits of this warp: s = wi + W * i, i < n.
+    const int n = wi < S ? (S - wi + W - 1) / W : 0;
+    const float* col = ws_o + static_cast<size_t>(row) * D + lane * PER;
+    const size_t split_stride = static_cast<size_t>(rows) * D;
 
-    float big_l = 0.f;
-    for (int s = lane; s < num_splits; s += 32) {
-        const float ms = ws_m[s * rows + row];
-        if (ms != -INFINITY) big_l += expf(ms - ref) * ws_l[s * rows + row];
-    }
-    big_l = warp_sum(big_l);
+    float x[BATCH][PER];
+    auto load_batch = [&](int b0) {
+#pragma unroll
+        for (int i = 0; i < BATCH; ++i) {
+            if (live && b0 + i < n) {
+                load_cols<PER>(x[i], col + static_cast<size_t>(wi + W * (b0 + i)) * split_stride);
+            } else {
+#pragma unroll
+                for (int e = 0; e < PER; ++e) x[i][e] = 0.f;
+            }
+        }
+    };
+    // The first batch goes out before the max pass, which it does not need.
+    load_batch(0);
+
+    float mx = -INFINITY;
+    if (live)
+        for (int s = lane; s < S; s += 32) mx = fmaxf(mx, ws_m[static_cast<size_t>(s) * rows + row]);
+    mx = warp_max(mx);
+    const float ref = (mx == -INFINITY) ? 0.f : mx;
 
     float acc[PER];
 #pragma unroll
-    for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-#pragma unroll 4
-    for (int s = 0; s < num_splits; ++s) {
-        const float ms = ws_m[s * rows + row];  // same address in every lane: one broadcast
-        if (ms == -INFINITY) continue;
-        const float w = expf(ms - ref);
-        const float* src = ws_o + (static_cast<size_t>(s) * rows + row) * D + lane * PER;
-        if constexpr (PER == 2) {
-            const float2 x = *reinterpret_cast<const float2*>(src);
-            acc[0] = fmaf(w, x.x, acc[0]);
-            acc[1] = fmaf(w, x.y, acc[1]);
-        } else {
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float lsum = 0.f;  // this lane's share of sum_s w_s l_s
+    for (int b0 = 0; b0 < n; b0 += BATCH) {
+        if (b0 > 0) load_batch(b0);
+        // Lane j holds the weight of the batch's j-th split.
+        float wj = 0.f;
+        if (live && lane < BATCH && b0 + lane < n) {
+            const size_t idx = static_cast<size_t>(wi + W * (b0 + lane)) * rows + row;
+            const float ms = ws_m[idx];
+            if (ms != -INFINITY) {
+                wj = expf(ms - ref);
+                lsum = fmaf(wj, ws_l[idx], lsum);
+            }
+        }
 #pragma unroll
-            for (int i = 0; i < PER; i += 4) {
-                const float4 x = *reinterpret_cast<const float4*>(src + i);
-                acc[i + 0] = fmaf(w, x.x, acc[i + 0]);
-                acc[i + 1] = fmaf(w, x.y, acc[i + 1]);
-                acc[i + 2] = fmaf(w, x.z, acc[i + 2]);
-                acc[i + 3] = fmaf(w, x.w, acc[i + 3]);
+        for (int i = 0; i < BATCH; ++i) {
+            const float w = __shfl_sync(0xffffffffu, wj, i);
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, x[i][e], acc[e]);
+        }
+    }
+    lsum = warp_sum(lsum);
+
+    if (W > 1) {  // the same for every thread of the launch
+#pragma unroll
+        for (int e = 0; e < PER; ++e) part[warp][lane * PER + e] = acc[e];
+        if (lane == 0) part_l[warp] = lsum;
+        __syncthreads();
+        if (wi == 0) {
+            for (int k = 1; k < W; ++k) {
+#pragma unroll
+                for (int e = 0; e < PER; ++e) acc[e] += part[warp + k][lane * PER + e];
+                lsum += part_l[warp + k];
             }
         }
     }
-    const float inv = (big_l > 0.f) ? 1.f / big_l : 0.f;
-    __nv_bfloat162 packed[PER / 2];
+    if (wi == 0 && live) {
+        const float inv = (lsum > 0.f) ? 1.f / lsum : 0.f;
+        __nv_bfloat162 packed[PER / 2];
 #pragma unroll
-    for (int i = 0; i < PER / 2; ++i)
-        packed[i] = __floats2bfloat162_rn(acc[2 * i] * inv, acc[2 * i + 1] * inv);
-    __nv_bfloat16* dst = o + static_cast<size_t>(row) * D + lane * PER;
-    if constexpr (PER == 2) {
-        *reinterpret_cast<__nv_bfloat162*>(dst) = packed[0];
-    } else if constexpr (PER == 4) {
-        *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(packed);
-    } else {
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(packed);
+        for (int e = 0; e < PER / 2; ++e)
+            packed[e] = __floats2bfloat162_rn(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+        __nv_bfloat16* dst = o + static_cast<size_t>(row) * D + lane * PER;
+        if constexpr (PER == 2) {
+            *reinterpret_cast<__nv_bfloat162*>(dst) = packed[0];
+        } else if constexpr (PER == 4) {
+            *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(packed);
+        } else {
+            *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(packed);
+        }
+        if (lane == 0) lse[row] = (lsum > 0.f) ? ref + logf(lsum) : -INFINITY;
     }
-    if (lane == 0) lse[row] = (big_l > 0.f) ? ref + logf(big_l) : -INFINITY;
+}
+
+// Blocks of this kernel the whole GPU holds at once at `threads` threads per
+// block (per-SM occupancy x SMs), queried once per device and block size.
+// Concurrent first calls may both query; they store the same value.
+template <int D>
+int combine_resident_blocks(int threads) {
+    static int cache[64][2];  // [device][threads == 256]
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    int& slot = cache[dev][threads == 256 ? 1 : 0];
+    if (slot == 0) {
+        int per_sm = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fa_combine_kernel<D>, threads, 0) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 1;
+        slot = (per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
+    }
+    return slot;
+}
+
+// Warps per row W (1, 2, 4 or 8): enough batches to cover the splits in one
+// round, unless that many warps per row would not let every row be resident
+// at once; then fewer warps, each taking several rounds of loads. Blocks hold
+// four warps (four rows at W = 1) or, at W = 8, eight.
+template <int D>
+cudaError_t launch_combine_d(const float* ws_o, const float* ws_m, const float* ws_l,
+                             __nv_bfloat16* o, float* lse, long long rows, int num_splits,
+                             cudaStream_t stream) {
+    using Sh = CombineShape<D>;
+    const int rounds = (num_splits + Sh::BATCH - 1) / Sh::BATCH;
+    int W = 1;
+    while (W < rounds && W < Sh::MAX_WARPS) W <<= 1;
+    auto blocks_for = [rows](int w) {
+        const int per_block = (w > 4 ? w : 4) / w;
+        return (rows + per_block - 1) / per_block;
+    };
+    while (W > 1 && blocks_for(W) > combine_resident_blocks<D>(W > 4 ? W * 32 : 128)) W >>= 1;
+    const int warps = W > 4 ? W : 4;
+    const long long blocks = blocks_for(W);
+    if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(warps * 32), 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, fa_combine_kernel<D>, ws_o, ws_m, ws_l, o, lse, rows,
+                              num_splits, W);
 }
 
 cudaError_t launch_combine(const float* ws_o, const float* ws_m, const float* ws_l, void* o,
                            float* lse, long long rows, int num_splits, int d,
                            cudaStream_t stream) {
-    const long long blocks = (rows + kCombineWarps - 1) / kCombineWarps;
-    if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
-    cfg.blockDim = dim3(kCombineWarps * 32, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
     auto* out = static_cast<__nv_bfloat16*>(o);
     switch (d) {
         case 64:
-            return cudaLaunchKernelEx(&cfg, fa_combine_kernel<64>, ws_o, ws_m, ws_l, out, lse, rows,
-                                      num_splits);
+            return launch_combine_d<64>(ws_o, ws_m, ws_l, out, lse, rows, num_splits, stream);
         case 128:
-            return cudaLaunchKernelEx(&cfg, fa_combine_kernel<128>, ws_o, ws_m, ws_l, out, lse,
-                                      rows, num_splits);
+            return launch_combine_d<128>(ws_o, ws_m, ws_l, out, lse, rows, num_splits, stream);
         case 256:
-            return cudaLaunchKernelEx(&cfg, fa_combine_kernel<256>, ws_o, ws_m, ws_l, out, lse,
-                                      rows, num_splits);
+            return launch_combine_d<256>(ws_o, ws_m, ws_l, out, lse, rows, num_splits, stream);
         default:
             return cudaErrorInvalidValue;
     }

@@ -221,6 +221,39 @@ def test_combine_of_oracle_partials(d):
     check(o[0], lse[0], o_ref, lse_ref, "combine")
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("S", [1, 3, 7, 33, 100, 256])
+def test_combine_split_counts(d, S):
+    """fa_combine over split counts from 1 to the maximum (256), fed oracle
+    partial states of contiguous key ranges, some of them empty; 2 x 37 rows,
+    so the last block of rows is ragged."""
+    rng = np.random.default_rng(1000 * d + S)
+    BH, Nq, Nk = 2, 37, 300
+    q = rng.standard_normal((BH, Nq, d))
+    k = rng.standard_normal((BH, Nk, d))
+    v = rng.standard_normal((BH, Nk, d))
+    cuts = np.sort(rng.integers(0, Nk + 1, size=S - 1))
+    edges = [0, *cuts.tolist(), Nk]
+    bounds = [(edges[s], edges[s + 1]) for s in range(S)]
+    ws = np.zeros((S * BH * Nq * (d + 2),), dtype=np.float32)
+    wo = ws[: S * BH * Nq * d].reshape(S, BH, Nq, d)
+    wm = ws[S * BH * Nq * d: S * BH * Nq * (d + 1)].reshape(S, BH, Nq)
+    wl = ws[S * BH * Nq * (d + 1):].reshape(S, BH, Nq)
+    o_ref = np.zeros((BH, Nq, d))
+    lse_ref = np.zeros((BH, Nq))
+    for h in range(BH):
+        s_full = oracle.scores_f64(q[h], k[h], 0.08, False)
+        states = oracle.split_states_f64(s_full, v[h], bounds)
+        for s, (m, l, u) in enumerate(states):
+            wm[s, h], wl[s, h], wo[s, h] = m, l, u
+        o_ref[h], lse_ref[h] = oracle.merge_states_f64(states)
+    o = torch.empty(1, BH, Nq, d, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(1, BH, Nq, dtype=torch.float32, device="cuda")
+    fa.fa_combine(torch.from_numpy(ws).cuda(), o, lse, 1, BH, Nq, d, S)
+    torch.cuda.synchronize()
+    check(o[0], lse[0], o_ref, lse_ref, f"combine S={S}")
+
+
 @pytest.mark.parametrize("causal", [False, True, "bottom_right"])
 def test_split_invariance(causal):
     """Output semantics do not change with the split count (FA-2 page, split
