@@ -16,12 +16,17 @@ Pages this oracle follows (cited by title and section):
 * The FA-3 page, section 7.2 "cuDNN 集成" — variable-length sequences as
   ragged tensors (``attention_varlen_f64``: one attention problem per packed
   sequence).
+* The FA-3 page, section 7.3 "BF16 / FP8 支持" — e4m3 inputs with fp32
+  statistics (``oracle.fp8``: the attention of the encoded values, an e4m3
+  decoder written from the format's bit fields, and the size of the error that
+  rounding P to e4m3 adds).
 * "AI 大模型之 FlashAttention_02" (the FA-2 page), section 3.1 and 4.1 — exact
   softmax attention, O(S²d); section "工程实操 沿键切分的归约与沿查询切分的区别" —
   split partial states (m, l, u) and the merge that rescales by exp(m_b − M).
 
 Every function is pinned by ``tests/test_oracle.py`` against values printed on
-the pages, closed forms, invariants, a library routine and brute force.
+the pages, closed forms, invariants, a library routine, brute force and (for
+the e4m3 error scale) a simulation of the error model it states.
 """
 
 from .attention import (  # noqa: F401
@@ -34,3 +39,4 @@ from .attention import (  # noqa: F401
     merge_states_f64,
     normalise_then_average_f64,
 )
+from . import fp8  # noqa: F401,E402

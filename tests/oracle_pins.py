@@ -476,6 +476,112 @@ def pin_varlen_independence(orc):
     assert not np.allclose(o1[4:9], o2[4:9])
 
 
+
+# --------------------------------------------------------------------------
+# FP8 (e4m3) inputs: the decoder, the attention of the encoded values, and the
+# size of the error that rounding P to e4m3 adds (module ``oracle.fp8``).
+# --------------------------------------------------------------------------
+
+def pin_e4m3_hand_values(f8):
+    """Codes whose values follow from the E4M3 bit fields by hand: sign,
+    exponent bias 7, subnormals m/8 * 2^-6, no infinities, NaN only at
+    S.1111.111 (so 0x7E = 1.75 * 2^8 = 448 is the largest finite value)."""
+    want = {0x00: 0.0, 0x38: 1.0, 0x40: 2.0, 0x3C: 1.5, 0x30: 0.5, 0xB8: -1.0,
+            0x7E: 448.0, 0xFE: -448.0, 0x78: 256.0, 0x77: 240.0, 0x01: 2.0 ** -9,
+            0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x0F: 1.875 * 2.0 ** -6}
+    got = f8.e4m3_decode(np.array(list(want), dtype=np.uint8))
+    assert np.array_equal(got, np.array(list(want.values()))), got
+    assert np.isnan(f8.e4m3_decode(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+    assert np.signbit(f8.e4m3_decode(np.array([0x80], dtype=np.uint8))[0])
+
+
+def pin_e4m3_vs_torch(f8):
+    """All 256 codes against torch's float8_e4m3fn conversion (an independent
+    library implementation of the same format)."""
+    import torch
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = f8.e4m3_decode(codes.numpy())
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+
+
+def _codes(rng, shape, scale):
+    """e4m3 codes of N(0,1) * scale values (rounded by torch, saturating)."""
+    import torch
+    x = torch.from_numpy(rng.standard_normal(shape) * scale)
+    return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def pin_fp8_single_key(f8):
+    """Nk = 1: O is the single value row, LSE its scaled score (exact)."""
+    rng = np.random.default_rng(31)
+    q8, k8, v8 = _codes(rng, (3, 1, 8), 16), _codes(rng, (3, 1, 8), 16), _codes(rng, (3, 1, 8), 16)
+    o, lse = f8.attention_fp8_f64(q8, k8, v8, 0.25, 0.125, 0.5, 0.3)
+    q = f8.e4m3_decode(q8) * 0.25
+    k = f8.e4m3_decode(k8) * 0.125
+    v = f8.e4m3_decode(v8) * 0.5
+    assert np.allclose(o, v, rtol=0, atol=1e-15)
+    assert np.allclose(lse[..., 0], 0.3 * (q * k).sum(-1)[..., 0], rtol=1e-14, atol=1e-14)
+
+
+def pin_fp8_descales(f8):
+    """The Q and K descales multiply the scores (the same as scaling ``scale``),
+    and the V descale multiplies O and leaves LSE alone."""
+    rng = np.random.default_rng(37)
+    q8, k8, v8 = (_codes(rng, (2, 9, 16), 8) for _ in range(3))
+    o1, l1 = f8.attention_fp8_f64(q8, k8, v8, 0.5, 0.25, 1.0, 0.2, True)
+    o2, l2 = f8.attention_fp8_f64(q8, k8, v8, 1.0, 1.0, 1.0, 0.025, True)
+    o3, l3 = f8.attention_fp8_f64(q8, k8, v8, 0.5, 0.25, 3.0, 0.2, True)
+    assert np.allclose(o1, o2, rtol=1e-12, atol=1e-12) and np.allclose(l1, l2, rtol=1e-12, atol=1e-12)
+    assert np.allclose(o3, 3.0 * o1, rtol=1e-12, atol=1e-12) and np.array_equal(l3, l1)
+
+
+def pin_p_sigma_closed_forms(f8):
+    """One key: p = 1 (normal), sigma = 2^-4/sqrt(3) |v|. Two keys with equal
+    scores: p = (1, 1), l = 2, sigma = 2^-4/sqrt(3) sqrt(v1^2 + v2^2) / 2."""
+    h = 2.0 ** -4 / math.sqrt(3.0)
+    one = np.array([[[0x38]]], dtype=np.uint8)
+    v8 = np.array([[[0x40, 0xC4]]], dtype=np.uint8)  # 2.0, -3.0
+    sig = f8.p_rounding_sigma(one, one, v8, 1.0, 1.0, 1.0, 1.0)
+    assert np.allclose(sig, h * np.array([[[2.0, 3.0]]]), rtol=1e-14, atol=0)
+    k8 = np.array([[[0x38], [0x38]]], dtype=np.uint8)
+    v8 = np.array([[[0x40], [0x44]]], dtype=np.uint8)  # 2.0, 3.0
+    sig = f8.p_rounding_sigma(one, k8, v8, 1.0, 1.0, 1.0, 1.0)
+    assert np.allclose(sig, h * math.sqrt(4.0 + 9.0) / 2.0, rtol=1e-14, atol=0)
+
+
+def pin_p_sigma_simulated(f8):
+    """Against a simulation of the model it states: independent errors uniform
+    within half a step on every p_j (relative 2^-4 when p_j * 2^6 is normal,
+    absolute 2^-16 below), 4000 draws; the sample standard deviation of the
+    error in O agrees with sigma within 10 %."""
+    rng = np.random.default_rng(41)
+    q8, k8, v8 = _codes(rng, (1, 3, 8), 4), _codes(rng, (1, 40, 8), 4), _codes(rng, (1, 40, 8), 4)
+    sig = f8.p_rounding_sigma(q8, k8, v8, 1.0, 1.0, 1.0, 0.35)
+    q = f8.e4m3_decode(q8)[0]
+    k = f8.e4m3_decode(k8)[0]
+    v = f8.e4m3_decode(v8)[0]
+    s = 0.35 * q @ k.T
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    l = p.sum(axis=1, keepdims=True)
+    normal = p * 2.0 ** 6 >= 2.0 ** -6
+    half = np.where(normal, 2.0 ** -4 * p, 2.0 ** -16)
+    u = rng.uniform(-1.0, 1.0, size=(4000,) + p.shape)
+    err = np.einsum("tqk,kd->tqd", u * half, v) / l
+    assert np.allclose(err.std(axis=0), sig[0], rtol=0.1, atol=0)
+
+
+FP8_PINS = [
+    pin_e4m3_hand_values,
+    pin_e4m3_vs_torch,
+    pin_fp8_single_key,
+    pin_fp8_descales,
+    pin_p_sigma_closed_forms,
+    pin_p_sigma_simulated,
+]
+
 ALL_PINS = [
     pin_split_example_block_states,
     pin_split_example_merge,

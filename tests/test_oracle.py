@@ -6,9 +6,15 @@ Runs on CPU only.  Each pin is documented in ``tests/oracle_pins.py``.
 import pytest
 
 import oracle
-from oracle_pins import ALL_PINS
+import oracle.fp8
+from oracle_pins import ALL_PINS, FP8_PINS
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=[p.__name__ for p in ALL_PINS])
 def test_pin(pin):
     pin(oracle)
+
+
+@pytest.mark.parametrize("pin", FP8_PINS, ids=[p.__name__ for p in FP8_PINS])
+def test_fp8_pin(pin):
+    pin(oracle.fp8)

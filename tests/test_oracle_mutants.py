@@ -13,10 +13,11 @@ import warnings
 
 import pytest
 
-from oracle_pins import ALL_PINS
+from oracle_pins import ALL_PINS, FP8_PINS
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                    "oracle", "attention.py")
+SRC_FP8 = os.path.join(os.path.dirname(SRC), "fp8.py")
 
 MUTANTS = [
     ("dropped scale", "s = float(scale) * (q[rows] @ k.T)", "s = (q[rows] @ k.T)"),
@@ -67,5 +68,45 @@ def test_mutant_is_caught(name, find, repl):
         try:
             pin(mod)
         except Exception as e:  # AssertionError, or a crash from a broken shape
+            caught.append((pin.__name__, type(e).__name__))
+    assert caught, f"mutant '{name}' passed every pin"
+
+
+FP8_MUTANTS = [
+    ("exponent bias 6", "np.exp2(e - 7.0)", "np.exp2(e - 6.0)"),
+    ("subnormal scale 2^-7", "m / 8.0 * 2.0 ** -6", "m / 8.0 * 2.0 ** -7"),
+    ("no implicit one", "(1.0 + m / 8.0) * np.exp2(e - 7.0)", "(m / 8.0) * np.exp2(e - 7.0)"),
+    ("four mantissa bits", "(1.0 + m / 8.0)", "(1.0 + m / 16.0)"),
+    ("sign ignored", "sign = np.where((c >> 7) & 1, -1.0, 1.0)", "sign = 1.0"),
+    ("e5m2 fields", "e = (c >> 3) & 0xF", "e = (c >> 2) & 0x1F"),
+    ("top exponent as NaN", "(e == 15) & (m == 7)", "(e == 15)"),
+    ("q descale dropped", "q = e4m3_decode(q8) * float(q_descale)\n    k = e4m3_decode(k8) * float(k_descale)\n    v = e4m3_decode(v8) * float(v_descale)\n    return",
+     "q = e4m3_decode(q8)\n    k = e4m3_decode(k8) * float(k_descale)\n    v = e4m3_decode(v8) * float(v_descale)\n    return"),
+    ("v descale squared", "v = e4m3_decode(v8) * float(v_descale)\n    return", "v = e4m3_decode(v8) * float(v_descale) ** 2\n    return"),
+    ("sigma without the 1/3", "(E4M3_REL_HALF_ULP * p) ** 2 / 3.0", "(E4M3_REL_HALF_ULP * p) ** 2"),
+    ("sigma over l, not l^2", "/ np.where(l > 0, l, 1.0) ** 2", "/ np.where(l > 0, l, 1.0)"),
+    ("sigma relative to the max", "(E4M3_REL_HALF_ULP * p) ** 2 / 3.0", "(E4M3_REL_HALF_ULP * 1.0) ** 2 / 3.0"),
+]
+
+
+def _load_fp8_mutant(find, repl):
+    with open(SRC_FP8, encoding="utf-8") as f:
+        src = f.read()
+    assert src.count(find) == 1, f"mutation anchor not unique: {find!r}"
+    src = src.replace(find, repl).replace("from .attention import", "from oracle.attention import")
+    mod = types.ModuleType("oracle_fp8_mutant")
+    exec(compile(src, "oracle_fp8_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name,find,repl", FP8_MUTANTS, ids=[m[0] for m in FP8_MUTANTS])
+def test_fp8_mutant_is_caught(name, find, repl):
+    mod = _load_fp8_mutant(find, repl)
+    caught = []
+    warnings.simplefilter("ignore", RuntimeWarning)
+    for pin in FP8_PINS:
+        try:
+            pin(mod)
+        except Exception as e:
             caught.append((pin.__name__, type(e).__name__))
     assert caught, f"mutant '{name}' passed every pin"
