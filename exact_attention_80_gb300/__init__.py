@@ -62,6 +62,8 @@ def load_library() -> ctypes.CDLL:
     lib.fa_combine.restype = i
     lib.fa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, f, i, vp]
     lib.fa_fwd_varlen.restype = i
+    lib.fa_fwd_fp8.argtypes = [vp, vp, vp, f, f, f, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_fwd_fp8.restype = i
     lib.fa_fwd_grid_ctas.argtypes = [i, i, i, i, i]
     lib.fa_fwd_grid_ctas.restype = ctypes.c_longlong
     lib.fa_device_status.argtypes = [vp, i]
@@ -132,6 +134,47 @@ def fa_fwd(q, k, v, o, lse, causal=False, scale: float | None = None, stream=Non
     st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
                                scale, causal_code(causal), _stream_handle(stream))
     _check(st, "fa_fwd")
+
+
+def _bhnd8(q, k, v):
+    import torch
+
+    ok_types = (torch.uint8, torch.float8_e4m3fn)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype not in ok_types:
+            raise TypeError(f"{name} must hold e4m3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
+        if t.dim() != 4 or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor [B, H, N, d]")
+    B, H, Nq, d = q.shape
+    if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
+    return int(B), int(H), int(Nq), int(k.shape[2]), int(d)
+
+
+def fa_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, o, lse,
+               causal=False, scale: float | None = None, stream=None):
+    """Fused forward on e4m3 inputs (include/fa.h, fa_fwd_fp8): ``q``, ``k``, ``v``
+    hold e4m3 codes [B,H,N,d] (uint8 or float8_e4m3fn), the value of a code being
+    its e4m3 value times the tensor's descale; ``o`` bf16 [B,H,Nq,d] and ``lse``
+    fp32 [B,H,Nq] are written."""
+    B, H, Nq, Nk, d = _bhnd8(q, k, v)
+    scale = default_scale(d) if scale is None else float(scale)
+    st = load_library().fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), float(q_descale), float(k_descale),
+                                   float(v_descale), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, scale,
+                                   causal_code(causal), _stream_handle(stream))
+    _check(st, "fa_fwd_fp8")
+
+
+def attention_fp8(q, k, v, q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0,
+                  causal=False, scale: float | None = None, stream=None):
+    """Allocate bf16 ``o`` and fp32 ``lse`` and run :func:`fa_fwd_fp8`."""
+    import torch
+
+    B, H, Nq, Nk, d = _bhnd8(q, k, v)
+    o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    fa_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o, lse, causal, scale, stream)
+    return o, lse
 
 
 def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal=False,

@@ -93,18 +93,22 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 128-byte swizzle; rows past N read as zeros.
 // 3-D bf16 map (d, rows, heads) with the given row and head strides in bytes,
 // box {64, box_rows, 1}, 128-byte swizzle.
+// Elements are bf16, or single bytes (e4m3) when `bytes`; either way the box is
+// one 128-byte swizzle row wide (64 bf16 or 128 bytes).
 bool encode_map(CUtensorMap* map, const void* base, int d, long long rows, long long heads,
-                unsigned long long row_stride, unsigned long long head_stride, int box_rows) {
+                unsigned long long row_stride, unsigned long long head_stride, int box_rows,
+                bool bytes = false) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
                                 static_cast<cuuint64_t>(heads)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride),
                                    static_cast<cuuint64_t>(head_stride)};
-    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(box_rows), 1u};
+    const cuuint32_t box[3] = {bytes ? 128u : 64u, static_cast<cuuint32_t>(box_rows), 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r =
-        enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+        enc(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -114,6 +118,12 @@ bool encode_map(CUtensorMap* map, const void* base, int d, long long rows, long 
 bool encode_rows_map(CUtensorMap* map, const void* base, int d, int N, int BH, int box_rows) {
     return encode_map(map, base, d, N, BH, static_cast<unsigned long long>(d) * 2,
                       static_cast<unsigned long long>(N) * d * 2, box_rows);
+}
+
+// Dense e4m3 [BH][N][d]: rows d bytes apart, heads N*d.
+bool encode_rows_map8(CUtensorMap* map, const void* base, int d, int N, int BH, int box_rows) {
+    return encode_map(map, base, d, N, BH, static_cast<unsigned long long>(d),
+                      static_cast<unsigned long long>(N) * d, box_rows, true);
 }
 
 // Token-major packed [total][H][d] (variable-length batches): tokens H*d*2 bytes
@@ -159,7 +169,7 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
                          float* ws, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                          int num_splits, int split_mode, cudaStream_t stream,
                          long long wait_limit = kDefaultWaitLimit, int withhold_q = 0,
-                         const Varlen* vl = nullptr) {
+                         const Varlen* vl = nullptr, const float* f8_descale = nullptr) {
     const FwdConfig c = fwd_config(d);
     const long long ctas = grid_ctas(B, H, Nq, d, num_splits);
     if (ctas < 1 || ctas > 0x7fffffffll) return FA_ERR_SHAPE;
@@ -177,6 +187,13 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
         p.total_q = vl->total_q;
         p.cu_q = vl->cu_q;
         p.cu_k = vl->cu_k;
+    } else if (f8_descale) {
+        // e4m3 Q, K, V; bf16 O (plain mode only).
+        if (!encode_rows_map8(&p.tm_q, q, d, Nq, BH, 128) ||
+            !encode_rows_map8(&p.tm_k, k, d, Nk, BH, c.bn) ||
+            !encode_rows_map8(&p.tm_v, v, d, Nk, BH, c.bn) ||
+            !encode_rows_map(&p.tm_o, o, d, Nq, BH, 128))
+            return FA_ERR_CUDA;
     } else {
         if (!encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
             !encode_rows_map(&p.tm_k, k, d, Nk, BH, c.bn) ||
@@ -211,12 +228,21 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     const long long ctas_per_head = static_cast<long long>(p.n_units) * num_splits;
     p.head_group = static_cast<int>(std::max<long long>(1, std::min<long long>(BH, sms / ctas_per_head)));
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.o_scale = 1.f;
+    if (f8_descale) {
+        p.scale_log2 *= f8_descale[0] * f8_descale[1];
+        p.o_scale = f8_descale[2];
+    }
     p.wait_limit = wait_limit;
     p.test_withhold_q = withhold_q;
     if (device_status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
 
     cudaError_t e = cudaErrorInvalidValue;
     const unsigned grid = static_cast<unsigned>(ctas);
+    if (f8_descale) {
+        e = (d == 128) ? launch_fwd_f8_d128(p, grid, stream) : cudaErrorInvalidValue;
+        return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    }
     switch (d) {
         case 64: e = launch_fwd_d64(p, grid, stream); break;
         case 128: e = launch_fwd_d128(p, grid, stream); break;
@@ -240,6 +266,24 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     if (!fa::aligned(o, 16) || !fa::aligned(lse, 4)) return FA_ERR_ALIGN;
     return fa::launch_forward(q, k, v, o, lse, nullptr, B, H, Nq, Nk, d, scale, causal, 1, 0,
                               stream);
+}
+
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
+                     float k_descale, float v_descale, void* o, float* lse, int B, int H, int Nq,
+                     int Nk, int d, float scale, int causal, cudaStream_t stream) {
+    fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
+    if (s != FA_OK) return s;
+    if (d != 128) return FA_ERR_HEADDIM;
+    if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
+    const float ds[3] = {q_descale, k_descale, v_descale};
+    for (float x : ds)
+        if (!std::isfinite(x) || !(x > 0.f)) return FA_ERR_SCALE;
+    const float s_eff = scale * q_descale * k_descale;
+    if (!std::isfinite(s_eff) || !(s_eff > 0.f)) return FA_ERR_SCALE;
+    if (!o || !lse) return FA_ERR_NULL;
+    if (!fa::aligned(o, 16) || !fa::aligned(lse, 4)) return FA_ERR_ALIGN;
+    return fa::launch_forward(q, k, v, o, lse, nullptr, B, H, Nq, Nk, d, scale, causal, 1, 0,
+                              stream, fa::kDefaultWaitLimit, 0, nullptr, ds);
 }
 
 size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {

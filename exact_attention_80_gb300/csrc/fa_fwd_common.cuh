@@ -14,6 +14,11 @@ constexpr int kBM = 128;  // query rows per tile = TMEM lanes
 // before the reference moves and O, l are rescaled: p <= 2^8 = 256 is exact
 // in bf16's exponent range and far from fp32 overflow.
 constexpr float kRescaleSlack = 8.0f;
+// e4m3 P: a smaller slack and a fixed shift, p = 2^(x - m + kP8Shift) with
+// x - m <= kP8Slack, so p <= 2^8 (e4m3 saturates at 448) and the row's largest
+// p is at least 2^6 (e4m3 is normal from 2^-6 up).
+constexpr float kP8Slack = 2.0f;
+constexpr float kP8Shift = 6.0f;
 
 // Ring position (slot, phase parity) of a sequence of K/V entries.
 template <int ST>
@@ -160,13 +165,16 @@ struct RowOut {
     size_t row_idx, lse_idx, part_idx;
     float m, m_true, l;
 
+    // `o_scale` multiplies the normalised O in plain mode (the V descale of
+    // 8-bit inputs; 1 otherwise).
     __device__ __forceinline__ RowOut(const FwdParams& p, const RowMap& rm, int bh, int split_idx,
-                                      int q_row, float m_, float m_true_, float l_)
+                                      int q_row, float m_, float m_true_, float l_,
+                                      float o_scale = 1.f)
         : row_ok(q_row < rm.len_q), split(p.split_mode != 0), m(m_), m_true(m_true_), l(l_) {
         row_idx = static_cast<size_t>(rm.o_base + static_cast<long long>(q_row) * rm.o_stride);
         lse_idx = static_cast<size_t>(rm.lse_base + q_row);
         part_idx = (static_cast<size_t>(split_idx) * p.BH + bh) * p.Nq + q_row;
-        if (!split) f = (l > 0.f) ? 1.f / l : 0.f;
+        if (!split) f = (l > 0.f) ? o_scale / l : 0.f;
         else f = (l > 0.f && m != m_true) ? ex2(m - m_true) : 1.f;
     }
     // Columns [32 cc, 32 cc + 32) of the row, fp32 bits (zero when the row saw
@@ -239,9 +247,10 @@ __device__ __forceinline__ void write_row(const FwdParams& p, const RowMap& rm, 
 }
 
 // Plain-mode epilogue of one 128-row query tile, run by the tile's 128
-// softmax threads (thread r = row r = TMEM lane r): O_t / l as bf16 is staged in
-// the tile's own Q shared memory (`q_tile`, free once the tile's last PV has
-// finished, as every S MMA reading Q came before it) in the 128-byte-swizzled
+// softmax threads (thread r = row r = TMEM lane r): o_scale * O_t / l as bf16
+// is staged at `q_tile` (128 x D bf16: the tile's own bf16 Q shared memory,
+// free once the tile's last PV has finished, as every S MMA reading Q came
+// before it; or a staging buffer of that size) in the 128-byte-swizzled
 // layout a Q load through the same kind of tensor map produces, and the
 // group's first warp writes the tile with TMA tensor stores (rows past Nq are
 // clipped). `bh` is the head coordinate of the O tensor map. `staged` is an
@@ -252,9 +261,9 @@ template <int D>
 __device__ __forceinline__ bool store_tile_tma(const FwdParams& p, const RowMap& rm, int bh, int q_row0,
                                                int r, int q_row, float m, float m_true, float l,
                                                uint32_t tO, uint32_t q_tile, uint32_t staged,
-                                               volatile uint32_t* abort_flag) {
+                                               volatile uint32_t* abort_flag, float o_scale = 1.f) {
     const int lane = r & 31;
-    const RowOut<D> out(p, rm, bh, 0, q_row, m, m_true, l);
+    const RowOut<D> out(p, rm, bh, 0, q_row, m, m_true, l, o_scale);
     const uint32_t swz = static_cast<uint32_t>(r & 7);
 #pragma unroll 1
     for (int cc = 0; cc < D / 32; ++cc) {

@@ -1,0 +1,8 @@
+// Forward kernel instantiation for e4m3 Q, K, V at head dim 128.
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+cudaError_t launch_fwd_f8_d128(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+    return launch_fwd<128, true>(p, grid, stream);
+}
+}  // namespace fa

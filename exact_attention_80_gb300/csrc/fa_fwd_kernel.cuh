@@ -4,7 +4,8 @@
 //                P handed to the PV MMA in TMEM over its S columns, the two
 //                tiles alternating on the tensor core.
 //   d = 256:     fa_fwd_tp.cuh — one query tile per CTA (O takes half of TMEM),
-//                BN = 64, S double-buffered in TMEM with P packed over it.
+//                BN = 96, S double-buffered in TMEM with P packed over it.
+//   e4m3 inputs: fa_fwd_tm.cuh's kernel instantiated for 8-bit operands.
 #pragma once
 
 #include <type_traits>
@@ -17,11 +18,13 @@ namespace fa {
 template <int D>
 using FwdLayout = std::conditional_t<D == 256, LayoutTP<D>, LayoutTM<D>>;
 
-template <int D>
+// F8: e4m3 inputs (d = 64 or 128 only: the two-tile kernel).
+template <int D, bool F8 = false>
 cudaError_t launch_fwd(const FwdParams& p, unsigned grid, cudaStream_t stream) {
-    using L = FwdLayout<D>;
+    using L = std::conditional_t<F8, LayoutTM<D, true>, FwdLayout<D>>;
     constexpr auto kernel = [] {
-        if constexpr (D == 256) return fa_fwd_tp_kernel<D>;
+        if constexpr (F8) return fa_fwd_tm8_kernel<D>;
+        else if constexpr (D == 256) return fa_fwd_tp_kernel<D>;
         else return fa_fwd_tm_kernel<D>;
     }();
     static bool attr_set[64] = {};

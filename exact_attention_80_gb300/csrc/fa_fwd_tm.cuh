@@ -39,6 +39,8 @@
 // (again bounded), TMEM is freed and the CTA exits.
 #pragma once
 
+#include <type_traits>
+
 #include "fa_fwd_common.cuh"
 
 namespace fa {
@@ -55,21 +57,38 @@ template <>
 struct TmCfg<128> {
     static constexpr int STAGES = 5, CTRL_REGS = 88, SOFTMAX_REGS = 208;
 };
-
+// 8-bit (e4m3) inputs: K/V slots are half the size, so the ring is deeper.
 template <int D>
+struct TmCfg8;
+template <>
+struct TmCfg8<128> {
+    static constexpr int STAGES = 8, CTRL_REGS = 88, SOFTMAX_REGS = 208;
+};
+
+// F8: Q, K, V are e4m3 (one byte per element) and both MMAs are
+// kind::f8f6f4; otherwise bf16 and kind::f16.
+template <int D, bool F8 = false>
 struct LayoutTM {
+    using Cfg = std::conditional_t<F8, TmCfg8<D>, TmCfg<D>>;
     static constexpr int Q_TILES = 2;
     static constexpr int BN = 128;
-    static constexpr int STAGES = TmCfg<D>::STAGES;
+    static constexpr int STAGES = Cfg::STAGES;
     static constexpr int THREADS = (4 + 4 * Q_TILES) * 32;
-    static constexpr int CHUNKS = D / 64;  // 64-element (128-byte) column chunks
+    static constexpr int EB = F8 ? 1 : 2;              // input bytes per element
+    static constexpr int CHUNK_ELEMS = 128 / EB;       // elements per 128-byte swizzle row
+    static constexpr int CHUNKS = D / CHUNK_ELEMS;     // column chunks of a Q/K/V row
+    static constexpr int K_MMA = 32 / EB;              // K elements per MMA instruction
 
     // shared memory (offsets from a 1024-aligned base)
-    static constexpr uint32_t Q_TILE_BYTES = kBM * D * 2;
-    static constexpr uint32_t SLOT_BYTES = BN * D * 2;
+    static constexpr uint32_t Q_TILE_BYTES = kBM * D * EB;
+    static constexpr uint32_t SLOT_BYTES = BN * D * EB;
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t SLOT_OFF = Q_OFF + Q_TILES * Q_TILE_BYTES;
-    static constexpr uint32_t BAR_OFF = SLOT_OFF + STAGES * SLOT_BYTES;
+    // bf16 O is staged for its TMA store in the tile's Q memory when that holds
+    // a bf16 tile; 8-bit Q tiles are half that size, so F8 has buffers of its own.
+    static constexpr uint32_t OST_OFF = SLOT_OFF + STAGES * SLOT_BYTES;
+    static constexpr uint32_t OST_TILE_BYTES = F8 ? kBM * D * 2 : 0;
+    static constexpr uint32_t BAR_OFF = OST_OFF + Q_TILES * OST_TILE_BYTES;
     static constexpr int BAR_QFULL = 0;                       // [tile] Q_t landed
     static constexpr int BAR_KVFULL = BAR_QFULL + Q_TILES;
     static constexpr int BAR_KVEMPTY = BAR_KVFULL + STAGES;
@@ -99,16 +118,15 @@ struct LayoutTM {
     // checked on the host.
     static constexpr bool REG_SPLIT = true;
     static constexpr int LAUNCH_REGS = 168;
-    static constexpr int CTRL_REGS = TmCfg<D>::CTRL_REGS;
-    static constexpr int SOFTMAX_REGS = TmCfg<D>::SOFTMAX_REGS;
+    static constexpr int CTRL_REGS = Cfg::CTRL_REGS;
+    static constexpr int SOFTMAX_REGS = Cfg::SOFTMAX_REGS;
     static_assert(128 * CTRL_REGS + 256 * SOFTMAX_REGS == THREADS * LAUNCH_REGS,
                   "register split must equal the launch allocation");
 };
 
-template <int D>
-__global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
-    fa_fwd_tm_kernel(const __grid_constant__ FwdParams p) {
-    using L = LayoutTM<D>;
+template <int D, bool F8>
+__device__ __forceinline__ void tm_forward(const FwdParams& p) {
+    using L = LayoutTM<D, F8>;
     constexpr int QT = L::Q_TILES;
     constexpr int BN = L::BN;
     constexpr int ST = L::STAGES;
@@ -177,7 +195,8 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128),
-                                    &p.tm_q, bar(L::BAR_QFULL + t), 64 * c, w.qbase + w.q0 + t * kBM, w.zq);
+                                    &p.tm_q, bar(L::BAR_QFULL + t), L::CHUNK_ELEMS * c, w.qbase + w.q0 + t * kBM,
+                                    w.zq);
                 }
             };
             // Q_0, K_0, then Q_1: the first S can start after two tiles' bytes.
@@ -203,7 +222,7 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
-                                    bar(L::BAR_KVFULL + pos.slot), 64 * c, row, w.zq);
+                                    bar(L::BAR_KVFULL + pos.slot), L::CHUNK_ELEMS * c, row, w.zq);
                 }
                 issued = e + 1;
                 pos.advance();
@@ -239,8 +258,10 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             auto wait_all = [&](uint32_t b, uint32_t parity, unsigned what) {
                 return __all_sync(0xffffffffu, wait_phase(b, parity, p, abort_flag, what));
             };
-            constexpr uint32_t IDESC_S = make_idesc_bf16(kBM, BN, false, false);
-            constexpr uint32_t IDESC_O = make_idesc_bf16(kBM, D, false, true);
+            constexpr uint32_t IDESC_S =
+                F8 ? make_idesc_e4m3(kBM, BN, false, false) : make_idesc_bf16(kBM, BN, false, false);
+            constexpr uint32_t IDESC_O =
+                F8 ? make_idesc_e4m3(kBM, D, false, true) : make_idesc_bf16(kBM, D, false, true);
             // Descriptors are built once; an operand at byte offset `off` from a
             // base adds off >> 4 to the low word (the 14-bit start field never
             // carries: shared addresses stay below 2^18).
@@ -256,26 +277,49 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             auto issue_s = [&](int t, int slot) {
                 const uint32_t qa = L::Q_OFF + t * L::Q_TILE_BYTES;
                 const uint32_t kb = L::SLOT_OFF + slot * L::SLOT_BYTES;
+                // One MMA takes 32 bytes of K (16 bf16 or 32 e4m3) of a 128-byte row.
+                if constexpr (F8) {
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t in_row = (kk & 3) * 32;  // 16 bf16 = 32 bytes of a 128-byte row
-                    if (leader)
-                        umma_ss(tmem + L::S_COL(t), desc(kmaj_lo, kmaj_hi, qa + (kk >> 2) * (kBM * 128) + in_row),
-                                desc(kmaj_lo, kmaj_hi, kb + (kk >> 2) * (BN * 128) + in_row), IDESC_S,
-                                kk > 0 ? 1u : 0u);
+                    for (int kk = 0; kk < D / L::K_MMA; ++kk) {
+                        const uint32_t in_row = (kk & 3) * 32;
+                        if (leader)
+                            umma_ss_f8(tmem + L::S_COL(t),
+                                       desc(kmaj_lo, kmaj_hi, qa + (kk >> 2) * (kBM * 128) + in_row),
+                                       desc(kmaj_lo, kmaj_hi, kb + (kk >> 2) * (BN * 128) + in_row), IDESC_S,
+                                       kk > 0 ? 1u : 0u);
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t in_row = (kk & 3) * 32;  // 16 bf16 = 32 bytes of a 128-byte row
+                        if (leader)
+                            umma_ss(tmem + L::S_COL(t), desc(kmaj_lo, kmaj_hi, qa + (kk >> 2) * (kBM * 128) + in_row),
+                                    desc(kmaj_lo, kmaj_hi, kb + (kk >> 2) * (BN * 128) + in_row), IDESC_S,
+                                    kk > 0 ? 1u : 0u);
+                    }
                 }
             };
-            // O_t += P_t V: A = P_t packed two bf16 per TMEM column (16 keys = 8
-            // columns), B = V MN-major (16 keys = two 8-row swizzle atoms,
-            // 2048 bytes; 64-column chunks of d BN*128 bytes apart).
+            // O_t += P_t V: A = P_t packed two bf16 (four e4m3) per TMEM column,
+            // so one MMA's K keys (16 bf16 or 32 e4m3) are 8 columns; B = V
+            // MN-major (K key rows of 128 bytes, K/8 swizzle atoms of 1024 bytes;
+            // 128-byte column chunks of d BN*128 bytes apart).
             auto issue_pv = [&](int t, int slot, bool accumulate) {
                 const uint32_t vb = L::SLOT_OFF + slot * L::SLOT_BYTES;
+                if constexpr (F8) {
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    if (leader)
-                        umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8,
-                                desc(vmn_lo, vmn_hi, vb + kk * 2048), IDESC_O,
-                                (accumulate || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < BN / L::K_MMA; ++kk)
+                        if (leader)
+                            umma_ts_f8(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8,
+                                       desc(vmn_lo, vmn_hi, vb + kk * (L::K_MMA * 128)), IDESC_O,
+                                       (accumulate || kk > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        if (leader)
+                            umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8,
+                                    desc(vmn_lo, vmn_hi, vb + kk * 2048), IDESC_O,
+                                    (accumulate || kk > 0) ? 1u : 0u);
+                }
             };
 
             // K/V entries in consumption order: K_0, then per step j: V_j, K_{j+1}.
@@ -380,6 +424,12 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
         const uint32_t tS = tmem + lane_field + L::S_COL(t);
         const uint32_t tO = tmem + lane_field + L::O_COL(t);
         const float sl2 = p.scale_log2;
+        // e4m3 P: with the reference at most kP8Slack below the true row max,
+        // p = 2^(x - m + kP8Shift) <= 2^8 stays inside e4m3's range (448) and
+        // the row's largest p is at least 2^6, so most of P is in e4m3's normal
+        // range. l sums the same scaled p, so O / l is unchanged; the LSE takes
+        // the shift back out.
+        constexpr float kSlack = F8 ? kP8Slack : kRescaleSlack;
         int n = w.n[0];
 #pragma unroll
         for (int i = 1; i < QT; ++i)
@@ -435,11 +485,11 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             // and the old reference is kept, so O and l need no rescale. The
             // result is the same: O/l and m + log2(l) do not depend on which
             // reference is used, only rounding does.
-            const bool move = m_tile > m + kRescaleSlack;
+            const bool move = m_tile > m + kSlack;
             const float m_new = move ? m_tile : m;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // all masked so far
             const float alpha = move ? ex2(m - m_use) : 1.f;
-            const float neg = -m_use;
+            const float neg = F8 ? kP8Shift - m_use : -m_use;
 
             // x = s*scale*log2e - m as packed fp32 pairs (one FFMA2 per two keys),
             // p = 2^x on the MUFU, row sums as four packed partial pairs; P goes
@@ -448,20 +498,43 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             const uint64_t sl2x2 = f2pack(sl2, sl2);
             const uint64_t negx2 = f2pack(neg, neg);
             uint64_t part2[4] = {0ull, 0ull, 0ull, 0ull};
+            if constexpr (F8) {
+                // e4m3 P: four keys per column, 32 columns (128 keys) at a time.
 #pragma unroll
-            for (int h = 0; h < BN / 64; ++h) {
-                uint32_t pk[32];
+                for (int h = 0; h < BN / 128; ++h) {
+                    uint32_t pk[32];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const int c = h * 64 + 2 * i;
-                    float x0, x1;
-                    f2unpack(ffma2(f2pack(s[c], s[c + 1]), sl2x2, negx2), x0, x1);
-                    const float e0 = ex2(x0);
-                    const float e1 = ex2(x1);
-                    part2[i & 3] = fadd2(part2[i & 3], f2pack(e0, e1));
-                    pk[i] = pack_bf16x2(e0, e1);
+                    for (int i = 0; i < 32; ++i) {
+                        const int c = h * 128 + 4 * i;
+                        float x0, x1, x2, x3;
+                        f2unpack(ffma2(f2pack(s[c], s[c + 1]), sl2x2, negx2), x0, x1);
+                        f2unpack(ffma2(f2pack(s[c + 2], s[c + 3]), sl2x2, negx2), x2, x3);
+                        const float e0 = ex2(x0);
+                        const float e1 = ex2(x1);
+                        const float e2 = ex2(x2);
+                        const float e3 = ex2(x3);
+                        part2[(2 * i) & 3] = fadd2(part2[(2 * i) & 3], f2pack(e0, e1));
+                        part2[(2 * i + 1) & 3] = fadd2(part2[(2 * i + 1) & 3], f2pack(e2, e3));
+                        pk[i] = pack_e4m3x4(e0, e1, e2, e3);
+                    }
+                    tmem_st32(tS + h * 32, pk);
                 }
-                tmem_st32(tS + h * 32, pk);
+            } else {
+#pragma unroll
+                for (int h = 0; h < BN / 64; ++h) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int c = h * 64 + 2 * i;
+                        float x0, x1;
+                        f2unpack(ffma2(f2pack(s[c], s[c + 1]), sl2x2, negx2), x0, x1);
+                        const float e0 = ex2(x0);
+                        const float e1 = ex2(x1);
+                        part2[i & 3] = fadd2(part2[i & 3], f2pack(e0, e1));
+                        pk[i] = pack_bf16x2(e0, e1);
+                    }
+                    tmem_st32(tS + h * 32, pk);
+                }
             }
 
             // O_t(j-1) is complete (the S_t(j) commit covers PV_t(j-1)); rescale
@@ -506,12 +579,23 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) tc_fence_after();
         }
-        if (ok && !p.split_mode && !p.varlen && n > 0) {
-            // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA.
-            store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
-                              sbase + L::Q_OFF + t * L::Q_TILE_BYTES, bar(L::BAR_OSTAGED + t), abort_flag);
-        } else if (ok) {
-            write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m, m_true, l, tO);
+        if constexpr (F8) {
+            // Plain mode only (the host rejects the others): bf16 o_scale * O_t / l
+            // staged in the tile's own buffer and written with TMA.
+            if (ok && n > 0)
+                store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m - kP8Shift, m_true, l, tO,
+                                  sbase + L::OST_OFF + t * L::OST_TILE_BYTES, bar(L::BAR_OSTAGED + t),
+                                  abort_flag, p.o_scale);
+            else if (ok)
+                write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m - kP8Shift, m_true, l, tO);
+        } else {
+            if (ok && !p.split_mode && !p.varlen && n > 0) {
+                // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA.
+                store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
+                                  sbase + L::Q_OFF + t * L::Q_TILE_BYTES, bar(L::BAR_OSTAGED + t), abort_flag);
+            } else if (ok) {
+                write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m, m_true, l, tO);
+            }
         }
     }
 
@@ -520,6 +604,21 @@ __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
+// bf16 Q, K, V.
+template <int D>
+__global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
+    fa_fwd_tm_kernel(const __grid_constant__ FwdParams p) {
+    tm_forward<D, false>(p);
+}
+
+// e4m3 Q, K, V with per-tensor descales (FA-3 page, section 7.3: 8-bit inputs
+// to both GEMMs, fp32 accumulation and fp32 softmax statistics).
+template <int D>
+__global__ void __launch_bounds__(LayoutTM<D, true>::THREADS, 1)
+    fa_fwd_tm8_kernel(const __grid_constant__ FwdParams p) {
+    tm_forward<D, true>(p);
 }
 
 }  // namespace fa

@@ -54,7 +54,8 @@ struct FwdParams {
     int n_units;             // query units of (tiles per CTA * 128) rows per head
     int kv_tiles_per_split;  // ceil(ceil(Nk/BN) / num_splits)
     int head_group;          // heads per scheduling group (CTA order)
-    float scale_log2;        // scale * log2(e)
+    float scale_log2;        // scale * log2(e) (8-bit inputs: times the Q and K descales)
+    float o_scale;           // 8-bit inputs: the V descale, applied to O at the end
     long long wait_limit;    // cycles
     int test_withhold_q;     // failure-detection test hook: 1 = never load Q
     unsigned* status;        // device status word
@@ -73,6 +74,8 @@ FwdConfig fwd_config(int d);
 cudaError_t launch_fwd_d64(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d256(const FwdParams& p, unsigned grid, cudaStream_t stream);
+// e4m3 Q, K, V (tm_q/tm_k/tm_v are byte maps, box {128, rows, 1}); d = 128.
+cudaError_t launch_fwd_f8_d128(const FwdParams& p, unsigned grid, cudaStream_t stream);
 
 cudaError_t launch_combine(const float* ws_o, const float* ws_m, const float* ws_l, void* o,
                            float* lse, long long rows, int num_splits, int d,

@@ -55,6 +55,23 @@ def make_varlen(lq, lk, H: int, d: int, seed: int):
     return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16), cu_q, cu_k
 
 
+def make_qkv_fp8(B: int, H: int, Nq: int, Nk: int, d: int, seed: int,
+                 descales=(2.0 ** -5, 2.0 ** -5, 2.0 ** -5)):
+    """e4m3 inputs: Q, K, V drawn N(0, 1) in float32 as in :func:`make_qkv`, each
+    divided by its descale, clamped to +-448 (e4m3's largest magnitude; torch's
+    cast does not saturate) and rounded to e4m3 by torch (nearest even).
+    Returns uint8 CPU tensors of e4m3 codes ``(q8, k8, v8)``; the value each code
+    stands for is its e4m3 value times the descale."""
+    import torch
+
+    g = torch.Generator().manual_seed(int(seed))
+    out = []
+    for shape, ds in zip(((B, H, Nq, d), (B, H, Nk, d), (B, H, Nk, d)), descales):
+        x = (torch.randn(shape, generator=g, dtype=torch.float32) / float(ds)).clamp(-448.0, 448.0)
+        out.append(x.to(torch.float8_e4m3fn).view(torch.uint8))
+    return tuple(out)
+
+
 def to_f64(t):
     """Exact upcast of a (bf16) torch tensor to a float64 numpy array."""
     return t.to(torch.float64).numpy()

@@ -155,6 +155,31 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
                         int causal, cudaStream_t stream);
 
 /*
+ * fa_fwd_fp8 — fused forward on 8-bit inputs (the FA-3 page, section 7.3
+ * "BF16 / FP8 支持": e4m3 operands for both GEMMs, fp32 accumulation, and the
+ * softmax max and sum kept in fp32).
+ *
+ *   q [B][H][Nq][d], k, v [B][H][Nk][d]: e4m3 codes, one byte each (OCP 8-bit
+ *   floating point, E4M3: bias 7, no infinities, max 448), 16-byte aligned.
+ *   The value of a code c of Q is decode(c) * q_descale (K, V likewise).
+ *   o [B][H][Nq][d] bf16 (written), lse [B][H][Nq] fp32 (written).
+ *
+ * Computes the same function as fa_fwd on those values: O = softmax(scale *
+ * Q K^T [+ mask]) V, LSE = ln of the softmax denominator. S is exact up to fp32
+ * accumulation. P is rounded to e4m3 per element for the PV GEMM: P is scaled
+ * so that each row's largest element lies in [2^6, 2^8], and the row sum l
+ * is taken before the rounding. So O carries a rounding error of relative
+ * size about 2^-4 / sqrt(3) per term, which averages over the keys. The LSE
+ * does not carry it.
+ * d = 128 only (else FA_ERR_HEADDIM). Plain mode only: no split-KV and no
+ * varlen. causal as fa_fwd. FA_ERR_SCALE if a descale is not finite and > 0,
+ * or if scale * q_descale * k_descale is not.
+ */
+fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
+                     float k_descale, float v_descale, void* o, float* lse, int B, int H,
+                     int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream);
+
+/*
  * fa_fwd_grid_ctas — number of CTAs fa_fwd (num_splits = 1) or
  * fa_fwd_splitkv would launch for this shape: B * H * ceil(Nq / BM) * num_splits,
  * BM = 256 query rows per CTA for d <= 128 (two 128-row tiles) and 128 for

@@ -37,7 +37,8 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     for want in ("fa_fwd", "fa_fwd_splitkv", "fa_combine", "fa_splitkv_workspace_bytes",
-                 "fa_status_string", "fa_fwd_grid_ctas", "fa_device_status", "fa_fwd_varlen"):
+                 "fa_status_string", "fa_fwd_grid_ctas", "fa_device_status", "fa_fwd_varlen",
+                 "fa_fwd_fp8"):
         assert want in names
 
 
@@ -111,6 +112,25 @@ def _varlen(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=FAKE, cq=FAKE, ck=FAKE, B=2
 ])
 def test_varlen_rejects(lib, kw, code):
     assert _varlen(lib, **kw) == code
+
+
+def _fp8(lib, q=FAKE, k=FAKE, v=FAKE, qd=0.03125, kd=0.03125, vd=0.03125, o=FAKE, lse=FAKE, B=1,
+         H=1, Nq=8, Nk=8, d=128, scale=0.088, causal=0):
+    return lib.fa_fwd_fp8(P(q), P(k), P(v), qd, kd, vd, P(o), P(lse), B, H, Nq, Nk, d, scale,
+                          causal, P(0))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(v=0), 1), (dict(o=0), 1), (dict(lse=0), 1),
+    (dict(Nq=0), 3), (dict(B=0), 3),
+    (dict(d=64), 4), (dict(d=256), 4), (dict(d=96), 4),
+    (dict(qd=0.0), 9), (dict(kd=-1.0), 9), (dict(vd=float("nan")), 9), (dict(vd=float("inf")), 9),
+    (dict(scale=0.0), 9), (dict(qd=1e-30, kd=1e-30), 9), (dict(qd=1e30, kd=1e30), 9),
+    (dict(q=FAKE + 8), 2), (dict(o=FAKE + 8), 2), (dict(lse=FAKE + 2), 2),
+    (dict(causal=3), 11),
+])
+def test_fp8_rejects(lib, kw, code):
+    assert _fp8(lib, **kw) == code
 
 
 def test_workspace_bytes(lib):

@@ -1,0 +1,116 @@
+"""GPU parity of the e4m3 forward (fa_fwd_fp8) against the float64 oracle of
+the encoded values.
+
+Tolerance, from the arithmetic (the FA-3 page, section 7.3, keeps the softmax
+statistics in fp32; P is rounded to e4m3 for the PV GEMM):
+* S is exact up to fp32 accumulation (products of e4m3 values are exact in
+  fp32), so the LSE meets the same bound as the bf16 path, 1e-3.
+* O carries the rounding of P to e4m3, error sigma_i per element from
+  ``oracle.fp8.p_rounding_sigma`` (independent half-step errors, relative 2^-4
+  on normal values), plus the bf16 rounding of O (relative 2^-8 at most, 2^-9
+  on average). Per element: |err| <= 6 sigma + 2^-8 |O| + 1e-3. Over a tensor,
+  to catch a bias that per-element bounds would let through: rms(err) <=
+  1.25 * sqrt(mean(sigma^2 + (2^-9 O)^2 / 3)) + 1e-5.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_80_gb300 as fa
+import oracle
+import oracle.fp8 as ofp8
+from exact_attention_80_gb300.inputs import f32, make_qkv_fp8
+
+pytestmark = pytest.mark.gpu
+
+LSE_TOL = 1e-3
+
+
+def check_fp8(o, lse, o_ref, lse_ref, sigma, what):
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.float().cpu().numpy().astype(np.float64)
+    err = np.abs(o - o_ref)
+    bound = 6.0 * sigma + 2.0 ** -8 * np.abs(o_ref) + 1e-3
+    worst = np.unravel_index(np.argmax(err - bound), err.shape)
+    assert (err <= bound).all(), (what, "element", worst, err[worst], bound[worst])
+    rms = math.sqrt(float(np.mean(err ** 2)))
+    model = math.sqrt(float(np.mean(sigma ** 2 + (2.0 ** -9 * o_ref) ** 2 / 3.0)))
+    assert rms <= 1.25 * model + 1e-5, (what, "rms", rms, model)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isneginf(lse), ~fin), what
+    if fin.any():
+        assert np.abs(lse[fin] - lse_ref[fin]).max() <= LSE_TOL, what
+    return rms, model
+
+
+def run_fp8(B, H, Nq, Nk, causal, seed, descales=(2.0 ** -5, 2.0 ** -5, 2.0 ** -5), d=128):
+    q8, k8, v8 = make_qkv_fp8(B, H, Nq, Nk, d, seed, descales)
+    scale = f32(1.0 / math.sqrt(d))
+    o, lse = fa.attention_fp8(q8.cuda(), k8.cuda(), v8.cuda(), *descales, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    return q8.numpy(), k8.numpy(), v8.numpy(), scale, o, lse
+
+
+CASES = [
+    # B, H, Nq, Nk, causal: tiles, a ragged tail, both masks, Nq != Nk
+    (1, 2, 256, 256, False),
+    (1, 2, 300, 333, False),
+    (1, 2, 300, 333, True),
+    (2, 3, 1000, 1500, False),
+    (1, 2, 700, 2000, "bottom_right"),
+    (1, 1, 1, 1, False),
+    (1, 1, 129, 1, False),
+    (1, 4, 2048, 2048, True),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,causal", CASES)
+def test_fp8_parity(B, H, Nq, Nk, causal):
+    descales = (2.0 ** -5, 2.0 ** -5, 2.0 ** -5)
+    q8, k8, v8, scale, o, lse = run_fp8(B, H, Nq, Nk, causal, 5100 + Nq + Nk, descales)
+    o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, causal)
+    sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, causal)
+    check_fp8(o, lse, o_ref, lse_ref, sigma, f"B{B} H{H} Nq{Nq} Nk{Nk} {causal}")
+
+
+def test_fp8_descales():
+    """Non-power-of-two descales, different per tensor, with codes that use
+    e4m3's whole range (|code value| up to 448)."""
+    descales = (0.0123, 0.0071, 0.3)
+    q8, k8, v8, scale, o, lse = run_fp8(1, 3, 400, 900, False, 5201, descales)
+    assert np.abs(ofp8.e4m3_decode(k8)).max() == ofp8.E4M3_MAX
+    o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, False)
+    sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, False)
+    check_fp8(o, lse, o_ref, lse_ref, sigma, "descales")
+
+
+def test_fp8_full_size_sampled_heads():
+    """The C2 shape (B=8, H=32, N=2048, d=128) in e4m3, as the bench times it:
+    every row of three heads against the oracle."""
+    B, H, N, d = 8, 32, 2048, 128
+    descales = (2.0 ** -5, 2.0 ** -5, 2.0 ** -5)
+    q8, k8, v8, scale, o, lse = run_fp8(B, H, N, N, False, 5301, descales, d)
+    for b, h in ((0, 0), (3, 17), (7, 31)):
+        o_ref, lse_ref = ofp8.attention_fp8_f64(q8[b, h], k8[b, h], v8[b, h], *descales, scale)
+        sigma = ofp8.p_rounding_sigma(q8[b, h], k8[b, h], v8[b, h], *descales, scale)
+        check_fp8(o[b, h], lse[b, h], o_ref, lse_ref, sigma, f"head {b},{h}")
+
+
+def test_fp8_matches_bf16_path_on_the_same_values():
+    """The e4m3 codes decoded to bf16 (exact: e4m3 values are bf16 values) run
+    through the bf16 kernel give the same LSE to fp32 rounding, and an O within
+    the e4m3 P-rounding bound of it."""
+    descales = (1.0, 1.0, 1.0)
+    q8, k8, v8, scale, o8, lse8 = run_fp8(1, 2, 512, 777, True, 5401, descales)
+    to_bf16 = lambda c: torch.from_numpy(ofp8.e4m3_decode(c)).to(torch.bfloat16).cuda()  # noqa: E731
+    o16, lse16 = fa.attention(to_bf16(q8), to_bf16(k8), to_bf16(v8), causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert (lse8 - lse16).abs().max().item() <= 1e-4
+    o_ref, _ = oracle.attention_f64(ofp8.e4m3_decode(q8), ofp8.e4m3_decode(k8), ofp8.e4m3_decode(v8),
+                                    scale, True)
+    sigma = ofp8.p_rounding_sigma(q8, k8, v8, 1.0, 1.0, 1.0, scale, True)
+    diff = (o8.float() - o16.float()).abs().cpu().numpy()
+    assert (diff <= 6.0 * sigma + 2.0 ** -7 * np.abs(o_ref) + 2e-3).all()
