@@ -326,7 +326,46 @@ def extra_workloads(device, stream, reps: int = 20):
         del q, k, v, o, lse
     out["varlen_causal"] = varlen_workload(device, stream, reps)
     out["c2_fp8"] = fp8_workload(device, stream, reps)
+    out["c5_fp8"] = fp8_decode_workload(device, stream, reps)
     return out
+
+
+def fp8_decode_workload(device, stream, reps):
+    """The C5 decode shape (B=1, H=8, Nq=128, Nk=131072, d=128) with e4m3 Q, K, V
+    (descales 2^-5) through fa_fwd_fp8_splitkv + fa_combine, at 16 splits and
+    at the split count that gives one CTA per SM. K and V are half the bytes of
+    bf16; split_gbs counts the bytes the split kernel moves."""
+    import torch
+
+    import exact_attention_80_gb300 as fa
+    from exact_attention_80_gb300.inputs import metric_flops
+
+    B, H, Nq, Nk, d = 1, 8, 128, 131072, 128
+    ds = 2.0 ** -5
+    gen = torch.Generator(device=device).manual_seed(1009)
+    q8, k8, v8 = ((torch.randn(shape, generator=gen, device=device) / ds)
+                  .clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+                  for shape in ((B, H, Nq, d), (B, H, Nk, d), (B, H, Nk, d)))
+    o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=device)
+    lse = torch.empty((B, H, Nq), device=device)
+    flops = metric_flops(B, H, Nq, Nk, d, False)
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    fill = max(1, min(fa.FA_MAX_SPLITS, sms // fa.fa_fwd_grid_ctas(B, H, Nq, d, 1)))
+    res = {}
+    for S in sorted({16, fill}):
+        ws = torch.empty(fa.fa_splitkv_workspace_bytes(B, H, Nq, d, S) // 4, device=device)
+        f_split = lambda: fa.fa_fwd_fp8_splitkv(q8, k8, v8, ds, ds, ds, ws, S, False, stream=stream)  # noqa
+        f_comb = lambda: fa.fa_combine(ws, o, lse, B, H, Nq, d, S, stream=stream)  # noqa
+        for _ in range(3):
+            f_split()
+            f_comb()
+        ms_s = statistics.median(time_launches(f_split, reps, stream, queue_ahead=True))
+        ms_c = statistics.median(time_launches(f_comb, reps, stream, queue_ahead=True))
+        moved = 2 * B * H * Nk * d + B * H * Nq * d + S * B * H * Nq * (d + 2) * 4
+        res[str(S)] = {"tflops": round(flops / (ms_s + ms_c) / 1e9, 1),
+                       "split_us": round(ms_s * 1e3, 1), "combine_us": round(ms_c * 1e3, 1),
+                       "split_gbs": round(moved / ms_s / 1e6, 1)}
+    return res
 
 
 def fp8_workload(device, stream, reps):

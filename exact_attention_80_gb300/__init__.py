@@ -64,6 +64,8 @@ def load_library() -> ctypes.CDLL:
     lib.fa_fwd_varlen.restype = i
     lib.fa_fwd_fp8.argtypes = [vp, vp, vp, f, f, f, vp, vp, i, i, i, i, i, f, i, vp]
     lib.fa_fwd_fp8.restype = i
+    lib.fa_fwd_fp8_splitkv.argtypes = [vp, vp, vp, f, f, f, vp, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_fp8_splitkv.restype = i
     lib.fa_fwd_grid_ctas.argtypes = [i, i, i, i, i]
     lib.fa_fwd_grid_ctas.restype = ctypes.c_longlong
     lib.fa_device_status.argtypes = [vp, i]
@@ -165,15 +167,36 @@ def fa_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, o,
     _check(st, "fa_fwd_fp8")
 
 
+def fa_fwd_fp8_splitkv(q, k, v, q_descale: float, k_descale: float, v_descale: float, workspace,
+                       num_splits: int, causal=False, scale: float | None = None, stream=None):
+    """Split-KV forward on e4m3 inputs into ``workspace`` (fp32, at least
+    ``fa_splitkv_workspace_bytes`` bytes); merge with :func:`fa_combine`."""
+    B, H, Nq, Nk, d = _bhnd8(q, k, v)
+    scale = default_scale(d) if scale is None else float(scale)
+    st = load_library().fa_fwd_fp8_splitkv(_ptr(q), _ptr(k), _ptr(v), float(q_descale),
+                                           float(k_descale), float(v_descale), _ptr(workspace), B, H,
+                                           Nq, Nk, d, scale, causal_code(causal), int(num_splits),
+                                           _stream_handle(stream))
+    _check(st, "fa_fwd_fp8_splitkv")
+
+
 def attention_fp8(q, k, v, q_descale: float = 1.0, k_descale: float = 1.0, v_descale: float = 1.0,
-                  causal=False, scale: float | None = None, stream=None):
-    """Allocate bf16 ``o`` and fp32 ``lse`` and run :func:`fa_fwd_fp8`."""
+                  causal=False, scale: float | None = None, num_splits: int = 1, stream=None):
+    """Allocate bf16 ``o`` and fp32 ``lse`` and run :func:`fa_fwd_fp8`, or, with
+    ``num_splits > 1``, :func:`fa_fwd_fp8_splitkv` and :func:`fa_combine`."""
     import torch
 
     B, H, Nq, Nk, d = _bhnd8(q, k, v)
     o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
-    fa_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o, lse, causal, scale, stream)
+    if num_splits == 1:
+        fa_fwd_fp8(q, k, v, q_descale, k_descale, v_descale, o, lse, causal, scale, stream)
+    else:
+        ws = torch.empty(fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits) // 4,
+                         dtype=torch.float32, device=q.device)
+        fa_fwd_fp8_splitkv(q, k, v, q_descale, k_descale, v_descale, ws, num_splits, causal, scale,
+                           stream)
+        fa_combine(ws, o, lse, B, H, Nq, d, num_splits, stream)
     return o, lse
 
 

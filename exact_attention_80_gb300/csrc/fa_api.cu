@@ -188,12 +188,12 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
         p.cu_q = vl->cu_q;
         p.cu_k = vl->cu_k;
     } else if (f8_descale) {
-        // e4m3 Q, K, V; bf16 O (plain mode only).
+        // e4m3 Q, K, V; bf16 O in plain mode.
         if (!encode_rows_map8(&p.tm_q, q, d, Nq, BH, 128) ||
             !encode_rows_map8(&p.tm_k, k, d, Nk, BH, c.bn) ||
-            !encode_rows_map8(&p.tm_v, v, d, Nk, BH, c.bn) ||
-            !encode_rows_map(&p.tm_o, o, d, Nq, BH, 128))
+            !encode_rows_map8(&p.tm_v, v, d, Nk, BH, c.bn))
             return FA_ERR_CUDA;
+        if (!split_mode && !encode_rows_map(&p.tm_o, o, d, Nq, BH, 128)) return FA_ERR_CUDA;
     } else {
         if (!encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
             !encode_rows_map(&p.tm_k, k, d, Nk, BH, c.bn) ||
@@ -284,6 +284,26 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, float q_descal
     if (!fa::aligned(o, 16) || !fa::aligned(lse, 4)) return FA_ERR_ALIGN;
     return fa::launch_forward(q, k, v, o, lse, nullptr, B, H, Nq, Nk, d, scale, causal, 1, 0,
                               stream, fa::kDefaultWaitLimit, 0, nullptr, ds);
+}
+
+fa_status fa_fwd_fp8_splitkv(const void* q, const void* k, const void* v, float q_descale,
+                             float k_descale, float v_descale, void* workspace, int B, int H,
+                             int Nq, int Nk, int d, float scale, int causal, int num_splits,
+                             cudaStream_t stream) {
+    fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
+    if (s != FA_OK) return s;
+    if (d != 128) return FA_ERR_HEADDIM;
+    if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
+    const float ds[3] = {q_descale, k_descale, v_descale};
+    for (float x : ds)
+        if (!std::isfinite(x) || !(x > 0.f)) return FA_ERR_SCALE;
+    const float s_eff = scale * q_descale * k_descale;
+    if (!std::isfinite(s_eff) || !(s_eff > 0.f)) return FA_ERR_SCALE;
+    if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_SPLITS;
+    if (!workspace || !fa::aligned(workspace, 16)) return FA_ERR_WORKSPACE;
+    return fa::launch_forward(q, k, v, nullptr, nullptr, static_cast<float*>(workspace), B, H, Nq,
+                              Nk, d, scale, causal, num_splits, 1, stream, fa::kDefaultWaitLimit, 0,
+                              nullptr, ds);
 }
 
 size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {

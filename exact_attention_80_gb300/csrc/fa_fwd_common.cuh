@@ -161,12 +161,13 @@ template <int D>
 struct RowOut {
     bool row_ok;
     bool split;
-    float f;  // plain: 1/l; split: move from the lazy reference m to m_true
+    float f;   // plain: o_scale/l; split: move from the lazy reference m to m_true
+    float fo;  // split: the factor on the partial O, f * o_scale (l takes f alone)
     size_t row_idx, lse_idx, part_idx;
     float m, m_true, l;
 
-    // `o_scale` multiplies the normalised O in plain mode (the V descale of
-    // 8-bit inputs; 1 otherwise).
+    // `o_scale` multiplies O, normalised (plain mode) or partial (split mode):
+    // the V descale of 8-bit inputs, 1 otherwise.
     __device__ __forceinline__ RowOut(const FwdParams& p, const RowMap& rm, int bh, int split_idx,
                                       int q_row, float m_, float m_true_, float l_,
                                       float o_scale = 1.f)
@@ -176,6 +177,7 @@ struct RowOut {
         part_idx = (static_cast<size_t>(split_idx) * p.BH + bh) * p.Nq + q_row;
         if (!split) f = (l > 0.f) ? o_scale / l : 0.f;
         else f = (l > 0.f && m != m_true) ? ex2(m - m_true) : 1.f;
+        fo = f * o_scale;
     }
     // Columns [32 cc, 32 cc + 32) of the row, fp32 bits (zero when the row saw
     // no key); `o` is scaled in place.
@@ -192,8 +194,8 @@ struct RowOut {
                     dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
             }
         } else {
-            if (f != 1.f) {
-                const uint64_t f2 = f2pack(f, f);
+            if (fo != 1.f) {
+                const uint64_t f2 = f2pack(fo, fo);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     float x0, x1;
@@ -229,8 +231,8 @@ struct RowOut {
 template <int D>
 __device__ __forceinline__ void write_row(const FwdParams& p, const RowMap& rm, int bh, int split,
                                           int q_row, int n, float m, float m_true, float l,
-                                          uint32_t tO) {
-    const RowOut<D> out(p, rm, bh, split, q_row, m, m_true, l);
+                                          uint32_t tO, float o_scale = 1.f) {
+    const RowOut<D> out(p, rm, bh, split, q_row, m, m_true, l, o_scale);
 #pragma unroll 1
     for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];

@@ -580,14 +580,15 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             if (ok) tc_fence_after();
         }
         if constexpr (F8) {
-            // Plain mode only (the host rejects the others): bf16 o_scale * O_t / l
-            // staged in the tile's own buffer and written with TMA.
-            if (ok && n > 0)
+            // Dense layouts only (the host rejects varlen). Plain mode: bf16
+            // o_scale * O_t / l staged in the tile's own buffer and written with
+            // TMA. Split mode: the partial state, O scaled by o_scale, per row.
+            if (ok && !p.split_mode && n > 0)
                 store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m - kP8Shift, m_true, l, tO,
                                   sbase + L::OST_OFF + t * L::OST_TILE_BYTES, bar(L::BAR_OSTAGED + t),
                                   abort_flag, p.o_scale);
             else if (ok)
-                write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m - kP8Shift, m_true, l, tO);
+                write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m - kP8Shift, m_true, l, tO, p.o_scale);
         } else {
             if (ok && !p.split_mode && !p.varlen && n > 0) {
                 // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA.

@@ -171,13 +171,27 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
  * is taken before the rounding. So O carries a rounding error of relative
  * size about 2^-4 / sqrt(3) per term, which averages over the keys. The LSE
  * does not carry it.
- * d = 128 only (else FA_ERR_HEADDIM). Plain mode only: no split-KV and no
- * varlen. causal as fa_fwd. FA_ERR_SCALE if a descale is not finite and > 0,
+ * d = 128 only (else FA_ERR_HEADDIM). No varlen; the split-KV form is
+ * fa_fwd_fp8_splitkv. causal as fa_fwd. FA_ERR_SCALE if a descale is not finite and > 0,
  * or if scale * q_descale * k_descale is not.
  */
 fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
                      float k_descale, float v_descale, void* o, float* lse, int B, int H,
                      int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream);
+
+/*
+ * fa_fwd_fp8_splitkv — fa_fwd_splitkv on e4m3 inputs: the key axis split as
+ * fa_fwd_splitkv splits it, partial states written to a workspace of
+ * fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits) bytes in the same fp32
+ * layout, merged by fa_combine. The partial O includes the V descale; m and l
+ * are those of the encoded values' scores. Arguments and status codes as
+ * fa_fwd_fp8, plus num_splits (FA_ERR_SPLITS) and the workspace
+ * (FA_ERR_WORKSPACE).
+ */
+fa_status fa_fwd_fp8_splitkv(const void* q, const void* k, const void* v, float q_descale,
+                             float k_descale, float v_descale, void* workspace, int B, int H,
+                             int Nq, int Nk, int d, float scale, int causal, int num_splits,
+                             cudaStream_t stream);
 
 /*
  * fa_fwd_grid_ctas — number of CTAs fa_fwd (num_splits = 1) or

@@ -38,7 +38,7 @@ def test_header_declares_the_api():
     names = declared_functions()
     for want in ("fa_fwd", "fa_fwd_splitkv", "fa_combine", "fa_splitkv_workspace_bytes",
                  "fa_status_string", "fa_fwd_grid_ctas", "fa_device_status", "fa_fwd_varlen",
-                 "fa_fwd_fp8"):
+                 "fa_fwd_fp8", "fa_fwd_fp8_splitkv"):
         assert want in names
 
 
@@ -131,6 +131,19 @@ def _fp8(lib, q=FAKE, k=FAKE, v=FAKE, qd=0.03125, kd=0.03125, vd=0.03125, o=FAKE
 ])
 def test_fp8_rejects(lib, kw, code):
     assert _fp8(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=0), 6), (dict(ws=FAKE + 4), 6), (dict(S=0), 5), (dict(S=257), 5), (dict(d=64), 4),
+    (dict(q=0), 1), (dict(vd=0.0), 9), (dict(causal=5), 11), (dict(Nk=0), 3),
+])
+def test_fp8_splitkv_rejects(lib, kw, code):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, qd=0.03125, kd=0.03125, vd=0.03125, ws=FAKE, B=1, H=1, Nq=8,
+             Nk=8, d=128, scale=0.088, causal=0, S=4)
+    a.update(kw)
+    assert lib.fa_fwd_fp8_splitkv(P(a["q"]), P(a["k"]), P(a["v"]), a["qd"], a["kd"], a["vd"],
+                                  P(a["ws"]), a["B"], a["H"], a["Nq"], a["Nk"], a["d"], a["scale"],
+                                  a["causal"], a["S"], P(0)) == code
 
 
 def test_workspace_bytes(lib):

@@ -46,10 +46,12 @@ def check_fp8(o, lse, o_ref, lse_ref, sigma, what):
     return rms, model
 
 
-def run_fp8(B, H, Nq, Nk, causal, seed, descales=(2.0 ** -5, 2.0 ** -5, 2.0 ** -5), d=128):
+def run_fp8(B, H, Nq, Nk, causal, seed, descales=(2.0 ** -5, 2.0 ** -5, 2.0 ** -5), d=128,
+            num_splits=1):
     q8, k8, v8 = make_qkv_fp8(B, H, Nq, Nk, d, seed, descales)
     scale = f32(1.0 / math.sqrt(d))
-    o, lse = fa.attention_fp8(q8.cuda(), k8.cuda(), v8.cuda(), *descales, causal=causal, scale=scale)
+    o, lse = fa.attention_fp8(q8.cuda(), k8.cuda(), v8.cuda(), *descales, causal=causal, scale=scale,
+                              num_splits=num_splits)
     torch.cuda.synchronize()
     return q8.numpy(), k8.numpy(), v8.numpy(), scale, o, lse
 
@@ -114,3 +116,28 @@ def test_fp8_matches_bf16_path_on_the_same_values():
     sigma = ofp8.p_rounding_sigma(q8, k8, v8, 1.0, 1.0, 1.0, scale, True)
     diff = (o8.float() - o16.float()).abs().cpu().numpy()
     assert (diff <= 6.0 * sigma + 2.0 ** -7 * np.abs(o_ref) + 2e-3).all()
+
+
+@pytest.mark.parametrize("S", [2, 3, 16, 64])
+@pytest.mark.parametrize("causal", [False, True, "bottom_right"])
+def test_fp8_splitkv(S, causal):
+    """fa_fwd_fp8_splitkv + fa_combine against the oracle, with the plain e4m3
+    bound (the split only regroups fp32 sums). Splits past the keys are empty."""
+    descales = (2.0 ** -5, 0.02, 0.3)
+    Nq, Nk = 200, 3000
+    q8, k8, v8, scale, o, lse = run_fp8(1, 2, Nq, Nk, causal, 5500 + S, descales, num_splits=S)
+    o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, causal)
+    sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, causal)
+    check_fp8(o, lse, o_ref, lse_ref, sigma, f"splits={S} {causal}")
+
+
+def test_fp8_decode_shape_split():
+    """The C5 decode shape (B=1, H=8, Nq=128, Nk=131072) in e4m3 with 16 splits:
+    one head's every row against the oracle."""
+    B, H, Nq, Nk, d = 1, 8, 128, 131072, 128
+    descales = (2.0 ** -5, 2.0 ** -5, 2.0 ** -5)
+    q8, k8, v8, scale, o, lse = run_fp8(B, H, Nq, Nk, False, 5601, descales, d, num_splits=16)
+    h = 5
+    o_ref, lse_ref = ofp8.attention_fp8_f64(q8[0, h], k8[0, h], v8[0, h], *descales, scale)
+    sigma = ofp8.p_rounding_sigma(q8[0, h], k8[0, h], v8[0, h], *descales, scale)
+    check_fp8(o[0, h], lse[0, h], o_ref, lse_ref, sigma, "c5 head 5")
