@@ -193,13 +193,13 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
             !encode_rows_map8(&p.tm_k, k, d, Nk, BH, c.bn) ||
             !encode_rows_map8(&p.tm_v, v, d, Nk, BH, c.bn))
             return FA_ERR_CUDA;
-        if (!split_mode && !encode_rows_map(&p.tm_o, o, d, Nq, BH, 128)) return FA_ERR_CUDA;
+        if (!split_mode && !encode_rows_map(&p.tm_o, o, d, Nq, BH, 32)) return FA_ERR_CUDA;
     } else {
         if (!encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
             !encode_rows_map(&p.tm_k, k, d, Nk, BH, c.bn) ||
             !encode_rows_map(&p.tm_v, v, d, Nk, BH, c.bn))
             return FA_ERR_CUDA;
-        if (!split_mode && !encode_rows_map(&p.tm_o, o, d, Nq, BH, 128)) return FA_ERR_CUDA;
+        if (!split_mode && !encode_rows_map(&p.tm_o, o, d, Nq, BH, d == 256 ? 128 : 32)) return FA_ERR_CUDA;
     }
     p.o = o;
     p.lse = lse;

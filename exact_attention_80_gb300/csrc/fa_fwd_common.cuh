@@ -301,4 +301,57 @@ __device__ __forceinline__ bool store_tile_tma(const FwdParams& p, const RowMap&
     return ok;
 }
 
+// Plain-mode epilogue of one 128-row query tile, per warp: o_scale * O_t / l as
+// bf16, one 64-column chunk at a time. Each warp stages its own 32 rows of the
+// chunk at `q_tile` (a 128 x D bf16 area: the tile's own bf16 Q shared memory,
+// free once the tile's last PV has finished, or a buffer of that size) in the
+// 128-byte-swizzled layout of the O tensor map, and writes them at once with a
+// TMA tensor store of a 32-row x 64-column box (rows past the sequence are
+// clipped; a warp whose rows all lie past it stores nothing). No warp waits for
+// another; each waits for its own stores to have read shared memory before it
+// leaves. `bh` is the head coordinate of the O tensor map (box rows 32).
+template <int D>
+__device__ __forceinline__ void store_rows_tma(const FwdParams& p, const RowMap& rm, int bh, int q_row0,
+                                               int r, int q_row, float m, float m_true, float l,
+                                               uint32_t tO, uint32_t q_tile, float o_scale = 1.f) {
+    const int lane = r & 31;
+    const int quarter = r >> 5;
+    const RowOut<D> out(p, rm, bh, 0, q_row, m, m_true, l, o_scale);
+    const uint32_t swz = static_cast<uint32_t>(r & 7);
+    const int wrow0 = q_row0 + quarter * 32;
+    const bool any_row = wrow0 < rm.len_q;
+#pragma unroll 1
+    for (int c = 0; c < D / 64; ++c) {
+        uint32_t a[32], b[32];
+        tmem_ld32(tO + c * 64, a);
+        tmem_ld32(tO + c * 64 + 32, b);
+        tmem_wait_ld();
+        const uint32_t line = q_tile + c * (kBM * 128) + r * 128;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t x0 = hh ? b[2 * i] : a[2 * i];
+                const uint32_t x1 = hh ? b[2 * i + 1] : a[2 * i + 1];
+                pk[i] = pack_bf16x2(__uint_as_float(x0) * out.f, __uint_as_float(x1) * out.f);
+            }
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu) {
+                const uint32_t u = static_cast<uint32_t>(hh * 4 + uu);
+                st_shared_v4(line + ((u ^ swz) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2], pk[4 * uu + 3]);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && any_row) {
+            tma_store_3d(&p.tm_o, q_tile + c * (kBM * 128) + quarter * (32 * 128), 64 * c, wrow0, bh);
+            bulk_commit_group();
+        }
+    }
+    out.finish(p);
+    if (lane == 0) bulk_wait_group_read0();
+    __syncwarp();
+}
+
 }  // namespace fa

@@ -95,8 +95,7 @@ struct LayoutTM {
     static constexpr int BAR_SFULL = BAR_KVEMPTY + STAGES;  // [tile] S_t(j) (and PV_t(j-1)) done
     static constexpr int BAR_PFULL = BAR_SFULL + Q_TILES;   // [tile] P_t(j) in TMEM (one arrival per warp)
     static constexpr int BAR_OFULL = BAR_PFULL + Q_TILES;   // [tile] last PV_t finished
-    static constexpr int BAR_OSTAGED = BAR_OFULL + Q_TILES; // [tile] bf16 O_t staged (one arrival per warp)
-    static constexpr int BAR_DRAIN = BAR_OSTAGED + Q_TILES;
+    static constexpr int BAR_DRAIN = BAR_OFULL + Q_TILES;
     static constexpr int NUM_BARS = BAR_DRAIN + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] tmem base, [1] abort
     static constexpr uint32_t BYTES = MISC_OFF + 16;
@@ -150,7 +149,6 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
         }
         for (int t = 0; t < QT; ++t) {
             mbar_init(bar(L::BAR_QFULL + t), 1);
-            mbar_init(bar(L::BAR_OSTAGED + t), 4);
             mbar_init(bar(L::BAR_SFULL + t), 1);
             mbar_init(bar(L::BAR_PFULL + t), 4);  // one arrival per warp of the group
             mbar_init(bar(L::BAR_OFULL + t), 1);
@@ -584,16 +582,16 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             // o_scale * O_t / l staged in the tile's own buffer and written with
             // TMA. Split mode: the partial state, O scaled by o_scale, per row.
             if (ok && !p.split_mode && n > 0)
-                store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m - kP8Shift, m_true, l, tO,
-                                  sbase + L::OST_OFF + t * L::OST_TILE_BYTES, bar(L::BAR_OSTAGED + t),
-                                  abort_flag, p.o_scale);
+                store_rows_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m - kP8Shift, m_true, l, tO,
+                                  sbase + L::OST_OFF + t * L::OST_TILE_BYTES, p.o_scale);
             else if (ok)
                 write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m - kP8Shift, m_true, l, tO, p.o_scale);
         } else {
             if (ok && !p.split_mode && !p.varlen && n > 0) {
-                // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA.
-                store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
-                                  sbase + L::Q_OFF + t * L::Q_TILE_BYTES, bar(L::BAR_OSTAGED + t), abort_flag);
+                // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA
+                // stores per warp.
+                store_rows_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
+                                  sbase + L::Q_OFF + t * L::Q_TILE_BYTES);
             } else if (ok) {
                 write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m, m_true, l, tO);
             }

@@ -31,7 +31,8 @@ struct FwdParams {
     CUtensorMap tm_q;  // bf16 [B*H][Nq][d], box {64, 128, 1}, 128B swizzle
     CUtensorMap tm_k;  // bf16 [B*H][Nk][d], box {64, BN, 1}
     CUtensorMap tm_v;  // same as tm_k
-    CUtensorMap tm_o;  // bf16 [B*H][Nq][d], box {64, 128, 1}, 128B swizzle (plain mode)
+    CUtensorMap tm_o;  // bf16 [B*H][Nq][d], box {64, 32 (d <= 128) or 128 (d = 256), 1},
+                       // 128B swizzle (plain mode)
     void* o;           // bf16 [B*H][Nq][d]      (plain mode)
     float* lse;        // fp32 [B*H][Nq]         (plain mode)
     float* ws_o;       // fp32 [S][B*H][Nq][d]   (split mode)
