@@ -269,6 +269,15 @@ def time_launches(fn, steps: int, stream, queue_ahead: bool = False):
     return [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
 
 
+def fill_splits(fa, B, H, Nq, d, sms):
+    """The largest split count whose split-KV grid still fits one CTA per SM."""
+    best = 1
+    for S in range(1, fa.FA_MAX_SPLITS + 1):
+        if fa.fa_fwd_grid_ctas(B, H, Nq, d, S) <= sms:
+            best = S
+    return best
+
+
 def extra_workloads(device, stream, reps: int = 20):
     """TFLOPS of the other benchmark workloads (seeded device-side N(0,1) bf16)."""
     import torch
@@ -301,9 +310,9 @@ def extra_workloads(device, stream, reps: int = 20):
             out[name] = {"tflops": round(flops / ms / 1e9, 1), "us": round(ms * 1e3, 1)}
         else:
             sweep = {}
-            # The printed split counts, plus the one that gives one CTA per SM.
+            # The printed split counts, plus the largest whose grid fits one CTA per SM.
             sms = torch.cuda.get_device_properties(device).multi_processor_count
-            fill = max(1, min(fa.FA_MAX_SPLITS, sms // fa.fa_fwd_grid_ctas(B, H, Nq, d, 1)))
+            fill = fill_splits(fa, B, H, Nq, d, sms)
             for S in sorted({1, 2, 3, 4, 16, 64, fill}):
                 ws = torch.empty(fa.fa_splitkv_workspace_bytes(B, H, Nq, d, S) // 4,
                                  device=device)
@@ -332,9 +341,9 @@ def extra_workloads(device, stream, reps: int = 20):
 
 def fp8_decode_workload(device, stream, reps):
     """The C5 decode shape (B=1, H=8, Nq=128, Nk=131072, d=128) with e4m3 Q, K, V
-    (descales 2^-5) through fa_fwd_fp8_splitkv + fa_combine, at 16 splits and
-    at the split count that gives one CTA per SM. K and V are half the bytes of
-    bf16; split_gbs counts the bytes the split kernel moves."""
+    (descales 2^-5) through fa_fwd_fp8_splitkv + fa_combine, at 16 splits and at
+    the largest split count whose grid fits one CTA per SM. K and V are half the
+    bytes of bf16; split_gbs counts the bytes the split kernel moves."""
     import torch
 
     import exact_attention_80_gb300 as fa
@@ -350,7 +359,7 @@ def fp8_decode_workload(device, stream, reps):
     lse = torch.empty((B, H, Nq), device=device)
     flops = metric_flops(B, H, Nq, Nk, d, False)
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    fill = max(1, min(fa.FA_MAX_SPLITS, sms // fa.fa_fwd_grid_ctas(B, H, Nq, d, 1)))
+    fill = fill_splits(fa, B, H, Nq, d, sms)
     res = {}
     for S in sorted({16, fill}):
         ws = torch.empty(fa.fa_splitkv_workspace_bytes(B, H, Nq, d, S) // 4, device=device)

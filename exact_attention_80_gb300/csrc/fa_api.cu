@@ -173,6 +173,7 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     const FwdConfig c = fwd_config(d);
     const long long ctas = grid_ctas(B, H, Nq, d, num_splits);
     if (ctas < 1 || ctas > 0x7fffffffll) return FA_ERR_SHAPE;
+    const bool dual = use_dual(Nq, d, num_splits, split_mode, vl != nullptr);
 
     FwdParams p;
     std::memset(&p, 0, sizeof(p));
@@ -238,14 +239,16 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     if (device_status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
 
     cudaError_t e = cudaErrorInvalidValue;
-    const unsigned grid = static_cast<unsigned>(ctas);
+    p.dual = dual ? 1 : 0;
+    const unsigned grid = static_cast<unsigned>(
+        dual ? static_cast<long long>(BH) * ((num_splits + 1) / 2) : ctas);
     if (f8_descale) {
-        e = (d == 128) ? launch_fwd_f8_d128(p, grid, stream) : cudaErrorInvalidValue;
+        if (d == 128) e = dual ? launch_fwd_f8_d128_dual(p, grid, stream) : launch_fwd_f8_d128(p, grid, stream);
         return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
     }
     switch (d) {
-        case 64: e = launch_fwd_d64(p, grid, stream); break;
-        case 128: e = launch_fwd_d128(p, grid, stream); break;
+        case 64: e = dual ? launch_fwd_d64_dual(p, grid, stream) : launch_fwd_d64(p, grid, stream); break;
+        case 128: e = dual ? launch_fwd_d128_dual(p, grid, stream) : launch_fwd_d128(p, grid, stream); break;
         case 256: e = launch_fwd_d256(p, grid, stream); break;
         default: break;
     }
@@ -380,6 +383,8 @@ long long fa_fwd_grid_ctas(int B, int H, int Nq, int d, int num_splits) {
     if (B < 1 || H < 1 || Nq < 1 || !fa::valid_d(d) || num_splits < 1 ||
         num_splits > FA_MAX_SPLITS)
         return -1;
+    if (fa::use_dual(Nq, d, num_splits, num_splits > 1, false))
+        return static_cast<long long>(B) * H * ((num_splits + 1) / 2);
     return fa::grid_ctas(B, H, Nq, d, num_splits);
 }
 

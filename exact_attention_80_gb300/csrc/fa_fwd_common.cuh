@@ -135,6 +135,56 @@ __device__ __forceinline__ void compute_work(const FwdParams& p, long long lin, 
     }
 }
 
+// Work of a dual-range CTA: split-KV with one query tile (Nq <= 128, dense).
+// Both query tiles of the CTA hold the same 128 rows; tile t takes key split
+// 2 * pair + t, so the two tiles still alternate on the tensor core. A tile
+// whose split index is past the last split has no work and writes nothing.
+struct WorkDual {
+    int bh;
+    int zq;
+    int q0;           // 0: the one query tile
+    int causal_off;
+    RowMap rm;
+    int split[2];     // key split of each tile (may be >= num_splits: no such split)
+    int kv_tile0[2];  // first key tile of each tile's split
+    int kv_end[2];    // exclusive key bound of each tile's split
+    int n[2];
+    int nmax;
+};
+
+// Pair `lin` of the dual-range grid: heads slowest, split pairs fastest.
+template <int BN>
+__device__ __forceinline__ void compute_work_dual(const FwdParams& p, long long lin, WorkDual& w) {
+    const int pairs = (p.num_splits + 1) / 2;
+    const int pair = static_cast<int>(lin % pairs);
+    w.bh = static_cast<int>(lin / pairs);
+    w.zq = w.bh;
+    w.q0 = 0;
+    w.rm.o_base = static_cast<long long>(w.bh) * p.Nq;
+    w.rm.lse_base = w.rm.o_base;
+    w.rm.o_stride = 1;
+    w.rm.len_q = p.Nq;
+    w.causal_off = p.causal_br ? p.Nk - p.Nq : 0;
+    const int total_tiles = (p.Nk + BN - 1) / BN;
+    w.nmax = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int s = 2 * pair + t;
+        w.split[t] = s;
+        const int t0 = min(s * p.kv_tiles_per_split, total_tiles);
+        const int t1 = min(t0 + p.kv_tiles_per_split, total_tiles);
+        w.kv_tile0[t] = t0;
+        w.kv_end[t] = min(p.Nk, t1 * BN);
+        int end = t1;
+        if (p.causal) {
+            const int last_key = min(kBM, p.Nq) - 1 + w.causal_off;
+            end = min(end, last_key < 0 ? 0 : last_key / BN + 1);
+        }
+        w.n[t] = (s < p.num_splits) ? max(0, end - t0) : 0;
+        w.nmax = max(w.nmax, w.n[t]);
+    }
+}
+
 // Bounded wait on an mbarrier phase. Returns false if this CTA is aborting
 // (honor_abort) or the wait ran past the limit (then raises the abort).
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const FwdParams& p,

@@ -6,4 +6,7 @@ namespace fa {
 cudaError_t launch_fwd_d128(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     return launch_fwd<128>(p, grid, stream);
 }
+cudaError_t launch_fwd_d128_dual(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+    return launch_fwd<128, false, true>(p, grid, stream);
+}
 }  // namespace fa

@@ -6,4 +6,7 @@ namespace fa {
 cudaError_t launch_fwd_d64(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     return launch_fwd<64>(p, grid, stream);
 }
+cudaError_t launch_fwd_d64_dual(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+    return launch_fwd<64, false, true>(p, grid, stream);
+}
 }  // namespace fa

@@ -5,4 +5,7 @@ namespace fa {
 cudaError_t launch_fwd_f8_d128(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     return launch_fwd<128, true>(p, grid, stream);
 }
+cudaError_t launch_fwd_f8_d128_dual(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+    return launch_fwd<128, true, true>(p, grid, stream);
+}
 }  // namespace fa

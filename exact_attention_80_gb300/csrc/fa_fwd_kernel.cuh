@@ -18,12 +18,15 @@ namespace fa {
 template <int D>
 using FwdLayout = std::conditional_t<D == 256, LayoutTP<D>, LayoutTM<D>>;
 
-// F8: e4m3 inputs (d = 64 or 128 only: the two-tile kernel).
-template <int D, bool F8 = false>
+// F8: e4m3 inputs. DUAL: dual-range split-KV CTAs (one query tile). Both are
+// forms of the two-tile kernel (d = 64 or 128).
+template <int D, bool F8 = false, bool DUAL = false>
 cudaError_t launch_fwd(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     using L = std::conditional_t<F8, LayoutTM<D, true>, FwdLayout<D>>;
     constexpr auto kernel = [] {
-        if constexpr (F8) return fa_fwd_tm8_kernel<D>;
+        if constexpr (F8 && DUAL) return fa_fwd_tm8d_kernel<D>;
+        else if constexpr (F8) return fa_fwd_tm8_kernel<D>;
+        else if constexpr (DUAL) return fa_fwd_tmd_kernel<D>;
         else if constexpr (D == 256) return fa_fwd_tp_kernel<D>;
         else return fa_fwd_tm_kernel<D>;
     }();

@@ -123,7 +123,174 @@ struct LayoutTM {
                   "register split must equal the launch allocation");
 };
 
+// Control warps of a dual-range CTA (split-KV with one query tile): the two
+// query tiles hold the same rows, Q is loaded once (tile 0's buffer) and read by
+// both tiles' S MMAs, and each tile streams the keys of its own split. K/V ring
+// entries in consumption order: K^0_0, K^1_0, then per step j and tile t (if the
+// tile has step j): V^t_j, then K^t_{j+1} if it has a next step. The issuer
+// takes each tile's step as one unit: wait P_t, V^t_j, PV_t; wait K^t_{j+1},
+// S_t(j+1); release both slots.
 template <int D, bool F8>
+__device__ __forceinline__ void tm_dual_control(const FwdParams& p, uint32_t sbase, uint32_t tmem,
+                                                volatile uint32_t* abort_flag, int warp) {
+    using L = LayoutTM<D, F8>;
+    constexpr int BN = L::BN;
+    constexpr int ST = L::STAGES;
+    auto bar = [&](int i) -> uint32_t { return sbase + L::BAR_OFF + 8u * i; };
+    WorkDual w;
+    compute_work_dual<BN>(p, blockIdx.x, w);
+    if (w.nmax == 0) return;
+    const bool leader = elect_one();
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (leader && !p.test_withhold_q) {
+            mbar_arrive_expect_tx(bar(L::BAR_QFULL + 0), L::Q_TILE_BYTES);
+#pragma unroll
+            for (int c = 0; c < L::CHUNKS; ++c)
+                tma_load_3d(sbase + L::Q_OFF + c * (kBM * 128), &p.tm_q, bar(L::BAR_QFULL + 0),
+                            L::CHUNK_ELEMS * c, w.q0, w.zq);
+        }
+        RingPos<ST> pos;
+        int issued = 0;
+        bool ok = true;
+        auto load_kv = [&](bool is_v, int t, int kv) -> bool {
+            if (issued >= ST) {
+                const bool okw = __all_sync(0xffffffffu, wait_phase(bar(L::BAR_KVEMPTY + pos.slot), pos.phase ^ 1u,
+                                                                    p, abort_flag, kStatusWaitKvEmpty));
+                if (!okw) return false;
+            }
+            if (leader) {
+                mbar_arrive_expect_tx(bar(L::BAR_KVFULL + pos.slot), L::SLOT_BYTES);
+                const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
+                const int row = ((t ? w.kv_tile0[1] : w.kv_tile0[0]) + kv) * BN;
+#pragma unroll
+                for (int c = 0; c < L::CHUNKS; ++c)
+                    tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
+                                bar(L::BAR_KVFULL + pos.slot), L::CHUNK_ELEMS * c, row, w.zq);
+            }
+            ++issued;
+            pos.advance();
+            return true;
+        };
+        for (int t = 0; t < 2 && ok; ++t)
+            if (w.n[t] > 0) ok = load_kv(false, t, 0);
+        for (int j = 0; j < w.nmax && ok; ++j) {
+            for (int t = 0; t < 2 && ok; ++t) {
+                if (j < w.n[t]) {
+                    ok = load_kv(true, t, j);
+                    if (ok && j + 1 < w.n[t]) ok = load_kv(false, t, j + 1);
+                }
+            }
+        }
+        if (ok) {
+            // Wait until the issuer has released every slot's last use, so no
+            // tcgen05.commit arrival is in flight when the CTA exits.
+            for (int e = max(0, issued - ST); e < issued && ok; ++e)
+                ok = __all_sync(0xffffffffu, wait_phase(bar(L::BAR_KVEMPTY + e % ST), (e / ST) & 1, p,
+                                                        abort_flag, kStatusWaitKvEmpty));
+        } else {
+            if (!p.test_withhold_q)
+                wait_phase(bar(L::BAR_QFULL + 0), 0, p, abort_flag, kStatusWaitDrain, false);
+            for (int e = max(0, issued - ST); e < issued; ++e)
+                wait_phase(bar(L::BAR_KVFULL + e % ST), (e / ST) & 1, p, abort_flag, kStatusWaitDrain,
+                           false);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        auto wait_all = [&](uint32_t b, uint32_t parity, unsigned what) {
+            return __all_sync(0xffffffffu, wait_phase(b, parity, p, abort_flag, what));
+        };
+        constexpr uint32_t IDESC_S =
+            F8 ? make_idesc_e4m3(kBM, BN, false, false) : make_idesc_bf16(kBM, BN, false, false);
+        constexpr uint32_t IDESC_O =
+            F8 ? make_idesc_e4m3(kBM, D, false, true) : make_idesc_bf16(kBM, D, false, true);
+        const uint64_t kmaj0 = make_sdesc_sw128(sbase, 16, 1024);
+        const uint64_t vmn0 = make_sdesc_sw128(sbase, BN * 128, 1024);
+        const uint32_t kmaj_lo = static_cast<uint32_t>(kmaj0);
+        const uint32_t kmaj_hi = static_cast<uint32_t>(kmaj0 >> 32);
+        const uint32_t vmn_lo = static_cast<uint32_t>(vmn0);
+        const uint32_t vmn_hi = static_cast<uint32_t>(vmn0 >> 32);
+        auto desc = [](uint32_t lo, uint32_t hi, uint32_t off) -> uint64_t {
+            return (static_cast<uint64_t>(hi) << 32) | (lo + (off >> 4));
+        };
+        // S_t = Q K^T from the one Q tile; O_t += P_t V as in the two-tile kernel.
+        auto issue_s = [&](int t, int slot) {
+            const uint32_t kb = L::SLOT_OFF + slot * L::SLOT_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < D / L::K_MMA; ++kk) {
+                const uint32_t in_row = (kk & 3) * 32;
+                const uint64_t a = desc(kmaj_lo, kmaj_hi, L::Q_OFF + (kk >> 2) * (kBM * 128) + in_row);
+                const uint64_t b = desc(kmaj_lo, kmaj_hi, kb + (kk >> 2) * (BN * 128) + in_row);
+                if (leader) {
+                    if constexpr (F8) umma_ss_f8(tmem + L::S_COL(t), a, b, IDESC_S, kk > 0 ? 1u : 0u);
+                    else umma_ss(tmem + L::S_COL(t), a, b, IDESC_S, kk > 0 ? 1u : 0u);
+                }
+            }
+        };
+        auto issue_pv = [&](int t, int slot, bool accumulate) {
+            const uint32_t vb = L::SLOT_OFF + slot * L::SLOT_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BN / L::K_MMA; ++kk) {
+                const uint64_t b = desc(vmn_lo, vmn_hi, vb + kk * (L::K_MMA * 128));
+                if (leader) {
+                    if constexpr (F8)
+                        umma_ts_f8(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8, b, IDESC_O,
+                                   (accumulate || kk > 0) ? 1u : 0u);
+                    else
+                        umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8, b, IDESC_O,
+                                (accumulate || kk > 0) ? 1u : 0u);
+                }
+            }
+        };
+        RingPos<ST> pos;
+        auto next_slot = [&](int& slot) -> bool {
+            slot = pos.slot;
+            if (!wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull)) return false;
+            pos.advance();
+            return true;
+        };
+        bool ok = wait_all(bar(L::BAR_QFULL + 0), 0, kStatusWaitQ);
+        for (int t = 0; t < 2 && ok; ++t) {
+            if (w.n[t] == 0) continue;
+            int ks;
+            ok = next_slot(ks);
+            if (!ok) break;
+            tc_fence_after();
+            issue_s(t, ks);
+            if (leader) umma_commit(bar(L::BAR_SFULL + t));
+            if (leader) umma_commit(bar(L::BAR_KVEMPTY + ks));
+        }
+        for (int j = 0; j < w.nmax && ok; ++j) {
+            for (int t = 0; t < 2 && ok; ++t) {
+                if (j >= w.n[t]) continue;
+                ok = wait_all(bar(L::BAR_PFULL + t), j & 1, kStatusWaitP);
+                int vs = 0;
+                if (ok) ok = next_slot(vs);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(t, vs, j > 0);
+                if (j + 1 < w.n[t]) {
+                    int ks;
+                    ok = next_slot(ks);
+                    if (!ok) break;
+                    issue_s(t, ks);
+                    if (leader) umma_commit(bar(L::BAR_SFULL + t));
+                    if (leader) umma_commit(bar(L::BAR_KVEMPTY + ks));
+                } else {
+                    if (leader) umma_commit(bar(L::BAR_OFULL + t));
+                }
+                if (leader) umma_commit(bar(L::BAR_KVEMPTY + vs));
+            }
+        }
+        // Every MMA this thread issued must finish before TMEM can be freed.
+        if (leader) umma_commit(bar(L::BAR_DRAIN));
+        wait_phase(bar(L::BAR_DRAIN), 0, p, abort_flag, kStatusWaitDrain, false);
+    }
+}
+
+// DUAL: split-KV with one query tile, both tiles on the same rows (see
+// tm_dual_control); the softmax groups then take their tile's own split.
+template <int D, bool F8, bool DUAL = false>
 __device__ __forceinline__ void tm_forward(const FwdParams& p) {
     using L = LayoutTM<D, F8>;
     constexpr int QT = L::Q_TILES;
@@ -177,6 +344,9 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
       if constexpr (L::REG_SPLIT) setmaxnreg_dec<L::CTRL_REGS>();
       // The work record is derived inside each role, after its register limit
       // is set, so that no role carries fields it does not use.
+      if constexpr (DUAL) {
+        tm_dual_control<D, F8>(p, sbase, tmem, abort_flag, warp);
+      } else {
       Work<QT> w;
       compute_work<QT, BN>(p, blockIdx.x, w);
       if (warp == 0) {
@@ -409,15 +579,28 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             wait_phase(bar(L::BAR_DRAIN), 0, p, abort_flag, kStatusWaitDrain, false);
         }
       }
+      }  // !DUAL
     } else {
         // ------------------------------------------------------------ softmax
         if constexpr (L::REG_SPLIT) setmaxnreg_inc<L::SOFTMAX_REGS>();
-        Work<QT> w;
-        compute_work<QT, BN>(p, blockIdx.x, w);
+        std::conditional_t<DUAL, WorkDual, Work<QT>> w;
+        if constexpr (DUAL) compute_work_dual<BN>(p, blockIdx.x, w);
+        else compute_work<QT, BN>(p, blockIdx.x, w);
         const int t = (warp - 4) >> 2;
         const int quarter = warp & 3;  // TMEM lane quarter this warp may access
         const int r = quarter * 32 + lane;
-        const int q_row = w.q0 + t * kBM + r;
+        const int q_row = w.q0 + (DUAL ? 0 : t * kBM) + r;
+        // This tile's key split: the CTA's, or its own in a dual-range CTA.
+        int kv_tile0_t, kv_end_t, split_t;
+        if constexpr (DUAL) {
+            kv_tile0_t = t ? w.kv_tile0[1] : w.kv_tile0[0];
+            kv_end_t = t ? w.kv_end[1] : w.kv_end[0];
+            split_t = t ? w.split[1] : w.split[0];
+        } else {
+            kv_tile0_t = w.kv_tile0;
+            kv_end_t = w.kv_end;
+            split_t = w.split;
+        }
         const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t tS = tmem + lane_field + L::S_COL(t);
         const uint32_t tO = tmem + lane_field + L::O_COL(t);
@@ -457,8 +640,8 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             // Mask: keys past the split / sequence end, and (causal) keys after
             // this row + causal_off. Keys past the sequence end are zero fill
             // (or the next packed sequence's tokens), so they must become -inf.
-            const int kv0 = (w.kv_tile0 + j) * BN;
-            int valid = w.kv_end - kv0;
+            const int kv0 = (kv_tile0_t + j) * BN;
+            int valid = kv_end_t - kv0;
             if (p.causal) valid = min(valid, q_row + w.causal_off - kv0 + 1);
             if (valid < BN) {
 #pragma unroll
@@ -584,16 +767,16 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             if (ok && !p.split_mode && n > 0)
                 store_rows_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m - kP8Shift, m_true, l, tO,
                                   sbase + L::OST_OFF + t * L::OST_TILE_BYTES, p.o_scale);
-            else if (ok)
-                write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m - kP8Shift, m_true, l, tO, p.o_scale);
+            else if (ok && (!DUAL || split_t < p.num_splits))
+                write_row<D>(p, w.rm, w.bh, split_t, q_row, n, m - kP8Shift, m_true, l, tO, p.o_scale);
         } else {
             if (ok && !p.split_mode && !p.varlen && n > 0) {
                 // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA
                 // stores per warp.
                 store_rows_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
                                   sbase + L::Q_OFF + t * L::Q_TILE_BYTES);
-            } else if (ok) {
-                write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m, m_true, l, tO);
+            } else if (ok && (!DUAL || split_t < p.num_splits)) {
+                write_row<D>(p, w.rm, w.bh, split_t, q_row, n, m, m_true, l, tO);
             }
         }
     }
@@ -618,6 +801,18 @@ template <int D>
 __global__ void __launch_bounds__(LayoutTM<D, true>::THREADS, 1)
     fa_fwd_tm8_kernel(const __grid_constant__ FwdParams p) {
     tm_forward<D, true>(p);
+}
+
+// Dual-range split-KV CTAs (one query tile), bf16 and e4m3 inputs.
+template <int D>
+__global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
+    fa_fwd_tmd_kernel(const __grid_constant__ FwdParams p) {
+    tm_forward<D, false, true>(p);
+}
+template <int D>
+__global__ void __launch_bounds__(LayoutTM<D, true>::THREADS, 1)
+    fa_fwd_tm8d_kernel(const __grid_constant__ FwdParams p) {
+    tm_forward<D, true, true>(p);
 }
 
 }  // namespace fa

@@ -55,6 +55,7 @@ struct FwdParams {
     int n_units;             // query units of (tiles per CTA * 128) rows per head
     int kv_tiles_per_split;  // ceil(ceil(Nk/BN) / num_splits)
     int head_group;          // heads per scheduling group (CTA order)
+    int dual;                // 1: dual-range split CTAs (split mode, Nq <= 128, d <= 128)
     float scale_log2;        // scale * log2(e) (8-bit inputs: times the Q and K descales)
     float o_scale;           // 8-bit inputs: the V descale, applied to O at the end
     long long wait_limit;    // cycles
@@ -77,6 +78,16 @@ cudaError_t launch_fwd_d128(const FwdParams& p, unsigned grid, cudaStream_t stre
 cudaError_t launch_fwd_d256(const FwdParams& p, unsigned grid, cudaStream_t stream);
 // e4m3 Q, K, V (tm_q/tm_k/tm_v are byte maps, box {128, rows, 1}); d = 128.
 cudaError_t launch_fwd_f8_d128(const FwdParams& p, unsigned grid, cudaStream_t stream);
+// Dual-range split-KV CTAs (p.dual = 1): grid B*H*ceil(num_splits / 2).
+cudaError_t launch_fwd_d64_dual(const FwdParams& p, unsigned grid, cudaStream_t stream);
+cudaError_t launch_fwd_d128_dual(const FwdParams& p, unsigned grid, cudaStream_t stream);
+cudaError_t launch_fwd_f8_d128_dual(const FwdParams& p, unsigned grid, cudaStream_t stream);
+
+// Split-KV launches with one query tile per head (Nq <= 128, d <= 128, dense)
+// run dual-range CTAs: two splits per CTA.
+inline bool use_dual(int Nq, int d, int num_splits, int split_mode, bool varlen) {
+    return split_mode && !varlen && num_splits >= 2 && Nq <= 128 && d <= 128;
+}
 
 cudaError_t launch_combine(const float* ws_o, const float* ws_m, const float* ws_l, void* o,
                            float* lse, long long rows, int num_splits, int d,

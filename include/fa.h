@@ -198,8 +198,12 @@ fa_status fa_fwd_fp8_splitkv(const void* q, const void* k, const void* v, float 
  * fa_fwd_splitkv would launch for this shape: B * H * ceil(Nq / BM) * num_splits,
  * BM = 256 query rows per CTA for d <= 128 (two 128-row tiles) and 128 for
  * d = 256 ("AI 大模型之 FlashAttention_02", section "从头级并行转向序列级并行" and
- * the printed CTA counts of section "本册配套实验验证记录"). Returns -1 when an
- * argument is out of range. Host-only; launches nothing.
+ * the printed CTA counts of section "本册配套实验验证记录"). Split-KV launches
+ * with num_splits >= 2, Nq <= 128 and d <= 128 run two splits per CTA (the two
+ * query-tile slots of a CTA hold the same rows, each with its own split), so
+ * they launch B * H * ceil(num_splits / 2) CTAs. fa_fwd_fp8 and
+ * fa_fwd_fp8_splitkv launch the same grids as fa_fwd and fa_fwd_splitkv.
+ * Returns -1 when an argument is out of range. Host-only; launches nothing.
  */
 long long fa_fwd_grid_ctas(int B, int H, int Nq, int d, int num_splits);
 

@@ -165,8 +165,12 @@ def test_cta_counts_match_printed_schedule(lib):
     assert fa.fa_fwd_grid_ctas(1, 8, 8192, 128) == by_tile[(1, 8, 8192, 256)]
     assert fa.fa_fwd_grid_ctas(1, 8, 8192, 64) == by_tile[(1, 8, 8192, 256)]
     assert fa.fa_fwd_grid_ctas(1, 8, 8192, 256) == by_tile[(1, 8, 8192, 128)]
-    # Splits multiply the grid; one CTA per head when a head has one query unit.
-    assert fa.fa_fwd_grid_ctas(1, 8, 128, 128, 64) == 8 * 64
+    # Splits multiply the grid; with one query tile per head, two splits share a
+    # CTA (one per query-tile slot).
+    assert fa.fa_fwd_grid_ctas(1, 8, 128, 128, 64) == 8 * 32
+    assert fa.fa_fwd_grid_ctas(1, 8, 128, 128, 19) == 8 * 10
+    assert fa.fa_fwd_grid_ctas(1, 8, 129, 128, 4) == 8 * 4
+    assert fa.fa_fwd_grid_ctas(1, 8, 128, 256, 4) == 8 * 4
     assert fa.fa_fwd_grid_ctas(1, 8, 8192, 128, 1) > g["heads_only_ctas"]["ctas"]
     assert fa.fa_fwd_grid_ctas(1, 8, 128, 100, 1) == -1
 

@@ -141,3 +141,15 @@ def test_fp8_decode_shape_split():
     o_ref, lse_ref = ofp8.attention_fp8_f64(q8[0, h], k8[0, h], v8[0, h], *descales, scale)
     sigma = ofp8.p_rounding_sigma(q8[0, h], k8[0, h], v8[0, h], *descales, scale)
     check_fp8(o[0, h], lse[0, h], o_ref, lse_ref, sigma, "c5 head 5")
+
+
+@pytest.mark.parametrize("S,Nq", [(2, 128), (7, 100), (40, 1)])
+def test_fp8_dual_range_split(S, Nq):
+    """e4m3 split-KV with one query tile (two splits per CTA), odd split counts
+    and splits without keys, against the oracle."""
+    descales = (2.0 ** -5, 0.02, 0.3)
+    q8, k8, v8, scale, o, lse = run_fp8(2, 2, Nq, 4000, "bottom_right", 5700 + S, descales,
+                                        num_splits=S)
+    o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, "bottom_right")
+    sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, "bottom_right")
+    check_fp8(o, lse, o_ref, lse_ref, sigma, f"dual S={S} Nq={Nq}")

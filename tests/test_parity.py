@@ -271,6 +271,24 @@ def test_split_invariance(causal):
         assert (x - outs[0]).abs().max().item() <= MAX_ABS
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("S", [2, 3, 5, 40])
+@pytest.mark.parametrize("Nq,causal", [(1, False), (77, False), (128, True), (100, "bottom_right"),
+                                       (64, "bottom_right")])
+def test_dual_range_split(d, S, Nq, causal):
+    """Split-KV with one query tile runs two splits per CTA (each query-tile
+    slot holds the same rows with its own split): odd split counts leave the
+    last CTA's second slot without a split, and 40 splits over 4000 keys leave
+    splits without keys. Element by element against the oracle."""
+    B, H, Nk = 2, 3, 4000
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 7100 + S + Nq)
+    scale = f32(1.0 / math.sqrt(d))
+    o_ref, lse_ref = oracle.attention_f64(to_f64(q), to_f64(k), to_f64(v), scale, causal)
+    o, lse = run_gpu(q, k, v, causal, scale, num_splits=S)
+    check(o, lse, o_ref, lse_ref, f"dual d={d} S={S} Nq={Nq} {causal}")
+    assert fa.fa_fwd_grid_ctas(B, H, Nq, d, S) == B * H * ((S + 1) // 2)
+
+
 @pytest.mark.parametrize("d", [64, 128, 256])
 def test_bottom_right_rows_without_keys_split(d):
     """Bottom-right with Nq > Nk through split-KV + combine: rows that see no key
