@@ -37,6 +37,13 @@
 // sets a shared abort flag and a bit in the device status word, the others
 // leave at their next wait, in-flight TMA copies and MMAs are waited for
 // (again bounded), TMEM is freed and the CTA exits.
+//
+// Compile-time forms of the one body (tm_forward<D, F8, DUAL>):
+//   F8    e4m3 Q, K, V: kind::f8f6f4 MMAs, P packed four e4m3 per TMEM column,
+//         bf16 O staged in buffers of its own (fa_fwd_tm8_kernel).
+//   DUAL  split-KV with one query tile: both tile slots on the same rows, each
+//         with its own key split (tm_dual_control; fa_fwd_tmd_kernel,
+//         fa_fwd_tm8d_kernel).
 #pragma once
 
 #include <type_traits>
