@@ -20,6 +20,9 @@ Pages this oracle follows (cited by title and section):
   statistics (``oracle.fp8``: the attention of the encoded values, an e4m3
   decoder written from the format's bit fields, and the size of the error that
   rounding P to e4m3 adds).
+* The FA-2 page, sections "warp之间怎样减少通信" and "训练与部署 切分与归约的反向
+  一致性" — the training backward, dQ, dK, dV with dK and dV accumulated across
+  query rows, and a printed score gradient (``oracle.backward``).
 * "AI 大模型之 FlashAttention_02" (the FA-2 page), section 3.1 and 4.1 — exact
   softmax attention, O(S²d); section "工程实操 沿键切分的归约与沿查询切分的区别" —
   split partial states (m, l, u) and the merge that rescales by exp(m_b − M).
@@ -39,4 +42,4 @@ from .attention import (  # noqa: F401
     merge_states_f64,
     normalise_then_average_f64,
 )
-from . import fp8  # noqa: F401,E402
+from . import backward, fp8  # noqa: F401,E402

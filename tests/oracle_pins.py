@@ -573,6 +573,99 @@ def pin_p_sigma_simulated(f8):
     assert np.allclose(err.std(axis=0), sig[0], rtol=0.1, atol=0)
 
 
+
+# --------------------------------------------------------------------------
+# Backward (module ``oracle.backward``): gradients of O with respect to Q, K, V.
+# --------------------------------------------------------------------------
+
+def pin_bwd_printed_gradient(bw, orc):
+    """The FA-2 page's printed score gradient (split-gradient section): with the
+    four-key example as a one-query, d = 1 attention (q = 1, k_j = score_j,
+    v_j = value_j, scale 1) and dO = 1, dK_j = dO * dS_j * q is the gradient of
+    the output with respect to score j."""
+    g = _golden("split_gradient.json")
+    q, k, v = _example_as_attention(g)
+    dq, dk, dv = bw.attention_backward_f64(q, k, v, np.ones((1, 1)), 1.0)
+    tol = _printed_tol(g) + 1e-8
+    assert np.allclose(dk[:, 0], g["d_output_d_scores"], rtol=0, atol=tol), dk[:, 0]
+    # dV_j = p_j; dQ = sum_j dS_j k_j.
+    p = np.exp(np.array(g["scores"]) - max(g["scores"]))
+    p /= p.sum()
+    assert np.allclose(dv[:, 0], p, rtol=0, atol=1e-15)
+    assert np.allclose(dq[0, 0], (dk[:, 0] * np.array(g["scores"])).sum(), rtol=0, atol=1e-14)
+
+
+def _loss(orc, q, k, v, do, scale, causal):
+    return float((orc.attention_f64(q, k, v, scale, causal)[0] * do).sum())
+
+
+def pin_bwd_finite_differences(bw, orc):
+    """Central differences of L = sum(dO * O) from the forward oracle, along
+    random directions in Q, K and V, for no mask and both causal alignments."""
+    rng = np.random.default_rng(43)
+    for causal, nq, nk in ((False, 5, 7), (True, 6, 6), ("bottom_right", 4, 9), ("bottom_right", 7, 3)):
+        q = rng.standard_normal((2, nq, 3))
+        k = rng.standard_normal((2, nk, 3))
+        v = rng.standard_normal((2, nk, 4))
+        do = rng.standard_normal((2, nq, 4))
+        dq, dk, dv = bw.attention_backward_f64(q, k, v, do, 0.7, causal)
+        h = 1e-6
+        for x, gx, which in ((q, dq, 0), (k, dk, 1), (v, dv, 2)):
+            u = rng.standard_normal(x.shape)
+            args = [q, k, v]
+            args[which] = x + h * u
+            lp = _loss(orc, *args, do, 0.7, causal)
+            args[which] = x - h * u
+            lm = _loss(orc, *args, do, 0.7, causal)
+            assert abs((lp - lm) / (2 * h) - (gx * u).sum()) <= 1e-7, (causal, which)
+
+
+def pin_bwd_torch_autograd(bw, orc):
+    """Against torch's float64 autograd through scaled_dot_product_attention on
+    the CPU, with an explicit boolean mask for the causal cases."""
+    import torch
+    rng = np.random.default_rng(47)
+    for causal, nq, nk in ((False, 9, 11), (True, 8, 8), ("bottom_right", 5, 12)):
+        q = rng.standard_normal((2, 3, nq, 6))
+        k = rng.standard_normal((2, 3, nk, 6))
+        v = rng.standard_normal((2, 3, nk, 5))
+        do = rng.standard_normal((2, 3, nq, 5))
+        tq, tk, tv = (torch.tensor(x, requires_grad=True) for x in (q, k, v))
+        mask = None
+        if causal:
+            off = 0 if causal is True else nk - nq
+            mask = torch.ones(nq, nk, dtype=torch.bool).tril(off)
+        out = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=0.45)
+        out.backward(torch.tensor(do))
+        dq, dk, dv = bw.attention_backward_f64(q, k, v, do, 0.45, causal)
+        for got, want in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+            assert np.allclose(got, want.numpy(), rtol=1e-10, atol=1e-12), causal
+
+
+def pin_bwd_closed_forms(bw, orc):
+    """One key: P = 1, so dV = sum of dO over the queries and dQ = dK = 0. Key
+    gradients sum to zero over the keys (each row of dS sums to zero)."""
+    rng = np.random.default_rng(53)
+    q = rng.standard_normal((4, 3))
+    k = rng.standard_normal((1, 3))
+    v = rng.standard_normal((1, 2))
+    do = rng.standard_normal((4, 2))
+    dq, dk, dv = bw.attention_backward_f64(q, k, v, do, 0.9)
+    assert np.allclose(dv[0], do.sum(axis=0), rtol=0, atol=1e-14)
+    assert np.abs(dq).max() <= 1e-14 and np.abs(dk).max() <= 1e-14
+    k = rng.standard_normal((6, 3))
+    v = rng.standard_normal((6, 2))
+    dq, dk, dv = bw.attention_backward_f64(q, k, v, do, 0.9, True)
+    assert np.abs(dk.sum(axis=0)).max() <= 1e-12
+
+
+BWD_PINS = [
+    pin_bwd_printed_gradient,
+    pin_bwd_finite_differences,
+    pin_bwd_torch_autograd,
+    pin_bwd_closed_forms,
+]
+
 FP8_PINS = [
     pin_e4m3_hand_values,
     pin_e4m3_vs_torch,

@@ -13,11 +13,13 @@ import warnings
 
 import pytest
 
-from oracle_pins import ALL_PINS, FP8_PINS
+import oracle
+from oracle_pins import ALL_PINS, BWD_PINS, FP8_PINS
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                    "oracle", "attention.py")
 SRC_FP8 = os.path.join(os.path.dirname(SRC), "fp8.py")
+SRC_BWD = os.path.join(os.path.dirname(SRC), "backward.py")
 
 MUTANTS = [
     ("dropped scale", "s = float(scale) * (q[rows] @ k.T)", "s = (q[rows] @ k.T)"),
@@ -107,6 +109,43 @@ def test_fp8_mutant_is_caught(name, find, repl):
     for pin in FP8_PINS:
         try:
             pin(mod)
+        except Exception as e:
+            caught.append((pin.__name__, type(e).__name__))
+    assert caught, f"mutant '{name}' passed every pin"
+
+
+BWD_MUTANTS = [
+    ("dV with the keys reversed", "dv[g] = p.T @ doh[g]", "dv[g] = p[:, ::-1].T @ doh[g]"),
+    ("dP from K instead of V", "dp = doh[g] @ vh[g].T", "dp = doh[g] @ np.resize(kh[g], vh[g].shape).T"),
+    ("D dropped", "ds = p * (dp - dd)", "ds = p * dp"),
+    ("D sign", "ds = p * (dp - dd)", "ds = p * (dp + dd)"),
+    ("D from the row max", "dd = (p * dp).sum(axis=1, keepdims=True)", "dd = dp.max(axis=1, keepdims=True)"),
+    ("dQ without scale", "dq[g] = float(scale) * (ds @ kh[g])", "dq[g] = ds @ kh[g]"),
+    ("dK without scale", "dk[g] = float(scale) * (ds.T @ qh[g])", "dk[g] = ds.T @ qh[g]"),
+    ("dK from dS, not its transpose", "dk[g] = float(scale) * (ds.T @ qh[g])", "dk[g] = float(scale) * (ds[::-1, ::-1].T @ qh[g])[:kh.shape[1]]"),
+    ("mask ignored", "            s = np.where(cols > rows + off, -np.inf, s)\n", "            pass\n"),
+    ("unnormalised P", "p = np.where(l > 0, e / np.where(l > 0, l, 1.0), 0.0)", "p = e"),
+]
+
+
+def _load_bwd_mutant(find, repl):
+    with open(SRC_BWD, encoding="utf-8") as f:
+        src = f.read()
+    assert src.count(find) == 1, f"mutation anchor not unique: {find!r}"
+    src = src.replace(find, repl).replace("from .attention import", "from oracle.attention import")
+    mod = types.ModuleType("oracle_bwd_mutant")
+    exec(compile(src, "oracle_bwd_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name,find,repl", BWD_MUTANTS, ids=[m[0] for m in BWD_MUTANTS])
+def test_bwd_mutant_is_caught(name, find, repl):
+    mod = _load_bwd_mutant(find, repl)
+    caught = []
+    warnings.simplefilter("ignore", RuntimeWarning)
+    for pin in BWD_PINS:
+        try:
+            pin(mod, oracle)
         except Exception as e:
             caught.append((pin.__name__, type(e).__name__))
     assert caught, f"mutant '{name}' passed every pin"
