@@ -66,6 +66,10 @@ def load_library() -> ctypes.CDLL:
     lib.fa_fwd_fp8.restype = i
     lib.fa_fwd_fp8_splitkv.argtypes = [vp, vp, vp, f, f, f, vp, i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_fp8_splitkv.restype = i
+    lib.fa_bwd_workspace_bytes.argtypes = [i, i, i, i]
+    lib.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
+    lib.fa_bwd.restype = i
     lib.fa_fwd_grid_ctas.argtypes = [i, i, i, i, i]
     lib.fa_fwd_grid_ctas.restype = ctypes.c_longlong
     lib.fa_device_status.argtypes = [vp, i]
@@ -198,6 +202,36 @@ def attention_fp8(q, k, v, q_descale: float = 1.0, k_descale: float = 1.0, v_des
                            stream)
         fa_combine(ws, o, lse, B, H, Nq, d, num_splits, stream)
     return o, lse
+
+
+def fa_bwd_workspace_bytes(B: int, H: int, Nq: int, d: int) -> int:
+    return int(load_library().fa_bwd_workspace_bytes(B, H, Nq, d))
+
+
+def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal=False,
+           scale: float | None = None, stream=None):
+    """Backward into caller-owned ``dq``, ``dk``, ``dv`` (bf16, shaped like q, k,
+    v), from bf16 ``o`` and ``dout`` and the forward's fp32 ``lse``; ``workspace``
+    fp32 of at least ``fa_bwd_workspace_bytes`` bytes (include/fa.h, fa_bwd)."""
+    B, H, Nq, Nk, d = _bhnd(q, k, v)
+    scale = default_scale(d) if scale is None else float(scale)
+    st = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
+                               _ptr(dk), _ptr(dv), _ptr(workspace), B, H, Nq, Nk, d, scale,
+                               causal_code(causal), _stream_handle(stream))
+    _check(st, "fa_bwd")
+
+
+def attention_backward(q, k, v, o, lse, dout, causal=False, scale: float | None = None,
+                       stream=None):
+    """Allocate ``(dq, dk, dv)`` and the workspace and run :func:`fa_bwd`."""
+    import torch
+
+    B, H, Nq, Nk, d = _bhnd(q, k, v)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(max(1, fa_bwd_workspace_bytes(B, H, Nq, d) // 4), dtype=torch.float32,
+                     device=q.device)
+    fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, ws, causal, scale, stream)
+    return dq, dk, dv
 
 
 def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, causal=False,

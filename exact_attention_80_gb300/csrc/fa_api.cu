@@ -309,6 +309,56 @@ fa_status fa_fwd_fp8_splitkv(const void* q, const void* k, const void* v, float 
                               nullptr, ds);
 }
 
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d) {
+    if (B < 1 || H < 1 || Nq < 1 || d != 128) return 0;
+    const size_t rows = static_cast<size_t>(B) * H * Nq;
+    return rows * (static_cast<size_t>(d) + 1) * sizeof(float);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
+                 int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream) {
+    fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
+    if (s != FA_OK) return s;
+    if (d != 128) return FA_ERR_HEADDIM;
+    if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
+    if (!o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+    if (!fa::aligned(o, 16) || !fa::aligned(dout, 16) || !fa::aligned(lse, 4) ||
+        !fa::aligned(dq, 16) || !fa::aligned(dk, 16) || !fa::aligned(dv, 16))
+        return FA_ERR_ALIGN;
+    if (!workspace || !fa::aligned(workspace, 16)) return FA_ERR_WORKSPACE;
+    const int BH = B * H;
+    const long long rows = static_cast<long long>(BH) * Nq;
+    float* dq_acc = static_cast<float*>(workspace);
+    float* dd = dq_acc + static_cast<size_t>(rows) * d;
+    fa::BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!fa::encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
+        !fa::encode_rows_map(&p.tm_k, k, d, Nk, BH, 128) ||
+        !fa::encode_rows_map(&p.tm_v, v, d, Nk, BH, 128) ||
+        !fa::encode_rows_map(&p.tm_do, dout, d, Nq, BH, 128))
+        return FA_ERR_CUDA;
+    p.lse = lse;
+    p.dd = dd;
+    p.dq_acc = dq_acc;
+    p.dk = dk;
+    p.dv = dv;
+    p.BH = BH;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.causal = causal ? 1 : 0;
+    p.causal_br = (causal == FA_CAUSAL_BOTTOM_RIGHT) ? 1 : 0;
+    p.k_tiles = (Nk + 127) / 128;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_limit = fa::kDefaultWaitLimit;
+    if (fa::device_status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::launch_bwd_pre(o, dout, dd, dq_acc, rows, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::launch_bwd_main(p, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::launch_bwd_dq(dq_acc, dq, rows * d, scale, stream) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
 size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
     if (B < 1 || H < 1 || Nq < 1 || !fa::valid_d(d) || num_splits < 1 ||
         num_splits > FA_MAX_SPLITS)

@@ -63,6 +63,32 @@ struct FwdParams {
     unsigned* status;        // device status word
 };
 
+// Backward (d = 128): one CTA per (head, 128-key tile).
+struct BwdParams {
+    CUtensorMap tm_q;   // bf16 [B*H][Nq][d], box {64, 128, 1}
+    CUtensorMap tm_k;   // bf16 [B*H][Nk][d], box {64, 128, 1}
+    CUtensorMap tm_v;   // same as tm_k
+    CUtensorMap tm_do;  // same as tm_q (dO)
+    const float* lse;   // fp32 [B*H][Nq], natural log (the forward's LSE)
+    const float* dd;    // fp32 [B*H][Nq], D_i = sum_c dO_ic O_ic
+    float* dq_acc;      // fp32 [B*H][Nq][d], zeroed, unscaled dS K accumulated
+    void* dk;           // bf16 [B*H][Nk][d]
+    void* dv;           // bf16 [B*H][Nk][d]
+    int BH, Nq, Nk;
+    int causal, causal_br;
+    int k_tiles;        // ceil(Nk / 128)
+    float scale;
+    float scale_log2;   // scale * log2(e)
+    long long wait_limit;
+    unsigned* status;
+};
+
+cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dd, float* dq_acc, long long rows,
+                           cudaStream_t stream);
+cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, long long elems, float scale,
+                          cudaStream_t stream);
+
 struct FwdConfig {
     int q_tiles;  // 128-row query tiles per CTA
     int bn;       // keys per KV tile

@@ -72,6 +72,13 @@ def make_qkv_fp8(B: int, H: int, Nq: int, Nk: int, d: int, seed: int,
     return tuple(out)
 
 
+def make_grad_output(B: int, H: int, Nq: int, d: int, seed: int):
+    """Upstream gradient dO for the backward: N(0, 1) in float32 from its own
+    seeded generator, rounded to bf16; a CPU tensor [B, H, Nq, d]."""
+    g = torch.Generator().manual_seed(int(seed))
+    return torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
 def to_f64(t):
     """Exact upcast of a (bf16) torch tensor to a float64 numpy array."""
     return t.to(torch.float64).numpy()

@@ -194,6 +194,36 @@ fa_status fa_fwd_fp8_splitkv(const void* q, const void* k, const void* v, float 
                              cudaStream_t stream);
 
 /*
+ * fa_bwd_workspace_bytes — bytes of the fp32 workspace fa_bwd needs: a dQ
+ * accumulator [B][H][Nq][d], then D [B][H][Nq]. 0 when an argument is out of
+ * range (d must be 128).
+ */
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d);
+
+/*
+ * fa_bwd — attention backward: dQ, dK, dV of O = softmax(scale Q K^T [+ mask]) V
+ * for the upstream gradient dO ("AI 大模型之 FlashAttention_02", sections
+ * "warp之间怎样减少通信" and "训练与部署 切分与归约的反向一致性": dK and dV are
+ * accumulated across query rows, a reduction direction the forward does not
+ * have).
+ *   q, o, dout [B][H][Nq][d] bf16, k, v [B][H][Nk][d] bf16 (read);
+ *   lse [B][H][Nq] fp32: the LSE fa_fwd wrote for the same q, k, v, causal, scale;
+ *   dq [B][H][Nq][d], dk, dv [B][H][Nk][d] bf16 (written);
+ *   workspace: fa_bwd_workspace_bytes(B, H, Nq, d) bytes, 16-byte aligned.
+ * With P = exp(scale Q K^T - LSE): dV = P^T dO, dS = P * (dO V^T - D) with
+ * D_i = sum_c dO_ic O_ic, dQ = scale dS K, dK = scale dS^T Q. Responsibilities:
+ * a preprocess launch forms D and zeroes the fp32 dQ accumulator; the main
+ * launch runs one CTA per (head, 128-key tile), which accumulates its keys' dK
+ * and dV over all query tiles in fp32 and adds its dS K to the dQ accumulator
+ * (fp32 atomic adds, across key tiles); a last launch writes dQ = scale times
+ * the accumulator in bf16. d = 128 only (else FA_ERR_HEADDIM); causal as fa_fwd.
+ * Three launches on `stream`, no synchronisation.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
+                 int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream);
+
+/*
  * fa_fwd_grid_ctas — number of CTAs fa_fwd (num_splits = 1) or
  * fa_fwd_splitkv would launch for this shape: B * H * ceil(Nq / BM) * num_splits,
  * BM = 256 query rows per CTA for d <= 128 (two 128-row tiles) and 128 for

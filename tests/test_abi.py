@@ -38,7 +38,7 @@ def test_header_declares_the_api():
     names = declared_functions()
     for want in ("fa_fwd", "fa_fwd_splitkv", "fa_combine", "fa_splitkv_workspace_bytes",
                  "fa_status_string", "fa_fwd_grid_ctas", "fa_device_status", "fa_fwd_varlen",
-                 "fa_fwd_fp8", "fa_fwd_fp8_splitkv"):
+                 "fa_fwd_fp8", "fa_fwd_fp8_splitkv", "fa_bwd", "fa_bwd_workspace_bytes"):
         assert want in names
 
 
@@ -144,6 +144,23 @@ def test_fp8_splitkv_rejects(lib, kw, code):
     assert lib.fa_fwd_fp8_splitkv(P(a["q"]), P(a["k"]), P(a["v"]), a["qd"], a["kd"], a["vd"],
                                   P(a["ws"]), a["B"], a["H"], a["Nq"], a["Nk"], a["d"], a["scale"],
                                   a["causal"], a["S"], P(0)) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), 1), (dict(o=0), 1), (dict(do=0), 1), (dict(lse=0), 1), (dict(dq=0), 1),
+    (dict(dk=0), 1), (dict(dv=0), 1), (dict(ws=0), 6), (dict(ws=FAKE + 4), 6),
+    (dict(d=64), 4), (dict(d=256), 4), (dict(Nq=0), 3), (dict(scale=0.0), 9), (dict(causal=3), 11),
+    (dict(dq=FAKE + 8), 2), (dict(o=FAKE + 2), 2), (dict(lse=FAKE + 2), 2),
+])
+def test_bwd_rejects(lib, kw, code):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, ws=FAKE,
+             B=1, H=1, Nq=8, Nk=8, d=128, scale=0.088, causal=0)
+    a.update(kw)
+    assert lib.fa_bwd(P(a["q"]), P(a["k"]), P(a["v"]), P(a["o"]), P(a["do"]), P(a["lse"]), P(a["dq"]),
+                      P(a["dk"]), P(a["dv"]), P(a["ws"]), a["B"], a["H"], a["Nq"], a["Nk"], a["d"],
+                      a["scale"], a["causal"], P(0)) == code
+    assert fa.fa_bwd_workspace_bytes(2, 3, 77, 128) == 2 * 3 * 77 * 129 * 4
+    assert fa.fa_bwd_workspace_bytes(2, 3, 77, 64) == 0
 
 
 def test_workspace_bytes(lib):

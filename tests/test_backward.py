@@ -1,0 +1,92 @@
+"""GPU parity of the backward (fa_bwd) against the float64 gradient oracle.
+
+Tolerance, from the arithmetic: the inputs are exact bf16, and every product is
+accumulated in fp32. Three quantities are rounded on the GPU: P and dS to bf16
+before their MMAs, and O to bf16 (the forward's output) before D = rowsum(dO O).
+Each rounding is about 2^-9 relative, and the gradients are rounded to bf16 at
+the end. Each gradient element sums many such terms, so the per-tensor bound is
+relative L2 <= 1e-2 (about 2.5x the bf16 unit 2^-8). The largest element error is
+bounded by 1e-2 of the tensor's largest magnitude, plus 1e-3.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import exact_attention_80_gb300 as fa
+import oracle
+import oracle.backward as obw
+from exact_attention_80_gb300.inputs import f32, make_grad_output, make_qkv, to_f64
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-2
+MAX_REL = 1e-2
+
+
+def check_grad(got, ref, what):
+    got = got.float().cpu().numpy().astype(np.float64)
+    scale = float(np.abs(ref).max())
+    err = np.abs(got - ref)
+    assert err.max() <= MAX_REL * scale + 1e-3, (what, "max", float(err.max()), scale)
+    # A zero reference (one key: dQ = dK = 0) has no relative L2; the element
+    # bound above is the whole check there.
+    den = float(np.linalg.norm(ref))
+    if den > 0:
+        assert float(np.linalg.norm(got - ref)) <= REL_L2 * den, (what, "rel-L2", float(np.linalg.norm(got - ref)) / den)
+
+
+def run_bwd(B, H, Nq, Nk, causal, seed, d=128):
+    q, k, v = make_qkv(B, H, Nq, Nk, d, seed)
+    do = make_grad_output(B, H, Nq, d, seed + 1)
+    scale = f32(1.0 / math.sqrt(d))
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.attention(qc, kc, vc, causal=causal, scale=scale)
+    dq, dk, dv = fa.attention_backward(qc, kc, vc, o, lse, doc, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(clear=True) == fa.FA_OK
+    ref = obw.attention_backward_f64(to_f64(q), to_f64(k), to_f64(v), to_f64(do), scale, causal)
+    return (dq, dk, dv), ref
+
+
+CASES = [
+    # B, H, Nq, Nk, causal
+    (1, 1, 128, 128, False),
+    (1, 2, 300, 333, False),
+    (1, 2, 300, 333, True),
+    (2, 3, 257, 511, True),
+    (1, 2, 384, 384, "bottom_right"),
+    (1, 2, 700, 200, "bottom_right"),   # rows without keys
+    (1, 1, 100, 300, True),             # keys no query sees: dK = dV = 0
+    (1, 2, 1, 1000, False),
+    (1, 1, 1000, 1, False),
+    (2, 2, 1024, 1024, False),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,causal", CASES)
+def test_backward_parity(B, H, Nq, Nk, causal):
+    got, ref = run_bwd(B, H, Nq, Nk, causal, 8100 + Nq + Nk)
+    for g, r, name in zip(got, ref, ("dq", "dk", "dv")):
+        check_grad(g, r, f"{name} B{B} H{H} Nq{Nq} Nk{Nk} {causal}")
+
+
+def test_backward_full_size_sampled_heads():
+    """The C2 shape (B=8, H=32, N=2048, d=128), causal: three heads against the
+    oracle."""
+    B, H, N, d = 8, 32, 2048, 128
+    q, k, v = make_qkv(B, H, N, N, d, 8201)
+    do = make_grad_output(B, H, N, d, 8202)
+    scale = f32(1.0 / math.sqrt(d))
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.attention(qc, kc, vc, causal=True, scale=scale)
+    dq, dk, dv = fa.attention_backward(qc, kc, vc, o, lse, doc, causal=True, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(clear=True) == fa.FA_OK
+    for b, h in ((0, 0), (4, 13), (7, 31)):
+        ref = obw.attention_backward_f64(to_f64(q[b, h]), to_f64(k[b, h]), to_f64(v[b, h]),
+                                         to_f64(do[b, h]), scale, True)
+        for g, r, name in zip((dq[b, h], dk[b, h], dv[b, h]), ref, ("dq", "dk", "dv")):
+            check_grad(g, r, f"{name} head {b},{h}")
