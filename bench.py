@@ -336,7 +336,38 @@ def extra_workloads(device, stream, reps: int = 20):
     out["varlen_causal"] = varlen_workload(device, stream, reps)
     out["c2_fp8"] = fp8_workload(device, stream, reps)
     out["c5_fp8"] = fp8_decode_workload(device, stream, reps)
+    out["c2_bwd"] = bwd_workload(device, stream, reps)
     return out
+
+
+def bwd_workload(device, stream, reps):
+    """The backward (fa_bwd) on the C2 shape (B=8, H=32, N=2048, d=128), both
+    masks, on seeded device-side N(0,1) bf16 inputs and upstream gradient; FLOPs
+    2.5x the forward's metric (five GEMMs against two). The three launches of one
+    call are timed together."""
+    import torch
+
+    import exact_attention_80_gb300 as fa
+    from exact_attention_80_gb300.inputs import metric_flops
+
+    B, H, N, d = 8, 32, 2048, 128
+    gen = torch.Generator(device=device).manual_seed(1010)
+    q, k, v, do = (torch.randn((B, H, N, d), generator=gen, device=device).to(torch.bfloat16)
+                   for _ in range(4))
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d) // 4, device=device)
+    res = {}
+    for causal in (False, True):
+        o, lse = fa.attention(q, k, v, causal=causal, stream=stream)
+        fn = lambda: fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, causal, stream=stream)  # noqa: E731
+        for _ in range(3):
+            fn()
+        ms = statistics.median(time_launches(fn, reps, stream, queue_ahead=True))
+        flops = 2.5 * metric_flops(B, H, N, N, d, causal)
+        res["causal" if causal else "non_causal"] = {"tflops": round(flops / ms / 1e9, 1),
+                                                     "us": round(ms * 1e3, 1)}
+        del o, lse
+    return res
 
 
 def fp8_decode_workload(device, stream, reps):

@@ -264,27 +264,30 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
         bool ok = true;
         for (int i = 0; i < n && ok; ++i) {
             const int q0 = (i0 + i) * kBwdTile;
+            // LSE (base 2) and D of query columns cc * 32 + lane, loaded before
+            // the wait for S^T and shared over the warp by shuffles: +inf LSE
+            // (P = 0) for rows past Nq or rows that saw no key.
+            float my_lse2[4], my_d[4];
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                const int q = q0 + cc * 32 + lane;
+                my_lse2[cc] = INFINITY;
+                my_d[cc] = 0.f;
+                if (q < p.Nq) {
+                    const float lse = p.lse[static_cast<size_t>(bh) * p.Nq + q];
+                    my_lse2[cc] = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
+                    my_d[cc] = p.dd[static_cast<size_t>(bh) * p.Nq + q];
+                }
+            }
             ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_SFULL), i & 1, p, abort_flag, kStatusWaitS));
             if (!ok) break;
             tc_fence_after();
             // 32 queries at a time: P^T and dS^T for this key row.
-#pragma unroll 1
+#pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 uint32_t sraw[32], draw[32];
                 tmem_ld32(tmem + lane_field + L::ST_COL + cc * 32, sraw);
                 tmem_ld32(tmem + lane_field + L::DP_COL + cc * 32, draw);
-                // LSE (base 2) and D of query column cc * 32 + lane, shared over
-                // the warp by shuffles: +inf LSE (P = 0) for rows past Nq or rows
-                // that saw no key.
-                float my_lse2 = INFINITY, my_d = 0.f;
-                {
-                    const int q = q0 + cc * 32 + lane;
-                    if (q < p.Nq) {
-                        const float lse = p.lse[static_cast<size_t>(bh) * p.Nq + q];
-                        my_lse2 = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
-                        my_d = p.dd[static_cast<size_t>(bh) * p.Nq + q];
-                    }
-                }
                 tmem_wait_ld();
                 uint32_t pk[16], dk[16];
 #pragma unroll
@@ -295,10 +298,14 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
                         const int c = cc * 32 + 2 * e + h;
                         const int q = q0 + c;
                         const bool vis = key < p.Nk && (!p.causal || key <= q + off);
-                        const float lse2 = __shfl_sync(0xffffffffu, my_lse2, 2 * e + h);
-                        const float dcol = __shfl_sync(0xffffffffu, my_d, 2 * e + h);
+                        const float lse2 = __shfl_sync(0xffffffffu, my_lse2[cc], 2 * e + h);
+                        const float dcol = __shfl_sync(0xffffffffu, my_d[cc], 2 * e + h);
+                        // The exponential runs for every element and the mask
+                        // selects after it (x is finite or -inf: no NaN), so the
+                        // chunk's elements have no branches between them.
                         const float x = __uint_as_float(sraw[2 * e + h]) * sl2 - lse2;
-                        const float pp = vis ? ex2(x) : 0.f;
+                        const float ex = ex2(x);
+                        const float pp = vis ? ex : 0.f;
                         pv[h] = pp;
                         dv[h] = pp * (__uint_as_float(draw[2 * e + h]) - dcol);
                     }
@@ -331,12 +338,16 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
                 uint32_t raw[32];
                 tmem_ld32(tmem + lane_field + L::ST_COL + cc * 32, raw);
                 tmem_wait_ld();
+                const int qc = q0 + cc * 32;
+                float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qc) * kBwdD + r;
+                if (qc + 32 <= p.Nq) {
+                    // A whole chunk of rows: 32 adds with no branch between them.
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int q = q0 + cc * 32 + e;
-                    if (q < p.Nq)
-                        atomicAdd(p.dq_acc + (static_cast<size_t>(bh) * p.Nq + q) * kBwdD + r,
-                                  __uint_as_float(raw[e]));
+                    for (int e = 0; e < 32; ++e) atomicAdd(dst + e * kBwdD, __uint_as_float(raw[e]));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (qc + e < p.Nq) atomicAdd(dst + e * kBwdD, __uint_as_float(raw[e]));
                 }
             }
             tc_fence_before();
