@@ -177,9 +177,10 @@ def measured_peaks():
         return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
 
 
-# Sources that do not build or launch the forward kernels: a change there leaves
-# their recorded DRAM traffic valid.
-NOT_FORWARD = ("fa_combine.cu", "fa_noalloc.cu")
+# Sources that do not build or launch the forward kernels (the split merge, the
+# allocation-free wrapper, the backward): a change there leaves their recorded
+# DRAM traffic valid.
+NOT_FORWARD = ("fa_combine.cu", "fa_noalloc.cu", "fa_bwd.cu")
 
 
 def kernel_source_hash() -> str:
