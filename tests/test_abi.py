@@ -42,6 +42,22 @@ def test_header_declares_the_api():
         assert want in names
 
 
+def test_header_is_plain_c(tmp_path):
+    """include/fa.h is a C interface: it compiles as C11 with warnings as errors."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    cuda_inc = os.path.join(os.path.dirname(os.path.dirname(fa_build.nvcc_path())), "include")
+    src = tmp_path / "c_client.c"
+    src.write_text('#include "fa.h"\nint main(void) { return fa_status_string(FA_OK) == 0; }\n')
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-fsyntax-only",
+                        "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
 def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), f"{name} declared in include/fa.h but not exported"
