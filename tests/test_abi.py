@@ -224,3 +224,17 @@ def test_python_binding_rejects_bad_tensors():
     qb = torch.zeros(1, 1, 8, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fa.fa_fwd(qb, qb, qb, qb, qb)  # CPU tensors are refused before any call
+
+
+def test_bench_fill_splits(lib):
+    """The bench's split count for one CTA per SM follows the grid the library
+    reports: two splits per CTA with one query tile, one otherwise."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    assert bench.fill_splits(fa, 1, 8, 128, 128, 152) == 38   # C5: 8 heads x 19 pairs
+    assert bench.fill_splits(fa, 1, 8, 128, 64, 152) == 38
+    assert bench.fill_splits(fa, 1, 8, 256, 128, 152) == 19   # two query tiles per CTA
+    assert bench.fill_splits(fa, 1, 8, 128, 256, 152) == 19   # d = 256: no dual-range CTAs
+    assert bench.fill_splits(fa, 1, 200, 128, 128, 152) == 1
