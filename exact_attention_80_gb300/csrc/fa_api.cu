@@ -311,8 +311,8 @@ fa_status fa_fwd_fp8_splitkv(const void* q, const void* k, const void* v, float 
 
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d) {
     if (B < 1 || H < 1 || Nq < 1 || d != 128) return 0;
-    const size_t rows = static_cast<size_t>(B) * H * Nq;
-    return rows * (static_cast<size_t>(d) + 1) * sizeof(float);
+    const size_t rows_pad = static_cast<size_t>(B) * H * ((static_cast<size_t>(Nq) + 127) / 128 * 128);
+    return rows_pad * (static_cast<size_t>(d) + 2) * sizeof(float);
 }
 
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -328,9 +328,11 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
         return FA_ERR_ALIGN;
     if (!workspace || !fa::aligned(workspace, 16)) return FA_ERR_WORKSPACE;
     const int BH = B * H;
-    const long long rows = static_cast<long long>(BH) * Nq;
+    const int Nq_pad = (Nq + 127) / 128 * 128;
+    const size_t rows_pad = static_cast<size_t>(BH) * Nq_pad;
     float* dq_acc = static_cast<float*>(workspace);
-    float* dd = dq_acc + static_cast<size_t>(rows) * d;
+    float* nlse2 = dq_acc + rows_pad * d;
+    float* ndd = nlse2 + rows_pad;
     fa::BwdParams p;
     std::memset(&p, 0, sizeof(p));
     if (!fa::encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
@@ -338,14 +340,15 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
         !fa::encode_rows_map(&p.tm_v, v, d, Nk, BH, 128) ||
         !fa::encode_rows_map(&p.tm_do, dout, d, Nq, BH, 128))
         return FA_ERR_CUDA;
-    p.lse = lse;
-    p.dd = dd;
+    p.nlse2 = nlse2;
+    p.ndd = ndd;
     p.dq_acc = dq_acc;
     p.dk = dk;
     p.dv = dv;
     p.BH = BH;
     p.Nq = Nq;
     p.Nk = Nk;
+    p.Nq_pad = Nq_pad;
     p.causal = causal ? 1 : 0;
     p.causal_br = (causal == FA_CAUSAL_BOTTOM_RIGHT) ? 1 : 0;
     p.k_tiles = (Nk + 127) / 128;
@@ -353,9 +356,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.scale_log2 = scale * 1.4426950408889634f;
     p.wait_limit = fa::kDefaultWaitLimit;
     if (fa::device_status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
-    if (fa::launch_bwd_pre(o, dout, dd, dq_acc, rows, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::launch_bwd_pre(o, dout, lse, nlse2, ndd, dq_acc, BH, Nq, Nq_pad, stream) != cudaSuccess)
+        return FA_ERR_CUDA;
     if (fa::launch_bwd_main(p, stream) != cudaSuccess) return FA_ERR_CUDA;
-    if (fa::launch_bwd_dq(dq_acc, dq, rows * d, scale, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::launch_bwd_dq(dq_acc, dq, BH, Nq, Nq_pad, scale, stream) != cudaSuccess) return FA_ERR_CUDA;
     return FA_OK;
 }
 

@@ -9,8 +9,9 @@
 //   dQ = scale dS K,  dK = scale dS^T Q.
 //
 // Responsibilities and accumulation (the page asks that they be written down):
-//   * fa_bwd_pre_kernel: D_i in fp32 from bf16 dO and O; zeroes the fp32 dQ
-//     accumulator.
+//   * fa_bwd_pre_kernel: per query row (rows padded to whole 128-row tiles),
+//     -LSE log2(e) and -D_i in fp32 (D_i from bf16 dO and O; padded rows and
+//     rows that saw no key get -inf and 0); zeroes the fp32 dQ accumulator.
 //   * fa_bwd_kernel: one CTA per (head, 128-key tile). It owns dK and dV of its
 //     keys and accumulates them over every query tile in TMEM (fp32), so they
 //     need no cross-CTA reduction. Its dQ contribution, dS K for its keys, is
@@ -19,16 +20,19 @@
 //   * fa_bwd_dq_kernel: dQ = scale * accumulator, to bf16.
 //
 // fa_bwd_kernel roles: warp 0 loads K and V once and (Q_i, dO_i) per query
-// tile into two buffers (TMA); warp 1 issues tcgen05 MMAs; warps 4-7 are the
-// compute group, thread r = TMEM lane r. Per query tile i:
+// tile into two buffers (TMA); warp 1 issues tcgen05 MMAs; warps 4-11 are the
+// compute group, two warps per TMEM lane quarter, each owning two 32-query
+// chunks (thread = TMEM lane = key row). Per query tile i:
 //   S^T = K Q_i^T and dP^T = V dO_i^T (lanes = keys, columns = queries);
 //   the compute group forms P^T = exp2(S^T scale log2e - LSE log2e) and
-//   dS^T = P^T (dP^T - D), writes both as bf16 into TMEM over the first half of
-//   their own columns, and dS^T into shared memory (128-byte swizzle);
+//   dS^T = P^T (dP^T - D), writes both as bf16 into TMEM over the first half
+//   of each chunk's own columns, and dS^T into shared memory (128-byte
+//   swizzle);
 //   dV += P^T dO_i and dK += dS^T Q_i (A from TMEM, B = dO_i / Q_i MN-major);
 //   dQ_i^T = K^T dS^T (A = K MN-major, B = dS^T from shared memory) into the
-//   S^T columns; the compute group (lane = head dim) adds it to the fp32
-//   accumulator, 32 consecutive floats per warp instruction.
+//   dP^T columns, so S^T of the next tile can be computed while the compute
+//   group (lane = head dim) adds dQ_i^T to the fp32 accumulator, 32
+//   consecutive floats per warp instruction.
 // Every mbarrier wait is bounded, as in the forward kernels.
 #include <cuda_bf16.h>
 
@@ -39,10 +43,14 @@ namespace fa {
 namespace {
 
 constexpr int kBwdD = 128;
-constexpr int kBwdTile = 128;  // keys per CTA, queries per step
+constexpr int kBwdTile = 128;   // keys per CTA, queries per step
+constexpr int kBwdGroups = 2;   // compute warps per TMEM lane quarter
+constexpr int kBwdChunks = (kBwdTile / 32) / kBwdGroups;  // 32-query chunks per compute warp
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct LayoutBwd {
-    static constexpr int THREADS = 256;
+    static constexpr int COMPUTE_WARPS = 4 * kBwdGroups;
+    static constexpr int THREADS = 128 + 32 * COMPUTE_WARPS;
     static constexpr uint32_t TILE_BYTES = kBwdTile * kBwdD * 2;  // 32 KB, two 64-column chunks
     static constexpr uint32_t CHUNK_BYTES = kBwdTile * 128;       // one 64-column chunk
     static constexpr uint32_t K_OFF = 0;
@@ -63,7 +71,7 @@ struct LayoutBwd {
     static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr uint32_t BYTES = MISC_OFF + 16;
     static constexpr size_t ALLOC_BYTES = BYTES + 1024;
-    // TMEM columns: S^T (then P^T, then dQ^T), dP^T (then dS^T), dV, dK.
+    // TMEM columns: S^T (then P^T), dP^T (then dS^T, then dQ^T), dV, dK.
     static constexpr uint32_t ST_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 384;
     static_assert(ALLOC_BYTES <= 232448, "shared memory over the 227 KB per-CTA limit");
 };
@@ -97,6 +105,50 @@ __device__ __forceinline__ void bwd_steps(const BwdParams& p, int kt, int& i0, i
     n = max(0, q_tiles - i0);
 }
 
+// P^T and dS^T of one 32-query chunk for this thread's key row: s and dp are
+// the chunk's S^T and dP^T columns, nl and nd point at the chunk's -LSE log2e
+// and -D (the same addresses for every lane: one broadcast load per four
+// queries). MASK: `lim` is the first visible chunk column (causal) and
+// `key_ok` whether the key exists; without MASK every entry is visible.
+template <bool MASK>
+__device__ __forceinline__ void bwd_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32],
+                                          const float* __restrict__ nl, const float* __restrict__ nd,
+                                          float sl2, int lim, bool key_ok, uint32_t (&pk)[16],
+                                          uint32_t (&dk)[16]) {
+    const uint64_t sl2x2 = f2pack(sl2, sl2);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const float4 l4 = __ldg(reinterpret_cast<const float4*>(nl) + u);
+        const float4 d4 = __ldg(reinterpret_cast<const float4*>(nd) + u);
+        const uint64_t x01 = ffma2(f2pack(__uint_as_float(s[4 * u]), __uint_as_float(s[4 * u + 1])), sl2x2,
+                                   f2pack(l4.x, l4.y));
+        const uint64_t x23 = ffma2(f2pack(__uint_as_float(s[4 * u + 2]), __uint_as_float(s[4 * u + 3])), sl2x2,
+                                   f2pack(l4.z, l4.w));
+        float x[4];
+        f2unpack(x01, x[0], x[1]);
+        f2unpack(x23, x[2], x[3]);
+        float pv[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            // The exponential runs for every element and the mask selects after
+            // it (x is finite or -inf: no NaN), so there are no branches.
+            const float ex = ex2(x[h]);
+            pv[h] = MASK ? ((key_ok && 4 * u + h >= lim) ? ex : 0.f) : ex;
+        }
+        const uint64_t g01 = fadd2(f2pack(__uint_as_float(dp[4 * u]), __uint_as_float(dp[4 * u + 1])),
+                                   f2pack(d4.x, d4.y));
+        const uint64_t g23 = fadd2(f2pack(__uint_as_float(dp[4 * u + 2]), __uint_as_float(dp[4 * u + 3])),
+                                   f2pack(d4.z, d4.w));
+        float ds[4];
+        f2unpack(fmul2(f2pack(pv[0], pv[1]), g01), ds[0], ds[1]);
+        f2unpack(fmul2(f2pack(pv[2], pv[3]), g23), ds[2], ds[3]);
+        pk[2 * u] = pack_bf16x2(pv[0], pv[1]);
+        pk[2 * u + 1] = pack_bf16x2(pv[2], pv[3]);
+        dk[2 * u] = pack_bf16x2(ds[0], ds[1]);
+        dk[2 * u + 1] = pack_bf16x2(ds[2], ds[3]);
+    }
+}
+
 __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
     using L = LayoutBwd;
     extern __shared__ uint8_t smem_raw[];
@@ -121,9 +173,9 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
             mbar_init(bar(L::BAR_QEMPTY + b), 1);
         }
         mbar_init(bar(L::BAR_SFULL), 1);
-        mbar_init(bar(L::BAR_PREADY), 4);
+        mbar_init(bar(L::BAR_PREADY), L::COMPUTE_WARPS);
         mbar_init(bar(L::BAR_DQFULL), 1);
-        mbar_init(bar(L::BAR_DQREAD), 4);
+        mbar_init(bar(L::BAR_DQREAD), L::COMPUTE_WARPS);
         mbar_init(bar(L::BAR_DRAIN), 1);
         *abort_flag = 0u;
         fence_mbar_init();
@@ -214,107 +266,95 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
         for (int i = 0; i < n && ok; ++i) {
             const int b = i & 1;
             ok = wait_all(bar(L::BAR_QFULL + b), (i >> 1) & 1, kStatusWaitQ);
-            // dQ^T of the previous tile sits in the S^T columns until read out.
-            if (ok && i > 0) ok = wait_all(bar(L::BAR_DQREAD), (i - 1) & 1, kStatusWaitO);
             if (!ok) break;
             tc_fence_after();
             const uint32_t qb = L::Q_OFF + b * L::TILE_BYTES;
             const uint32_t dob = L::DO_OFF + b * L::TILE_BYTES;
-            mma_t(L::ST_COL, L::K_OFF, qb);   // S^T = K Q^T
+            // S^T = K Q^T. The S^T columns last held P^T of the previous tile,
+            // which its dV MMAs (issued earlier, run in order) have consumed.
+            mma_t(L::ST_COL, L::K_OFF, qb);
+            // dQ^T of the previous tile sits in the dP^T columns until read out.
+            if (i > 0) {
+                ok = wait_all(bar(L::BAR_DQREAD), (i - 1) & 1, kStatusWaitO);
+                if (!ok) break;
+                tc_fence_after();
+            }
             mma_t(L::DP_COL, L::V_OFF, dob);  // dP^T = V dO^T
             if (leader) umma_commit(bar(L::BAR_SFULL));
             ok = wait_all(bar(L::BAR_PREADY), i & 1, kStatusWaitP);
             if (!ok) break;
             tc_fence_after();
-            // dV += P^T dO and dK += dS^T Q: A from TMEM (16 queries = 8 columns),
-            // B MN-major (16 query rows = 2048 bytes).
+            // dV += P^T dO and dK += dS^T Q: A from TMEM (16 queries = 8 packed
+            // columns, each 32-query chunk packed into the first 16 columns of its
+            // own 32), B MN-major (16 query rows = 2048 bytes).
 #pragma unroll
             for (int kk = 0; kk < kBwdTile / 16; ++kk) {
                 const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                const uint32_t pcol = 32 * (kk >> 1) + 8 * (kk & 1);
                 const uint64_t bdo = desc(mn_lo, mn_hi, dob + kk * 2048);
                 const uint64_t bq = desc(mn_lo, mn_hi, qb + kk * 2048);
                 if (leader) {
-                    umma_ts(tmem + L::DV_COL, tmem + L::ST_COL + kk * 8, bdo, IDESC_ACC, acc);
-                    umma_ts(tmem + L::DK_COL, tmem + L::DP_COL + kk * 8, bq, IDESC_ACC, acc);
+                    umma_ts(tmem + L::DV_COL, tmem + L::ST_COL + pcol, bdo, IDESC_ACC, acc);
+                    umma_ts(tmem + L::DK_COL, tmem + L::DP_COL + pcol, bq, IDESC_ACC, acc);
                 }
             }
-            // dQ^T = K^T dS^T into the S^T columns (after the dV MMAs that read
-            // P^T there, in issue order): A = K MN-major (M = head dim), B = dS^T
+            if (leader) umma_commit(bar(L::BAR_QEMPTY + b));
+            // dQ^T = K^T dS^T into the dP^T columns (after the dK MMAs that read
+            // dS^T there, in issue order): A = K MN-major (M = head dim), B = dS^T
             // MN-major (N = queries), 16 keys = 2048 bytes per step.
 #pragma unroll
             for (int kk = 0; kk < kBwdTile / 16; ++kk) {
                 const uint64_t a = desc(mn_lo, mn_hi, L::K_OFF + kk * 2048);
                 const uint64_t bds = desc(mn_lo, mn_hi, L::DS_OFF + kk * 2048);
-                if (leader) umma_ss(tmem + L::ST_COL, a, bds, IDESC_DQ, kk > 0 ? 1u : 0u);
+                if (leader) umma_ss(tmem + L::DP_COL, a, bds, IDESC_DQ, kk > 0 ? 1u : 0u);
             }
             if (leader) umma_commit(bar(L::BAR_DQFULL));
-            if (leader) umma_commit(bar(L::BAR_QEMPTY + b));
         }
         if (leader) umma_commit(bar(L::BAR_DRAIN));
         bwd_wait(bar(L::BAR_DRAIN), 0, p, abort_flag, kStatusWaitDrain, false);
     } else if (warp >= 4) {
         // ------------------------------------------------------------ compute group
         const int quarter = warp & 3;
+        const int grp = (warp - 4) >> 2;
         const int r = quarter * 32 + lane;   // TMEM lane: key row, or head dim for dQ^T
         const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
         const int key = k0 + r;
+        const bool key_ok = key < p.Nk;
+        const bool key_tail = k0 + kBwdTile > p.Nk;
         const int off = p.causal_br ? p.Nk - p.Nq : 0;
         const float sl2 = p.scale_log2;
-        constexpr float kLog2e = 1.4426950408889634f;
+        const size_t row0 = static_cast<size_t>(bh) * p.Nq_pad;
         bool ok = true;
         for (int i = 0; i < n && ok; ++i) {
             const int q0 = (i0 + i) * kBwdTile;
-            // LSE (base 2) and D of query columns cc * 32 + lane, loaded before
-            // the wait for S^T and shared over the warp by shuffles: +inf LSE
-            // (P = 0) for rows past Nq or rows that saw no key.
-            float my_lse2[4], my_d[4];
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                const int q = q0 + cc * 32 + lane;
-                my_lse2[cc] = INFINITY;
-                my_d[cc] = 0.f;
-                if (q < p.Nq) {
-                    const float lse = p.lse[static_cast<size_t>(bh) * p.Nq + q];
-                    my_lse2[cc] = (lse == -INFINITY) ? INFINITY : lse * kLog2e;
-                    my_d[cc] = p.dd[static_cast<size_t>(bh) * p.Nq + q];
-                }
-            }
+            // Every entry of the tile is visible unless the tile holds missing
+            // keys or (causal) crosses the diagonal; padded query rows carry
+            // -inf as -LSE log2e, so their P is 0 either way.
+            const bool masked = key_tail || (p.causal && k0 + kBwdTile - 1 > q0 + off);
             ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_SFULL), i & 1, p, abort_flag, kStatusWaitS));
             if (!ok) break;
             tc_fence_after();
-            // 32 queries at a time: P^T and dS^T for this key row.
-#pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
+#pragma unroll 1
+            for (int j = 0; j < kBwdChunks; ++j) {
+                const int cc = grp * kBwdChunks + j;
                 uint32_t sraw[32], draw[32];
                 tmem_ld32(tmem + lane_field + L::ST_COL + cc * 32, sraw);
                 tmem_ld32(tmem + lane_field + L::DP_COL + cc * 32, draw);
                 tmem_wait_ld();
+                const float* nl = p.nlse2 + row0 + q0 + cc * 32;
+                const float* nd = p.ndd + row0 + q0 + cc * 32;
                 uint32_t pk[16], dk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pv[2], dv[2];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int c = cc * 32 + 2 * e + h;
-                        const int q = q0 + c;
-                        const bool vis = key < p.Nk && (!p.causal || key <= q + off);
-                        const float lse2 = __shfl_sync(0xffffffffu, my_lse2[cc], 2 * e + h);
-                        const float dcol = __shfl_sync(0xffffffffu, my_d[cc], 2 * e + h);
-                        // The exponential runs for every element and the mask
-                        // selects after it (x is finite or -inf: no NaN), so the
-                        // chunk's elements have no branches between them.
-                        const float x = __uint_as_float(sraw[2 * e + h]) * sl2 - lse2;
-                        const float ex = ex2(x);
-                        const float pp = vis ? ex : 0.f;
-                        pv[h] = pp;
-                        dv[h] = pp * (__uint_as_float(draw[2 * e + h]) - dcol);
-                    }
-                    pk[e] = pack_bf16x2(pv[0], pv[1]);
-                    dk[e] = pack_bf16x2(dv[0], dv[1]);
+                if (masked) {
+                    // Key row `key` is visible to query q iff key <= q + off.
+                    const int lim = p.causal ? key - off - q0 - cc * 32 : -1;
+                    bwd_chunk<true>(sraw, draw, nl, nd, sl2, lim, key_ok, pk, dk);
+                } else {
+                    bwd_chunk<false>(sraw, draw, nl, nd, sl2, 0, true, pk, dk);
                 }
-                // P^T over S^T's columns [16 cc, 16 cc + 16), dS^T over dP^T's.
-                tmem_st16(tmem + lane_field + L::ST_COL + cc * 16, pk);
-                tmem_st16(tmem + lane_field + L::DP_COL + cc * 16, dk);
+                // P^T and dS^T over the first 16 of the chunk's own 32 columns
+                // (no other warp reads or writes them).
+                tmem_st16(tmem + lane_field + L::ST_COL + cc * 32, pk);
+                tmem_st16(tmem + lane_field + L::DP_COL + cc * 32, dk);
                 // dS^T into shared memory: row r, queries 32 cc .. 32 cc + 31.
                 const uint32_t line = sbase + L::DS_OFF + (cc >> 1) * L::CHUNK_BYTES + r * 128;
                 const uint32_t swz = static_cast<uint32_t>(r & 7);
@@ -329,40 +369,35 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::BAR_PREADY));
-            // dQ^T: lane r = head dim r, columns = this tile's queries.
+            // dQ^T: lane r = head dim r, columns = this tile's queries. The
+            // accumulator has rows for whole tiles, so every add is in bounds.
             ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_DQFULL), i & 1, p, abort_flag, kStatusWaitO));
             if (!ok) break;
             tc_fence_after();
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int j = 0; j < kBwdChunks; ++j) {
+                const int cc = grp * kBwdChunks + j;
                 uint32_t raw[32];
-                tmem_ld32(tmem + lane_field + L::ST_COL + cc * 32, raw);
+                tmem_ld32(tmem + lane_field + L::DP_COL + cc * 32, raw);
                 tmem_wait_ld();
-                const int qc = q0 + cc * 32;
-                float* dst = p.dq_acc + (static_cast<size_t>(bh) * p.Nq + qc) * kBwdD + r;
-                if (qc + 32 <= p.Nq) {
-                    // A whole chunk of rows: 32 adds with no branch between them.
+                float* dst = p.dq_acc + (row0 + q0 + cc * 32) * kBwdD + r;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) atomicAdd(dst + e * kBwdD, __uint_as_float(raw[e]));
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (qc + e < p.Nq) atomicAdd(dst + e * kBwdD, __uint_as_float(raw[e]));
-                }
+                for (int e = 0; e < 32; ++e) atomicAdd(dst + e * kBwdD, __uint_as_float(raw[e]));
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::BAR_DQREAD));
         }
-        // dK (scaled) and dV of this key row; zero when no query tile sees it.
-        // tcgen05.ld is warp-collective: the loads run for the whole warp (`ok`
-        // is warp-uniform), and only the stores check that the key exists.
+        // dK (scaled) and dV of this key row, 32 head-dim columns per chunk;
+        // zero when no query tile sees it. tcgen05.ld is warp-collective: the
+        // loads run for the whole warp (`ok` is warp-uniform), and only the
+        // stores check that the key exists.
         if (ok) {
-            const bool store = key < p.Nk;
             __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(p.dk) + (static_cast<size_t>(bh) * p.Nk + key) * kBwdD;
             __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(p.dv) + (static_cast<size_t>(bh) * p.Nk + key) * kBwdD;
 #pragma unroll 1
-            for (int cc = 0; cc < 4; ++cc) {
+            for (int j = 0; j < kBwdChunks; ++j) {
+                const int cc = grp * kBwdChunks + j;
                 uint32_t kr[32], vr[32];
                 if (n > 0) {
                     tmem_ld32(tmem + lane_field + L::DK_COL + cc * 32, kr);
@@ -378,7 +413,7 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
                     kp[e] = pack_bf16x2(__uint_as_float(kr[2 * e]) * p.scale, __uint_as_float(kr[2 * e + 1]) * p.scale);
                     vp[e] = pack_bf16x2(__uint_as_float(vr[2 * e]), __uint_as_float(vr[2 * e + 1]));
                 }
-                if (store) {
+                if (key_ok) {
                     uint4* dk4 = reinterpret_cast<uint4*>(dkp + cc * 32);
                     uint4* dv4 = reinterpret_cast<uint4*>(dvp + cc * 32);
 #pragma unroll
@@ -398,55 +433,75 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// D_i = sum_c dO_ic O_ic (fp32 from bf16) and a zeroed dQ accumulator row; one
-// warp per row, four columns per lane.
+// Per padded query row (one warp per row, four columns per lane): -D_i =
+// -sum_c dO_ic O_ic (fp32 from bf16), -LSE log2e, and a zeroed dQ accumulator
+// row. Rows past Nq get -inf and 0; so do rows whose LSE is -inf (no key).
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dout,
-                                                         float* __restrict__ dd, float* __restrict__ dq_acc,
-                                                         long long rows) {
+                                                         const float* __restrict__ lse,
+                                                         float* __restrict__ nlse2, float* __restrict__ ndd,
+                                                         float* __restrict__ dq_acc, long long rows_pad,
+                                                         int Nq, int Nq_pad) {
+    const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows_pad) return;
+    const long long bh = row / Nq_pad;
+    const int q = static_cast<int>(row - bh * Nq_pad);
+    float s = 0.f, nl = -INFINITY;
+    if (q < Nq) {
+        const size_t src_row = static_cast<size_t>(bh) * Nq + q;
+        const size_t base = src_row * kBwdD + lane * 4;
+        const uint2 ov = *reinterpret_cast<const uint2*>(o + base);
+        const uint2 dv = *reinterpret_cast<const uint2*>(dout + base);
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+        for (int e = 0; e < 2; ++e) {
+            const float2 a = __bfloat1622float2(o2[e]);
+            const float2 b = __bfloat1622float2(d2[e]);
+            s = fmaf(a.x, b.x, s);
+            s = fmaf(a.y, b.y, s);
+        }
+        for (int w = 16; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
+        const float l = lse[src_row];
+        nl = (l == -INFINITY) ? -INFINITY : -(l * kLog2e);
+    }
+    if (lane == 0) {
+        ndd[row] = -s;
+        nlse2[row] = nl;
+    }
+    *reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * kBwdD + lane * 4) =
+        make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// dQ = scale * accumulator, to bf16: one warp per query row, four columns per
+// lane, reading the accumulator's padded rows.
+__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ acc,
+                                                        __nv_bfloat16* __restrict__ dq, long long rows,
+                                                        int Nq, int Nq_pad, float scale) {
     const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    const size_t base = static_cast<size_t>(row) * kBwdD + lane * 4;
-    const uint2 ov = *reinterpret_cast<const uint2*>(o + base);
-    const uint2 dv = *reinterpret_cast<const uint2*>(dout + base);
-    const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-    const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
-    float s = 0.f;
-    for (int e = 0; e < 2; ++e) {
-        const float2 a = __bfloat1622float2(o2[e]);
-        const float2 b = __bfloat1622float2(d2[e]);
-        s = fmaf(a.x, b.x, s);
-        s = fmaf(a.y, b.y, s);
-    }
-    for (int w = 16; w > 0; w >>= 1) s += __shfl_xor_sync(0xffffffffu, s, w);
-    if (lane == 0) dd[row] = s;
-    *reinterpret_cast<float4*>(dq_acc + base) = make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
-// dQ = scale * accumulator, to bf16, four elements per thread.
-__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ acc,
-                                                        __nv_bfloat16* __restrict__ dq, long long elems,
-                                                        float scale) {
-    const long long i = (static_cast<long long>(blockIdx.x) * 256 + threadIdx.x) * 4;
-    if (i >= elems) return;
-    const float4 a = *reinterpret_cast<const float4*>(acc + i);
+    const long long bh = row / Nq;
+    const long long arow = bh * Nq_pad + (row - bh * Nq);
+    const float4 a = *reinterpret_cast<const float4*>(acc + static_cast<size_t>(arow) * kBwdD + lane * 4);
     __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
     __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
     uint2 out;
     out.x = *reinterpret_cast<uint32_t*>(&lo);
     out.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(dq + i) = out;
+    *reinterpret_cast<uint2*>(dq + static_cast<size_t>(row) * kBwdD + lane * 4) = out;
 }
 
 }  // namespace
 
-cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dd, float* dq_acc, long long rows,
-                           cudaStream_t stream) {
-    const long long blocks = (rows + 7) / 8;
+cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, float* nlse2, float* ndd,
+                           float* dq_acc, int BH, int Nq, int Nq_pad, cudaStream_t stream) {
+    const long long rows_pad = static_cast<long long>(BH) * Nq_pad;
+    const long long blocks = (rows_pad + 7) / 8;
     if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
     fa_bwd_pre_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), dd, dq_acc, rows);
+        static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, nlse2, ndd,
+        dq_acc, rows_pad, Nq, Nq_pad);
     return cudaGetLastError();
 }
 
@@ -467,12 +522,13 @@ cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, long long elems, float scale,
+cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, int BH, int Nq, int Nq_pad, float scale,
                           cudaStream_t stream) {
-    const long long blocks = (elems / 4 + 255) / 256;
+    const long long rows = static_cast<long long>(BH) * Nq;
+    const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
     fa_bwd_dq_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        dq_acc, static_cast<__nv_bfloat16*>(dq), elems, scale);
+        dq_acc, static_cast<__nv_bfloat16*>(dq), rows, Nq, Nq_pad, scale);
     return cudaGetLastError();
 }
 

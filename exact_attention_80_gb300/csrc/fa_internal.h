@@ -69,12 +69,13 @@ struct BwdParams {
     CUtensorMap tm_k;   // bf16 [B*H][Nk][d], box {64, 128, 1}
     CUtensorMap tm_v;   // same as tm_k
     CUtensorMap tm_do;  // same as tm_q (dO)
-    const float* lse;   // fp32 [B*H][Nq], natural log (the forward's LSE)
-    const float* dd;    // fp32 [B*H][Nq], D_i = sum_c dO_ic O_ic
-    float* dq_acc;      // fp32 [B*H][Nq][d], zeroed, unscaled dS K accumulated
+    const float* nlse2; // fp32 [B*H][Nq_pad]: -LSE log2(e); -inf past Nq or with no key
+    const float* ndd;   // fp32 [B*H][Nq_pad]: -D_i = -sum_c dO_ic O_ic; 0 past Nq
+    float* dq_acc;      // fp32 [B*H][Nq_pad][d], zeroed, unscaled dS K accumulated
     void* dk;           // bf16 [B*H][Nk][d]
     void* dv;           // bf16 [B*H][Nk][d]
     int BH, Nq, Nk;
+    int Nq_pad;         // Nq rounded up to whole 128-row query tiles
     int causal, causal_br;
     int k_tiles;        // ceil(Nk / 128)
     float scale;
@@ -83,10 +84,10 @@ struct BwdParams {
     unsigned* status;
 };
 
-cudaError_t launch_bwd_pre(const void* o, const void* dout, float* dd, float* dq_acc, long long rows,
-                           cudaStream_t stream);
+cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, float* nlse2, float* ndd,
+                           float* dq_acc, int BH, int Nq, int Nq_pad, cudaStream_t stream);
 cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, long long elems, float scale,
+cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, int BH, int Nq, int Nq_pad, float scale,
                           cudaStream_t stream);
 
 struct FwdConfig {

@@ -194,9 +194,10 @@ fa_status fa_fwd_fp8_splitkv(const void* q, const void* k, const void* v, float 
                              cudaStream_t stream);
 
 /*
- * fa_bwd_workspace_bytes — bytes of the fp32 workspace fa_bwd needs: a dQ
- * accumulator [B][H][Nq][d], then D [B][H][Nq]. 0 when an argument is out of
- * range (d must be 128).
+ * fa_bwd_workspace_bytes — bytes of the fp32 workspace fa_bwd needs, with the
+ * query rows of each head padded to Nq_pad = 128 * ceil(Nq / 128): a dQ
+ * accumulator [B][H][Nq_pad][d], then -LSE log2(e) and -D, each
+ * [B][H][Nq_pad]. 0 when an argument is out of range (d must be 128).
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d);
 
@@ -212,11 +213,11 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d);
  *   workspace: fa_bwd_workspace_bytes(B, H, Nq, d) bytes, 16-byte aligned.
  * With P = exp(scale Q K^T - LSE): dV = P^T dO, dS = P * (dO V^T - D) with
  * D_i = sum_c dO_ic O_ic, dQ = scale dS K, dK = scale dS^T Q. Responsibilities:
- * a preprocess launch forms D and zeroes the fp32 dQ accumulator; the main
- * launch runs one CTA per (head, 128-key tile), which accumulates its keys' dK
- * and dV over all query tiles in fp32 and adds its dS K to the dQ accumulator
- * (fp32 atomic adds, across key tiles); a last launch writes dQ = scale times
- * the accumulator in bf16. d = 128 only (else FA_ERR_HEADDIM); causal as fa_fwd.
+ * a preprocess launch forms D and LSE log2(e) per padded row and zeroes the
+ * fp32 dQ accumulator; the main launch runs one CTA per (head, 128-key tile),
+ * which accumulates its keys' dK and dV over all query tiles in fp32 and adds
+ * its dS K to the dQ accumulator (fp32 atomic adds, across key tiles); a last
+ * launch writes dQ = scale times the accumulator in bf16. d = 128 only (else FA_ERR_HEADDIM); causal as fa_fwd.
  * Three launches on `stream`, no synchronisation.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,

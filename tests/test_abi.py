@@ -175,7 +175,8 @@ def test_bwd_rejects(lib, kw, code):
     assert lib.fa_bwd(P(a["q"]), P(a["k"]), P(a["v"]), P(a["o"]), P(a["do"]), P(a["lse"]), P(a["dq"]),
                       P(a["dk"]), P(a["dv"]), P(a["ws"]), a["B"], a["H"], a["Nq"], a["Nk"], a["d"],
                       a["scale"], a["causal"], P(0)) == code
-    assert fa.fa_bwd_workspace_bytes(2, 3, 77, 128) == 2 * 3 * 77 * 129 * 4
+    assert fa.fa_bwd_workspace_bytes(2, 3, 77, 128) == 2 * 3 * 128 * 130 * 4
+    assert fa.fa_bwd_workspace_bytes(1, 1, 129, 128) == 256 * 130 * 4
     assert fa.fa_bwd_workspace_bytes(2, 3, 77, 64) == 0
 
 

@@ -73,6 +73,43 @@ def test_backward_parity(B, H, Nq, Nk, causal):
         check_grad(g, r, f"{name} B{B} H{H} Nq{Nq} Nk{Nk} {causal}")
 
 
+def test_backward_negative_scores_key_tail():
+    """Every score near -200 (Q along u, K against it): LSE is about -190, so an
+    unmasked missing key of the ragged last key tile (its S reads 0) would give
+    exp(190) = inf in fp32 and NaN in dQ. The missing keys are masked.
+
+    dV takes the usual bounds. dQ_i = scale sum_j dS_ij K_j, and every K_j
+    carries the common part -c u while sum_j dS_ij = 0, so the bf16 rounding of
+    dS (2^-9) is amplified by about c / sqrt(d) ~ 4 against dQ's own size; dK
+    sees the same part of Q. Rounding P, dS and O to bf16 in a float64 model of
+    this input gives 2.6 % (dQ) and 0.75 % (dK) of the largest element: dQ takes
+    5e-2 and dK 2e-2, for both the element bound and the relative L2."""
+    B, H, Nq, Nk, d = 1, 2, 200, 300, 128
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 8301)
+    do = make_grad_output(B, H, Nq, d, 8302)
+    scale = f32(1.0 / math.sqrt(d))
+    u = torch.zeros(d)
+    u[:8] = 1.0 / math.sqrt(8.0)
+    c = math.sqrt(200.0 / scale)
+    q = (q.float() + c * u).to(torch.bfloat16)
+    k = (k.float() - c * u).to(torch.bfloat16)
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.attention(qc, kc, vc, scale=scale)
+    assert lse.max().item() < -150.0
+    dq, dk, dv = fa.attention_backward(qc, kc, vc, o, lse, doc, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(clear=True) == fa.FA_OK
+    rq, rk, rv = obw.attention_backward_f64(to_f64(q), to_f64(k), to_f64(v), to_f64(do), scale)
+    for g, name in ((dq, "dq"), (dk, "dk"), (dv, "dv")):
+        assert torch.isfinite(g).all(), name
+    check_grad(dv, rv, "dv negative scores")
+    for g, r, tol, name in ((dq, rq, 5e-2, "dq"), (dk, rk, 2e-2, "dk")):
+        got = g.float().cpu().numpy().astype(np.float64)
+        err = np.abs(got - r)
+        assert err.max() <= tol * np.abs(r).max(), (name, float(err.max()))
+        assert np.linalg.norm(got - r) <= tol * np.linalg.norm(r), name
+
+
 def test_backward_full_size_sampled_heads():
     """The C2 shape (B=8, H=32, N=2048, d=128), causal: three heads against the
     oracle."""
