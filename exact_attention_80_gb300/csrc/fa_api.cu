@@ -1,6 +1,7 @@
-// fa_api.cu — the C ABI declared in include/fa.h: argument validation, TMA
-// tensor-map encoding, work partition and kernel dispatch. Host code only,
-// apart from the device status word defined here.
+// fa_api.cu — the C ABI declared in include/fa.h (the backward's entry points
+// live beside its kernels in fa_bwd.cu): argument validation, TMA tensor-map
+// encoding, work partition and kernel dispatch. Host code only, apart from the
+// device status word defined here.
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -72,6 +73,10 @@ cudaError_t sm_count(int* out) {
     return e;
 }
 
+}  // namespace
+
+// Argument checks and tensor maps shared with the backward's entry points
+// (declared in fa_internal.h).
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool valid_d(int d) { return d == 64 || d == 128 || d == 256; }
 
@@ -148,6 +153,8 @@ fa_status check_common(const void* q, const void* k, const void* v, int B, int H
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16)) return FA_ERR_ALIGN;
     return FA_OK;
 }
+
+namespace {
 
 long long grid_ctas(int B, int H, int Nq, int d, int num_splits) {
     const FwdConfig c = fwd_config(d);
@@ -307,60 +314,6 @@ fa_status fa_fwd_fp8_splitkv(const void* q, const void* k, const void* v, float 
     return fa::launch_forward(q, k, v, nullptr, nullptr, static_cast<float*>(workspace), B, H, Nq,
                               Nk, d, scale, causal, num_splits, 1, stream, fa::kDefaultWaitLimit, 0,
                               nullptr, ds);
-}
-
-size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d) {
-    if (B < 1 || H < 1 || Nq < 1 || d != 128) return 0;
-    const size_t rows_pad = static_cast<size_t>(B) * H * ((static_cast<size_t>(Nq) + 127) / 128 * 128);
-    return rows_pad * (static_cast<size_t>(d) + 2) * sizeof(float);
-}
-
-fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                 const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
-                 int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream) {
-    fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
-    if (s != FA_OK) return s;
-    if (d != 128) return FA_ERR_HEADDIM;
-    if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
-    if (!o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
-    if (!fa::aligned(o, 16) || !fa::aligned(dout, 16) || !fa::aligned(lse, 4) ||
-        !fa::aligned(dq, 16) || !fa::aligned(dk, 16) || !fa::aligned(dv, 16))
-        return FA_ERR_ALIGN;
-    if (!workspace || !fa::aligned(workspace, 16)) return FA_ERR_WORKSPACE;
-    const int BH = B * H;
-    const int Nq_pad = (Nq + 127) / 128 * 128;
-    const size_t rows_pad = static_cast<size_t>(BH) * Nq_pad;
-    float* dq_acc = static_cast<float*>(workspace);
-    float* nlse2 = dq_acc + rows_pad * d;
-    float* ndd = nlse2 + rows_pad;
-    fa::BwdParams p;
-    std::memset(&p, 0, sizeof(p));
-    if (!fa::encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
-        !fa::encode_rows_map(&p.tm_k, k, d, Nk, BH, 128) ||
-        !fa::encode_rows_map(&p.tm_v, v, d, Nk, BH, 128) ||
-        !fa::encode_rows_map(&p.tm_do, dout, d, Nq, BH, 128))
-        return FA_ERR_CUDA;
-    p.nlse2 = nlse2;
-    p.ndd = ndd;
-    p.dq_acc = dq_acc;
-    p.dk = dk;
-    p.dv = dv;
-    p.BH = BH;
-    p.Nq = Nq;
-    p.Nk = Nk;
-    p.Nq_pad = Nq_pad;
-    p.causal = causal ? 1 : 0;
-    p.causal_br = (causal == FA_CAUSAL_BOTTOM_RIGHT) ? 1 : 0;
-    p.k_tiles = (Nk + 127) / 128;
-    p.scale = scale;
-    p.scale_log2 = scale * 1.4426950408889634f;
-    p.wait_limit = fa::kDefaultWaitLimit;
-    if (fa::device_status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
-    if (fa::launch_bwd_pre(o, dout, lse, nlse2, ndd, dq_acc, BH, Nq, Nq_pad, stream) != cudaSuccess)
-        return FA_ERR_CUDA;
-    if (fa::launch_bwd_main(p, stream) != cudaSuccess) return FA_ERR_CUDA;
-    if (fa::launch_bwd_dq(dq_acc, dq, BH, Nq, Nq_pad, scale, stream) != cudaSuccess) return FA_ERR_CUDA;
-    return FA_OK;
 }
 
 size_t fa_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {

@@ -1,4 +1,5 @@
-// fa_bwd.cu — attention backward for head dim 128: dQ, dK, dV.
+// fa_bwd.cu — attention backward for head dim 128: dQ, dK, dV. Holds the
+// backward's kernels and its C entry points (fa_bwd_workspace_bytes, fa_bwd).
 //
 // What is computed (the plain definition of the forward differentiated; the
 // FA-2 page, "AI 大模型之 FlashAttention_02", sections "warp之间怎样减少通信" and
@@ -36,10 +37,35 @@
 // Every mbarrier wait is bounded, as in the forward kernels.
 #include <cuda_bf16.h>
 
+#include <cstring>
+
+#include "fa.h"
 #include "fa_internal.h"
 #include "sm103_ptx.cuh"
 
 namespace fa {
+
+// Kernel parameters, filled by fa_bwd below.
+struct BwdParams {
+    CUtensorMap tm_q;   // bf16 [B*H][Nq][d], box {64, 128, 1}
+    CUtensorMap tm_k;   // bf16 [B*H][Nk][d], box {64, 128, 1}
+    CUtensorMap tm_v;   // same as tm_k
+    CUtensorMap tm_do;  // same as tm_q (dO)
+    const float* nlse2; // fp32 [B*H][Nq_pad]: -LSE log2(e); -inf past Nq or with no key
+    const float* ndd;   // fp32 [B*H][Nq_pad]: -D_i = -sum_c dO_ic O_ic; 0 past Nq
+    float* dq_acc;      // fp32 [B*H][Nq_pad][d], zeroed, unscaled dS K accumulated
+    void* dk;           // bf16 [B*H][Nk][d]
+    void* dv;           // bf16 [B*H][Nk][d]
+    int BH, Nq, Nk;
+    int Nq_pad;         // Nq rounded up to whole 128-row query tiles
+    int causal, causal_br;
+    int k_tiles;        // ceil(Nk / 128)
+    float scale;
+    float scale_log2;   // scale * log2(e)
+    long long wait_limit;
+    unsigned* status;
+};
+
 namespace {
 
 constexpr int kBwdD = 128;
@@ -533,3 +559,61 @@ cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, int BH, int Nq, int Nq_
 }
 
 }  // namespace fa
+
+extern "C" {
+
+size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d) {
+    if (B < 1 || H < 1 || Nq < 1 || d != 128) return 0;
+    const size_t rows_pad = static_cast<size_t>(B) * H * ((static_cast<size_t>(Nq) + 127) / 128 * 128);
+    return rows_pad * (static_cast<size_t>(d) + 2) * sizeof(float);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
+                 int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream) {
+    fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
+    if (s != FA_OK) return s;
+    if (d != 128) return FA_ERR_HEADDIM;
+    if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
+    if (!o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
+    if (!fa::aligned(o, 16) || !fa::aligned(dout, 16) || !fa::aligned(lse, 4) ||
+        !fa::aligned(dq, 16) || !fa::aligned(dk, 16) || !fa::aligned(dv, 16))
+        return FA_ERR_ALIGN;
+    if (!workspace || !fa::aligned(workspace, 16)) return FA_ERR_WORKSPACE;
+    const int BH = B * H;
+    const int Nq_pad = (Nq + 127) / 128 * 128;
+    const size_t rows_pad = static_cast<size_t>(BH) * Nq_pad;
+    float* dq_acc = static_cast<float*>(workspace);
+    float* nlse2 = dq_acc + rows_pad * d;
+    float* ndd = nlse2 + rows_pad;
+    fa::BwdParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!fa::encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
+        !fa::encode_rows_map(&p.tm_k, k, d, Nk, BH, 128) ||
+        !fa::encode_rows_map(&p.tm_v, v, d, Nk, BH, 128) ||
+        !fa::encode_rows_map(&p.tm_do, dout, d, Nq, BH, 128))
+        return FA_ERR_CUDA;
+    p.nlse2 = nlse2;
+    p.ndd = ndd;
+    p.dq_acc = dq_acc;
+    p.dk = dk;
+    p.dv = dv;
+    p.BH = BH;
+    p.Nq = Nq;
+    p.Nk = Nk;
+    p.Nq_pad = Nq_pad;
+    p.causal = causal ? 1 : 0;
+    p.causal_br = (causal == FA_CAUSAL_BOTTOM_RIGHT) ? 1 : 0;
+    p.k_tiles = (Nk + 127) / 128;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_limit = fa::kDefaultWaitLimit;
+    if (fa::device_status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::launch_bwd_pre(o, dout, lse, nlse2, ndd, dq_acc, BH, Nq, Nq_pad, stream) != cudaSuccess)
+        return FA_ERR_CUDA;
+    if (fa::launch_bwd_main(p, stream) != cudaSuccess) return FA_ERR_CUDA;
+    if (fa::launch_bwd_dq(dq_acc, dq, BH, Nq, Nq_pad, scale, stream) != cudaSuccess) return FA_ERR_CUDA;
+    return FA_OK;
+}
+
+}  // extern "C"

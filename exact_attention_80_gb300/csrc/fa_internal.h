@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
+#include "fa.h"
+
 namespace fa {
 
 // Bits of the device status word (one per kind of bounded wait that gave up).
@@ -64,32 +66,6 @@ struct FwdParams {
 };
 
 // Backward (d = 128): one CTA per (head, 128-key tile).
-struct BwdParams {
-    CUtensorMap tm_q;   // bf16 [B*H][Nq][d], box {64, 128, 1}
-    CUtensorMap tm_k;   // bf16 [B*H][Nk][d], box {64, 128, 1}
-    CUtensorMap tm_v;   // same as tm_k
-    CUtensorMap tm_do;  // same as tm_q (dO)
-    const float* nlse2; // fp32 [B*H][Nq_pad]: -LSE log2(e); -inf past Nq or with no key
-    const float* ndd;   // fp32 [B*H][Nq_pad]: -D_i = -sum_c dO_ic O_ic; 0 past Nq
-    float* dq_acc;      // fp32 [B*H][Nq_pad][d], zeroed, unscaled dS K accumulated
-    void* dk;           // bf16 [B*H][Nk][d]
-    void* dv;           // bf16 [B*H][Nk][d]
-    int BH, Nq, Nk;
-    int Nq_pad;         // Nq rounded up to whole 128-row query tiles
-    int causal, causal_br;
-    int k_tiles;        // ceil(Nk / 128)
-    float scale;
-    float scale_log2;   // scale * log2(e)
-    long long wait_limit;
-    unsigned* status;
-};
-
-cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, float* nlse2, float* ndd,
-                           float* dq_acc, int BH, int Nq, int Nq_pad, cudaStream_t stream);
-cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream);
-cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, int BH, int Nq, int Nq_pad, float scale,
-                          cudaStream_t stream);
-
 struct FwdConfig {
     int q_tiles;  // 128-row query tiles per CTA
     int bn;       // keys per KV tile
@@ -122,5 +98,16 @@ cudaError_t launch_combine(const float* ws_o, const float* ws_m, const float* ws
 
 // Address of the device status word on the current device (cached per device).
 cudaError_t device_status_ptr(unsigned** ptr);
+
+// Host-side argument checks and tensor maps (fa_api.cu), shared by the
+// forward and backward entry points.
+bool aligned(const void* p, uintptr_t a);
+bool valid_causal(int causal);
+// Non-null q, k, v; B, H, Nq, Nk >= 1 with B * H in int; d in {64, 128, 256};
+// finite scale > 0; q, k, v 16-byte aligned.
+fa_status check_common(const void* q, const void* k, const void* v, int B, int H, int Nq, int Nk,
+                       int d, float scale);
+// bf16 [BH][N][d] as a 3-D TMA map, box {64, box_rows, 1}, 128-byte swizzle.
+bool encode_rows_map(CUtensorMap* map, const void* base, int d, int N, int BH, int box_rows);
 
 }  // namespace fa
