@@ -1,8 +1,11 @@
-"""GB300 (sm_103a) exact attention forward: Python binding of ``libfa_gb300.so``.
+"""GB300 (sm_103a) exact attention (forward, split-KV merge, e4m3 forward,
+backward): Python binding of ``libfa_gb300.so``.
 
 The functions below carry the names of the C ABI in ``include/fa.h`` and only
 marshal arguments: every step of the computation runs in the library's CUDA
-kernels. PyTorch supplies device memory and the current CUDA stream. There is
+kernels. PyTorch supplies device memory and the current CUDA stream. The
+library receives bare pointers and cannot see a buffer's size, so the binding
+checks every tensor's dtype, shape, device and layout before the call. There is
 no fallback: if the library is missing or a call fails, an exception says so.
 """
 
@@ -101,6 +104,37 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
 
 
+def _need(t, name, shape, dtype, device):
+    """Raise unless ``t`` is a contiguous tensor of ``dtype`` and ``shape`` on
+    ``device``: the library writes through a bare pointer."""
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor on {device}")
+    if tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _need_workspace(t, nbytes: int, name: str, device):
+    """Raise unless ``t`` is a contiguous float32 tensor on ``device`` of at least
+    ``nbytes`` bytes (0: the arguments are out of range, for the library to
+    reject)."""
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32, got {t.dtype}")
+    if t.device != device or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous tensor on {device}")
+    if nbytes > 0 and t.numel() * 4 < nbytes:
+        raise ValueError(f"{name} holds {t.numel() * 4} bytes; the call needs {nbytes}")
+
+
 def _bhnd(q, k, v):
     import torch
 
@@ -109,10 +143,19 @@ def _bhnd(q, k, v):
             raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
         if t.dim() != 4 or not t.is_contiguous() or not t.is_cuda:
             raise ValueError(f"{name} must be a contiguous CUDA tensor [B, H, N, d]")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k and v must be on the same device")
     B, H, Nq, d = q.shape
     if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
         raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
     return int(B), int(H), int(Nq), int(k.shape[2]), int(d)
+
+
+def _need_o_lse(o, lse, B, H, Nq, d, device):
+    import torch
+
+    _need(o, "o", (B, H, Nq, d), torch.bfloat16, device)
+    _need(lse, "lse", (B, H, Nq), torch.float32, device)
 
 
 def causal_code(causal) -> int:
@@ -136,6 +179,7 @@ def default_scale(d: int) -> float:
 def fa_fwd(q, k, v, o, lse, causal=False, scale: float | None = None, stream=None):
     """Fused forward into caller-owned ``o`` (bf16 [B,H,Nq,d]) and ``lse`` (fp32 [B,H,Nq])."""
     B, H, Nq, Nk, d = _bhnd(q, k, v)
+    _need_o_lse(o, lse, B, H, Nq, d, q.device)
     scale = default_scale(d) if scale is None else float(scale)
     st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
                                scale, causal_code(causal), _stream_handle(stream))
@@ -151,6 +195,8 @@ def _bhnd8(q, k, v):
             raise TypeError(f"{name} must hold e4m3 codes (uint8 or float8_e4m3fn), got {t.dtype}")
         if t.dim() != 4 or not t.is_contiguous() or not t.is_cuda:
             raise ValueError(f"{name} must be a contiguous CUDA tensor [B, H, N, d]")
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k and v must be on the same device")
     B, H, Nq, d = q.shape
     if k.shape[:2] != (B, H) or k.shape[3] != d or v.shape != k.shape:
         raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)}")
@@ -164,6 +210,7 @@ def fa_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float, o,
     its e4m3 value times the tensor's descale; ``o`` bf16 [B,H,Nq,d] and ``lse``
     fp32 [B,H,Nq] are written."""
     B, H, Nq, Nk, d = _bhnd8(q, k, v)
+    _need_o_lse(o, lse, B, H, Nq, d, q.device)
     scale = default_scale(d) if scale is None else float(scale)
     st = load_library().fa_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), float(q_descale), float(k_descale),
                                    float(v_descale), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, scale,
@@ -176,6 +223,8 @@ def fa_fwd_fp8_splitkv(q, k, v, q_descale: float, k_descale: float, v_descale: f
     """Split-KV forward on e4m3 inputs into ``workspace`` (fp32, at least
     ``fa_splitkv_workspace_bytes`` bytes); merge with :func:`fa_combine`."""
     B, H, Nq, Nk, d = _bhnd8(q, k, v)
+    _need_workspace(workspace, fa_splitkv_workspace_bytes(B, H, Nq, d, int(num_splits)), "workspace",
+                    q.device)
     scale = default_scale(d) if scale is None else float(scale)
     st = load_library().fa_fwd_fp8_splitkv(_ptr(q), _ptr(k), _ptr(v), float(q_descale),
                                            float(k_descale), float(v_descale), _ptr(workspace), B, H,
@@ -213,7 +262,17 @@ def fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, causal=False,
     """Backward into caller-owned ``dq``, ``dk``, ``dv`` (bf16, shaped like q, k,
     v), from bf16 ``o`` and ``dout`` and the forward's fp32 ``lse``; ``workspace``
     fp32 of at least ``fa_bwd_workspace_bytes`` bytes (include/fa.h, fa_bwd)."""
+    import torch
+
     B, H, Nq, Nk, d = _bhnd(q, k, v)
+    dev = q.device
+    _need(o, "o", (B, H, Nq, d), torch.bfloat16, dev)
+    _need(dout, "dout", (B, H, Nq, d), torch.bfloat16, dev)
+    _need(lse, "lse", (B, H, Nq), torch.float32, dev)
+    _need(dq, "dq", (B, H, Nq, d), torch.bfloat16, dev)
+    _need(dk, "dk", (B, H, Nk, d), torch.bfloat16, dev)
+    _need(dv, "dv", (B, H, Nk, d), torch.bfloat16, dev)
+    _need_workspace(workspace, fa_bwd_workspace_bytes(B, H, Nq, d), "workspace", dev)
     scale = default_scale(d) if scale is None else float(scale)
     st = load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse), _ptr(dq),
                                _ptr(dk), _ptr(dv), _ptr(workspace), B, H, Nq, Nk, d, scale,
@@ -249,8 +308,15 @@ def fa_fwd_varlen(q, k, v, o, lse, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int
             raise ValueError("cu_seqlens must be contiguous CUDA int32 [B+1]")
     if lse.dtype != torch.float32 or not lse.is_contiguous() or not lse.is_cuda:
         raise ValueError("lse must be contiguous CUDA fp32 [H, total_q]")
+    if any(t.device != q.device for t in (k, v, o, lse, cu_seqlens_q, cu_seqlens_k)):
+        raise ValueError("every tensor must be on q's device")
     total_q, H, d = (int(x) for x in q.shape)
     total_k = int(k.shape[0])
+    if tuple(o.shape) != tuple(q.shape) or tuple(k.shape) != (total_k, H, d) or v.shape != k.shape:
+        raise ValueError(f"shape mismatch q{tuple(q.shape)} k{tuple(k.shape)} v{tuple(v.shape)} "
+                         f"o{tuple(o.shape)}")
+    if tuple(lse.shape) != (H, total_q):
+        raise ValueError(f"lse must have shape {(H, total_q)}, got {tuple(lse.shape)}")
     B = int(cu_seqlens_q.shape[0]) - 1
     if int(cu_seqlens_k.shape[0]) != B + 1 or B < 1:
         raise ValueError("cu_seqlens_q and cu_seqlens_k must both have B+1 >= 2 entries")
@@ -282,6 +348,8 @@ def fa_fwd_splitkv(q, k, v, workspace, num_splits: int, causal=False,
                    scale: float | None = None, stream=None):
     """Split-KV partial states into ``workspace`` (see include/fa.h for the layout)."""
     B, H, Nq, Nk, d = _bhnd(q, k, v)
+    _need_workspace(workspace, fa_splitkv_workspace_bytes(B, H, Nq, d, int(num_splits)), "workspace",
+                    q.device)
     scale = default_scale(d) if scale is None else float(scale)
     st = load_library().fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(workspace), B, H, Nq, Nk,
                                        d, scale, causal_code(causal), int(num_splits),
@@ -292,6 +360,9 @@ def fa_fwd_splitkv(q, k, v, workspace, num_splits: int, causal=False,
 def fa_combine(workspace, o, lse, B: int, H: int, Nq: int, d: int, num_splits: int,
                stream=None):
     """Merge partial states from ``workspace`` into ``o`` and ``lse``."""
+    _need_o_lse(o, lse, B, H, Nq, d, o.device if hasattr(o, "device") else None)
+    _need_workspace(workspace, fa_splitkv_workspace_bytes(int(B), int(H), int(Nq), int(d), int(num_splits)),
+                    "workspace", o.device)
     st = load_library().fa_combine(_ptr(workspace), _ptr(o), _ptr(lse), int(B), int(H), int(Nq),
                                    int(d), int(num_splits), _stream_handle(stream))
     _check(st, "fa_combine")
@@ -335,6 +406,7 @@ def fa_fwd_splitkv_static(q, k, v, o, lse, num_splits: int, causal=False,
     not allocate device memory; calls that overlap on the GPU share that buffer
     and race (see include/fa.h)."""
     B, H, Nq, Nk, d = _bhnd(q, k, v)
+    _need_o_lse(o, lse, B, H, Nq, d, q.device)
     scale = default_scale(d) if scale is None else float(scale)
     lib = load_library()
     fn = lib.fa_fwd_splitkv_static
