@@ -573,6 +573,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream) {
     fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
     if (s != FA_OK) return s;
+    // Query rows are padded to whole 128-row tiles and key tiles counted in
+    // int: both lengths must leave room for that rounding.
+    if (Nq > 0x7fffffff - 127 || Nk > 0x7fffffff - 127) return FA_ERR_SHAPE;
     if (d != 128) return FA_ERR_HEADDIM;
     if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
     if (!o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;

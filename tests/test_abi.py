@@ -167,6 +167,7 @@ def test_fp8_splitkv_rejects(lib, kw, code):
     (dict(dk=0), 1), (dict(dv=0), 1), (dict(ws=0), 6), (dict(ws=FAKE + 4), 6),
     (dict(d=64), 4), (dict(d=256), 4), (dict(Nq=0), 3), (dict(scale=0.0), 9), (dict(causal=3), 11),
     (dict(dq=FAKE + 8), 2), (dict(o=FAKE + 2), 2), (dict(lse=FAKE + 2), 2),
+    (dict(Nq=2**31 - 100), 3), (dict(Nk=2**31 - 100), 3),  # no room to round up to 128-row tiles
 ])
 def test_bwd_rejects(lib, kw, code):
     a = dict(q=FAKE, k=FAKE, v=FAKE, o=FAKE, do=FAKE, lse=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, ws=FAKE,
