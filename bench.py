@@ -12,8 +12,10 @@ d=256, split-KV + combine sweep).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Under ``torchrun`` each rank runs the same per-GPU workload (weak scaling, no
-data exchange: heads are independent); timing takes the max over ranks.
+With ``--gpus N`` > 1 and no torchrun environment the script starts N ranks
+itself; under ``torchrun`` WORLD_SIZE must equal N. Each rank runs the same
+per-GPU workload (weak scaling, no data exchange: heads are independent);
+timing takes the max over ranks.
 ``--impl reference`` times the float64 oracle on the host cores instead.
 """
 
@@ -279,6 +281,29 @@ def fill_splits(fa, B, H, Nq, d, sms):
     return best
 
 
+def device_qkv(c: dict, gen, device):
+    """Seeded N(0,1) bf16 Q, K, V of workload ``c`` drawn on the device. A
+    workload with ``outlier_frac`` (the large-head-dim one) gets the recipe of
+    ``inputs.make_qkv`` on the device generator: per (b, h), floor(frac * Nk)
+    distinct key rows chosen by a seeded permutation are scaled by 8 in fp32
+    before the bf16 rounding."""
+    import torch
+
+    B, H, Nq, Nk, d = c["B"], c["H"], c["Nq"], c["Nk"], c["d"]
+    gen.manual_seed(c["seed"])
+    q = torch.randn((B, H, Nq, d), generator=gen, device=device)
+    k = torch.randn((B, H, Nk, d), generator=gen, device=device)
+    v = torch.randn((B, H, Nk, d), generator=gen, device=device)
+    frac = c.get("outlier_frac", 0.0)
+    if frac > 0.0:
+        count = int(math.floor(frac * Nk))
+        rows = torch.rand((B * H, Nk), generator=gen, device=device).argsort(dim=1)[:, :count]
+        kh = k.view(B * H, Nk, d)
+        kh.scatter_(1, rows[:, :, None].expand(-1, -1, d),
+                    kh.gather(1, rows[:, :, None].expand(-1, -1, d)) * 8.0)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
 def extra_workloads(device, stream, reps: int = 20):
     """TFLOPS of the other benchmark workloads (seeded device-side N(0,1) bf16)."""
     import torch
@@ -296,10 +321,7 @@ def extra_workloads(device, stream, reps: int = 20):
     for name in ("c1", "c2_causal", "c3", "c3_causal", "c4", "prefill_bottom_right", "c5"):
         c = configs[name]
         B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
-        gen.manual_seed(c["seed"])
-        q = torch.randn((B, H, Nq, d), generator=gen, device=device).to(torch.bfloat16)
-        k = torch.randn((B, H, Nk, d), generator=gen, device=device).to(torch.bfloat16)
-        v = torch.randn((B, H, Nk, d), generator=gen, device=device).to(torch.bfloat16)
+        q, k, v = device_qkv(c, gen, device)
         o = torch.empty_like(q)
         lse = torch.empty((B, H, Nq), device=device)
         flops = metric_flops(B, H, Nq, Nk, d, causal)
@@ -309,6 +331,9 @@ def extra_workloads(device, stream, reps: int = 20):
                 fn()
             ms = statistics.median(time_launches(fn, reps, stream, queue_ahead=True))
             out[name] = {"tflops": round(flops / ms / 1e9, 1), "us": round(ms * 1e3, 1)}
+            if c.get("outlier_frac"):
+                out[name]["inputs"] = (f"N(0,1) bf16, {c['outlier_frac']:.0%} of K rows per head "
+                                       "scaled x8 (seeded permutation)")
         else:
             sweep = {}
             # The printed split counts, plus the largest whose grid fits one CTA per SM.
@@ -466,6 +491,93 @@ def varlen_workload(device, stream, reps):
             "tokens": total}
 
 
+def run_case(args) -> None:
+    """Runs one workload's kernels alone, ``--warmup`` untimed then ``--steps``
+    timed calls, and prints their mean device time: the target of an ncu
+    capture, which then sees only these launches. Cases:
+
+    ``fwd:<workload>``        fa_fwd on a benchmark workload (c1 .. c4)
+    ``split:<S>``             fa_fwd_splitkv + fa_combine on c5 with S splits
+    ``fp8``                   fa_fwd_fp8 on the c2 shape (e4m3, descales 2^-5)
+    ``bwd:<B>x<H>x<N>[:causal]``  fa_bwd at d = 128
+    """
+    import torch
+
+    import exact_attention_80_gb300 as fa
+    from exact_attention_80_gb300.inputs import CONFIGS
+
+    torch.cuda.set_device(0)
+    device = torch.device("cuda", 0)
+    fa.load_library()
+    stream = torch.cuda.current_stream(device)
+    gen = torch.Generator(device=device)
+    kind, _, arg = args.case.partition(":")
+    fns = {}
+    if kind == "fwd":
+        c = CONFIGS[arg]
+        q, k, v = device_qkv(c, gen, device)
+        o, lse = torch.empty_like(q), torch.empty(q.shape[:3], device=device)
+        fns["fa_fwd"] = lambda: fa.fa_fwd(q, k, v, o, lse, c["causal"], stream=stream)
+    elif kind == "split":
+        c = CONFIGS["c5"]
+        S = int(arg)
+        B, H, Nq, d = c["B"], c["H"], c["Nq"], c["d"]
+        q, k, v = device_qkv(c, gen, device)
+        o, lse = torch.empty_like(q), torch.empty(q.shape[:3], device=device)
+        ws = torch.empty(fa.fa_splitkv_workspace_bytes(B, H, Nq, d, S) // 4, device=device)
+        fns["fa_fwd_splitkv"] = lambda: fa.fa_fwd_splitkv(q, k, v, ws, S, False, stream=stream)
+        fns["fa_combine"] = lambda: fa.fa_combine(ws, o, lse, B, H, Nq, d, S, stream=stream)
+    elif kind == "fp8":
+        ds = 2.0 ** -5
+        gen.manual_seed(1008)
+        q8, k8, v8 = ((torch.randn((8, 32, 2048, 128), generator=gen, device=device) / ds)
+                      .clamp(-448.0, 448.0).to(torch.float8_e4m3fn) for _ in range(3))
+        o = torch.empty((8, 32, 2048, 128), dtype=torch.bfloat16, device=device)
+        lse = torch.empty((8, 32, 2048), device=device)
+        fns["fa_fwd_fp8"] = lambda: fa.fa_fwd_fp8(q8, k8, v8, ds, ds, ds, o, lse, False, stream=stream)
+    elif kind == "bwd":
+        shape, _, mask = arg.partition(":")
+        B, H, N = (int(x) for x in shape.split("x"))
+        causal = mask == "causal"
+        gen.manual_seed(1010)
+        q, k, v, do = (torch.randn((B, H, N, 128), generator=gen, device=device).to(torch.bfloat16)
+                       for _ in range(4))
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, 128) // 4, device=device)
+        o, lse = fa.attention(q, k, v, causal=causal, stream=stream)
+        fns["fa_bwd"] = lambda: fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, causal, stream=stream)
+    else:
+        raise SystemExit(f"unknown case {args.case!r}")
+    for _ in range(args.warmup):
+        for fn in fns.values():
+            fn()
+    torch.cuda.synchronize()
+    times = {name: statistics.mean(time_launches(fn, args.steps, stream)) for name, fn in fns.items()}
+    if fa.fa_device_status(clear=True, stream=stream) != fa.FA_OK:
+        raise RuntimeError("device status reports a timed-out wait")
+    print(f"case {args.case}: " + ", ".join(f"{n} {t * 1e3:.1f} us" for n, t in times.items()))
+
+
+def workload_config(wl: str, world: int) -> dict:
+    """The ``config`` object of both arms' JSON lines for workload ``wl``."""
+    from exact_attention_80_gb300.inputs import CONFIGS
+
+    c = CONFIGS[wl]
+    B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
+    in_bytes = (B * H * Nq * d + 2 * B * H * Nk * d) * 2
+    cfg = {"workload": f"{wl}: B={B} H={H} Nq={Nq} Nk={Nk} d={d} "
+                       f"{'causal' if causal else 'non-causal'}",
+           "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": causal,
+           "seed": c["seed"], "per_rank_batch": B,
+           "l2": (f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB of Q/K/V per rank vs "
+                  f"{L2_BYTES / 2**20:.0f} MiB L2); no flush") if in_bytes > L2_BYTES else
+                 "inputs smaller than L2",
+           "parallelism": f"replicas x{world} (independent heads, no exchange)"}
+    if c.get("outlier_frac"):
+        cfg["outliers"] = f"{c['outlier_frac']:.0%} of K rows per head scaled x8"
+    return cfg
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -485,13 +597,12 @@ def run_ours(args):
     c = CONFIGS[wl]
     B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
     seed = shard_seed(c["seed"], rank)
-    q_h, k_h, v_h = make_qkv(B, H, Nq, Nk, d, seed)
+    q_h, k_h, v_h = make_qkv(B, H, Nq, Nk, d, seed, outlier_frac=c.get("outlier_frac", 0.0))
     scale = f32(1.0 / math.sqrt(d))
     q, k, v = q_h.to(device), k_h.to(device), v_h.to(device)
     o = torch.empty_like(q)
     lse = torch.empty((B, H, Nq), dtype=torch.float32, device=device)
     flops = metric_flops(B, H, Nq, Nk, d, causal)
-    in_bytes = 3 * q.numel() * 2 if Nq == Nk else (q.numel() + 2 * k.numel()) * 2
 
     step = lambda: fa.fa_fwd(q, k, v, o, lse, causal, scale, stream=stream)  # noqa: E731
 
@@ -517,19 +628,19 @@ def run_ours(args):
     value = dist_sum(flops, world, device) * args.steps / (total_ms / 1e3) / 1e12
     avg_launch_ms = statistics.mean(per_step)
 
-    # ---- numeric check outside the timed window (sampled rows vs the oracle)
+    # ---- numeric check outside the timed window: one whole (b, h) head, chosen
+    # by the seed, element by element against the oracle
     rng = np.random.default_rng(seed)
-    worst = 0.0
-    o_cpu, lse_cpu = o.float().cpu(), lse.cpu()
-    for _ in range(8):
-        b, h, i = int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(Nq))
-        ro, rl = oracle.attention_rows_f64(to_f64(q_h[b, h]), to_f64(k_h[b, h]),
-                                           to_f64(v_h[b, h]), scale, causal, [i])
-        worst = max(worst, float(np.abs(o_cpu[b, h, i].numpy() - ro[0]).max()))
-        if abs(float(lse_cpu[b, h, i]) - rl[0]) > 1e-3:
-            raise RuntimeError("bench parity check failed on LSE")
-    if worst > 2e-2:
-        raise RuntimeError(f"bench parity check failed: max-abs {worst:.3e}")
+    b, h = int(rng.integers(B)), int(rng.integers(H))
+    ro, rl = oracle.attention_f64(to_f64(q_h[b, h]), to_f64(k_h[b, h]), to_f64(v_h[b, h]), scale,
+                                  causal)
+    got = o[b, h].float().cpu().numpy().astype(np.float64)
+    worst = float(np.abs(got - ro).max())
+    rel = float(np.linalg.norm(got - ro) / np.linalg.norm(ro))
+    lse_err = float(np.abs(lse[b, h].cpu().numpy() - rl).max())
+    if not (worst <= 2e-2 and rel <= 5e-3 and lse_err <= 1e-3):
+        raise RuntimeError(f"bench parity check failed on head ({b}, {h}): max-abs {worst:.3e}, "
+                           f"rel-L2 {rel:.3e}, LSE {lse_err:.3e}")
 
     # ---- end to end through the public API from pinned host buffers
     qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
@@ -537,20 +648,22 @@ def run_ours(args):
     lp = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
 
     def e2e_step():
-        q.copy_(qp, non_blocking=True)
-        k.copy_(kp, non_blocking=True)
-        v.copy_(vp, non_blocking=True)
-        fa.fa_fwd(q, k, v, o, lse, causal, scale, stream=stream)
-        op.copy_(o, non_blocking=True)
-        lp.copy_(lse, non_blocking=True)
+        # Host-to-device copies of one slice of the batch overlap the kernel of
+        # the previous slice and the copy back of the one before.
+        fa.fa_fwd_from_host(qp, kp, vp, op, lp, q, k, v, o, lse, causal, scale,
+                            chunks=args.e2e_chunks, stream=stream)
 
     e2e_steps = max(3, min(args.steps, 50))
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
+    e2e_err = float((op.float() - o.float().cpu()).abs().max())
+    if e2e_err != 0.0:
+        raise RuntimeError(f"end-to-end output differs from the device-resident one ({e2e_err:.3e})")
     dist_barrier(world, device)
     e2e_ms = dist_max(sum(time_launches(e2e_step, e2e_steps, stream)), world, device) / e2e_steps
     e2e_value = dist_sum(flops, world, device) / (e2e_ms / 1e3) / 1e12
+    e2e_launches = min(args.e2e_chunks, B)
     h2d = (qp.numel() + kp.numel() + vp.numel()) * 2
     d2h = op.numel() * 2 + lp.numel() * 4
 
@@ -566,21 +679,16 @@ def run_ours(args):
     if world == 1 and not args.no_cpu_baseline:
         tf, heads, secs = oracle_sample(c, args.cpu_budget, seed)
         cpu = {"value": round(tf, 6), "unit": "TFLOPS", "cores": cpu_threads(), "kind": "oracle",
-               "sample": f"{heads} of the {B * H} (b,h) heads of {wl}, float64 NumPy, "
-                         f"{secs:.1f} s"}
+               "sample": f"{heads} passes of the float64 NumPy oracle over one seeded "
+                         f"{c['Nq']}x{c['Nk']} d={d} head of {wl} (the same synthetic head each "
+                         f"time, all its queries against all its keys), {secs:.1f} s"}
     line = {
         "metric": "attention fwd TFLOPS (bf16, 4*B*H*Nq*Nk*d, halved for causal)",
         "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16)",
-        "config": {"workload": f"{wl}: B={B} H={H} Nq={Nq} Nk={Nk} d={d} "
-                               f"{'causal' if causal else 'non-causal'}",
-                   "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": causal,
-                   "seed": seed, "per_rank_batch": B,
-                   "l2": f"inputs larger than L2 ({in_bytes / 2**20:.0f} MiB of Q/K/V per rank "
-                         f"vs {L2_BYTES / 2**20:.0f} MiB L2); no flush",
-                   "parallelism": f"replicas x{world} (independent heads, no exchange)"},
+        "config": workload_config(wl, world),
         "roofline": {"bound": "tensor", "kernel": kernel_name(d),
                      "achieved": round(achieved, 1), "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tf, 4),
@@ -588,11 +696,13 @@ def run_ours(args):
                      "traffic": recorded_traffic(kernel_name(d), wl),
                      "flops_per_launch": flops},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                "how": f"fa_fwd_from_host: the batch in {e2e_launches} slices along B, host-to-device "
+                       "copies, kernels and device-to-host copies on three streams"},
         "gpu_launches": args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
-        "parity_sampled_max_abs": worst,
+        "parity_whole_head": {"head": [b, h], "max_abs": worst, "rel_l2": rel, "lse_abs": lse_err},
         "other_workloads": extras,
     }
     return line
@@ -639,9 +749,7 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) bf16, upcast to float64)",
-        "config": {"workload": f"{wl}: B={B} H={H} Nq={Nq} Nk={Nk} d={d} "
-                               f"{'causal' if causal else 'non-causal'}",
-                   "B": B, "H": H, "Nq": Nq, "Nk": Nk, "d": d, "causal": causal},
+        "config": workload_config(wl, world),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cpu_threads(),
                          "kind": "oracle",
                          "sample": f"each step = {rows_per_step} query rows of one (b,h) head "
@@ -651,7 +759,21 @@ def run_reference(args):
     }
 
 
+def launch_ranks(n: int, argv: list[str]) -> int:
+    """Re-runs this script as ``n`` ranks on this node (one per GPU) under
+    torch.distributed.run with a loopback rendezvous; returns its exit code."""
+    import socket
+
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -662,7 +784,24 @@ def main(argv=None):
                     help="seconds of float64 oracle work for cpu_baseline")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=4,
+                    help="slices of the batch whose copies overlap the kernels end to end")
+    ap.add_argument("--case", default=None,
+                    help="run one workload's kernels only, for an ncu capture (see run_case)")
     args = ap.parse_args(argv)
+    if args.case:
+        run_case(args)
+        return 0
+    if args.gpus < 1:
+        ap.error("--gpus must be >= 1")
+    world_env = os.environ.get("WORLD_SIZE")
+    if world_env is None and args.gpus > 1:
+        # One process per GPU: start the ranks here rather than run as one.
+        return launch_ranks(args.gpus, argv)
+    if int(world_env or "1") != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but WORLD_SIZE={world_env}: launch one rank per GPU "
+              f"(or leave WORLD_SIZE unset and let --gpus start them)", file=sys.stderr)
+        return 2
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     line = run_reference(args) if args.impl == "reference" else run_ours(args)
@@ -673,7 +812,8 @@ def main(argv=None):
 
         if dist.is_initialized():
             dist.destroy_process_group()
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -416,3 +416,65 @@ def fa_fwd_splitkv_static(q, k, v, o, lse, num_splits: int, causal=False,
     st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d, scale,
             causal_code(causal), int(num_splits), _stream_handle(stream))
     _check(st, "fa_fwd_splitkv_static")
+
+
+_SIDE_STREAMS = {}
+
+
+def _side_streams(device):
+    """Two streams per device, for host-to-device and device-to-host copies."""
+    import torch
+
+    key = torch.device(device).index
+    if key not in _SIDE_STREAMS:
+        _SIDE_STREAMS[key] = (torch.cuda.Stream(device=device), torch.cuda.Stream(device=device))
+    return _SIDE_STREAMS[key]
+
+
+def fa_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse, causal=False,
+                     scale: float | None = None, chunks: int = 4, stream=None):
+    """The forward of :func:`fa_fwd` on inputs and outputs in pinned host memory.
+
+    ``q_host``, ``k_host``, ``v_host`` (bf16 [B,H,N,d]) are copied into the
+    device tensors ``q``, ``k``, ``v`` of the same shapes, the forward writes the
+    device ``o``, ``lse``, and they are copied back into ``o_host``, ``lse_host``.
+    The batch is cut into ``chunks`` slices along B so that the copies of one
+    slice overlap the kernel of another: host-to-device copies on one side
+    stream, the kernels on ``stream``, device-to-host copies on another. Every
+    call starts after the work already queued on ``stream`` and ``stream`` waits
+    for the last copy back, so a caller synchronises on ``stream`` alone.
+    """
+    import torch
+
+    B, H, Nq, Nk, d = _bhnd(q, k, v)
+    _need_o_lse(o, lse, B, H, Nq, d, q.device)
+    cpu = torch.device("cpu")
+    for name, t, dev_t in (("q_host", q_host, q), ("k_host", k_host, k), ("v_host", v_host, v),
+                           ("o_host", o_host, o), ("lse_host", lse_host, lse)):
+        _need(t, name, tuple(dev_t.shape), dev_t.dtype, cpu)
+        if not t.is_pinned():
+            raise ValueError(f"{name} must be in pinned host memory")
+    chunks = max(1, min(int(chunks), B))
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    s_in, s_out = _side_streams(q.device)
+    s_in.wait_stream(stream)
+    bounds = [(B * i // chunks, B * (i + 1) // chunks) for i in range(chunks)]
+    done_out = None
+    for b0, b1 in bounds:
+        with torch.cuda.stream(s_in):
+            for src, dst in ((q_host, q), (k_host, k), (v_host, v)):
+                dst[b0:b1].copy_(src[b0:b1], non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+        stream.wait_event(ev_in)
+        fa_fwd(q[b0:b1], k[b0:b1], v[b0:b1], o[b0:b1], lse[b0:b1], causal, scale, stream)
+        ev_c = torch.cuda.Event()
+        ev_c.record(stream)
+        s_out.wait_event(ev_c)
+        with torch.cuda.stream(s_out):
+            o_host[b0:b1].copy_(o[b0:b1], non_blocking=True)
+            lse_host[b0:b1].copy_(lse[b0:b1], non_blocking=True)
+            done_out = torch.cuda.Event()
+            done_out.record(s_out)
+    stream.wait_event(done_out)

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstring>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include <cudaTypedefs.h>
@@ -19,21 +20,42 @@ namespace fa {
 // Error word raised by kernels whose bounded waits give up (bits: fa_internal.h).
 __device__ unsigned g_fa_device_status = 0u;
 
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* a = nullptr;
+        void* b = nullptr;
+        cudaDriverEntryPointQueryResult qa = cudaDriverEntryPointSymbolNotFound;
+        cudaDriverEntryPointQueryResult qb = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) ==
+                cudaSuccess &&
+            qa == cudaDriverEntryPointSuccess &&
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+                cudaSuccess &&
+            qb == cudaDriverEntryPointSuccess) {
+            get_current = reinterpret_cast<GetCurrent>(a);
+            get_id = reinterpret_cast<GetId>(b);
+        }
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
 cudaError_t device_status_ptr(unsigned** ptr) {
-    static unsigned* cache[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && cache[dev]) {
-        *ptr = cache[dev];
-        return cudaSuccess;
-    }
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_fa_device_status);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) cache[dev] = static_cast<unsigned*>(p);
-    *ptr = static_cast<unsigned*>(p);
-    return cudaSuccess;
+    static ContextCache<unsigned*> cache;
+    return cache.get(ptr, [](unsigned** out) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_fa_device_status);
+        *out = static_cast<unsigned*>(p);
+        return e;
+    });
 }
 
 FwdConfig fwd_config(int d) {
@@ -60,16 +82,19 @@ FwdConfig fwd_config(int d) {
 namespace {
 
 cudaError_t sm_count(int* out) {
-    static int cache[64] = {};
+    static std::atomic<int> cache[64] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && cache[dev] > 0) {
-        *out = cache[dev];
-        return cudaSuccess;
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) {
+            *out = c;
+            return cudaSuccess;
+        }
     }
     e = cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess && dev >= 0 && dev < 64) cache[dev] = *out;
+    if (e == cudaSuccess && dev >= 0 && dev < 64) cache[dev].store(*out, std::memory_order_relaxed);
     return e;
 }
 

@@ -532,16 +532,15 @@ cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, fl
 }
 
 cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream) {
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    // Kernel attributes belong to the context: set once per device and context.
+    static ContextCache<int> attr_set;
+    int done = 0;
+    const cudaError_t e = attr_set.get(&done, [](int* out) {
+        *out = 1;
+        return cudaFuncSetAttribute(fa_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(LayoutBwd::ALLOC_BYTES));
+    });
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fa_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(LayoutBwd::ALLOC_BYTES));
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
     const long long ctas = static_cast<long long>(p.BH) * p.k_tiles;
     if (ctas < 1 || ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
     fa_bwd_kernel<<<static_cast<unsigned>(ctas), LayoutBwd::THREADS, LayoutBwd::ALLOC_BYTES, stream>>>(p);

@@ -13,6 +13,7 @@
 // warp reads a split's row as one contiguous 4d-byte segment. With W > 1 the
 // warps' sums meet in shared memory; every warp computes the same M, so no
 // rescaling is needed there.
+#include <atomic>
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
@@ -157,22 +158,25 @@ __global__ void __launch_bounds__(256)
 
 // Blocks of this kernel the whole GPU holds at once at `threads` threads per
 // block (per-SM occupancy x SMs), queried once per device and block size.
-// Concurrent first calls may both query; they store the same value.
+// Concurrent first calls may both query; they store the same value through an
+// atomic, so the cache is race-free.
 template <int D>
 int combine_resident_blocks(int threads) {
-    static int cache[64][2];  // [device][threads == 256]
+    static std::atomic<int> cache[64][2];  // [device][threads == 256]
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
-    int& slot = cache[dev][threads == 256 ? 1 : 0];
-    if (slot == 0) {
+    std::atomic<int>& slot = cache[dev][threads == 256 ? 1 : 0];
+    int value = slot.load(std::memory_order_relaxed);
+    if (value == 0) {
         int per_sm = 0, sms = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fa_combine_kernel<D>, threads, 0) !=
                 cudaSuccess ||
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return 1;
-        slot = (per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
+        value = (per_sm > 0 ? per_sm : 1) * (sms > 0 ? sms : 1);
+        slot.store(value, std::memory_order_relaxed);
     }
-    return slot;
+    return value;
 }
 
 // Warps per row W (1, 2, 4 or 8): enough batches to cover the splits in one

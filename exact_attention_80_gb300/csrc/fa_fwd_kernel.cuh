@@ -30,23 +30,22 @@ cudaError_t launch_fwd(const FwdParams& p, unsigned grid, cudaStream_t stream) {
         else if constexpr (D == 256) return fa_fwd_tp_kernel<D>;
         else return fa_fwd_tm_kernel<D>;
     }();
-    static bool attr_set[64] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    // Kernel attributes belong to the context: set once per device and context.
+    static ContextCache<int> attr_set;
+    int done = 0;
+    cudaError_t e = attr_set.get(&done, [kernel](int* out) {
         if constexpr (L::REG_SPLIT) {
             // The setmaxnreg split is sized for exactly LAUNCH_REGS per thread.
             cudaFuncAttributes a;
-            e = cudaFuncGetAttributes(&a, kernel);
-            if (e != cudaSuccess) return e;
+            cudaError_t err = cudaFuncGetAttributes(&a, kernel);
+            if (err != cudaSuccess) return err;
             if (a.numRegs != L::LAUNCH_REGS) return cudaErrorInvalidKernelImage;
         }
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(L::ALLOC_BYTES));
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_set[dev] = true;
-    }
+        *out = 1;
+        return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(L::ALLOC_BYTES));
+    });
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
     cfg.blockDim = dim3(L::THREADS, 1, 1);

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_runtime_api.h>
 
@@ -96,8 +97,57 @@ cudaError_t launch_combine(const float* ws_o, const float* ws_m, const float* ws
                            float* lse, long long rows, int num_splits, int d,
                            cudaStream_t stream);
 
-// Address of the device status word on the current device (cached per device).
+// Address of the device status word on the current device (cached per device
+// and context).
 cudaError_t device_status_ptr(unsigned** ptr);
+
+// Unique identifier of the calling thread's current CUDA context (cuCtxGetId),
+// or 0 when there is none or the driver does not provide the call.
+unsigned long long current_context_id();
+
+// A value bound to a device's CUDA context: a device symbol's address, or the
+// fact that a kernel attribute has been set. Cached per device; derived again
+// when the device's current context is not the one it was derived in (after
+// cudaDeviceReset, or when the primary context was released and re-created), so
+// no stale address is ever handed to a kernel. Safe to call from several host
+// threads at once.
+template <typename T>
+class ContextCache {
+  public:
+    // `derive(T*)` computes the value with the device current; its error is returned.
+    template <typename F>
+    cudaError_t get(T* out, F&& derive) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+        const unsigned long long ctx = current_context_id();
+        std::lock_guard<std::mutex> lock(mutex_);
+        Entry& en = entries_[dev];
+        if (en.valid && ctx != 0 && en.ctx == ctx) {
+            *out = en.value;
+            return cudaSuccess;
+        }
+        T value{};
+        e = derive(&value);
+        if (e != cudaSuccess) return e;
+        en.value = value;
+        en.ctx = current_context_id();  // the derivation may have created the context
+        en.valid = true;
+        *out = value;
+        return cudaSuccess;
+    }
+
+  private:
+    static constexpr int kMaxDevices = 64;
+    struct Entry {
+        unsigned long long ctx = 0;
+        T value{};
+        bool valid = false;
+    };
+    std::mutex mutex_;
+    Entry entries_[kMaxDevices];
+};
 
 // Host-side argument checks and tensor maps (fa_api.cu), shared by the
 // forward and backward entry points.

@@ -1,9 +1,8 @@
 // fa_noalloc.cu — fa_fwd_splitkv_static: the split-KV forward and merge with
 // their partial states in a library-owned static device buffer, for callers
 // that cannot allocate device memory themselves (see include/fa.h).
-#include <mutex>
-
 #include "fa.h"
+#include "fa_internal.h"
 
 namespace fa {
 namespace {
@@ -13,28 +12,18 @@ namespace {
 // address looked up below, never this symbol.
 static __device__ __align__(256) float g_static_scratch[FA_STATIC_SCRATCH_BYTES / sizeof(float)];
 
-std::mutex g_scratch_mutex;
-float* g_scratch_ptr[64] = {};
-
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current) and cached.
+// Device address of the scratch on the current device, looked up with that
+// device current (cudaGetSymbolAddress) on the first call in each CUDA context
+// and cached; a new context (after cudaDeviceReset) gets a fresh lookup.
 cudaError_t static_scratch(float** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
+    static ContextCache<float*> cache;
+    return cache.get(out, [](float** ptr) {
         void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = static_cast<float*>(p);
-    }
-    *out = g_scratch_ptr[dev];
-    return cudaSuccess;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+        *ptr = static_cast<float*>(p);
+        return e;
+    });
 }
-
-bool valid_head_dim(int d) { return d == 64 || d == 128 || d == 256; }
 
 }  // namespace
 }  // namespace fa
@@ -43,11 +32,14 @@ extern "C" fa_status fa_fwd_splitkv_static(const void* q, const void* k, const v
                                            float* lse, int B, int H, int Nq, int Nk, int d,
                                            float scale, int causal, int num_splits,
                                            cudaStream_t stream) {
-    // Everything checkable on the host is checked before the size test and
-    // before any CUDA call; the calls below repeat the full validation.
-    if (!q || !k || !v || !o || !lse) return FA_ERR_NULL;
-    if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return FA_ERR_SHAPE;
-    if (!fa::valid_head_dim(d)) return FA_ERR_HEADDIM;
+    // Everything checkable on the host (pointers, alignment, shapes, scale,
+    // mask, split count) is checked before the size test and before any CUDA
+    // call, so a refused call has queued no work; the calls below repeat it.
+    const fa_status s0 = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
+    if (s0 != FA_OK) return s0;
+    if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
+    if (!o || !lse) return FA_ERR_NULL;
+    if (!fa::aligned(o, 16) || !fa::aligned(lse, 4)) return FA_ERR_ALIGN;
     if (num_splits < 1 || num_splits > FA_MAX_SPLITS) return FA_ERR_SPLITS;
     const size_t need = fa_splitkv_workspace_bytes(B, H, Nq, d, num_splits);
     if (need == 0) return FA_ERR_SHAPE;

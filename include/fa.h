@@ -267,7 +267,13 @@ fa_status fa_device_status(cudaStream_t stream, int clear);
  *     with your own workspace).
  *   - The first call on a device looks up that device's address of the buffer
  *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is cached per device and CUDA
+ *     context: after cudaDeviceReset, or once the primary context has been
+ *     released and re-created, the next call looks it up again (so that call,
+ *     too, belongs before any capture) and no stale address is ever used.
+ *   - Pointers, alignment, shapes, scale, mask and split count are checked
+ *     before the size test and before any CUDA call: a refused call queues no
+ *     work and leaves the buffer untouched.
  *   - All calls on a device share the one buffer and it keeps the last call's
  *     contents. Nothing in it needs to start at zero: the split kernel writes
  *     every entry the merge reads. Calls whose work overlaps on the GPU (other

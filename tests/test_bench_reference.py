@@ -46,4 +46,36 @@ def test_reference_other_workloads(workload):
 
 
 def test_reference_other_ranks_print_nothing():
-    assert _run({"RANK": "1", "WORLD_SIZE": "2"}, "--steps", "1", "--warmup", "0") == []
+    assert _run({"RANK": "1", "WORLD_SIZE": "2"}, "--gpus", "2", "--steps", "1", "--warmup", "0") == []
+
+
+def test_gpus_flag_starts_the_ranks_itself():
+    """--gpus 2 with no torchrun environment starts two ranks; rank 0 prints
+    the one line and reports n_gpus = 2."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "0", "--workload", "c1"],
+                       capture_output=True, text=True, cwd=ROOT, env=env, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(x) for x in r.stdout.splitlines() if x.strip().startswith("{")]
+    assert len(lines) == 1 and lines[0]["n_gpus"] == 2 and lines[0]["impl"] == "reference"
+
+
+def test_gpus_flag_must_match_world_size():
+    env = dict(os.environ, RANK="0", WORLD_SIZE="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, cwd=ROOT, env=env, timeout=300)
+    assert r.returncode != 0 and "WORLD_SIZE" in r.stderr
+    assert not r.stdout.strip()
+
+
+def test_reference_config_matches_our_arm():
+    """Both arms' JSON lines carry the same config object."""
+    import bench
+
+    d = json.loads(_run({"RANK": "0", "WORLD_SIZE": "1"}, "--steps", "1", "--warmup", "0")[0])
+    assert d["config"] == bench.workload_config("c2", 1)
+    for key in ("seed", "l2", "parallelism", "per_rank_batch"):
+        assert key in d["config"]

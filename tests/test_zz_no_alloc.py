@@ -5,8 +5,9 @@ budgeted by a host framework's own allocator; serving loops where an
 allocation could stall the device). It keeps the split partial states in the
 library's static device buffer instead of a caller workspace. These tests call
 it through the C ABI and check, on two calls in a row, that it gives what the
-workspace path (fa_fwd_splitkv + fa_combine) gives, within the parity
-tolerances used everywhere else. This file is collected last on purpose.
+workspace path (fa_fwd_splitkv + fa_combine) gives and what the float64 oracle
+gives, within the parity tolerances used everywhere else. This file is
+collected last on purpose.
 """
 
 import ctypes
@@ -51,6 +52,40 @@ def test_rejects_partial_states_beyond_the_static_buffer():
     assert fn(P(fake), P(fake), P(fake), P(fake), P(fake), 1, 8, 128, 4096, 128, 0.088, 0, 0, P(0)) == 5
 
 
+def test_refuses_misaligned_outputs_before_any_launch():
+    """A misaligned o or lse, an unknown mask or a bad scale is refused on the
+    host with the status fa_fwd would give, before the size test and before any
+    CUDA call, so no work is queued (fake pointers are never used)."""
+    fn = _static_fn()
+    fake = 0x10000
+    args = (1, 8, 128, 4096, 128)
+    assert fn(P(fake), P(fake), P(fake), P(fake + 8), P(fake), *args, 0.088, 0, 4, P(0)) == 2
+    assert fn(P(fake), P(fake), P(fake), P(fake), P(fake + 2), *args, 0.088, 0, 4, P(0)) == 2
+    assert fn(P(fake), P(fake + 8), P(fake), P(fake), P(fake), *args, 0.088, 0, 4, P(0)) == 2
+    assert fn(P(fake), P(fake), P(fake), P(fake), P(fake), *args, 0.088, 7, 4, P(0)) == 11
+    assert fn(P(fake), P(fake), P(fake), P(fake), P(fake), *args, -1.0, 0, 4, P(0)) == 9
+    # ... and the misaligned output is refused even when the partial states
+    # would not fit the buffer either.
+    assert fn(P(fake), P(fake), P(fake), P(fake + 8), P(fake), 1, 8, 128, 4096, 128, 0.088, 0, 64,
+              P(0)) == 2
+
+
+def _compare_oracle(o, lse, q, k, v, scale, causal):
+    """Element by element against the float64 oracle."""
+    import numpy as np
+
+    import oracle
+    from exact_attention_80_gb300.inputs import to_f64
+
+    o_ref, lse_ref = oracle.attention_f64(to_f64(q.cpu()), to_f64(k.cpu()), to_f64(v.cpu()), scale,
+                                          causal)
+    got = o.float().cpu().numpy().astype(np.float64)
+    max_abs = float(np.abs(got - o_ref).max())
+    rel = float(np.linalg.norm(got - o_ref) / np.linalg.norm(o_ref))
+    lerr = float(np.abs(lse.cpu().numpy() - lse_ref).max())
+    assert max_abs <= MAX_ABS and rel <= REL_L2 and lerr <= LSE_ABS, (max_abs, rel, lerr)
+
+
 def _compare(o, lse, o_ref, lse_ref):
     a, b = o.float(), o_ref.float()
     max_abs = (a - b).abs().max().item()
@@ -84,3 +119,4 @@ def test_static_scratch_matches_workspace_path(B, H, Nq, Nk, d, causal, splits):
         assert fa.fa_device_status(clear=True) == fa.FA_OK
         assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
         _compare(o, lse, o_ref, lse_ref)
+        _compare_oracle(o, lse, q, k, v, scale, causal)
