@@ -207,27 +207,40 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 // accumulator row: normalised O (bf16) and LSE in plain mode, or the
 // unnormalised partial state (O, m, l) in split mode. Deferred normalisation:
 // one division per row, at the write.
+//
+// Two row sums arrive: `l`, the sum of the exponentials as computed (fp32, for
+// the LSE and the partial l), and `l_o`, the denominator of O: the sum of the
+// weights the PV MMA actually multiplied V by (P rounded to bf16), as far as
+// the softmax tracked them (l plus the rounding error of each key tile's
+// largest p). O / l_o keeps the dominant keys' weights consistent with the
+// rounded P, so a row dominated by one key gives that key's V up to the output
+// rounding. Paths that do not track the rounding pass l_o = l.
 template <int D>
 struct RowOut {
     bool row_ok;
     bool split;
-    float f;   // plain: o_scale/l; split: move from the lazy reference m to m_true
-    float fo;  // split: the factor on the partial O, f * o_scale (l takes f alone)
+    float f;   // plain: o_scale/l_o; split: move from the lazy reference m to m_true
+    float fo;  // split: the factor on the partial O, f * o_scale * l / l_o (l takes f alone)
     size_t row_idx, lse_idx, part_idx;
     float m, m_true, l;
 
     // `o_scale` multiplies O, normalised (plain mode) or partial (split mode):
-    // the V descale of 8-bit inputs, 1 otherwise.
+    // the V descale of 8-bit inputs, 1 otherwise. In split mode O is scaled by
+    // l / l_o, so that the partial (u, l) satisfies u / l = O / l_o.
     __device__ __forceinline__ RowOut(const FwdParams& p, const RowMap& rm, int bh, int split_idx,
-                                      int q_row, float m_, float m_true_, float l_,
+                                      int q_row, float m_, float m_true_, float l_, float l_o,
                                       float o_scale = 1.f)
         : row_ok(q_row < rm.len_q), split(p.split_mode != 0), m(m_), m_true(m_true_), l(l_) {
         row_idx = static_cast<size_t>(rm.o_base + static_cast<long long>(q_row) * rm.o_stride);
         lse_idx = static_cast<size_t>(rm.lse_base + q_row);
         part_idx = (static_cast<size_t>(split_idx) * p.BH + bh) * p.Nq + q_row;
-        if (!split) f = (l > 0.f) ? o_scale / l : 0.f;
-        else f = (l > 0.f && m != m_true) ? ex2(m - m_true) : 1.f;
-        fo = f * o_scale;
+        if (!split) {
+            f = (l_o > 0.f) ? o_scale / l_o : 0.f;
+            fo = f;
+        } else {
+            f = (l > 0.f && m != m_true) ? ex2(m - m_true) : 1.f;
+            fo = f * o_scale * ((l_o > 0.f && l_o != l) ? l / l_o : 1.f);
+        }
     }
     // Columns [32 cc, 32 cc + 32) of the row, fp32 bits (zero when the row saw
     // no key); `o` is scaled in place.
@@ -280,9 +293,9 @@ struct RowOut {
 // tO, D fp32 columns; not read when n == 0), a chunk at a time.
 template <int D>
 __device__ __forceinline__ void write_row(const FwdParams& p, const RowMap& rm, int bh, int split,
-                                          int q_row, int n, float m, float m_true, float l,
+                                          int q_row, int n, float m, float m_true, float l, float l_o,
                                           uint32_t tO, float o_scale = 1.f) {
-    const RowOut<D> out(p, rm, bh, split, q_row, m, m_true, l, o_scale);
+    const RowOut<D> out(p, rm, bh, split, q_row, m, m_true, l, l_o, o_scale);
 #pragma unroll 1
     for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
@@ -312,10 +325,10 @@ __device__ __forceinline__ void write_row(const FwdParams& p, const RowMap& rm, 
 template <int D>
 __device__ __forceinline__ bool store_tile_tma(const FwdParams& p, const RowMap& rm, int bh, int q_row0,
                                                int r, int q_row, float m, float m_true, float l,
-                                               uint32_t tO, uint32_t q_tile, uint32_t staged,
+                                               float l_o, uint32_t tO, uint32_t q_tile, uint32_t staged,
                                                volatile uint32_t* abort_flag, float o_scale = 1.f) {
     const int lane = r & 31;
-    const RowOut<D> out(p, rm, bh, 0, q_row, m, m_true, l, o_scale);
+    const RowOut<D> out(p, rm, bh, 0, q_row, m, m_true, l, l_o, o_scale);
     const uint32_t swz = static_cast<uint32_t>(r & 7);
 #pragma unroll 1
     for (int cc = 0; cc < D / 32; ++cc) {
@@ -363,10 +376,10 @@ __device__ __forceinline__ bool store_tile_tma(const FwdParams& p, const RowMap&
 template <int D>
 __device__ __forceinline__ void store_rows_tma(const FwdParams& p, const RowMap& rm, int bh, int q_row0,
                                                int r, int q_row, float m, float m_true, float l,
-                                               uint32_t tO, uint32_t q_tile, float o_scale = 1.f) {
+                                               float l_o, uint32_t tO, uint32_t q_tile, float o_scale = 1.f) {
     const int lane = r & 31;
     const int quarter = r >> 5;
-    const RowOut<D> out(p, rm, bh, 0, q_row, m, m_true, l, o_scale);
+    const RowOut<D> out(p, rm, bh, 0, q_row, m, m_true, l, l_o, o_scale);
     const uint32_t swz = static_cast<uint32_t>(r & 7);
     const int wrow0 = q_row0 + quarter * 32;
     const bool any_row = wrow0 < rm.len_q;

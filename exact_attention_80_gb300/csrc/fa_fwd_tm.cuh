@@ -626,6 +626,9 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
         float m = -INFINITY;       // exponent reference (base-2 units of scale*log2e*s)
         float m_true = -INFINITY;  // true running row max, same units
         float l = 0.f;             // running sum relative to m
+        // bf16 P: the rounding error of each key tile's largest p, relative to m
+        // like l. l + lc is the denominator of O (see RowOut).
+        float lc = 0.f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             ok = wait_phase(bar(L::BAR_SFULL + t), j & 1, p, abort_flag, kStatusWaitS);
@@ -666,7 +669,8 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
                 a2 = max3f(a2, s[c + 4], s[c + 5]);
                 a3 = max3f(a3, s[c + 6], s[c + 7]);
             }
-            const float m_tile = max3f(a0, a1, fmaxf(a2, a3)) * sl2;  // base-2 units
+            const float s_max = max3f(a0, a1, fmaxf(a2, a3));
+            const float m_tile = s_max * sl2;  // base-2 units
             m_true = fmaxf(m_true, m_tile);
             // The exponent reference m only moves when this tile's max exceeds it
             // by more than kRescaleSlack; otherwise every p = 2^(x - m) <= 2^slack
@@ -759,6 +763,13 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             const float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
                               ((part[4] + part[5]) + (part[6] + part[7]));
             l = l * alpha + sum;
+            if constexpr (!F8) {
+                // The tile's largest p exactly as the loop above computed it (the
+                // same FMA and ex2), and what rounding it to bf16 changed (exact:
+                // both lie within a factor of two). 0 for a fully masked row.
+                const float p_max = ex2(__fmaf_rn(s_max, sl2, neg));
+                lc = lc * alpha + (round_bf16(p_max) - p_max);
+            }
             m = m_new;
         }
 
@@ -772,18 +783,18 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             // o_scale * O_t / l staged in the tile's own buffer and written with
             // TMA. Split mode: the partial state, O scaled by o_scale, per row.
             if (ok && !p.split_mode && n > 0)
-                store_rows_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m - kP8Shift, m_true, l, tO,
+                store_rows_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m - kP8Shift, m_true, l, l, tO,
                                   sbase + L::OST_OFF + t * L::OST_TILE_BYTES, p.o_scale);
             else if (ok && (!DUAL || split_t < p.num_splits))
-                write_row<D>(p, w.rm, w.bh, split_t, q_row, n, m - kP8Shift, m_true, l, tO, p.o_scale);
+                write_row<D>(p, w.rm, w.bh, split_t, q_row, n, m - kP8Shift, m_true, l, l, tO, p.o_scale);
         } else {
             if (ok && !p.split_mode && !p.varlen && n > 0) {
                 // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA
                 // stores per warp.
-                store_rows_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
+                store_rows_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, l + lc, tO,
                                   sbase + L::Q_OFF + t * L::Q_TILE_BYTES);
             } else if (ok && (!DUAL || split_t < p.num_splits)) {
-                write_row<D>(p, w.rm, w.bh, split_t, q_row, n, m, m_true, l, tO);
+                write_row<D>(p, w.rm, w.bh, split_t, q_row, n, m, m_true, l, l + lc, tO);
             }
         }
     }

@@ -357,6 +357,9 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
         float m = -INFINITY;       // exponent reference (base-2 units of scale*log2e*s)
         float m_true = -INFINITY;  // true running row max, same units
         float l = 0.f;             // running sum relative to m
+        // The rounding error of each key tile's largest p when P is rounded to
+        // bf16, relative to m like l. l + lc is the denominator of O (see RowOut).
+        float lc = 0.f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             const int b = j & 1;
@@ -400,7 +403,8 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
                 a2 = max3f(a2, s[c + 4], s[c + 5]);
                 a3 = max3f(a3, s[c + 6], s[c + 7]);
             }
-            const float m_tile = max3f(a0, a1, fmaxf(a2, a3)) * sl2;  // base-2 units
+            const float s_max = max3f(a0, a1, fmaxf(a2, a3));
+            const float m_tile = s_max * sl2;  // base-2 units
             m_true = fmaxf(m_true, m_tile);
             // The exponent reference m only moves when this tile's max exceeds it
             // by more than kRescaleSlack; otherwise every p = 2^(x - m) <= 2^slack
@@ -488,6 +492,11 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             const float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
                               ((part[4] + part[5]) + (part[6] + part[7]));
             l = l * alpha + sum;
+            // The tile's largest p exactly as computed above (same FMA and ex2)
+            // and what rounding it to bf16 changed (exact: both lie within a
+            // factor of two). 0 for a fully masked row.
+            const float p_max = ex2(__fmaf_rn(s_max, sl2, neg));
+            lc = lc * alpha + (round_bf16(p_max) - p_max);
             m = m_new;
         }
 
@@ -498,10 +507,10 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
         }
         if (ok && !p.split_mode && !p.varlen && n > 0) {
             // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA.
-            store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, tO,
+            store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, l + lc, tO,
                               sbase + L::Q_OFF + t * L::Q_TILE_BYTES, bar(L::BAR_OSTAGED + t), abort_flag);
         } else if (ok) {
-            write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m, m_true, l, tO);
+            write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m, m_true, l, l + lc, tO);
         }
     }
 

@@ -323,6 +323,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// x rounded to bf16 (nearest even), as the fp32 value that bf16 stands for
+// (bf16 is the upper half of an fp32).
+__device__ __forceinline__ float round_bf16(float x) {
+    return __uint_as_float(pack_bf16x2(x, 0.f) << 16);
+}
+
 // Four floats as e4m3 (round to nearest even, saturating to +-448), a0 in the
 // lowest byte. The cvt puts its first source in the upper byte of each pair.
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {

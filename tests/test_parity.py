@@ -108,6 +108,37 @@ def test_outlier_keys_and_other_scales(d):
             check(o, lse, o_ref, lse_ref, f"d={d} scale={scale} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_dominant_key_weight_matches_rounded_p(d, splits):
+    """Rows dominated by one key whose p is not a power of two relative to the
+    exponent reference: key 0 sets the reference (score 20), key 200 in a later
+    key tile scores 25, less than 8 base-2 units above it, so its p = 2^7.2 is
+    rounded to bf16 for the PV product (relative error up to 2^-8). O must
+    still equal that key's V (values in [4, 8)) up to the bf16 output rounding:
+    the kernel divides O by the weights the product used. With O divided by
+    the unrounded sum, an element could be off by up to 2^-8 of its value
+    before the output rounding, and land a whole bf16 step away."""
+    Nq, Nk = 128, 400
+    g = torch.Generator().manual_seed(600 + d)
+    q = torch.zeros(1, 1, Nq, d)
+    q[..., 0] = 1.0
+    k = torch.randn(1, 1, Nk, d, generator=g) * 0.5
+    k[0, 0, 0, 0] = 20.0
+    k[0, 0, 200, 0] = 25.0
+    v = torch.randn(1, 1, Nk, d, generator=g)
+    mag = 4.0 + 4.0 * torch.rand(d, generator=g)
+    v[0, 0, 200] = torch.where(torch.rand(d, generator=g) < 0.5, -mag, mag)
+    q, k, v = (t.to(torch.bfloat16) for t in (q, k, v))
+    o, lse = run_gpu(q, k, v, False, 1.0, num_splits=splits)
+    o_ref, lse_ref = oracle.attention_f64(to_f64(q), to_f64(k), to_f64(v), 1.0, False)
+    got = o.float().cpu().numpy().astype(np.float64)
+    half_ulp = np.exp2(np.floor(np.log2(np.abs(o_ref))) - 8)  # bf16: 8 significand bits
+    assert np.all(np.abs(got - o_ref) <= half_ulp + 1e-3)
+    assert np.abs(lse.cpu().numpy() - lse_ref).max() <= LSE_ABS
+    check(o, lse, o_ref, lse_ref, f"dominant key d={d}")
+
+
 def test_worked_example_on_gpu():
     """The FA-2 page's four-key example as a real kernel call: d=64, scale 1,
     q = e0, K rows = score_j * e0, V rows = value_j * e0 (all exact in bf16)."""
