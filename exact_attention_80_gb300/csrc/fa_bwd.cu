@@ -20,20 +20,26 @@
 //     summed across CTAs (across key tiles).
 //   * fa_bwd_dq_kernel: dQ = scale * accumulator, to bf16.
 //
-// fa_bwd_kernel roles: warp 0 loads K and V once and (Q_i, dO_i) per query
-// tile into two buffers (TMA); warp 1 issues tcgen05 MMAs; warps 4-11 are the
-// compute group, two warps per TMEM lane quarter, each owning two 32-query
-// chunks (thread = TMEM lane = key row). Per query tile i:
-//   S^T = K Q_i^T and dP^T = V dO_i^T (lanes = keys, columns = queries);
+// fa_bwd_kernel steps over the queries 64 at a time. Roles: warp 0 loads K
+// and V once and, per step, Q, dO and the step's -LSE log2e and -D into a ring
+// of three slots (TMA); warp 1 issues tcgen05 MMAs; warps 4-11 are the compute
+// group, two warps per TMEM lane quarter, one per 32-query chunk of a step
+// (thread = TMEM lane = key row); warps 12-15 read dQ^T out (lane = head dim).
+// TMEM holds two step buffers of 128 columns beside dV and dK. Per step h
+// (buffer h & 1):
+//   S^T = K Q_h^T and dP^T = V dO_h^T (lanes = keys, 64 query columns each);
 //   the compute group forms P^T = exp2(S^T scale log2e - LSE log2e) and
 //   dS^T = P^T (dP^T - D), writes both as bf16 into TMEM over the first half
 //   of each chunk's own columns, and dS^T into shared memory (128-byte
 //   swizzle);
-//   dV += P^T dO_i and dK += dS^T Q_i (A from TMEM, B = dO_i / Q_i MN-major);
-//   dQ_i^T = K^T dS^T (A = K MN-major, B = dS^T from shared memory) into the
-//   dP^T columns, so S^T of the next tile can be computed while the compute
-//   group (lane = head dim) adds dQ_i^T to the fp32 accumulator, 32
-//   consecutive floats per warp instruction.
+//   dV += P^T dO_h and dK += dS^T Q_h (A from TMEM, B = dO_h / Q_h MN-major);
+//   dQ_h^T = K^T dS^T (A = K MN-major, B = dS^T from shared memory) over the
+//   buffer's S^T columns; the readout group takes it out of TMEM, releases the
+//   buffer and adds it to the fp32 accumulator, 32 consecutive floats per warp
+//   instruction.
+// The issuer runs the MMAs in pairs of steps, S^T and dP^T of two steps then
+// dV, dK and dQ^T of the same two, so that each of the three groups (tensor
+// core, compute, readout) always has the other step's work to overlap.
 // Every mbarrier wait is bounded, as in the forward kernels.
 #include <cuda_bf16.h>
 
@@ -47,7 +53,7 @@ namespace fa {
 
 // Kernel parameters, filled by fa_bwd below.
 struct BwdParams {
-    CUtensorMap tm_q;   // bf16 [B*H][Nq][d], box {64, 128, 1}
+    CUtensorMap tm_q;   // bf16 [B*H][Nq][d], box {64, 64, 1}
     CUtensorMap tm_k;   // bf16 [B*H][Nk][d], box {64, 128, 1}
     CUtensorMap tm_v;   // same as tm_k
     CUtensorMap tm_do;  // same as tm_q (dO)
@@ -69,37 +75,56 @@ struct BwdParams {
 namespace {
 
 constexpr int kBwdD = 128;
-constexpr int kBwdTile = 128;   // keys per CTA, queries per step
-constexpr int kBwdGroups = 2;   // compute warps per TMEM lane quarter
-constexpr int kBwdChunks = (kBwdTile / 32) / kBwdGroups;  // 32-query chunks per compute warp
+constexpr int kBwdKeys = 128;   // keys per CTA (TMEM lanes of S^T, dP^T, dV, dK)
+constexpr int kBwdHalf = 64;    // queries per step
+constexpr int kBwdStages = 3;   // Q/dO (+ -LSE log2e, -D) ring slots
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct LayoutBwd {
-    static constexpr int COMPUTE_WARPS = 4 * kBwdGroups;
-    static constexpr int THREADS = 128 + 32 * COMPUTE_WARPS;
-    static constexpr uint32_t TILE_BYTES = kBwdTile * kBwdD * 2;  // 32 KB, two 64-column chunks
-    static constexpr uint32_t CHUNK_BYTES = kBwdTile * 128;       // one 64-column chunk
+    // warp 0 producer, warp 1 issuer, warps 2-3 idle, warps 4-11 compute (two
+    // per TMEM lane quarter, one per 32-query chunk of a step), warps 12-15
+    // dQ readout (one per lane quarter).
+    static constexpr int COMPUTE_WARPS = 8;
+    static constexpr int READOUT_WARPS = 4;
+    static constexpr int THREADS = 128 + 32 * (COMPUTE_WARPS + READOUT_WARPS);
+    static constexpr uint32_t KV_CHUNK = kBwdKeys * 128;            // 16 KB: 64 columns of K or V
+    static constexpr uint32_t KV_BYTES = 2 * KV_CHUNK;              // 32 KB
+    static constexpr uint32_t QH_CHUNK = kBwdHalf * 128;            // 8 KB: 64 columns of a step's Q or dO
+    static constexpr uint32_t QH_BYTES = 2 * QH_CHUNK;              // 16 KB
+    static constexpr uint32_t ROWS_BYTES = kBwdHalf * 4;            // 256 B of -LSE log2e (or -D)
+    static constexpr uint32_t STAGE_BYTES = 2 * QH_BYTES;           // Q and dO of a step
+    static constexpr uint32_t DS_BYTES = kBwdKeys * kBwdHalf * 2;   // 16 KB: dS^T bf16 [keys][64 queries]
+    // Swizzled tiles start on 1024-byte boundaries (the MMA descriptors'
+    // base offset is 0); the per-row arrays need 16 bytes.
     static constexpr uint32_t K_OFF = 0;
-    static constexpr uint32_t V_OFF = K_OFF + TILE_BYTES;
-    static constexpr uint32_t Q_OFF = V_OFF + TILE_BYTES;        // [2]
-    static constexpr uint32_t DO_OFF = Q_OFF + 2 * TILE_BYTES;   // [2]
-    static constexpr uint32_t DS_OFF = DO_OFF + 2 * TILE_BYTES;  // dS^T, bf16 [keys][queries]
-    static constexpr uint32_t BAR_OFF = DS_OFF + TILE_BYTES;
+    static constexpr uint32_t V_OFF = K_OFF + KV_BYTES;
+    static constexpr uint32_t STAGE_OFF = V_OFF + KV_BYTES;          // [stage]: Q, dO
+    static constexpr uint32_t Q_IN = 0, DO_IN = QH_BYTES;
+    static constexpr uint32_t DS_OFF = STAGE_OFF + kBwdStages * STAGE_BYTES;  // [buffer]
+    static constexpr uint32_t ROWS_OFF = DS_OFF + 2 * DS_BYTES;     // [stage]: -LSE log2e, -D
+    static constexpr uint32_t NL_IN = 0, ND_IN = ROWS_BYTES;
+    static constexpr uint32_t BAR_OFF = ROWS_OFF + kBwdStages * 2 * ROWS_BYTES;
+    static_assert(STAGE_OFF % 1024 == 0 && STAGE_BYTES % 1024 == 0 && QH_CHUNK % 1024 == 0 &&
+                      DS_OFF % 1024 == 0 && DS_BYTES % 1024 == 0, "swizzle atoms must be 1024-aligned");
     static constexpr int BAR_KV = 0;
-    static constexpr int BAR_QFULL = 1;    // [2]
-    static constexpr int BAR_QEMPTY = 3;   // [2]
-    static constexpr int BAR_SFULL = 5;    // S^T and dP^T done
-    static constexpr int BAR_PREADY = 6;   // P^T, dS^T written (one arrival per compute warp)
-    static constexpr int BAR_DQFULL = 7;   // dQ^T done (and every earlier MMA)
-    static constexpr int BAR_DQREAD = 8;   // dQ^T read out (one arrival per compute warp)
-    static constexpr int BAR_DRAIN = 9;
-    static constexpr int NUM_BARS = 10;
+    static constexpr int BAR_QFULL = 1;                    // [stage]
+    static constexpr int BAR_QEMPTY = BAR_QFULL + kBwdStages;   // [stage]
+    static constexpr int BAR_SFULL = BAR_QEMPTY + kBwdStages;   // [buffer] S^T, dP^T done
+    static constexpr int BAR_PREADY = BAR_SFULL + 2;    // [buffer] P^T, dS^T written (one arrival per compute warp)
+    static constexpr int BAR_DQFULL = BAR_PREADY + 2;   // [buffer] dQ^T done (and every earlier MMA)
+    static constexpr int BAR_DQREAD = BAR_DQFULL + 2;   // [buffer] dQ^T read (one arrival per readout warp)
+    static constexpr int BAR_DRAIN = BAR_DQREAD + 2;
+    static constexpr int NUM_BARS = BAR_DRAIN + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr uint32_t BYTES = MISC_OFF + 16;
     static constexpr size_t ALLOC_BYTES = BYTES + 1024;
-    // TMEM columns: S^T (then P^T), dP^T (then dS^T, then dQ^T), dV, dK.
-    static constexpr uint32_t ST_COL = 0, DP_COL = 128, DV_COL = 256, DK_COL = 384;
+    // TMEM columns. Buffer b (b = step & 1) at 128 b: S^T in its first 64
+    // columns (then P^T packed over their first halves, then dQ^T), dP^T in
+    // the next 64 (then dS^T packed over their first halves). dV and dK last.
+    __host__ __device__ static constexpr uint32_t BUF_COL(int b) { return 128u * static_cast<uint32_t>(b); }
+    static constexpr uint32_t DP_IN = 64, DV_COL = 256, DK_COL = 384;
     static_assert(ALLOC_BYTES <= 232448, "shared memory over the 227 KB per-CTA limit");
+    static_assert(THREADS * 128 <= 65536, "registers: 128 per thread at most");
 };
 
 __device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, const BwdParams& p,
@@ -118,38 +143,38 @@ __device__ __forceinline__ bool bwd_wait(uint32_t bar, uint32_t parity, const Bw
     }
 }
 
-// Query tiles a key tile sees: all of them, or (causal) those with a row at or
-// after the tile's first key minus the alignment offset.
-__device__ __forceinline__ void bwd_steps(const BwdParams& p, int kt, int& i0, int& n) {
-    const int q_tiles = (p.Nq + kBwdTile - 1) / kBwdTile;
-    i0 = 0;
+// The 64-query steps a key tile sees: all of them, or (causal) those with a
+// row at or after the tile's first key minus the alignment offset.
+__device__ __forceinline__ void bwd_steps(const BwdParams& p, int kt, int& h0, int& n) {
+    const int steps = (p.Nq + kBwdHalf - 1) / kBwdHalf;
+    h0 = 0;
     if (p.causal) {
         const int off = p.causal_br ? p.Nk - p.Nq : 0;
-        const int first_row = kt * kBwdTile - off;  // key k is visible to rows >= k - off
-        i0 = first_row <= 0 ? 0 : first_row / kBwdTile;
+        const int first_row = kt * kBwdKeys - off;  // key k is visible to rows >= k - off
+        h0 = first_row <= 0 ? 0 : first_row / kBwdHalf;
     }
-    n = max(0, q_tiles - i0);
+    n = max(0, steps - h0);
 }
 
 // P^T and dS^T of one 32-query chunk for this thread's key row: s and dp are
-// the chunk's S^T and dP^T columns, nl and nd point at the chunk's -LSE log2e
-// and -D (the same addresses for every lane: one broadcast load per four
-// queries). MASK: `lim` is the first visible chunk column (causal) and
-// `key_ok` whether the key exists; without MASK every entry is visible.
+// the chunk's S^T and dP^T columns, nl and nd the chunk's -LSE log2e and -D in
+// shared memory (the same addresses for every lane: broadcast loads). MASK:
+// `lim` is the first visible chunk column (causal) and `key_ok` whether the
+// key exists; without MASK every entry is visible.
 template <bool MASK>
-__device__ __forceinline__ void bwd_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32],
-                                          const float* __restrict__ nl, const float* __restrict__ nd,
-                                          float sl2, int lim, bool key_ok, uint32_t (&pk)[16],
+__device__ __forceinline__ void bwd_chunk(const uint32_t (&s)[32], const uint32_t (&dp)[32], uint32_t nl,
+                                          uint32_t nd, float sl2, int lim, bool key_ok, uint32_t (&pk)[16],
                                           uint32_t (&dk)[16]) {
     const uint64_t sl2x2 = f2pack(sl2, sl2);
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
-        const float4 l4 = __ldg(reinterpret_cast<const float4*>(nl) + u);
-        const float4 d4 = __ldg(reinterpret_cast<const float4*>(nd) + u);
+        float l4[4], d4[4];
+        ld_shared_v4f(nl + 16 * u, l4);
+        ld_shared_v4f(nd + 16 * u, d4);
         const uint64_t x01 = ffma2(f2pack(__uint_as_float(s[4 * u]), __uint_as_float(s[4 * u + 1])), sl2x2,
-                                   f2pack(l4.x, l4.y));
+                                   f2pack(l4[0], l4[1]));
         const uint64_t x23 = ffma2(f2pack(__uint_as_float(s[4 * u + 2]), __uint_as_float(s[4 * u + 3])), sl2x2,
-                                   f2pack(l4.z, l4.w));
+                                   f2pack(l4[2], l4[3]));
         float x[4];
         f2unpack(x01, x[0], x[1]);
         f2unpack(x23, x[2], x[3]);
@@ -162,9 +187,9 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t (&s)[32], const uint32_
             pv[h] = MASK ? ((key_ok && 4 * u + h >= lim) ? ex : 0.f) : ex;
         }
         const uint64_t g01 = fadd2(f2pack(__uint_as_float(dp[4 * u]), __uint_as_float(dp[4 * u + 1])),
-                                   f2pack(d4.x, d4.y));
+                                   f2pack(d4[0], d4[1]));
         const uint64_t g23 = fadd2(f2pack(__uint_as_float(dp[4 * u + 2]), __uint_as_float(dp[4 * u + 3])),
-                                   f2pack(d4.z, d4.w));
+                                   f2pack(d4[2], d4[3]));
         float ds[4];
         f2unpack(fmul2(f2pack(pv[0], pv[1]), g01), ds[0], ds[1]);
         f2unpack(fmul2(f2pack(pv[2], pv[3]), g23), ds[2], ds[3]);
@@ -175,6 +200,13 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t (&s)[32], const uint32_
     }
 }
 
+// One CTA per (head, 128-key tile), stepping over the queries 64 at a time.
+// Step h uses TMEM buffer h & 1 and ring slot h % 3. The issuer runs the MMAs
+// in pairs of steps: S^T and dP^T of steps 2k+2 and 2k+3 (each needs its
+// buffer's dQ^T of two steps back read out), then dV, dK and dQ^T of steps
+// 2k+2 and 2k+3 (each needs its P^T and dS^T). While the tensor core runs one
+// step's MMAs, the compute group forms P^T and dS^T of the other and the
+// readout group adds the previous dQ^T to the accumulator.
 __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
     using L = LayoutBwd;
     extern __shared__ uint8_t smem_raw[];
@@ -188,20 +220,23 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
 
     const int bh = blockIdx.x / p.k_tiles;
     const int kt = blockIdx.x % p.k_tiles;
-    const int k0 = kt * kBwdTile;
-    int i0, n;
-    bwd_steps(p, kt, i0, n);
+    const int k0 = kt * kBwdKeys;
+    int h0, n;
+    bwd_steps(p, kt, h0, n);
+    const size_t row0 = static_cast<size_t>(bh) * p.Nq_pad;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::BAR_KV), 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(bar(L::BAR_QFULL + b), 1);
-            mbar_init(bar(L::BAR_QEMPTY + b), 1);
+        for (int st = 0; st < kBwdStages; ++st) {
+            mbar_init(bar(L::BAR_QFULL + st), 1);
+            mbar_init(bar(L::BAR_QEMPTY + st), 1);
         }
-        mbar_init(bar(L::BAR_SFULL), 1);
-        mbar_init(bar(L::BAR_PREADY), L::COMPUTE_WARPS);
-        mbar_init(bar(L::BAR_DQFULL), 1);
-        mbar_init(bar(L::BAR_DQREAD), L::COMPUTE_WARPS);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar(L::BAR_SFULL + b), 1);
+            mbar_init(bar(L::BAR_PREADY + b), L::COMPUTE_WARPS);
+            mbar_init(bar(L::BAR_DQFULL + b), 1);
+            mbar_init(bar(L::BAR_DQREAD + b), L::READOUT_WARPS);
+        }
         mbar_init(bar(L::BAR_DRAIN), 1);
         *abort_flag = 0u;
         fence_mbar_init();
@@ -225,42 +260,45 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
         // ------------------------------------------------------------ producer
         const bool leader = elect_one();
         if (leader) {
-            mbar_arrive_expect_tx(bar(L::BAR_KV), 2 * L::TILE_BYTES);
+            mbar_arrive_expect_tx(bar(L::BAR_KV), 2 * L::KV_BYTES);
             for (int c = 0; c < 2; ++c) {
-                tma_load_3d(sbase + L::K_OFF + c * L::CHUNK_BYTES, &p.tm_k, bar(L::BAR_KV), 64 * c, k0, bh);
-                tma_load_3d(sbase + L::V_OFF + c * L::CHUNK_BYTES, &p.tm_v, bar(L::BAR_KV), 64 * c, k0, bh);
+                tma_load_3d(sbase + L::K_OFF + c * L::KV_CHUNK, &p.tm_k, bar(L::BAR_KV), 64 * c, k0, bh);
+                tma_load_3d(sbase + L::V_OFF + c * L::KV_CHUNK, &p.tm_v, bar(L::BAR_KV), 64 * c, k0, bh);
             }
         }
         bool ok = true;
         int issued = 0;
-        for (int i = 0; i < n && ok; ++i) {
-            const int b = i & 1;
-            if (i >= 2)
-                ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_QEMPTY + b), ((i >> 1) - 1) & 1, p,
+        for (int h = 0; h < n && ok; ++h) {
+            const int st = h % kBwdStages;
+            if (h >= kBwdStages)
+                ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_QEMPTY + st), ((h / kBwdStages) - 1) & 1, p,
                                                       abort_flag, kStatusWaitKvEmpty));
             if (!ok) break;
             if (leader) {
-                const int q0 = (i0 + i) * kBwdTile;
-                mbar_arrive_expect_tx(bar(L::BAR_QFULL + b), 2 * L::TILE_BYTES);
+                const int q0 = (h0 + h) * kBwdHalf;
+                const uint32_t sb = sbase + L::STAGE_OFF + st * L::STAGE_BYTES;
+                const uint32_t rb = sbase + L::ROWS_OFF + st * 2 * L::ROWS_BYTES;
+                mbar_arrive_expect_tx(bar(L::BAR_QFULL + st), L::STAGE_BYTES + 2 * L::ROWS_BYTES);
                 for (int c = 0; c < 2; ++c) {
-                    tma_load_3d(sbase + L::Q_OFF + b * L::TILE_BYTES + c * L::CHUNK_BYTES, &p.tm_q,
-                                bar(L::BAR_QFULL + b), 64 * c, q0, bh);
-                    tma_load_3d(sbase + L::DO_OFF + b * L::TILE_BYTES + c * L::CHUNK_BYTES, &p.tm_do,
-                                bar(L::BAR_QFULL + b), 64 * c, q0, bh);
+                    tma_load_3d(sb + L::Q_IN + c * L::QH_CHUNK, &p.tm_q, bar(L::BAR_QFULL + st), 64 * c, q0, bh);
+                    tma_load_3d(sb + L::DO_IN + c * L::QH_CHUNK, &p.tm_do, bar(L::BAR_QFULL + st), 64 * c, q0, bh);
                 }
+                bulk_load(rb + L::NL_IN, p.nlse2 + row0 + q0, L::ROWS_BYTES, bar(L::BAR_QFULL + st));
+                bulk_load(rb + L::ND_IN, p.ndd + row0 + q0, L::ROWS_BYTES, bar(L::BAR_QFULL + st));
             }
-            issued = i + 1;
+            issued = h + 1;
         }
         if (ok) {
-            // The issuer's last buffer releases: no commit arrival may still be in
+            // The issuer's last slot releases: no commit arrival may still be in
             // flight when the CTA exits.
-            for (int i = max(0, n - 2); i < n && ok; ++i)
-                ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_QEMPTY + (i & 1)), (i >> 1) & 1, p, abort_flag,
-                                                      kStatusWaitKvEmpty));
+            for (int h = max(0, n - kBwdStages); h < n && ok; ++h)
+                ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_QEMPTY + h % kBwdStages), (h / kBwdStages) & 1, p,
+                                                      abort_flag, kStatusWaitKvEmpty));
         } else {
             bwd_wait(bar(L::BAR_KV), 0, p, abort_flag, kStatusWaitDrain, false);
-            for (int i = max(0, issued - 2); i < issued; ++i)
-                bwd_wait(bar(L::BAR_QFULL + (i & 1)), (i >> 1) & 1, p, abort_flag, kStatusWaitDrain, false);
+            for (int h = max(0, issued - kBwdStages); h < issued; ++h)
+                bwd_wait(bar(L::BAR_QFULL + h % kBwdStages), (h / kBwdStages) & 1, p, abort_flag,
+                         kStatusWaitDrain, false);
         }
     } else if (warp == 1 && n > 0) {
         // ------------------------------------------------------------ MMA issuer
@@ -268,162 +306,173 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
         auto wait_all = [&](uint32_t b, uint32_t parity, unsigned what) {
             return __all_sync(0xffffffffu, bwd_wait(b, parity, p, abort_flag, what));
         };
-        constexpr uint32_t IDESC_T = make_idesc_bf16(128, 128, false, false);  // S^T, dP^T
-        constexpr uint32_t IDESC_ACC = make_idesc_bf16(128, 128, false, true);  // dV, dK
-        constexpr uint32_t IDESC_DQ = make_idesc_bf16(128, 128, true, true);    // dQ^T
+        constexpr uint32_t IDESC_S = make_idesc_bf16(128, kBwdHalf, false, false);  // S^T, dP^T
+        constexpr uint32_t IDESC_ACC = make_idesc_bf16(128, kBwdD, false, true);    // dV, dK
+        constexpr uint32_t IDESC_DQ = make_idesc_bf16(128, kBwdHalf, true, true);   // dQ^T
+        // K-major operands (8-row groups 1024 bytes apart); MN-major ones with
+        // their 64-element chunks KV_CHUNK (K as A of dQ^T) or QH_CHUNK (Q, dO
+        // as B of dK, dV) apart; dS^T is one 64-query chunk.
         const uint64_t kmaj0 = make_sdesc_sw128(sbase, 16, 1024);
-        const uint64_t mn0 = make_sdesc_sw128(sbase, L::CHUNK_BYTES, 1024);
+        const uint64_t kmn0 = make_sdesc_sw128(sbase, L::KV_CHUNK, 1024);
+        const uint64_t qmn0 = make_sdesc_sw128(sbase, L::QH_CHUNK, 1024);
         const uint32_t kmaj_lo = static_cast<uint32_t>(kmaj0), kmaj_hi = static_cast<uint32_t>(kmaj0 >> 32);
-        const uint32_t mn_lo = static_cast<uint32_t>(mn0), mn_hi = static_cast<uint32_t>(mn0 >> 32);
+        const uint32_t kmn_lo = static_cast<uint32_t>(kmn0), kmn_hi = static_cast<uint32_t>(kmn0 >> 32);
+        const uint32_t qmn_lo = static_cast<uint32_t>(qmn0), qmn_hi = static_cast<uint32_t>(qmn0 >> 32);
         auto desc = [](uint32_t lo, uint32_t hi, uint32_t off) -> uint64_t {
             return (static_cast<uint64_t>(hi) << 32) | (lo + (off >> 4));
         };
-        // D(lanes = rows of a) = a b^T over the head dim, both K-major tiles.
-        auto mma_t = [&](uint32_t d_col, uint32_t a_off, uint32_t b_off) {
+        // S^T_h = K Q_h^T and dP^T_h = V dO_h^T into buffer h & 1 (lanes = keys,
+        // 64 query columns each), reading ring slot h % 3.
+        auto issue_sdp = [&](int h) -> bool {
+            const int st = h % kBwdStages;
+            if (!wait_all(bar(L::BAR_QFULL + st), (h / kBwdStages) & 1, kStatusWaitQ)) return false;
+            tc_fence_after();
+            const uint32_t sb = L::STAGE_OFF + st * L::STAGE_BYTES;
+            const uint32_t col = L::BUF_COL(h & 1);
 #pragma unroll
             for (int kk = 0; kk < kBwdD / 16; ++kk) {
-                const uint32_t in_row = (kk & 3) * 32 + (kk >> 2) * L::CHUNK_BYTES;
-                const uint64_t a = desc(kmaj_lo, kmaj_hi, a_off + in_row);
-                const uint64_t b = desc(kmaj_lo, kmaj_hi, b_off + in_row);
-                if (leader) umma_ss(tmem + d_col, a, b, IDESC_T, kk > 0 ? 1u : 0u);
-            }
-        };
-        bool ok = wait_all(bar(L::BAR_KV), 0, kStatusWaitKvFull);
-        for (int i = 0; i < n && ok; ++i) {
-            const int b = i & 1;
-            ok = wait_all(bar(L::BAR_QFULL + b), (i >> 1) & 1, kStatusWaitQ);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t qb = L::Q_OFF + b * L::TILE_BYTES;
-            const uint32_t dob = L::DO_OFF + b * L::TILE_BYTES;
-            // S^T = K Q^T. The S^T columns last held P^T of the previous tile,
-            // which its dV MMAs (issued earlier, run in order) have consumed.
-            mma_t(L::ST_COL, L::K_OFF, qb);
-            // dQ^T of the previous tile sits in the dP^T columns until read out.
-            if (i > 0) {
-                ok = wait_all(bar(L::BAR_DQREAD), (i - 1) & 1, kStatusWaitO);
-                if (!ok) break;
-                tc_fence_after();
-            }
-            mma_t(L::DP_COL, L::V_OFF, dob);  // dP^T = V dO^T
-            if (leader) umma_commit(bar(L::BAR_SFULL));
-            ok = wait_all(bar(L::BAR_PREADY), i & 1, kStatusWaitP);
-            if (!ok) break;
-            tc_fence_after();
-            // dV += P^T dO and dK += dS^T Q: A from TMEM (16 queries = 8 packed
-            // columns, each 32-query chunk packed into the first 16 columns of its
-            // own 32), B MN-major (16 query rows = 2048 bytes).
-#pragma unroll
-            for (int kk = 0; kk < kBwdTile / 16; ++kk) {
-                const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                const uint32_t pcol = 32 * (kk >> 1) + 8 * (kk & 1);
-                const uint64_t bdo = desc(mn_lo, mn_hi, dob + kk * 2048);
-                const uint64_t bq = desc(mn_lo, mn_hi, qb + kk * 2048);
+                const uint32_t in_a = (kk & 3) * 32 + (kk >> 2) * L::KV_CHUNK;
+                const uint32_t in_b = (kk & 3) * 32 + (kk >> 2) * L::QH_CHUNK;
+                const uint64_t ak = desc(kmaj_lo, kmaj_hi, L::K_OFF + in_a);
+                const uint64_t av = desc(kmaj_lo, kmaj_hi, L::V_OFF + in_a);
+                const uint64_t bq = desc(kmaj_lo, kmaj_hi, sb + L::Q_IN + in_b);
+                const uint64_t bdo = desc(kmaj_lo, kmaj_hi, sb + L::DO_IN + in_b);
                 if (leader) {
-                    umma_ts(tmem + L::DV_COL, tmem + L::ST_COL + pcol, bdo, IDESC_ACC, acc);
-                    umma_ts(tmem + L::DK_COL, tmem + L::DP_COL + pcol, bq, IDESC_ACC, acc);
+                    umma_ss(tmem + col, ak, bq, IDESC_S, kk > 0 ? 1u : 0u);
+                    umma_ss(tmem + col + L::DP_IN, av, bdo, IDESC_S, kk > 0 ? 1u : 0u);
                 }
             }
-            if (leader) umma_commit(bar(L::BAR_QEMPTY + b));
-            // dQ^T = K^T dS^T into the dP^T columns (after the dK MMAs that read
-            // dS^T there, in issue order): A = K MN-major (M = head dim), B = dS^T
-            // MN-major (N = queries), 16 keys = 2048 bytes per step.
+            if (leader) umma_commit(bar(L::BAR_SFULL + (h & 1)));
+            return true;
+        };
+        // dV += P^T_h dO_h, dK += dS^T_h Q_h (A from TMEM: 16 queries = 8 packed
+        // columns, each 32-query chunk packed into the first 16 of its own 32;
+        // B MN-major, 16 query rows = 2048 bytes), then dQ^T_h = K^T dS^T_h
+        // over buffer h & 1's S^T columns (after the dV MMAs that read P^T
+        // there, in issue order): A = K MN-major (M = head dim), B = dS^T
+        // MN-major (N = queries), 16 keys = 2048 bytes per MMA.
+        auto issue_vkq = [&](int h, bool first) -> bool {
+            const int b = h & 1;
+            if (!wait_all(bar(L::BAR_PREADY + b), (h >> 1) & 1, kStatusWaitP)) return false;
+            tc_fence_after();
+            const int st = h % kBwdStages;
+            const uint32_t sb = L::STAGE_OFF + st * L::STAGE_BYTES;
+            const uint32_t col = L::BUF_COL(b);
 #pragma unroll
-            for (int kk = 0; kk < kBwdTile / 16; ++kk) {
-                const uint64_t a = desc(mn_lo, mn_hi, L::K_OFF + kk * 2048);
-                const uint64_t bds = desc(mn_lo, mn_hi, L::DS_OFF + kk * 2048);
-                if (leader) umma_ss(tmem + L::DP_COL, a, bds, IDESC_DQ, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kBwdHalf / 16; ++kk) {
+                const uint32_t acc = (!first || kk > 0) ? 1u : 0u;
+                const uint32_t pcol = col + 32 * (kk >> 1) + 8 * (kk & 1);
+                const uint64_t bdo = desc(qmn_lo, qmn_hi, sb + L::DO_IN + kk * 2048);
+                const uint64_t bq = desc(qmn_lo, qmn_hi, sb + L::Q_IN + kk * 2048);
+                if (leader) {
+                    umma_ts(tmem + L::DV_COL, tmem + pcol, bdo, IDESC_ACC, acc);
+                    umma_ts(tmem + L::DK_COL, tmem + pcol + L::DP_IN, bq, IDESC_ACC, acc);
+                }
             }
-            if (leader) umma_commit(bar(L::BAR_DQFULL));
+            if (leader) umma_commit(bar(L::BAR_QEMPTY + st));
+            const uint32_t dsb = L::DS_OFF + b * L::DS_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < kBwdKeys / 16; ++kk) {
+                const uint64_t a = desc(kmn_lo, kmn_hi, L::K_OFF + kk * 2048);
+                const uint64_t bds = desc(qmn_lo, qmn_hi, dsb + kk * 2048);
+                if (leader) umma_ss(tmem + col, a, bds, IDESC_DQ, kk > 0 ? 1u : 0u);
+            }
+            if (leader) umma_commit(bar(L::BAR_DQFULL + b));
+            return true;
+        };
+        bool ok = wait_all(bar(L::BAR_KV), 0, kStatusWaitKvFull);
+        if (ok) ok = issue_sdp(0);
+        if (ok && n > 1) ok = issue_sdp(1);
+        for (int a = 0; a < n && ok; a += 2) {
+            ok = issue_vkq(a, a == 0);
+            if (ok && a + 1 < n) ok = issue_vkq(a + 1, false);
+            // The next pair's S^T and dP^T, each once the readout group has taken
+            // the dQ^T of two steps back out of its buffer.
+            for (int h = a + 2; h < a + 4 && h < n && ok; ++h) {
+                ok = wait_all(bar(L::BAR_DQREAD + (h & 1)), ((h - 2) >> 1) & 1, kStatusWaitO);
+                if (ok) {
+                    tc_fence_after();
+                    ok = issue_sdp(h);
+                }
+            }
         }
         if (leader) umma_commit(bar(L::BAR_DRAIN));
         bwd_wait(bar(L::BAR_DRAIN), 0, p, abort_flag, kStatusWaitDrain, false);
-    } else if (warp >= 4) {
+    } else if (warp >= 4 && warp < 4 + L::COMPUTE_WARPS) {
         // ------------------------------------------------------------ compute group
         const int quarter = warp & 3;
-        const int grp = (warp - 4) >> 2;
-        const int r = quarter * 32 + lane;   // TMEM lane: key row, or head dim for dQ^T
+        const int g = (warp - 4) >> 2;       // 32-query chunk of each step
+        const int r = quarter * 32 + lane;   // TMEM lane: key row
         const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
         const int key = k0 + r;
         const bool key_ok = key < p.Nk;
-        const bool key_tail = k0 + kBwdTile > p.Nk;
+        const bool key_tail = k0 + kBwdKeys > p.Nk;
         const int off = p.causal_br ? p.Nk - p.Nq : 0;
         const float sl2 = p.scale_log2;
-        const size_t row0 = static_cast<size_t>(bh) * p.Nq_pad;
         bool ok = true;
-        for (int i = 0; i < n && ok; ++i) {
-            const int q0 = (i0 + i) * kBwdTile;
-            // Every entry of the tile is visible unless the tile holds missing
+        for (int h = 0; h < n && ok; ++h) {
+            const int b = h & 1;
+            const int q0 = (h0 + h) * kBwdHalf;
+            // Every entry of the step is visible unless the tile holds missing
             // keys or (causal) crosses the diagonal; padded query rows carry
             // -inf as -LSE log2e, so their P is 0 either way.
-            const bool masked = key_tail || (p.causal && k0 + kBwdTile - 1 > q0 + off);
-            ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_SFULL), i & 1, p, abort_flag, kStatusWaitS));
+            const bool masked = key_tail || (p.causal && k0 + kBwdKeys - 1 > q0 + off);
+            ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_SFULL + b), (h >> 1) & 1, p, abort_flag, kStatusWaitS));
             if (!ok) break;
             tc_fence_after();
-#pragma unroll 1
-            for (int j = 0; j < kBwdChunks; ++j) {
-                const int cc = grp * kBwdChunks + j;
-                uint32_t sraw[32], draw[32];
-                tmem_ld32(tmem + lane_field + L::ST_COL + cc * 32, sraw);
-                tmem_ld32(tmem + lane_field + L::DP_COL + cc * 32, draw);
-                tmem_wait_ld();
-                const float* nl = p.nlse2 + row0 + q0 + cc * 32;
-                const float* nd = p.ndd + row0 + q0 + cc * 32;
-                uint32_t pk[16], dk[16];
-                if (masked) {
-                    // Key row `key` is visible to query q iff key <= q + off.
-                    const int lim = p.causal ? key - off - q0 - cc * 32 : -1;
-                    bwd_chunk<true>(sraw, draw, nl, nd, sl2, lim, key_ok, pk, dk);
-                } else {
-                    bwd_chunk<false>(sraw, draw, nl, nd, sl2, 0, true, pk, dk);
-                }
-                // P^T and dS^T over the first 16 of the chunk's own 32 columns
-                // (no other warp reads or writes them).
-                tmem_st16(tmem + lane_field + L::ST_COL + cc * 32, pk);
-                tmem_st16(tmem + lane_field + L::DP_COL + cc * 32, dk);
-                // dS^T into shared memory: row r, queries 32 cc .. 32 cc + 31.
-                const uint32_t line = sbase + L::DS_OFF + (cc >> 1) * L::CHUNK_BYTES + r * 128;
-                const uint32_t swz = static_cast<uint32_t>(r & 7);
+            const uint32_t col = L::BUF_COL(b) + 32 * g;
+            uint32_t sraw[32], draw[32];
+            tmem_ld32(tmem + lane_field + col, sraw);
+            tmem_ld32(tmem + lane_field + col + L::DP_IN, draw);
+            tmem_wait_ld();
+            // The slot's -LSE log2e and -D for this chunk's 32 queries (the S^T
+            // commit implies the slot's loads landed: the issuer waited for them).
+            const uint32_t rb = sbase + L::ROWS_OFF + (h % kBwdStages) * 2 * L::ROWS_BYTES;
+            const uint32_t nl = rb + L::NL_IN + 128 * g;
+            const uint32_t nd = rb + L::ND_IN + 128 * g;
+            uint32_t pk[16], dk[16];
+            if (masked) {
+                // Key row `key` is visible to query q iff key <= q + off.
+                const int lim = p.causal ? key - off - q0 - 32 * g : -1;
+                bwd_chunk<true>(sraw, draw, nl, nd, sl2, lim, key_ok, pk, dk);
+            } else {
+                bwd_chunk<false>(sraw, draw, nl, nd, sl2, 0, true, pk, dk);
+            }
+            // P^T and dS^T over the first 16 of the chunk's own 32 columns (no
+            // other warp reads or writes them).
+            tmem_st16(tmem + lane_field + col, pk);
+            tmem_st16(tmem + lane_field + col + L::DP_IN, dk);
+            // dS^T into shared memory: row r, queries 32 g .. 32 g + 31 of the
+            // step's 128-byte row (128-byte swizzle).
+            const uint32_t line = sbase + L::DS_OFF + b * L::DS_BYTES + r * 128;
+            const uint32_t swz = static_cast<uint32_t>(r & 7);
 #pragma unroll
-                for (int uu = 0; uu < 4; ++uu) {
-                    const uint32_t u = static_cast<uint32_t>((cc & 1) * 4 + uu);
-                    st_shared_v4(line + ((u ^ swz) << 4), dk[4 * uu], dk[4 * uu + 1], dk[4 * uu + 2], dk[4 * uu + 3]);
-                }
+            for (int uu = 0; uu < 4; ++uu) {
+                const uint32_t u = static_cast<uint32_t>(g * 4 + uu);
+                st_shared_v4(line + ((u ^ swz) << 4), dk[4 * uu], dk[4 * uu + 1], dk[4 * uu + 2], dk[4 * uu + 3]);
             }
             fence_proxy_async_smem();
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::BAR_PREADY));
-            // dQ^T: lane r = head dim r, columns = this tile's queries. The
-            // accumulator has rows for whole tiles, so every add is in bounds.
-            ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_DQFULL), i & 1, p, abort_flag, kStatusWaitO));
-            if (!ok) break;
-            tc_fence_after();
-#pragma unroll 1
-            for (int j = 0; j < kBwdChunks; ++j) {
-                const int cc = grp * kBwdChunks + j;
-                uint32_t raw[32];
-                tmem_ld32(tmem + lane_field + L::DP_COL + cc * 32, raw);
-                tmem_wait_ld();
-                float* dst = p.dq_acc + (row0 + q0 + cc * 32) * kBwdD + r;
-#pragma unroll
-                for (int e = 0; e < 32; ++e) atomicAdd(dst + e * kBwdD, __uint_as_float(raw[e]));
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::BAR_DQREAD));
+            if (lane == 0) mbar_arrive(bar(L::BAR_PREADY + b));
         }
-        // dK (scaled) and dV of this key row, 32 head-dim columns per chunk;
-        // zero when no query tile sees it. tcgen05.ld is warp-collective: the
-        // loads run for the whole warp (`ok` is warp-uniform), and only the
-        // stores check that the key exists.
+        // dK (scaled) and dV of this key row, head-dim columns 64 g .. 64 g + 63,
+        // once every MMA has finished (the last dQ^T commit covers them all);
+        // zero when no query step sees the key tile. tcgen05.ld is
+        // warp-collective: the loads run for the whole warp (`ok` is
+        // warp-uniform), and only the stores check that the key exists.
+        if (ok && n > 0) {
+            ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_DQFULL + ((n - 1) & 1)), ((n - 1) >> 1) & 1, p,
+                                                  abort_flag, kStatusWaitO));
+            if (ok) tc_fence_after();
+        }
         if (ok) {
             __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(p.dk) + (static_cast<size_t>(bh) * p.Nk + key) * kBwdD;
             __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(p.dv) + (static_cast<size_t>(bh) * p.Nk + key) * kBwdD;
 #pragma unroll 1
-            for (int j = 0; j < kBwdChunks; ++j) {
-                const int cc = grp * kBwdChunks + j;
+            for (int j = 0; j < 2; ++j) {
+                const int cc = 2 * g + j;
                 uint32_t kr[32], vr[32];
                 if (n > 0) {
                     tmem_ld32(tmem + lane_field + L::DK_COL + cc * 32, kr);
@@ -449,6 +498,34 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
                     }
                 }
             }
+        }
+    } else if (warp >= 4 + L::COMPUTE_WARPS && n > 0) {
+        // ------------------------------------------------------------ dQ readout
+        // Lane r = head dim r; columns = the step's 64 queries. The TMEM loads
+        // finish before the buffer is released; the atomic adds follow. The
+        // accumulator has rows for whole 128-row tiles, so every add is in
+        // bounds.
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+        bool ok = true;
+        for (int h = 0; h < n && ok; ++h) {
+            const int b = h & 1;
+            ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_DQFULL + b), (h >> 1) & 1, p, abort_flag, kStatusWaitO));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t lo[32], hi[32];
+            tmem_ld32(tmem + lane_field + L::BUF_COL(b), lo);
+            tmem_ld32(tmem + lane_field + L::BUF_COL(b) + 32, hi);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::BAR_DQREAD + b));
+            float* dst = p.dq_acc + (row0 + static_cast<size_t>(h0 + h) * kBwdHalf) * kBwdD + r;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) atomicAdd(dst + e * kBwdD, __uint_as_float(lo[e]));
+#pragma unroll
+            for (int e = 0; e < 32; ++e) atomicAdd(dst + (32 + e) * kBwdD, __uint_as_float(hi[e]));
         }
     }
 
@@ -590,10 +667,10 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     float* ndd = nlse2 + rows_pad;
     fa::BwdParams p;
     std::memset(&p, 0, sizeof(p));
-    if (!fa::encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
+    if (!fa::encode_rows_map(&p.tm_q, q, d, Nq, BH, 64) ||
         !fa::encode_rows_map(&p.tm_k, k, d, Nk, BH, 128) ||
         !fa::encode_rows_map(&p.tm_v, v, d, Nk, BH, 128) ||
-        !fa::encode_rows_map(&p.tm_do, dout, d, Nq, BH, 128))
+        !fa::encode_rows_map(&p.tm_do, dout, d, Nq, BH, 64))
         return FA_ERR_CUDA;
     p.nlse2 = nlse2;
     p.ndd = ndd;

@@ -28,6 +28,14 @@ from .attention import attention_f64
 _ONE_THREAD = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
 
 
+def _bwd_head_task(args):
+    from .backward import attention_backward_f64
+
+    index, q, k, v, do, scale, causal = args
+    grads = attention_backward_f64(*(np.asarray(x, dtype=np.float64) for x in (q, k, v, do)), scale, causal)
+    return (index,) + tuple(grads)
+
+
 def _head_task(args):
     index, q, k, v, scale, causal = args
     o, lse = attention_f64(np.asarray(q, dtype=np.float64), np.asarray(k, dtype=np.float64),
@@ -62,6 +70,12 @@ class HeadPool:
         """``tasks`` yields ``(index, q [Nq, d], k [Nk, d], v [Nk, dv], scale,
         causal)``; yields ``(index, O [Nq, dv], LSE [Nq])`` in completion order."""
         yield from self._pool.imap_unordered(_head_task, tasks)
+
+    def backward_heads(self, tasks):
+        """``tasks`` yields ``(index, q, k, v, do, scale, causal)`` per head;
+        yields ``(index, dQ, dK, dV)`` from
+        :func:`oracle.backward.attention_backward_f64`, in completion order."""
+        yield from self._pool.imap_unordered(_bwd_head_task, tasks)
 
     def close(self):
         self._pool.close()

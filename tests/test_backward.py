@@ -110,10 +110,19 @@ def test_backward_negative_scores_key_tail():
         assert np.linalg.norm(got - r) <= tol * np.linalg.norm(r), name
 
 
+@pytest.fixture(scope="module")
+def head_pool():
+    from oracle.parallel import HeadPool
+
+    with HeadPool() as pool:
+        yield pool
+
+
 @pytest.mark.parametrize("causal", [True, False])
-def test_backward_full_size_sampled_heads(causal):
-    """The C2 shape (B=8, H=32, N=2048, d=128), as the bench times it: three
-    heads against the oracle."""
+def test_backward_full_size_every_head(head_pool, causal):
+    """The C2 shape (B=8, H=32, N=2048, d=128), as the bench times it: dQ, dK
+    and dV of every head against the oracle (run per head in worker
+    processes), each head held to the per-tensor bounds."""
     B, H, N, d = 8, 32, 2048, 128
     q, k, v = make_qkv(B, H, N, N, d, 8201)
     do = make_grad_output(B, H, N, d, 8202)
@@ -123,8 +132,13 @@ def test_backward_full_size_sampled_heads(causal):
     dq, dk, dv = fa.attention_backward(qc, kc, vc, o, lse, doc, causal=causal, scale=scale)
     torch.cuda.synchronize()
     assert fa.fa_device_status(clear=True) == fa.FA_OK
-    for b, h in ((0, 0), (4, 13), (7, 31)):
-        ref = obw.attention_backward_f64(to_f64(q[b, h]), to_f64(k[b, h]), to_f64(v[b, h]),
-                                         to_f64(do[b, h]), scale, causal)
-        for g, r, name in zip((dq[b, h], dk[b, h], dv[b, h]), ref, ("dq", "dk", "dv")):
-            check_grad(g, r, f"{name} head {b},{h} causal={causal}")
+    got = [t.reshape(B * H, N, d).cpu() for t in (dq, dk, dv)]
+    qh, kh, vh, doh = (t.reshape(B * H, N, d) for t in (q, k, v, do))
+    tasks = ((i, qh[i].float().numpy(), kh[i].float().numpy(), vh[i].float().numpy(),
+              doh[i].float().numpy(), scale, causal) for i in range(B * H))
+    seen = 0
+    for i, *ref in head_pool.backward_heads(tasks):
+        for g, r, name in zip(got, ref, ("dq", "dk", "dv")):
+            check_grad(g[i], r, f"{name} head {i} causal={causal}")
+        seen += 1
+    assert seen == B * H
