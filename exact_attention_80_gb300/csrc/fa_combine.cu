@@ -5,14 +5,19 @@
 //   L = sum_s w_s l_s,   O = (sum_s w_s O_s) / L,   LSE = M + ln L.
 // Splits with m_s = -inf (empty, or every key masked) get weight 0.
 //
-// HBM-bound, and short: at decode shapes the whole workspace is a few MB, so
-// the kernel is one round of loads if every load is in flight at once. W warps
-// share a row (W = 1, 2, 4 or 8, from the split count); warp w takes splits
-// w, w + W, ... in batches of up to 16 partial rows, whose loads all go out
-// before the weights are known. Each lane owns d/32 consecutive columns, so a
-// warp reads a split's row as one contiguous 4d-byte segment. With W > 1 the
-// warps' sums meet in shared memory; every warp computes the same M, so no
-// rescaling is needed there.
+// HBM-bound and short: at decode shapes the whole workspace is a few tens of
+// MB, more than the register file of the GPU can hold in flight, so a warp
+// must stream: W warps share a row (W = 1, 2, 4 or 8, from the split count);
+// warp w takes splits w, w + W, ... in batches of partial rows (64 floats per
+// lane per batch), and the loads of its next batch are in flight while it sums
+// the current one (two register buffers). Each lane owns d/32 consecutive
+// columns, so a warp reads a split's row as one contiguous 4d-byte segment with
+// vector loads. Before it waits for anything a warp has its first two batches
+// and the row's m and l of every split (lane-strided) in flight; it then forms
+// M, the weights w_s = exp(m_s - M) (each by the lane that loaded m_s, kept in
+// shared memory for the whole warp) and L = sum_s w_s l_s. With W > 1 the
+// warps' sums meet in shared memory; every warp computes the same M and L, so
+// no rescaling is needed there.
 #include <atomic>
 #include <cuda_bf16.h>
 
@@ -34,8 +39,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <int D>
 struct CombineShape {
     static constexpr int PER = D / 32;                     // columns per lane: 2, 4, 8
-    static constexpr int BATCH = PER >= 8 ? 8 : 16;        // partial rows in flight per warp
+    static constexpr int BATCH = 32 / PER;                 // partial rows per batch (32 floats a lane)
     static constexpr int MAX_WARPS = 8;                    // warps per row, at most
+    static constexpr int MREGS = FA_MAX_SPLITS / 32;       // m (and l) values per lane
 };
 
 // One lane's PER consecutive floats of a partial row.
@@ -66,7 +72,7 @@ __global__ void __launch_bounds__(256)
     using Sh = CombineShape<D>;
     constexpr int PER = Sh::PER, BATCH = Sh::BATCH;
     __shared__ float part[Sh::MAX_WARPS][D];
-    __shared__ float part_l[Sh::MAX_WARPS];
+    __shared__ float wsh[Sh::MAX_WARPS][FA_MAX_SPLITS];
 
     const int S = num_splits;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -75,15 +81,15 @@ __global__ void __launch_bounds__(256)
     const long long row = static_cast<long long>(blockIdx.x) * rows_per_block + r;
     const bool live = row < rows;
     // Splits of this warp: s = wi + W * i, i < n.
-    const int n = wi < S ? (S - wi + W - 1) / W : 0;
-    const float* col = ws_o + static_cast<size_t>(row) * D + lane * PER;
+    const int n = (live && wi < S) ? (S - wi + W - 1) / W : 0;
+    const float* col = ws_o + static_cast<size_t>(live ? row : 0) * D + lane * PER;
     const size_t split_stride = static_cast<size_t>(rows) * D;
 
-    float x[BATCH][PER];
-    auto load_batch = [&](int b0) {
+    float xa[BATCH][PER], xb[BATCH][PER];
+    auto load_batch = [&](float (&x)[BATCH][PER], int b0) {
 #pragma unroll
         for (int i = 0; i < BATCH; ++i) {
-            if (live && b0 + i < n) {
+            if (b0 + i < n) {
                 load_cols<PER>(x[i], col + static_cast<size_t>(wi + W * (b0 + i)) * split_stride);
             } else {
 #pragma unroll
@@ -91,50 +97,63 @@ __global__ void __launch_bounds__(256)
             }
         }
     };
-    // The first batch goes out before the max pass, which it does not need.
-    load_batch(0);
+    load_batch(xa, 0);
+    load_batch(xb, BATCH);
 
+    // m and l of split lane + 32 k, then M, the weights and L.
+    float mv[Sh::MREGS], lv[Sh::MREGS];
     float mx = -INFINITY;
-    if (live)
-        for (int s = lane; s < S; s += 32) mx = fmaxf(mx, ws_m[static_cast<size_t>(s) * rows + row]);
+#pragma unroll
+    for (int k = 0; k < Sh::MREGS; ++k) {
+        const int sp = lane + 32 * k;
+        const bool ok = live && sp < S;
+        const size_t idx = static_cast<size_t>(ok ? sp : 0) * rows + (live ? row : 0);
+        mv[k] = ok ? ws_m[idx] : -INFINITY;
+        lv[k] = ok ? ws_l[idx] : 0.f;
+        mx = fmaxf(mx, mv[k]);
+    }
     mx = warp_max(mx);
     const float ref = (mx == -INFINITY) ? 0.f : mx;
+    float lsum = 0.f;
+#pragma unroll
+    for (int k = 0; k < Sh::MREGS; ++k) {
+        const int sp = lane + 32 * k;
+        const float wk = (mv[k] == -INFINITY) ? 0.f : expf(mv[k] - ref);
+        lsum = fmaf(wk, lv[k], lsum);
+        if (sp < S) wsh[warp][sp] = wk;
+    }
+    lsum = warp_sum(lsum);
+    __syncwarp();
 
     float acc[PER];
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    float lsum = 0.f;  // this lane's share of sum_s w_s l_s
-    for (int b0 = 0; b0 < n; b0 += BATCH) {
-        if (b0 > 0) load_batch(b0);
-        // Lane j holds the weight of the batch's j-th split.
-        float wj = 0.f;
-        if (live && lane < BATCH && b0 + lane < n) {
-            const size_t idx = static_cast<size_t>(wi + W * (b0 + lane)) * rows + row;
-            const float ms = ws_m[idx];
-            if (ms != -INFINITY) {
-                wj = expf(ms - ref);
-                lsum = fmaf(wj, ws_l[idx], lsum);
-            }
-        }
+    auto sum_batch = [&](const float (&x)[BATCH][PER], int b0) {
 #pragma unroll
         for (int i = 0; i < BATCH; ++i) {
-            const float w = __shfl_sync(0xffffffffu, wj, i);
+            if (b0 + i < n) {
+                const float w = wsh[warp][wi + W * (b0 + i)];
 #pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, x[i][e], acc[e]);
+                for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, x[i][e], acc[e]);
+            }
         }
+    };
+    // Two batches per trip: while one buffer is summed, the other's loads fly.
+    for (int b0 = 0; b0 < n; b0 += 2 * BATCH) {
+        sum_batch(xa, b0);
+        if (b0 + 2 * BATCH < n) load_batch(xa, b0 + 2 * BATCH);
+        if (b0 + BATCH < n) sum_batch(xb, b0 + BATCH);
+        if (b0 + 3 * BATCH < n) load_batch(xb, b0 + 3 * BATCH);
     }
-    lsum = warp_sum(lsum);
 
     if (W > 1) {  // the same for every thread of the launch
 #pragma unroll
         for (int e = 0; e < PER; ++e) part[warp][lane * PER + e] = acc[e];
-        if (lane == 0) part_l[warp] = lsum;
         __syncthreads();
         if (wi == 0) {
             for (int k = 1; k < W; ++k) {
 #pragma unroll
                 for (int e = 0; e < PER; ++e) acc[e] += part[warp + k][lane * PER + e];
-                lsum += part_l[warp + k];
             }
         }
     }
@@ -179,18 +198,18 @@ int combine_resident_blocks(int threads) {
     return value;
 }
 
-// Warps per row W (1, 2, 4 or 8): enough batches to cover the splits in one
-// round, unless that many warps per row would not let every row be resident
-// at once; then fewer warps, each taking several rounds of loads. Blocks hold
-// four warps (four rows at W = 1) or, at W = 8, eight.
+// Warps per row W (1, 2, 4 or 8): enough for two batches per warp (one trip of
+// the streaming loop), reduced while the grid would not fit on the GPU in one
+// wave; then each warp streams more batches. Blocks hold four warps (four rows
+// at W = 1) or, at W = 8, eight.
 template <int D>
 cudaError_t launch_combine_d(const float* ws_o, const float* ws_m, const float* ws_l,
                              __nv_bfloat16* o, float* lse, long long rows, int num_splits,
                              cudaStream_t stream) {
     using Sh = CombineShape<D>;
-    const int rounds = (num_splits + Sh::BATCH - 1) / Sh::BATCH;
+    const int trips = (num_splits + 2 * Sh::BATCH - 1) / (2 * Sh::BATCH);
     int W = 1;
-    while (W < rounds && W < Sh::MAX_WARPS) W <<= 1;
+    while (W < trips && W < Sh::MAX_WARPS) W <<= 1;
     auto blocks_for = [rows](int w) {
         const int per_block = (w > 4 ? w : 4) / w;
         return (rows + per_block - 1) / per_block;
