@@ -359,11 +359,45 @@ def extra_workloads(device, stream, reps: int = 20):
                     "combine_gbs": round(comb_bytes / ms_c / 1e6, 1)}
             out[name] = sweep
         del q, k, v, o, lse
+    out["c3_tile_sweep"] = tile_sweep(device, stream, reps)
     out["varlen_causal"] = varlen_workload(device, stream, reps)
     out["c2_fp8"] = fp8_workload(device, stream, reps)
     out["c5_fp8"] = fp8_decode_workload(device, stream, reps)
     out["c2_bwd"] = bwd_workload(device, stream, reps)
     return out
+
+
+def tile_sweep(device, stream, reps):
+    """The long-sequence workload (B=1, H=8, N=8192, d=128), both masks, at each
+    query-tile size a CTA can own: 256 rows (two 128-row tiles, fa_fwd's
+    choice) and 128 rows (one tile, fa_fwd_rows). Tiles of 64 rows are not
+    offered (a 128-row tile is the MMA height with one TMEM lane per row)."""
+    import torch
+
+    import exact_attention_80_gb300 as fa
+    from exact_attention_80_gb300.inputs import CONFIGS, metric_flops
+
+    res = {}
+    gen = torch.Generator(device=device)
+    for name in ("c3", "c3_causal"):
+        c = CONFIGS[name]
+        B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
+        q, k, v = device_qkv(c, gen, device)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Nq), device=device)
+        flops = metric_flops(B, H, Nq, Nk, d, causal)
+        line = {}
+        for rows in (256, 128):
+            fn = lambda: fa.fa_fwd_rows(q, k, v, o, lse, rows, causal, stream=stream)  # noqa: E731
+            for _ in range(3):
+                fn()
+            ms = statistics.median(time_launches(fn, reps, stream, queue_ahead=True))
+            line[f"rows_{rows}"] = {"tflops": round(flops / ms / 1e9, 1), "us": round(ms * 1e3, 1),
+                                    "ctas": B * H * -(-Nq // rows)}
+        line["rows_64"] = "not offered"
+        res[name] = line
+        del q, k, v, o, lse
+    return res
 
 
 def bwd_workload(device, stream, reps):

@@ -23,6 +23,7 @@ STATUS_NAMES = {
     0: "FA_OK", 1: "FA_ERR_NULL", 2: "FA_ERR_ALIGN", 3: "FA_ERR_SHAPE", 4: "FA_ERR_HEADDIM",
     5: "FA_ERR_SPLITS", 6: "FA_ERR_WORKSPACE", 7: "FA_ERR_CUDA", 8: "FA_ERR_TIMEOUT",
     9: "FA_ERR_SCALE", 10: "FA_ERR_SCRATCH", 11: "FA_ERR_CAUSAL", 12: "FA_ERR_SEQLENS",
+    13: "FA_ERR_TILE",
 }
 # Causal mask modes (include/fa.h): key j visible to query i iff j <= i (top-left)
 # or j <= i + Nk - Nq (bottom-right).
@@ -57,6 +58,8 @@ def load_library() -> ctypes.CDLL:
     vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_fwd_rows.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_rows.restype = i
     lib.fa_splitkv_workspace_bytes.argtypes = [i, i, i, i, i]
     lib.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
@@ -184,6 +187,19 @@ def fa_fwd(q, k, v, o, lse, causal=False, scale: float | None = None, stream=Non
     st = load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
                                scale, causal_code(causal), _stream_handle(stream))
     _check(st, "fa_fwd")
+
+
+def fa_fwd_rows(q, k, v, o, lse, rows_per_cta: int, causal=False, scale: float | None = None,
+                stream=None):
+    """:func:`fa_fwd` with ``rows_per_cta`` query rows per CTA (include/fa.h,
+    fa_fwd_rows: 128 or 256 at d <= 128, 128 at d = 256)."""
+    B, H, Nq, Nk, d = _bhnd(q, k, v)
+    _need_o_lse(o, lse, B, H, Nq, d, q.device)
+    scale = default_scale(d) if scale is None else float(scale)
+    st = load_library().fa_fwd_rows(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                                    scale, causal_code(causal), int(rows_per_cta),
+                                    _stream_handle(stream))
+    _check(st, "fa_fwd_rows")
 
 
 def _bhnd8(q, k, v):

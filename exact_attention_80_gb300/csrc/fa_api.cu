@@ -181,9 +181,9 @@ fa_status check_common(const void* q, const void* k, const void* v, int B, int H
 
 namespace {
 
-long long grid_ctas(int B, int H, int Nq, int d, int num_splits) {
+long long grid_ctas(int B, int H, int Nq, int d, int num_splits, int tiles_per_cta = 0) {
     const FwdConfig c = fwd_config(d);
-    const long long rows_per_cta = 128ll * c.q_tiles;
+    const long long rows_per_cta = 128ll * (tiles_per_cta > 0 ? tiles_per_cta : c.q_tiles);
     const long long units = (Nq + rows_per_cta - 1) / rows_per_cta;
     return static_cast<long long>(B) * H * units * num_splits;
 }
@@ -201,9 +201,11 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
                          float* ws, int B, int H, int Nq, int Nk, int d, float scale, int causal,
                          int num_splits, int split_mode, cudaStream_t stream,
                          long long wait_limit = kDefaultWaitLimit, int withhold_q = 0,
-                         const Varlen* vl = nullptr, const float* f8_descale = nullptr) {
+                         const Varlen* vl = nullptr, const float* f8_descale = nullptr,
+                         int tiles_per_cta = 0) {
     const FwdConfig c = fwd_config(d);
-    const long long ctas = grid_ctas(B, H, Nq, d, num_splits);
+    if (tiles_per_cta <= 0) tiles_per_cta = c.q_tiles;
+    const long long ctas = grid_ctas(B, H, Nq, d, num_splits, tiles_per_cta);
     if (ctas < 1 || ctas > 0x7fffffffll) return FA_ERR_SHAPE;
     const bool dual = use_dual(Nq, d, num_splits, split_mode, vl != nullptr);
 
@@ -252,6 +254,7 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     p.num_splits = num_splits;
     p.split_mode = split_mode;
     p.n_units = static_cast<int>(ctas / (static_cast<long long>(BH) * num_splits));
+    p.tiles_per_cta = tiles_per_cta;
     const int kv_tiles = (Nk + c.bn - 1) / c.bn;
     // (Varlen: one split; every sequence's key tiles fit in ceil(total_k / BN).)
     p.kv_tiles_per_split = (kv_tiles + num_splits - 1) / num_splits;
@@ -301,6 +304,20 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     if (!fa::aligned(o, 16) || !fa::aligned(lse, 4)) return FA_ERR_ALIGN;
     return fa::launch_forward(q, k, v, o, lse, nullptr, B, H, Nq, Nk, d, scale, causal, 1, 0,
                               stream);
+}
+
+fa_status fa_fwd_rows(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, float scale, int causal, int rows_per_cta,
+                      cudaStream_t stream) {
+    fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
+    if (s != FA_OK) return s;
+    if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
+    if (!o || !lse) return FA_ERR_NULL;
+    if (!fa::aligned(o, 16) || !fa::aligned(lse, 4)) return FA_ERR_ALIGN;
+    const int slots = fa::fwd_config(d).q_tiles;
+    if (rows_per_cta % 128 != 0 || rows_per_cta < 128 || rows_per_cta / 128 > slots) return FA_ERR_TILE;
+    return fa::launch_forward(q, k, v, o, lse, nullptr, B, H, Nq, Nk, d, scale, causal, 1, 0,
+                              stream, fa::kDefaultWaitLimit, 0, nullptr, nullptr, rows_per_cta / 128);
 }
 
 fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
@@ -457,6 +474,8 @@ const char* fa_status_string(fa_status status) {
             return "FA_ERR_CAUSAL: causal must be FA_CAUSAL_NONE, _TOP_LEFT or _BOTTOM_RIGHT";
         case FA_ERR_SEQLENS:
             return "FA_ERR_SEQLENS: cu_seqlens are not a valid partition (see fa_fwd_varlen)";
+        case FA_ERR_TILE:
+            return "FA_ERR_TILE: rows_per_cta is not offered for this head dim (see fa_fwd_rows)";
     }
     return "unknown fa_status";
 }

@@ -77,7 +77,7 @@ __device__ __forceinline__ void compute_work(const FwdParams& p, long long lin, 
     const int heads_here = min(p.head_group, p.BH - group * p.head_group);
     const int unit = p.n_units - 1 - r / heads_here;
     w.bh = group * p.head_group + r % heads_here;
-    w.q0 = unit * QT * kBM;
+    w.q0 = unit * p.tiles_per_cta * kBM;
     // The sequence's rows and keys: the whole head (dense), or the packed
     // sequence b of a variable-length batch.
     int len_q = p.Nq, len_k = p.Nk;
@@ -121,7 +121,7 @@ __device__ __forceinline__ void compute_work(const FwdParams& p, long long lin, 
     for (int t = 0; t < QT; ++t) {
         const int row0 = w.q0 + t * kBM;
         int n = 0;
-        if (row0 < len_q) {
+        if (t < p.tiles_per_cta && row0 < len_q) {
             int end = t1;
             if (p.causal) {
                 // Keys up to the tile's last row + causal_off; none if that is < 0.

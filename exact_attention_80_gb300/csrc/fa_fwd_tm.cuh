@@ -778,6 +778,9 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             ok = __all_sync(0xffffffffu, ok);
             if (ok) tc_fence_after();
         }
+        // A tile slot the CTA does not own (one tile per CTA, fa_fwd_rows) writes
+        // nothing: its rows belong to another CTA.
+        if (!DUAL && t >= p.tiles_per_cta) ok = false;
         if constexpr (F8) {
             // Dense layouts only (the host rejects varlen). Plain mode: bf16
             // o_scale * O_t / l staged in the tile's own buffer and written with

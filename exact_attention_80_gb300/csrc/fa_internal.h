@@ -55,7 +55,8 @@ struct FwdParams {
     const int* cu_k;
     int num_splits;          // 1 in plain mode
     int split_mode;          // 0: write O/LSE, 1: write partial (O, m, l)
-    int n_units;             // query units of (tiles per CTA * 128) rows per head
+    int n_units;             // query units of (tiles_per_cta * 128) rows per head
+    int tiles_per_cta;       // 128-row query tiles a CTA owns (up to the kernel's tile slots)
     int kv_tiles_per_split;  // ceil(ceil(Nk/BN) / num_splits)
     int head_group;          // heads per scheduling group (CTA order)
     int dual;                // 1: dual-range split CTAs (split mode, Nq <= 128, d <= 128)

@@ -61,7 +61,8 @@ typedef enum {
     FA_ERR_SCALE = 9,      /* scale is not finite or not > 0 */
     FA_ERR_SCRATCH = 10,   /* fa_fwd_splitkv_static: partial states exceed FA_STATIC_SCRATCH_BYTES */
     FA_ERR_CAUSAL = 11,    /* causal is not FA_CAUSAL_NONE, _TOP_LEFT or _BOTTOM_RIGHT */
-    FA_ERR_SEQLENS = 12    /* fa_fwd_varlen: cu_seqlens not a valid partition (from fa_device_status) */
+    FA_ERR_SEQLENS = 12,   /* fa_fwd_varlen: cu_seqlens not a valid partition (from fa_device_status) */
+    FA_ERR_TILE = 13       /* fa_fwd_rows: rows_per_cta not offered for this head dim */
 } fa_status;
 
 #define FA_CAUSAL_NONE 0
@@ -223,6 +224,24 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d);
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                  const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
                  int Nq, int Nk, int d, float scale, int causal, cudaStream_t stream);
+
+/*
+ * fa_fwd_rows — fa_fwd with the query rows a CTA owns chosen by the caller:
+ * the query-tile sweep of the long-sequence workload (B = 1, H = 8,
+ * N = 8192: query tiles split across CTAs, with several tile sizes; "AI 大模型之
+ * FlashAttention_02", section "从头级并行转向序列级并行", and the tile sizes
+ * of section "本册配套实验验证记录"). rows_per_cta = 256 is fa_fwd's own
+ * choice at d <= 128: two 128-row tiles that alternate on the tensor core.
+ * rows_per_cta = 128 gives each CTA one 128-row tile (the other tile slot
+ * idles), so twice as many CTAs share the GPU and each computes alone. At
+ * d = 256 only 128 is offered (fa_fwd's choice there). A 128-row tile is the
+ * tcgen05 MMA height with one TMEM lane per query row; tiles of 64 rows are
+ * not offered. Other values: FA_ERR_TILE. Arguments, layouts and the other
+ * status codes are those of fa_fwd; the result equals fa_fwd's bit for bit.
+ */
+fa_status fa_fwd_rows(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                      int H, int Nq, int Nk, int d, float scale, int causal, int rows_per_cta,
+                      cudaStream_t stream);
 
 /*
  * fa_fwd_grid_ctas — number of CTAs fa_fwd (num_splits = 1) or

@@ -38,7 +38,8 @@ def test_header_declares_the_api():
     names = declared_functions()
     for want in ("fa_fwd", "fa_fwd_splitkv", "fa_combine", "fa_splitkv_workspace_bytes",
                  "fa_status_string", "fa_fwd_grid_ctas", "fa_device_status", "fa_fwd_varlen",
-                 "fa_fwd_fp8", "fa_fwd_fp8_splitkv", "fa_bwd", "fa_bwd_workspace_bytes"):
+                 "fa_fwd_fp8", "fa_fwd_fp8_splitkv", "fa_bwd", "fa_bwd_workspace_bytes",
+                 "fa_fwd_rows"):
         assert want in names
 
 
@@ -240,3 +241,20 @@ def test_bench_fill_splits(lib):
     assert bench.fill_splits(fa, 1, 8, 256, 128, 152) == 19   # two query tiles per CTA
     assert bench.fill_splits(fa, 1, 8, 128, 256, 152) == 19   # d = 256: no dual-range CTAs
     assert bench.fill_splits(fa, 1, 200, 128, 128, 152) == 1
+
+
+def test_rows_per_cta_refused_before_any_cuda_call(lib):
+    """fa_fwd_rows offers 128 or 256 query rows per CTA at d <= 128 and 128 at
+    d = 256; anything else is FA_ERR_TILE (13), checked on the host (fake
+    pointers are never used)."""
+    fn = lib.fa_fwd_rows
+    i, f = ctypes.c_int, ctypes.c_float
+    fn.argtypes = [P, P, P, P, P, i, i, i, i, i, f, i, i, P]
+    fn.restype = i
+    fake = P(0x10000)
+    for d, rows in ((128, 64), (128, 384), (64, 192), (256, 256), (128, 0), (256, 64)):
+        assert fn(fake, fake, fake, fake, fake, 1, 8, 1024, 1024, d, 0.1, 0, rows, P(0)) == 13, (d, rows)
+    assert lib.fa_status_string(13).decode().startswith("FA_ERR_TILE")
+    # A head dim outside the set is still FA_ERR_HEADDIM, and bad pointers keep their codes.
+    assert fn(fake, fake, fake, fake, fake, 1, 8, 1024, 1024, 96, 0.1, 0, 128, P(0)) == 4
+    assert fn(fake, fake, fake, P(0), fake, 1, 8, 1024, 1024, 128, 0.1, 0, 128, P(0)) == 1

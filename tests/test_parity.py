@@ -59,6 +59,17 @@ def run_gpu(q, k, v, causal, scale, num_splits=1):
     return o, lse
 
 
+def run_gpu_rows(q, k, v, causal, scale, rows_per_cta):
+    qc, kc, vc = q.cuda(), k.cuda(), v.cuda()
+    B, H, Nq, d = q.shape
+    o = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    fa.fa_fwd_rows(qc, kc, vc, o, lse, rows_per_cta, causal, scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(clear=True) == fa.FA_OK
+    return o, lse
+
+
 SMALL = [
     # B, H, Nq, Nk, d, causal
     (1, 1, 128, 128, 64, False),
@@ -452,15 +463,19 @@ class WholeCheck:
         return self.max_abs, rel, self.lse_err
 
 
-def whole_tensor_check(pool, c, inputs, splits=(1,)):
-    """Runs the GPU path once per split count and compares each whole output
-    with the oracle, head by head."""
+def whole_tensor_check(pool, c, inputs, splits=(1,), rows_per_cta=None):
+    """Runs the GPU path once per split count (or, with ``rows_per_cta``,
+    fa_fwd_rows) and compares each whole output with the oracle, head by
+    head."""
     q, k, v = inputs
     B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
     scale = f32(1.0 / math.sqrt(d))
     outs = {}
     for S in splits:
-        o, lse = run_gpu(q, k, v, causal, scale, num_splits=S)
+        if rows_per_cta is None:
+            o, lse = run_gpu(q, k, v, causal, scale, num_splits=S)
+        else:
+            o, lse = run_gpu_rows(q, k, v, causal, scale, rows_per_cta)
         outs[S] = (o.float().cpu().numpy().reshape(B * H, Nq, d), lse.cpu().numpy().reshape(B * H, Nq))
         del o, lse
     qh, kh, vh = (t.reshape(B * H, -1, d) for t in (q, k, v))
@@ -498,3 +513,28 @@ def test_full_size_bottom_right_prefill(head_pool):
     with the bottom-right causal mask, B=1, H=32, d=128."""
     c = dict(B=1, H=32, Nq=4096, Nk=8192, d=128, causal="bottom_right", name="prefill")
     whole_tensor_check(head_pool, c, make_qkv(1, 32, 4096, 8192, 128, 1006))
+
+
+@pytest.mark.parametrize("name", ["c3", "c3_causal"])
+def test_full_size_one_tile_per_cta(head_pool, name):
+    """The long-sequence workload's query-tile sweep point of 128 rows per CTA
+    (fa_fwd_rows): whole O and LSE against the oracle."""
+    c = dict(CONFIGS[name], name=name + " rows=128")
+    whole_tensor_check(head_pool, c, config_inputs(name), rows_per_cta=128)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True, "bottom_right"])
+def test_rows_per_cta_equal_fa_fwd(d, causal):
+    """A row's arithmetic does not depend on which CTA or tile slot computes
+    it: fa_fwd_rows gives fa_fwd's output bit for bit on ragged shapes, for
+    every offered tile size, and matches the oracle."""
+    B, H, Nq, Nk = 2, 3, 389, 457
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 960 + d)
+    scale = f32(1.0 / math.sqrt(d))
+    o_ref, lse_ref = run_gpu(q, k, v, causal, scale)
+    for rows in ((128, 256) if d <= 128 else (128,)):
+        o, lse = run_gpu_rows(q, k, v, causal, scale, rows)
+        assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref), rows
+    oo, ll = oracle.attention_f64(to_f64(q), to_f64(k), to_f64(v), scale, causal)
+    check(o, lse, oo, ll, f"rows d={d} {causal}")
