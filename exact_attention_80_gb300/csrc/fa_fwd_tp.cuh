@@ -60,7 +60,12 @@ struct LayoutTP {
     static constexpr int Q_TILES = TpCfg<D>::Q_TILES;
     static constexpr int BN = TpCfg<D>::BN;
     static constexpr int STAGES = TpCfg<D>::STAGES;
-    static constexpr int THREADS = (4 + 4 * Q_TILES) * 32;
+    // Warps: 0-3 control, then one softmax warpgroup per query tile, then one
+    // correction warpgroup per query tile (rescales O when the exponent
+    // reference moves, off the softmax's path).
+    static constexpr int SOFTMAX_WARP0 = 4;
+    static constexpr int CORR_WARP0 = SOFTMAX_WARP0 + 4 * Q_TILES;
+    static constexpr int THREADS = (CORR_WARP0 + 4 * Q_TILES) * 32;
     static constexpr int CHUNKS = D / 64;  // 64-element (128-byte) column chunks
 
     // shared memory (offsets from a 1024-aligned base)
@@ -68,7 +73,10 @@ struct LayoutTP {
     static constexpr uint32_t SLOT_BYTES = BN * D * 2;
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t SLOT_OFF = Q_OFF + Q_TILES * Q_TILE_BYTES;
-    static constexpr uint32_t BAR_OFF = SLOT_OFF + STAGES * SLOT_BYTES;
+    // Per-row rescale factors alpha of a step, for the correction group:
+    // [tile][step parity][row] floats.
+    static constexpr uint32_t ALPHA_OFF = SLOT_OFF + STAGES * SLOT_BYTES;
+    static constexpr uint32_t BAR_OFF = ALPHA_OFF + Q_TILES * 2 * kBM * 4;
     static constexpr int BAR_QFULL = 0;
     static constexpr int BAR_KVFULL = 1;
     static constexpr int BAR_KVEMPTY = BAR_KVFULL + STAGES;
@@ -80,7 +88,12 @@ struct LayoutTP {
     static constexpr int BAR_PVDONE = BAR_PFULL + 2 * Q_TILES; // [tile]
     static constexpr int BAR_OFULL = BAR_PVDONE + Q_TILES;     // [tile]
     static constexpr int BAR_OSTAGED = BAR_OFULL + Q_TILES;    // [tile] bf16 O_t staged (one arrival per warp)
-    static constexpr int BAR_DRAIN = BAR_OSTAGED + Q_TILES;
+    // [tile][step parity]: the step's alpha published (one arrival per softmax
+    // warp); O rescaled for the step, or found to need none (one arrival per
+    // correction warp).
+    static constexpr int BAR_ALPHA = BAR_OSTAGED + Q_TILES;
+    static constexpr int BAR_OREADY = BAR_ALPHA + 2 * Q_TILES;
+    static constexpr int BAR_DRAIN = BAR_OREADY + 2 * Q_TILES;
     static constexpr int NUM_BARS = BAR_DRAIN + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] tmem base, [1] abort
     static constexpr uint32_t BYTES = MISC_OFF + 16;
@@ -149,6 +162,10 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             mbar_init(bar(L::BAR_PVDONE + t), 1);
             mbar_init(bar(L::BAR_OFULL + t), 1);
             mbar_init(bar(L::BAR_OSTAGED + t), 4);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(bar(L::BAR_ALPHA + 2 * t + b), 4);
+                mbar_init(bar(L::BAR_OREADY + 2 * t + b), 4);
+            }
         }
         mbar_init(bar(L::BAR_DRAIN), 1);
         *abort_flag = 0u;
@@ -321,6 +338,8 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
                 for (int t = 0; t < QT; ++t) {
                     if (ok && j < w.n[t]) {
                         ok = wait_all(bar(L::BAR_PFULL + 2 * t + (j & 1)), (j >> 1) & 1, kStatusWaitP);
+                        // ... and O_t rescaled for step j by the correction group.
+                        if (ok) ok = wait_all(bar(L::BAR_OREADY + 2 * t + (j & 1)), (j >> 1) & 1, kStatusWaitO);
                         if (!ok) break;
                         tc_fence_after();
                         issue_pv(t, j & 1, pos.slot, j > 0);
@@ -339,10 +358,62 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             wait_phase(bar(L::BAR_DRAIN), 0, p, abort_flag, kStatusWaitDrain, false);
         }
       }
+    } else if (warp >= L::CORR_WARP0) {
+        // ------------------------------------------------------------ correction
+        // Warp CORR_WARP0 + 4 t + q rescales the O rows of lane quarter q of tile
+        // t: per step j > 0 it reads the rows' alpha(j); if any differs from 1 it
+        // waits for PV_t(j - 1) to finish and multiplies the rows' O by alpha(j)
+        // in TMEM. Either way it then releases step j's PV (O_ready). Taking the
+        // rescale out of the softmax's path lets the exponentials of step j run
+        // while O is rescaled.
+        const int t = (warp - L::CORR_WARP0) >> 2;
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t tO = tmem + lane_field + L::O_COL(t);
+        int n = w.n[0];
+#pragma unroll
+        for (int i = 1; i < QT; ++i)
+            if (t == i) n = w.n[i];
+        for (int j = 0; j < n; ++j) {
+            const int b = j & 1;
+            bool ok = wait_phase(bar(L::BAR_ALPHA + 2 * t + b), (j >> 1) & 1, p, abort_flag, kStatusWaitS);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            const float alpha = ld_shared_f32(sbase + L::ALPHA_OFF + ((t * 2 + b) * kBM + r) * 4);
+            // O does not exist before the first PV (which overwrites it).
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+                // PV_t(j-1) has finished writing O (its commit is PV_done phase j-1).
+                ok = wait_phase(bar(L::BAR_PVDONE + t), (j - 1) & 1, p, abort_flag, kStatusWaitO);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t ax2 = f2pack(alpha, alpha);
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + cc * 32, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float x0, x1;
+                        f2unpack(fmul2(f2pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), ax2),
+                                 x0, x1);
+                        o[2 * i] = __float_as_uint(x0);
+                        o[2 * i + 1] = __float_as_uint(x1);
+                    }
+                    tmem_st32(tO + cc * 32, o);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::BAR_OREADY + 2 * t + b));
+        }
     } else {
         // ------------------------------------------------------------ softmax
         if constexpr (L::REG_SPLIT) setmaxnreg_inc<L::SOFTMAX_REGS>();
-        const int t = (warp - 4) >> 2;
+        const int t = (warp - L::SOFTMAX_WARP0) >> 2;
         const int quarter = warp & 3;  // TMEM lane quarter this warp may access
         const int r = quarter * 32 + lane;
         const int q_row = w.q0 + t * kBM + r;
@@ -417,34 +488,12 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             const float alpha = move ? ex2(m - m_use) : 1.f;
             const float neg = -m_use;
 
-            // Rescale the accumulator before this step's PV. PV_t(j-1) may still
-            // be running: wait for it first (its commit is BAR_PVDONE phase j-1).
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-                bool pv_ok = wait_phase(bar(L::BAR_PVDONE + t), (j - 1) & 1, p, abort_flag,
-                                        kStatusWaitO);
-                pv_ok = __all_sync(0xffffffffu, pv_ok);
-                if (!pv_ok) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint64_t ax2 = f2pack(alpha, alpha);
-#pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t o[32];
-                    tmem_ld32(tO + cc * 32, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float x0, x1;
-                        f2unpack(fmul2(f2pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])), ax2),
-                                 x0, x1);
-                        o[2 * i] = __float_as_uint(x0);
-                        o[2 * i + 1] = __float_as_uint(x1);
-                    }
-                    tmem_st32(tO + cc * 32, o);
-                }
-            }
+            // The accumulator's rescale for this step is the correction group's:
+            // publish alpha (the step parity's slot is free: the correction group
+            // read it two steps ago, before the PV this step's S waited behind).
+            st_shared_f32(sbase + L::ALPHA_OFF + ((t * 2 + b) * kBM + r) * 4, alpha);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::BAR_ALPHA + 2 * t + b));
 
             // x = s*scale*log2e - m as packed fp32 pairs (one FFMA2 per two keys),
             // p = 2^x on the MUFU, row sums as four packed partial pairs.

@@ -68,6 +68,16 @@ __device__ __forceinline__ void ld_shared_v4f(uint32_t addr, float (&x)[4]) {
                  : "memory");
 }
 
+// 4-byte shared-memory store and load.
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // One lane of a converged warp (the lowest active lane): the warp runs a loop
 // with uniform values and only the elected lane issues tcgen05 / TMA work, so
 // the operands stay in warp-uniform registers.
