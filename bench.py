@@ -362,6 +362,8 @@ def extra_workloads(device, stream, reps: int = 20):
     out["c3_tile_sweep"] = tile_sweep(device, stream, reps)
     out["varlen_causal"] = varlen_workload(device, stream, reps)
     out["c2_fp8"] = fp8_workload(device, stream, reps)
+    out["c4_fp8"] = fp8_workload(device, stream, reps, shape=(8, 16, 8191, 256), causal=True,
+                                 seed=1011)
     out["c5_fp8"] = fp8_decode_workload(device, stream, reps)
     out["c2_bwd"] = bwd_workload(device, stream, reps)
     return out
@@ -468,30 +470,32 @@ def fp8_decode_workload(device, stream, reps):
     return res
 
 
-def fp8_workload(device, stream, reps):
-    """The C2 shape (B=8, H=32, N=2048, d=128, non-causal) with e4m3 Q, K, V
-    (N(0,1) / 2^-5 rounded to e4m3, descales 2^-5), through fa_fwd_fp8. Its
-    roofline peak is the measured bf16 peak times 2, the nominal fp8/bf16 dense
-    ratio."""
+def fp8_workload(device, stream, reps, shape=(8, 32, 2048, 128), causal=False, seed=1008):
+    """A workload shape (default C2: B=8, H=32, N=2048, d=128, non-causal) with
+    e4m3 Q, K, V (N(0,1) / 2^-5 rounded to e4m3, descales 2^-5), through
+    fa_fwd_fp8. Its roofline peak is the measured bf16 peak times 2, the nominal
+    fp8/bf16 dense ratio."""
     import torch
 
     import exact_attention_80_gb300 as fa
     from exact_attention_80_gb300.inputs import metric_flops
 
-    B, H, N, d = 8, 32, 2048, 128
+    B, H, N, d = shape
     ds = 2.0 ** -5
-    gen = torch.Generator(device=device).manual_seed(1008)
+    gen = torch.Generator(device=device).manual_seed(seed)
     q8, k8, v8 = ((torch.randn((B, H, N, d), generator=gen, device=device) / ds)
                   .clamp(-448.0, 448.0).to(torch.float8_e4m3fn) for _ in range(3))
     o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=device)
     lse = torch.empty((B, H, N), device=device)
-    fn = lambda: fa.fa_fwd_fp8(q8, k8, v8, ds, ds, ds, o, lse, False, stream=stream)  # noqa: E731
+    fn = lambda: fa.fa_fwd_fp8(q8, k8, v8, ds, ds, ds, o, lse, causal, stream=stream)  # noqa: E731
     for _ in range(3):
         fn()
     ms = statistics.median(time_launches(fn, reps, stream, queue_ahead=True))
-    tflops = metric_flops(B, H, N, N, d, False) / ms / 1e9
+    tflops = metric_flops(B, H, N, N, d, causal) / ms / 1e9
     peak_tf, _, kind = measured_peaks()
-    return {"tflops": round(tflops, 1), "us": round(ms * 1e3, 1), "kernel": "fa_fwd_tm8_kernel<128>",
+    kernel = "fa_fwd_tp8_kernel<256>" if d == 256 else f"fa_fwd_tm8_kernel<{d}>"
+    return {"tflops": round(tflops, 1), "us": round(ms * 1e3, 1), "kernel": kernel,
+            "shape": f"B={B} H={H} N={N} d={d} {'causal' if causal else 'non-causal'}",
             "roofline_frac": round(tflops / (2.0 * peak_tf), 4),
             "peak": f"2 x {kind} bf16 burst = {2.0 * peak_tf:.1f} TFLOP/s"}
 

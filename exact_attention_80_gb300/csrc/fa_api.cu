@@ -228,7 +228,7 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
             !encode_rows_map8(&p.tm_k, k, d, Nk, BH, c.bn) ||
             !encode_rows_map8(&p.tm_v, v, d, Nk, BH, c.bn))
             return FA_ERR_CUDA;
-        if (!split_mode && !encode_rows_map(&p.tm_o, o, d, Nq, BH, 32)) return FA_ERR_CUDA;
+        if (!split_mode && !encode_rows_map(&p.tm_o, o, d, Nq, BH, d == 256 ? 128 : 32)) return FA_ERR_CUDA;
     } else {
         if (!encode_rows_map(&p.tm_q, q, d, Nq, BH, 128) ||
             !encode_rows_map(&p.tm_k, k, d, Nk, BH, c.bn) ||
@@ -279,6 +279,7 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
         dual ? static_cast<long long>(BH) * ((num_splits + 1) / 2) : ctas);
     if (f8_descale) {
         if (d == 128) e = dual ? launch_fwd_f8_d128_dual(p, grid, stream) : launch_fwd_f8_d128(p, grid, stream);
+        else if (d == 256) e = launch_fwd_f8_d256(p, grid, stream);
         return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
     }
     switch (d) {
@@ -325,7 +326,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, float q_descal
                      int Nk, int d, float scale, int causal, cudaStream_t stream) {
     fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
     if (s != FA_OK) return s;
-    if (d != 128) return FA_ERR_HEADDIM;
+    if (d != 128 && d != 256) return FA_ERR_HEADDIM;
     if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
     const float ds[3] = {q_descale, k_descale, v_descale};
     for (float x : ds)
@@ -344,7 +345,7 @@ fa_status fa_fwd_fp8_splitkv(const void* q, const void* k, const void* v, float 
                              cudaStream_t stream) {
     fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
     if (s != FA_OK) return s;
-    if (d != 128) return FA_ERR_HEADDIM;
+    if (d != 128 && d != 256) return FA_ERR_HEADDIM;
     if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
     const float ds[3] = {q_descale, k_descale, v_descale};
     for (float x : ds)

@@ -1,4 +1,4 @@
-// Forward kernel instantiation for e4m3 Q, K, V at head dim 128.
+// Forward kernel instantiations for e4m3 Q, K, V at head dims 128 and 256.
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
@@ -7,5 +7,8 @@ cudaError_t launch_fwd_f8_d128(const FwdParams& p, unsigned grid, cudaStream_t s
 }
 cudaError_t launch_fwd_f8_d128_dual(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     return launch_fwd<128, true, true>(p, grid, stream);
+}
+cudaError_t launch_fwd_f8_d256(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+    return launch_fwd<256, true>(p, grid, stream);
 }
 }  // namespace fa

@@ -5,7 +5,8 @@
 //                tiles alternating on the tensor core.
 //   d = 256:     fa_fwd_tp.cuh — one query tile per CTA (O takes half of TMEM),
 //                BN = 96, S double-buffered in TMEM with P packed over it.
-//   e4m3 inputs: fa_fwd_tm.cuh's kernel instantiated for 8-bit operands.
+//   e4m3 inputs: the same kernels instantiated for 8-bit operands (d = 128:
+//                fa_fwd_tm.cuh; d = 256: fa_fwd_tp.cuh).
 #pragma once
 
 #include <type_traits>
@@ -22,9 +23,11 @@ using FwdLayout = std::conditional_t<D == 256, LayoutTP<D>, LayoutTM<D>>;
 // forms of the two-tile kernel (d = 64 or 128).
 template <int D, bool F8 = false, bool DUAL = false>
 cudaError_t launch_fwd(const FwdParams& p, unsigned grid, cudaStream_t stream) {
-    using L = std::conditional_t<F8, LayoutTM<D, true>, FwdLayout<D>>;
+    using L = std::conditional_t<F8, std::conditional_t<D == 256, LayoutTP<D, true>, LayoutTM<D, true>>,
+                                 FwdLayout<D>>;
     constexpr auto kernel = [] {
         if constexpr (F8 && DUAL) return fa_fwd_tm8d_kernel<D>;
+        else if constexpr (F8 && D == 256) return fa_fwd_tp8_kernel<D>;
         else if constexpr (F8) return fa_fwd_tm8_kernel<D>;
         else if constexpr (DUAL) return fa_fwd_tmd_kernel<D>;
         else if constexpr (D == 256) return fa_fwd_tp_kernel<D>;

@@ -55,22 +55,32 @@ struct TpCfg<256> {
     static constexpr int Q_TILES = 1, BN = 96, STAGES = 3;
 };
 
-template <int D>
+// F8: e4m3 Q, K, V (one byte per element) and kind::f8f6f4 MMAs; otherwise
+// bf16 and kind::f16.
+template <int D, bool F8 = false>
 struct LayoutTP {
     static constexpr int Q_TILES = TpCfg<D>::Q_TILES;
     static constexpr int BN = TpCfg<D>::BN;
-    static constexpr int STAGES = TpCfg<D>::STAGES;
+    // 8-bit K/V slots are half the size: six of them fit beside the Q tile.
+    static constexpr int STAGES = F8 ? 6 : TpCfg<D>::STAGES;
+    static constexpr int EB = F8 ? 1 : 2;              // input bytes per element
+    static constexpr int CHUNK_ELEMS = 128 / EB;       // elements per 128-byte swizzle row
+    static constexpr int K_MMA = 32 / EB;              // K elements per MMA instruction
     // Warps: 0-3 control, then one softmax warpgroup per query tile, then one
     // correction warpgroup per query tile (rescales O when the exponent
     // reference moves, off the softmax's path).
     static constexpr int SOFTMAX_WARP0 = 4;
     static constexpr int CORR_WARP0 = SOFTMAX_WARP0 + 4 * Q_TILES;
     static constexpr int THREADS = (CORR_WARP0 + 4 * Q_TILES) * 32;
-    static constexpr int CHUNKS = D / 64;  // 64-element (128-byte) column chunks
+    static constexpr int CHUNKS = D / CHUNK_ELEMS;  // 128-byte column chunks of a row
 
     // shared memory (offsets from a 1024-aligned base)
-    static constexpr uint32_t Q_TILE_BYTES = kBM * D * 2;
-    static constexpr uint32_t SLOT_BYTES = BN * D * 2;
+    static constexpr uint32_t Q_TILE_BYTES = kBM * D * EB;
+    static constexpr uint32_t SLOT_BYTES = BN * D * EB;
+    // bf16 O is staged for its TMA store in the tile's Q memory when that holds
+    // a bf16 tile; with 8-bit inputs in the K/V slots, which are all free once
+    // the last PV has finished (every load was consumed).
+    static_assert(!F8 || STAGES * BN * D * EB >= kBM * D * 2, "O staging fits the K/V slots");
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t SLOT_OFF = Q_OFF + Q_TILES * Q_TILE_BYTES;
     // Per-row rescale factors alpha of a step, for the correction group:
@@ -126,10 +136,9 @@ struct LayoutTP {
     static_assert(65536 / THREADS >= LAUNCH_REGS || !REG_SPLIT, "launch registers");
 };
 
-template <int D>
-__global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
-    fa_fwd_tp_kernel(const __grid_constant__ FwdParams p) {
-    using L = LayoutTP<D>;
+template <int D, bool F8>
+__device__ __forceinline__ void tp_forward(const FwdParams& p) {
+    using L = LayoutTP<D, F8>;
     constexpr int QT = L::Q_TILES;
     constexpr int BN = L::BN;
     constexpr int ST = L::STAGES;
@@ -206,7 +215,8 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128),
-                                    &p.tm_q, bar(L::BAR_QFULL), 64 * c, w.qbase + w.q0 + t * kBM, w.zq);
+                                    &p.tm_q, bar(L::BAR_QFULL), L::CHUNK_ELEMS * c, w.qbase + w.q0 + t * kBM,
+                                    w.zq);
                 }
             }
             // Entry e of the sequence: K_0; then for step j: K_{j+1} (if any), V_j.
@@ -240,7 +250,7 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
-                                    bar(L::BAR_KVFULL + pos.slot), 64 * c, row, w.zq);
+                                    bar(L::BAR_KVFULL + pos.slot), L::CHUNK_ELEMS * c, row, w.zq);
                 }
                 issued = e + 1;
                 pos.advance();
@@ -272,29 +282,40 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             auto wait_all = [&](uint32_t b, uint32_t parity, unsigned what) {
                 return __all_sync(0xffffffffu, wait_phase(b, parity, p, abort_flag, what));
             };
-            constexpr uint32_t IDESC_S = make_idesc_bf16(kBM, BN, false, false);
-            constexpr uint32_t IDESC_O = make_idesc_bf16(kBM, D, false, true);
+            constexpr uint32_t IDESC_S =
+                F8 ? make_idesc_e4m3(kBM, BN, false, false) : make_idesc_bf16(kBM, BN, false, false);
+            constexpr uint32_t IDESC_O =
+                F8 ? make_idesc_e4m3(kBM, D, false, true) : make_idesc_bf16(kBM, D, false, true);
             auto issue_s = [&](int t, int b, int slot) {
                 const uint32_t qa = sbase + L::Q_OFF + t * L::Q_TILE_BYTES;
                 const uint32_t kb = sbase + L::SLOT_OFF + slot * L::SLOT_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int kk = 0; kk < D / L::K_MMA; ++kk) {
                     const uint32_t in_row = (kk & 3) * 32;  // 16 bf16 = 32 bytes of a 128-byte row
                     const uint64_t a = make_sdesc_sw128(qa + (kk >> 2) * (kBM * 128) + in_row, 16, 1024);
                     const uint64_t bd = make_sdesc_sw128(kb + (kk >> 2) * (BN * 128) + in_row, 16, 1024);
-                    if (leader) umma_ss(tmem + L::S_COL(t, b), a, bd, IDESC_S, kk > 0 ? 1u : 0u);
+                    if (leader) {
+                        if constexpr (F8) umma_ss_f8(tmem + L::S_COL(t, b), a, bd, IDESC_S, kk > 0 ? 1u : 0u);
+                        else umma_ss(tmem + L::S_COL(t, b), a, bd, IDESC_S, kk > 0 ? 1u : 0u);
+                    }
                 }
             };
             auto issue_pv = [&](int t, int b, int slot, bool accumulate) {
                 const uint32_t vb = sbase + L::SLOT_OFF + slot * L::SLOT_BYTES;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    // V is MN-major: 16 keys = two 8-row swizzle atoms (2048 bytes);
-                    // 64-column chunks of d are BN*128 bytes apart.
-                    const uint64_t bd = make_sdesc_sw128(vb + kk * 2048, BN * 128, 1024);
-                    if (leader)
-                        umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t, b) + kk * 8, bd, IDESC_O,
-                                (accumulate || kk > 0) ? 1u : 0u);
+                for (int kk = 0; kk < BN / L::K_MMA; ++kk) {
+                    // V is MN-major: one MMA's K_MMA keys are K_MMA rows of 128
+                    // bytes (2048 or 4096 bytes); 128-byte column chunks of d are
+                    // BN*128 bytes apart. A = P, K_MMA keys = 8 TMEM columns.
+                    const uint64_t bd = make_sdesc_sw128(vb + kk * (L::K_MMA * 128), BN * 128, 1024);
+                    if (leader) {
+                        if constexpr (F8)
+                            umma_ts_f8(tmem + L::O_COL(t), tmem + L::S_COL(t, b) + kk * 8, bd, IDESC_O,
+                                       (accumulate || kk > 0) ? 1u : 0u);
+                        else
+                            umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t, b) + kk * 8, bd, IDESC_O,
+                                    (accumulate || kk > 0) ? 1u : 0u);
+                    }
                 }
             };
 
@@ -482,11 +503,15 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             // and the old reference is kept, so O and l need no rescale. The
             // result is the same: O/l and m + log2(l) do not depend on which
             // reference is used, only rounding does.
-            const bool move = m_tile > m + kRescaleSlack;
+            // e4m3 P: a slack of kP8Slack and p = 2^(x - m + kP8Shift), so the
+            // row's largest p lies in [2^6, 2^8], inside e4m3's range and mostly
+            // in its normal range; l sums the same scaled p, and the LSE takes the
+            // shift back out.
+            const bool move = m_tile > m + (F8 ? kP8Slack : kRescaleSlack);
             const float m_new = move ? m_tile : m;
             const float m_use = (m_new == -INFINITY) ? 0.f : m_new;  // all masked so far
             const float alpha = move ? ex2(m - m_use) : 1.f;
-            const float neg = -m_use;
+            const float neg = F8 ? kP8Shift - m_use : -m_use;
 
             // The accumulator's rescale for this step is the correction group's:
             // publish alpha (the step parity's slot is free: the correction group
@@ -500,6 +525,30 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             const uint64_t sl2x2 = f2pack(sl2, sl2);
             const uint64_t negx2 = f2pack(neg, neg);
             uint64_t part2[4] = {0ull, 0ull, 0ull, 0ull};
+            if constexpr (F8) {
+                // e4m3 P: four keys per TMEM column, key 4i + k in byte k of
+                // column i; BN / 4 columns in stores of 8 (32 keys).
+                static_assert(BN % 32 == 0, "e4m3 P in whole 8-column stores");
+#pragma unroll
+                for (int g = 0; g < BN / 32; ++g) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int c = g * 32 + 4 * i;
+                        float x0, x1, x2, x3;
+                        f2unpack(ffma2(f2pack(s[c], s[c + 1]), sl2x2, negx2), x0, x1);
+                        f2unpack(ffma2(f2pack(s[c + 2], s[c + 3]), sl2x2, negx2), x2, x3);
+                        const float e0 = ex2(x0);
+                        const float e1 = ex2(x1);
+                        const float e2 = ex2(x2);
+                        const float e3 = ex2(x3);
+                        part2[(2 * i) & 3] = fadd2(part2[(2 * i) & 3], f2pack(e0, e1));
+                        part2[(2 * i + 1) & 3] = fadd2(part2[(2 * i + 1) & 3], f2pack(e2, e3));
+                        pk[i] = pack_e4m3x4(e0, e1, e2, e3);
+                    }
+                    tmem_st8(tS + g * 8, pk);
+                }
+            } else {
 #pragma unroll
             for (int cc = 0; cc < BN / 64; ++cc) {
                 uint32_t pk[32];
@@ -530,6 +579,7 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
                 }
                 tmem_st16(tS + c0 / 2, pk);
             }
+            }  // bf16 P
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar(L::BAR_PFULL + 2 * t + b));
@@ -541,11 +591,13 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             const float sum = ((part[0] + part[1]) + (part[2] + part[3])) +
                               ((part[4] + part[5]) + (part[6] + part[7]));
             l = l * alpha + sum;
-            // The tile's largest p exactly as computed above (same FMA and ex2)
-            // and what rounding it to bf16 changed (exact: both lie within a
-            // factor of two). 0 for a fully masked row.
-            const float p_max = ex2(__fmaf_rn(s_max, sl2, neg));
-            lc = lc * alpha + (round_bf16(p_max) - p_max);
+            if constexpr (!F8) {
+                // The tile's largest p exactly as computed above (same FMA and
+                // ex2) and what rounding it to bf16 changed (exact: both lie
+                // within a factor of two). 0 for a fully masked row.
+                const float p_max = ex2(__fmaf_rn(s_max, sl2, neg));
+                lc = lc * alpha + (round_bf16(p_max) - p_max);
+            }
             m = m_new;
         }
 
@@ -554,12 +606,19 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
             ok = __all_sync(0xffffffffu, ok);
             if (ok) tc_fence_after();
         }
+        // 8-bit inputs: the O scale is the V descale, and the reference carries
+        // the P shift, which the LSE takes back out.
+        const float o_scale = F8 ? p.o_scale : 1.f;
+        const float m_out = F8 ? m - kP8Shift : m;
+        const float l_o = F8 ? l : l + lc;
         if (ok && !p.split_mode && !p.varlen && n > 0) {
-            // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA.
-            store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, l + lc, tO,
-                              sbase + L::Q_OFF + t * L::Q_TILE_BYTES, bar(L::BAR_OSTAGED + t), abort_flag);
+            // Plain mode: bf16 O_t staged in Q_t's shared memory (8-bit inputs: in
+            // the K/V slots), written with TMA.
+            const uint32_t staging = F8 ? sbase + L::SLOT_OFF : sbase + L::Q_OFF + t * L::Q_TILE_BYTES;
+            store_tile_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m_out, m_true, l, l_o, tO, staging,
+                              bar(L::BAR_OSTAGED + t), abort_flag, o_scale);
         } else if (ok) {
-            write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m, m_true, l, l + lc, tO);
+            write_row<D>(p, w.rm, w.bh, w.split, q_row, n, m_out, m_true, l, l_o, tO, o_scale);
         }
     }
 
@@ -568,6 +627,21 @@ __global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, L::TMEM_COLS);
+}
+
+// bf16 Q, K, V.
+template <int D>
+__global__ void __launch_bounds__(LayoutTP<D>::THREADS, 1)
+    fa_fwd_tp_kernel(const __grid_constant__ FwdParams p) {
+    tp_forward<D, false>(p);
+}
+
+// e4m3 Q, K, V with per-tensor descales (FA-3 page, section 7.3: 8-bit inputs
+// to both GEMMs, fp32 accumulation and fp32 softmax statistics).
+template <int D>
+__global__ void __launch_bounds__(LayoutTP<D, true>::THREADS, 1)
+    fa_fwd_tp8_kernel(const __grid_constant__ FwdParams p) {
+    tp_forward<D, true>(p);
 }
 
 }  // namespace fa

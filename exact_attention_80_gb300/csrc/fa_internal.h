@@ -81,8 +81,9 @@ FwdConfig fwd_config(int d);
 cudaError_t launch_fwd_d64(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d256(const FwdParams& p, unsigned grid, cudaStream_t stream);
-// e4m3 Q, K, V (tm_q/tm_k/tm_v are byte maps, box {128, rows, 1}); d = 128.
+// e4m3 Q, K, V (tm_q/tm_k/tm_v are byte maps, box {128, rows, 1}); d = 128, 256.
 cudaError_t launch_fwd_f8_d128(const FwdParams& p, unsigned grid, cudaStream_t stream);
+cudaError_t launch_fwd_f8_d256(const FwdParams& p, unsigned grid, cudaStream_t stream);
 // Dual-range split-KV CTAs (p.dual = 1): grid B*H*ceil(num_splits / 2).
 cudaError_t launch_fwd_d64_dual(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128_dual(const FwdParams& p, unsigned grid, cudaStream_t stream);

@@ -153,3 +153,47 @@ def test_fp8_dual_range_split(S, Nq):
     o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, "bottom_right")
     sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, "bottom_right")
     check_fp8(o, lse, o_ref, lse_ref, sigma, f"dual S={S} Nq={Nq}")
+
+
+D256_CASES = [
+    # B, H, Nq, Nk, causal: the d = 256 kernel (one 128-row tile per CTA, key
+    # tiles of 96): tails in both, both masks, Nq != Nk
+    (1, 2, 128, 96, False),
+    (1, 2, 300, 333, False),
+    (1, 2, 300, 333, True),
+    (2, 2, 700, 1000, "bottom_right"),
+    (1, 1, 1, 1, False),
+    (1, 2, 1000, 300, True),
+]
+
+
+@pytest.mark.parametrize("B,H,Nq,Nk,causal", D256_CASES)
+def test_fp8_parity_d256(B, H, Nq, Nk, causal):
+    descales = (2.0 ** -5, 2.0 ** -5, 2.0 ** -5)
+    q8, k8, v8, scale, o, lse = run_fp8(B, H, Nq, Nk, causal, 5500 + Nq + Nk, descales, d=256)
+    o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, causal)
+    sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, causal)
+    check_fp8(o, lse, o_ref, lse_ref, sigma, f"d256 B{B} H{H} Nq{Nq} Nk{Nk} {causal}")
+
+
+@pytest.mark.parametrize("S", [2, 5])
+def test_fp8_splitkv_d256(S):
+    """d = 256 e4m3 through split-KV + merge, non-power-of-two descales."""
+    descales = (0.0123, 0.0071, 0.3)
+    q8, k8, v8, scale, o, lse = run_fp8(1, 3, 200, 1500, "bottom_right", 5600 + S, descales, d=256,
+                                        num_splits=S)
+    o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, "bottom_right")
+    sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, "bottom_right")
+    check_fp8(o, lse, o_ref, lse_ref, sigma, f"d256 splits={S}")
+
+
+def test_fp8_full_size_d256_sampled_heads():
+    """The large-head-dim workload's shape (B=8, H=16, N=8191, d=256, causal) in
+    e4m3, as the bench times it: every row of three heads against the oracle."""
+    B, H, N, d = 8, 16, 8191, 256
+    descales = (2.0 ** -5, 2.0 ** -5, 2.0 ** -5)
+    q8, k8, v8, scale, o, lse = run_fp8(B, H, N, N, True, 5701, descales, d)
+    for b, h in ((0, 0), (4, 9), (7, 15)):
+        o_ref, lse_ref = ofp8.attention_fp8_f64(q8[b, h], k8[b, h], v8[b, h], *descales, scale, True)
+        sigma = ofp8.p_rounding_sigma(q8[b, h], k8[b, h], v8[b, h], *descales, scale, True)
+        check_fp8(o[b, h], lse[b, h], o_ref, lse_ref, sigma, f"d256 head {b},{h}")
