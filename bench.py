@@ -366,6 +366,7 @@ def extra_workloads(device, stream, reps: int = 20):
                                  seed=1011)
     out["c5_fp8"] = fp8_decode_workload(device, stream, reps)
     out["c2_bwd"] = bwd_workload(device, stream, reps)
+    out["c2_bwd_d64"] = bwd_workload(device, stream, reps, d=64)
     return out
 
 
@@ -402,17 +403,17 @@ def tile_sweep(device, stream, reps):
     return res
 
 
-def bwd_workload(device, stream, reps):
-    """The backward (fa_bwd) on the C2 shape (B=8, H=32, N=2048, d=128), both
-    masks, on seeded device-side N(0,1) bf16 inputs and upstream gradient; FLOPs
-    2.5x the forward's metric (five GEMMs against two). The three launches of one
-    call are timed together."""
+def bwd_workload(device, stream, reps, d=128):
+    """The backward (fa_bwd) on the C2 shape (B=8, H=32, N=2048) at head dim d
+    (128, or 64), both masks, on seeded device-side N(0,1) bf16 inputs and
+    upstream gradient; FLOPs 2.5x the forward's metric (five GEMMs against two).
+    The three launches of one call are timed together."""
     import torch
 
     import exact_attention_80_gb300 as fa
     from exact_attention_80_gb300.inputs import metric_flops
 
-    B, H, N, d = 8, 32, 2048, 128
+    B, H, N = 8, 32, 2048
     gen = torch.Generator(device=device).manual_seed(1010)
     q, k, v, do = (torch.randn((B, H, N, d), generator=gen, device=device).to(torch.bfloat16)
                    for _ in range(4))
@@ -537,7 +538,7 @@ def run_case(args) -> None:
     ``fwd:<workload>``        fa_fwd on a benchmark workload (c1 .. c4)
     ``split:<S>``             fa_fwd_splitkv + fa_combine on c5 with S splits
     ``fp8``                   fa_fwd_fp8 on the c2 shape (e4m3, descales 2^-5)
-    ``bwd:<B>x<H>x<N>[:causal]``  fa_bwd at d = 128
+    ``bwd:<B>x<H>x<N>[x<d>][:causal]``  fa_bwd (d = 128 unless given)
     """
     import torch
 
@@ -575,13 +576,15 @@ def run_case(args) -> None:
         fns["fa_fwd_fp8"] = lambda: fa.fa_fwd_fp8(q8, k8, v8, ds, ds, ds, o, lse, False, stream=stream)
     elif kind == "bwd":
         shape, _, mask = arg.partition(":")
-        B, H, N = (int(x) for x in shape.split("x"))
+        dims = [int(x) for x in shape.split("x")]
+        B, H, N = dims[:3]
+        d = dims[3] if len(dims) > 3 else 128
         causal = mask == "causal"
         gen.manual_seed(1010)
-        q, k, v, do = (torch.randn((B, H, N, 128), generator=gen, device=device).to(torch.bfloat16)
+        q, k, v, do = (torch.randn((B, H, N, d), generator=gen, device=device).to(torch.bfloat16)
                        for _ in range(4))
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, 128) // 4, device=device)
+        ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d) // 4, device=device)
         o, lse = fa.attention(q, k, v, causal=causal, stream=stream)
         fns["fa_bwd"] = lambda: fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, causal, stream=stream)
     else:

@@ -1,4 +1,4 @@
-// fa_bwd.cu — attention backward for head dim 128: dQ, dK, dV. Holds the
+// fa_bwd.cu — attention backward for head dims 64 and 128: dQ, dK, dV. Holds the
 // backward's kernels and its C entry points (fa_bwd_workspace_bytes, fa_bwd).
 //
 // What is computed (the plain definition of the forward differentiated; the
@@ -41,6 +41,12 @@
 // dV, dK and dQ^T of the same two, so that each of the three groups (tensor
 // core, compute, readout) always has the other step's work to overlap.
 // Every mbarrier wait is bounded, as in the forward kernels.
+//
+// Head dim 64: the same steps with half-width K, V, Q and dO tiles and 64
+// TMEM columns each for dV and dK. dQ^T keeps M = 128 (head-dim lanes): its A
+// operand, K read MN-major, has a second 64-dim chunk of zeros that the CTA
+// writes once, so lanes 64-127 of dQ^T are zero and only the readout warps of
+// lanes 0-63 take it out.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -53,7 +59,7 @@ namespace fa {
 
 // Kernel parameters, filled by fa_bwd below.
 struct BwdParams {
-    CUtensorMap tm_q;   // bf16 [B*H][Nq][d], box {64, 64, 1}
+    CUtensorMap tm_q;   // bf16 [B*H][Nq][d], box {64, 64, 1} (64 head-dim columns)
     CUtensorMap tm_k;   // bf16 [B*H][Nk][d], box {64, 128, 1}
     CUtensorMap tm_v;   // same as tm_k
     CUtensorMap tm_do;  // same as tm_q (dO)
@@ -74,31 +80,37 @@ struct BwdParams {
 
 namespace {
 
-constexpr int kBwdD = 128;
 constexpr int kBwdKeys = 128;   // keys per CTA (TMEM lanes of S^T, dP^T, dV, dK)
 constexpr int kBwdHalf = 64;    // queries per step
 constexpr int kBwdStages = 3;   // Q/dO (+ -LSE log2e, -D) ring slots
 constexpr float kLog2e = 1.4426950408889634f;
 
+template <int D>
 struct LayoutBwd {
+    static_assert(D == 64 || D == 128, "head dim 64 or 128");
     // warp 0 producer, warp 1 issuer, warps 2-3 idle, warps 4-11 compute (two
     // per TMEM lane quarter, one per 32-query chunk of a step), warps 12-15
-    // dQ readout (one per lane quarter).
+    // dQ readout (one per lane quarter; at D = 64 the first two only).
     static constexpr int COMPUTE_WARPS = 8;
     static constexpr int READOUT_WARPS = 4;
+    static constexpr int READOUT_ACTIVE = D / 32;                   // lane quarters holding dQ^T
+    static constexpr int CHUNKS = D / 64;                           // 64-column chunks of a row
     static constexpr int THREADS = 128 + 32 * (COMPUTE_WARPS + READOUT_WARPS);
     static constexpr uint32_t KV_CHUNK = kBwdKeys * 128;            // 16 KB: 64 columns of K or V
-    static constexpr uint32_t KV_BYTES = 2 * KV_CHUNK;              // 32 KB
+    // K always spans two chunks: dQ^T reads it as an M = 128 operand, and at
+    // D = 64 the second chunk is zeros.
+    static constexpr uint32_t K_BYTES = 2 * KV_CHUNK;
+    static constexpr uint32_t V_BYTES = CHUNKS * KV_CHUNK;
     static constexpr uint32_t QH_CHUNK = kBwdHalf * 128;            // 8 KB: 64 columns of a step's Q or dO
-    static constexpr uint32_t QH_BYTES = 2 * QH_CHUNK;              // 16 KB
+    static constexpr uint32_t QH_BYTES = CHUNKS * QH_CHUNK;
     static constexpr uint32_t ROWS_BYTES = kBwdHalf * 4;            // 256 B of -LSE log2e (or -D)
     static constexpr uint32_t STAGE_BYTES = 2 * QH_BYTES;           // Q and dO of a step
     static constexpr uint32_t DS_BYTES = kBwdKeys * kBwdHalf * 2;   // 16 KB: dS^T bf16 [keys][64 queries]
     // Swizzled tiles start on 1024-byte boundaries (the MMA descriptors'
     // base offset is 0); the per-row arrays need 16 bytes.
     static constexpr uint32_t K_OFF = 0;
-    static constexpr uint32_t V_OFF = K_OFF + KV_BYTES;
-    static constexpr uint32_t STAGE_OFF = V_OFF + KV_BYTES;          // [stage]: Q, dO
+    static constexpr uint32_t V_OFF = K_OFF + K_BYTES;
+    static constexpr uint32_t STAGE_OFF = V_OFF + V_BYTES;           // [stage]: Q, dO
     static constexpr uint32_t Q_IN = 0, DO_IN = QH_BYTES;
     static constexpr uint32_t DS_OFF = STAGE_OFF + kBwdStages * STAGE_BYTES;  // [buffer]
     static constexpr uint32_t ROWS_OFF = DS_OFF + 2 * DS_BYTES;     // [stage]: -LSE log2e, -D
@@ -120,7 +132,8 @@ struct LayoutBwd {
     static constexpr size_t ALLOC_BYTES = BYTES + 1024;
     // TMEM columns. Buffer b (b = step & 1) at 128 b: S^T in its first 64
     // columns (then P^T packed over their first halves, then dQ^T), dP^T in
-    // the next 64 (then dS^T packed over their first halves). dV and dK last.
+    // the next 64 (then dS^T packed over their first halves). dV and dK last
+    // (D columns each).
     __host__ __device__ static constexpr uint32_t BUF_COL(int b) { return 128u * static_cast<uint32_t>(b); }
     static constexpr uint32_t DP_IN = 64, DV_COL = 256, DK_COL = 384;
     static_assert(ALLOC_BYTES <= 232448, "shared memory over the 227 KB per-CTA limit");
@@ -207,8 +220,9 @@ __device__ __forceinline__ void bwd_chunk(const uint32_t (&s)[32], const uint32_
 // 2k+2 and 2k+3 (each needs its P^T and dS^T). While the tensor core runs one
 // step's MMAs, the compute group forms P^T and dS^T of the other and the
 // readout group adds the previous dQ^T to the accumulator.
-__global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
-    using L = LayoutBwd;
+template <int D>
+__global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p) {
+    using L = LayoutBwd<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(smem);
@@ -235,7 +249,7 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
             mbar_init(bar(L::BAR_SFULL + b), 1);
             mbar_init(bar(L::BAR_PREADY + b), L::COMPUTE_WARPS);
             mbar_init(bar(L::BAR_DQFULL + b), 1);
-            mbar_init(bar(L::BAR_DQREAD + b), L::READOUT_WARPS);
+            mbar_init(bar(L::BAR_DQREAD + b), L::READOUT_ACTIVE);
         }
         mbar_init(bar(L::BAR_DRAIN), 1);
         *abort_flag = 0u;
@@ -251,6 +265,15 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
         tmem_alloc(sbase + L::MISC_OFF, 512);
         tmem_relinquish();
     }
+    if constexpr (D == 64) {
+        // The zero second chunk of K (head dims 64-127 of dQ^T's A operand),
+        // written through the generic proxy and fenced for the MMAs.
+        const uint32_t z = sbase + L::K_OFF + L::KV_CHUNK + 32u * threadIdx.x;
+        static_assert(L::THREADS * 32 == L::KV_CHUNK, "one 32-byte piece per thread");
+        st_shared_v4(z, 0u, 0u, 0u, 0u);
+        st_shared_v4(z + 16, 0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -260,8 +283,8 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
         // ------------------------------------------------------------ producer
         const bool leader = elect_one();
         if (leader) {
-            mbar_arrive_expect_tx(bar(L::BAR_KV), 2 * L::KV_BYTES);
-            for (int c = 0; c < 2; ++c) {
+            mbar_arrive_expect_tx(bar(L::BAR_KV), 2 * L::V_BYTES);
+            for (int c = 0; c < L::CHUNKS; ++c) {
                 tma_load_3d(sbase + L::K_OFF + c * L::KV_CHUNK, &p.tm_k, bar(L::BAR_KV), 64 * c, k0, bh);
                 tma_load_3d(sbase + L::V_OFF + c * L::KV_CHUNK, &p.tm_v, bar(L::BAR_KV), 64 * c, k0, bh);
             }
@@ -279,7 +302,7 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
                 const uint32_t sb = sbase + L::STAGE_OFF + st * L::STAGE_BYTES;
                 const uint32_t rb = sbase + L::ROWS_OFF + st * 2 * L::ROWS_BYTES;
                 mbar_arrive_expect_tx(bar(L::BAR_QFULL + st), L::STAGE_BYTES + 2 * L::ROWS_BYTES);
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < L::CHUNKS; ++c) {
                     tma_load_3d(sb + L::Q_IN + c * L::QH_CHUNK, &p.tm_q, bar(L::BAR_QFULL + st), 64 * c, q0, bh);
                     tma_load_3d(sb + L::DO_IN + c * L::QH_CHUNK, &p.tm_do, bar(L::BAR_QFULL + st), 64 * c, q0, bh);
                 }
@@ -307,7 +330,7 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
             return __all_sync(0xffffffffu, bwd_wait(b, parity, p, abort_flag, what));
         };
         constexpr uint32_t IDESC_S = make_idesc_bf16(128, kBwdHalf, false, false);  // S^T, dP^T
-        constexpr uint32_t IDESC_ACC = make_idesc_bf16(128, kBwdD, false, true);    // dV, dK
+        constexpr uint32_t IDESC_ACC = make_idesc_bf16(128, D, false, true);        // dV, dK
         constexpr uint32_t IDESC_DQ = make_idesc_bf16(128, kBwdHalf, true, true);   // dQ^T
         // K-major operands (8-row groups 1024 bytes apart); MN-major ones with
         // their 64-element chunks KV_CHUNK (K as A of dQ^T) or QH_CHUNK (Q, dO
@@ -330,7 +353,7 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
             const uint32_t sb = L::STAGE_OFF + st * L::STAGE_BYTES;
             const uint32_t col = L::BUF_COL(h & 1);
 #pragma unroll
-            for (int kk = 0; kk < kBwdD / 16; ++kk) {
+            for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t in_a = (kk & 3) * 32 + (kk >> 2) * L::KV_CHUNK;
                 const uint32_t in_b = (kk & 3) * 32 + (kk >> 2) * L::QH_CHUNK;
                 const uint64_t ak = desc(kmaj_lo, kmaj_hi, L::K_OFF + in_a);
@@ -457,7 +480,7 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::BAR_PREADY + b));
         }
-        // dK (scaled) and dV of this key row, head-dim columns 64 g .. 64 g + 63,
+        // dK (scaled) and dV of this key row, head-dim columns D/2 g .. D/2 g + D/2 - 1,
         // once every MMA has finished (the last dQ^T commit covers them all);
         // zero when no query step sees the key tile. tcgen05.ld is
         // warp-collective: the loads run for the whole warp (`ok` is
@@ -468,11 +491,11 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
             if (ok) tc_fence_after();
         }
         if (ok) {
-            __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(p.dk) + (static_cast<size_t>(bh) * p.Nk + key) * kBwdD;
-            __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(p.dv) + (static_cast<size_t>(bh) * p.Nk + key) * kBwdD;
+            __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(p.dk) + (static_cast<size_t>(bh) * p.Nk + key) * D;
+            __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(p.dv) + (static_cast<size_t>(bh) * p.Nk + key) * D;
 #pragma unroll 1
-            for (int j = 0; j < 2; ++j) {
-                const int cc = 2 * g + j;
+            for (int j = 0; j < L::CHUNKS; ++j) {
+                const int cc = L::CHUNKS * g + j;
                 uint32_t kr[32], vr[32];
                 if (n > 0) {
                     tmem_ld32(tmem + lane_field + L::DK_COL + cc * 32, kr);
@@ -499,12 +522,13 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
                 }
             }
         }
-    } else if (warp >= 4 + L::COMPUTE_WARPS && n > 0) {
+    } else if (warp >= 4 + L::COMPUTE_WARPS && (warp & 3) < L::READOUT_ACTIVE && n > 0) {
         // ------------------------------------------------------------ dQ readout
         // Lane r = head dim r; columns = the step's 64 queries. The TMEM loads
         // finish before the buffer is released; the atomic adds follow. The
         // accumulator has rows for whole 128-row tiles, so every add is in
-        // bounds.
+        // bounds. (Warps 12-15 cover lane quarters 0-3: warp & 3 is the
+        // quarter.)
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
@@ -521,11 +545,11 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::BAR_DQREAD + b));
-            float* dst = p.dq_acc + (row0 + static_cast<size_t>(h0 + h) * kBwdHalf) * kBwdD + r;
+            float* dst = p.dq_acc + (row0 + static_cast<size_t>(h0 + h) * kBwdHalf) * D + r;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) atomicAdd(dst + e * kBwdD, __uint_as_float(lo[e]));
+            for (int e = 0; e < 32; ++e) atomicAdd(dst + e * D, __uint_as_float(lo[e]));
 #pragma unroll
-            for (int e = 0; e < 32; ++e) atomicAdd(dst + (32 + e) * kBwdD, __uint_as_float(hi[e]));
+            for (int e = 0; e < 32; ++e) atomicAdd(dst + (32 + e) * D, __uint_as_float(hi[e]));
         }
     }
 
@@ -536,9 +560,10 @@ __global__ void __launch_bounds__(LayoutBwd::THREADS, 1) fa_bwd_kernel(const __g
     if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// Per padded query row (one warp per row, four columns per lane): -D_i =
+// Per padded query row (one warp per row, D / 32 columns per lane): -D_i =
 // -sum_c dO_ic O_ic (fp32 from bf16), -LSE log2e, and a zeroed dQ accumulator
 // row. Rows past Nq get -inf and 0; so do rows whose LSE is -inf (no key).
+template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dout,
                                                          const float* __restrict__ lse,
@@ -553,12 +578,11 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
     float s = 0.f, nl = -INFINITY;
     if (q < Nq) {
         const size_t src_row = static_cast<size_t>(bh) * Nq + q;
-        const size_t base = src_row * kBwdD + lane * 4;
-        const uint2 ov = *reinterpret_cast<const uint2*>(o + base);
-        const uint2 dv = *reinterpret_cast<const uint2*>(dout + base);
-        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
-        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
-        for (int e = 0; e < 2; ++e) {
+        const size_t base = src_row * D + lane * (D / 32);
+        const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(o + base);
+        const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(dout + base);
+#pragma unroll
+        for (int e = 0; e < D / 64; ++e) {
             const float2 a = __bfloat1622float2(o2[e]);
             const float2 b = __bfloat1622float2(d2[e]);
             s = fmaf(a.x, b.x, s);
@@ -572,12 +596,16 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
         ndd[row] = -s;
         nlse2[row] = nl;
     }
-    *reinterpret_cast<float4*>(dq_acc + static_cast<size_t>(row) * kBwdD + lane * 4) =
-        make_float4(0.f, 0.f, 0.f, 0.f);
+    float* z = dq_acc + static_cast<size_t>(row) * D + lane * (D / 32);
+    if constexpr (D == 128)
+        *reinterpret_cast<float4*>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
+    else
+        *reinterpret_cast<float2*>(z) = make_float2(0.f, 0.f);
 }
 
-// dQ = scale * accumulator, to bf16: one warp per query row, four columns per
-// lane, reading the accumulator's padded rows.
+// dQ = scale * accumulator, to bf16: one warp per query row, D / 32 columns
+// per lane, reading the accumulator's padded rows.
+template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ acc,
                                                         __nv_bfloat16* __restrict__ dq, long long rows,
                                                         int Nq, int Nq_pad, float scale) {
@@ -586,52 +614,74 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict_
     if (row >= rows) return;
     const long long bh = row / Nq;
     const long long arow = bh * Nq_pad + (row - bh * Nq);
-    const float4 a = *reinterpret_cast<const float4*>(acc + static_cast<size_t>(arow) * kBwdD + lane * 4);
-    __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
-    uint2 out;
-    out.x = *reinterpret_cast<uint32_t*>(&lo);
-    out.y = *reinterpret_cast<uint32_t*>(&hi);
-    *reinterpret_cast<uint2*>(dq + static_cast<size_t>(row) * kBwdD + lane * 4) = out;
+    const float* src = acc + static_cast<size_t>(arow) * D + lane * (D / 32);
+    __nv_bfloat16* dst = dq + static_cast<size_t>(row) * D + lane * (D / 32);
+    if constexpr (D == 128) {
+        const float4 a = *reinterpret_cast<const float4*>(src);
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
+        uint2 out;
+        out.x = *reinterpret_cast<uint32_t*>(&lo);
+        out.y = *reinterpret_cast<uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(dst) = out;
+    } else {
+        const float2 a = *reinterpret_cast<const float2*>(src);
+        *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+    }
 }
 
 }  // namespace
 
+template <int D>
 cudaError_t launch_bwd_pre(const void* o, const void* dout, const float* lse, float* nlse2, float* ndd,
                            float* dq_acc, int BH, int Nq, int Nq_pad, cudaStream_t stream) {
     const long long rows_pad = static_cast<long long>(BH) * Nq_pad;
     const long long blocks = (rows_pad + 7) / 8;
     if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-    fa_bwd_pre_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+    fa_bwd_pre_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, nlse2, ndd,
         dq_acc, rows_pad, Nq, Nq_pad);
     return cudaGetLastError();
 }
 
+template <int D>
 cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream) {
+    using L = LayoutBwd<D>;
     // Kernel attributes belong to the context: set once per device and context.
     static ContextCache<int> attr_set;
     int done = 0;
     const cudaError_t e = attr_set.get(&done, [](int* out) {
         *out = 1;
-        return cudaFuncSetAttribute(fa_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(LayoutBwd::ALLOC_BYTES));
+        return cudaFuncSetAttribute(fa_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(L::ALLOC_BYTES));
     });
     if (e != cudaSuccess) return e;
     const long long ctas = static_cast<long long>(p.BH) * p.k_tiles;
     if (ctas < 1 || ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-    fa_bwd_kernel<<<static_cast<unsigned>(ctas), LayoutBwd::THREADS, LayoutBwd::ALLOC_BYTES, stream>>>(p);
+    fa_bwd_kernel<D><<<static_cast<unsigned>(ctas), L::THREADS, L::ALLOC_BYTES, stream>>>(p);
     return cudaGetLastError();
 }
 
+template <int D>
 cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, int BH, int Nq, int Nq_pad, float scale,
                           cudaStream_t stream) {
     const long long rows = static_cast<long long>(BH) * Nq;
     const long long blocks = (rows + 7) / 8;
     if (blocks > 0x7fffffffll) return cudaErrorInvalidConfiguration;
-    fa_bwd_dq_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+    fa_bwd_dq_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         dq_acc, static_cast<__nv_bfloat16*>(dq), rows, Nq, Nq_pad, scale);
     return cudaGetLastError();
+}
+
+// The three launches of one backward call at head dim D.
+template <int D>
+cudaError_t launch_bwd(const BwdParams& p, const void* o, const void* dout, const float* lse, void* dq,
+                       cudaStream_t stream) {
+    cudaError_t e = launch_bwd_pre<D>(o, dout, lse, const_cast<float*>(p.nlse2), const_cast<float*>(p.ndd),
+                                      p.dq_acc, p.BH, p.Nq, p.Nq_pad, stream);
+    if (e == cudaSuccess) e = launch_bwd_main<D>(p, stream);
+    if (e == cudaSuccess) e = launch_bwd_dq<D>(p.dq_acc, dq, p.BH, p.Nq, p.Nq_pad, p.scale, stream);
+    return e;
 }
 
 }  // namespace fa
@@ -639,7 +689,7 @@ cudaError_t launch_bwd_dq(const float* dq_acc, void* dq, int BH, int Nq, int Nq_
 extern "C" {
 
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d) {
-    if (B < 1 || H < 1 || Nq < 1 || d != 128) return 0;
+    if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128)) return 0;
     const size_t rows_pad = static_cast<size_t>(B) * H * ((static_cast<size_t>(Nq) + 127) / 128 * 128);
     return rows_pad * (static_cast<size_t>(d) + 2) * sizeof(float);
 }
@@ -652,7 +702,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     // Query rows are padded to whole 128-row tiles and key tiles counted in
     // int: both lengths must leave room for that rounding.
     if (Nq > 0x7fffffff - 127 || Nk > 0x7fffffff - 127) return FA_ERR_SHAPE;
-    if (d != 128) return FA_ERR_HEADDIM;
+    if (d != 64 && d != 128) return FA_ERR_HEADDIM;
     if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
     if (!o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
     if (!fa::aligned(o, 16) || !fa::aligned(dout, 16) || !fa::aligned(lse, 4) ||
@@ -688,11 +738,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.scale_log2 = scale * 1.4426950408889634f;
     p.wait_limit = fa::kDefaultWaitLimit;
     if (fa::device_status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
-    if (fa::launch_bwd_pre(o, dout, lse, nlse2, ndd, dq_acc, BH, Nq, Nq_pad, stream) != cudaSuccess)
-        return FA_ERR_CUDA;
-    if (fa::launch_bwd_main(p, stream) != cudaSuccess) return FA_ERR_CUDA;
-    if (fa::launch_bwd_dq(dq_acc, dq, BH, Nq, Nq_pad, scale, stream) != cudaSuccess) return FA_ERR_CUDA;
-    return FA_OK;
+    const cudaError_t e = d == 64 ? fa::launch_bwd<64>(p, o, dout, lse, dq, stream)
+                                  : fa::launch_bwd<128>(p, o, dout, lse, dq, stream);
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 }  // extern "C"
