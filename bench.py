@@ -364,6 +364,7 @@ def extra_workloads(device, stream, reps: int = 20):
     out["c2_fp8"] = fp8_workload(device, stream, reps)
     out["c4_fp8"] = fp8_workload(device, stream, reps, shape=(8, 16, 8191, 256), causal=True,
                                  seed=1011)
+    out["c2_fp8_d64"] = fp8_workload(device, stream, reps, shape=(8, 32, 2048, 64), seed=1012)
     out["c5_fp8"] = fp8_decode_workload(device, stream, reps)
     out["c2_bwd"] = bwd_workload(device, stream, reps)
     out["c2_bwd_d64"] = bwd_workload(device, stream, reps, d=64)
@@ -537,7 +538,8 @@ def run_case(args) -> None:
 
     ``fwd:<workload>``        fa_fwd on a benchmark workload (c1 .. c4)
     ``split:<S>``             fa_fwd_splitkv + fa_combine on c5 with S splits
-    ``fp8``                   fa_fwd_fp8 on the c2 shape (e4m3, descales 2^-5)
+    ``fp8[:<d>]``             fa_fwd_fp8 on the c2 shape at head dim d (default 128;
+                              e4m3, descales 2^-5)
     ``bwd:<B>x<H>x<N>[x<d>][:causal]``  fa_bwd (d = 128 unless given)
     """
     import torch
@@ -568,10 +570,11 @@ def run_case(args) -> None:
         fns["fa_combine"] = lambda: fa.fa_combine(ws, o, lse, B, H, Nq, d, S, stream=stream)
     elif kind == "fp8":
         ds = 2.0 ** -5
+        d = int(arg) if arg else 128
         gen.manual_seed(1008)
-        q8, k8, v8 = ((torch.randn((8, 32, 2048, 128), generator=gen, device=device) / ds)
+        q8, k8, v8 = ((torch.randn((8, 32, 2048, d), generator=gen, device=device) / ds)
                       .clamp(-448.0, 448.0).to(torch.float8_e4m3fn) for _ in range(3))
-        o = torch.empty((8, 32, 2048, 128), dtype=torch.bfloat16, device=device)
+        o = torch.empty((8, 32, 2048, d), dtype=torch.bfloat16, device=device)
         lse = torch.empty((8, 32, 2048), device=device)
         fns["fa_fwd_fp8"] = lambda: fa.fa_fwd_fp8(q8, k8, v8, ds, ds, ds, o, lse, False, stream=stream)
     elif kind == "bwd":

@@ -123,8 +123,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 128-byte swizzle; rows past N read as zeros.
 // 3-D bf16 map (d, rows, heads) with the given row and head strides in bytes,
 // box {64, box_rows, 1}, 128-byte swizzle.
-// Elements are bf16, or single bytes (e4m3) when `bytes`; either way the box is
-// one 128-byte swizzle row wide (64 bf16 or 128 bytes).
+// Elements are bf16, or single bytes (e4m3) when `bytes`; the box is one
+// 128-byte swizzle row wide (64 bf16 or 128 bytes), except for 64-byte e4m3
+// rows (d = 64), which take a 64-byte box and the 64-byte swizzle.
 bool encode_map(CUtensorMap* map, const void* base, int d, long long rows, long long heads,
                 unsigned long long row_stride, unsigned long long head_stride, int box_rows,
                 bool bytes = false) {
@@ -134,12 +135,13 @@ bool encode_map(CUtensorMap* map, const void* base, int d, long long rows, long 
                                 static_cast<cuuint64_t>(heads)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_stride),
                                    static_cast<cuuint64_t>(head_stride)};
-    const cuuint32_t box[3] = {bytes ? 128u : 64u, static_cast<cuuint32_t>(box_rows), 1u};
+    const bool row64 = bytes && d == 64;
+    const cuuint32_t box[3] = {bytes ? (row64 ? 64u : 128u) : 64u, static_cast<cuuint32_t>(box_rows), 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUresult r =
         enc(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
             const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, row64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -278,7 +280,8 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     const unsigned grid = static_cast<unsigned>(
         dual ? static_cast<long long>(BH) * ((num_splits + 1) / 2) : ctas);
     if (f8_descale) {
-        if (d == 128) e = dual ? launch_fwd_f8_d128_dual(p, grid, stream) : launch_fwd_f8_d128(p, grid, stream);
+        if (d == 64) e = dual ? launch_fwd_f8_d64_dual(p, grid, stream) : launch_fwd_f8_d64(p, grid, stream);
+        else if (d == 128) e = dual ? launch_fwd_f8_d128_dual(p, grid, stream) : launch_fwd_f8_d128(p, grid, stream);
         else if (d == 256) e = launch_fwd_f8_d256(p, grid, stream);
         return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
     }
@@ -326,7 +329,7 @@ fa_status fa_fwd_fp8(const void* q, const void* k, const void* v, float q_descal
                      int Nk, int d, float scale, int causal, cudaStream_t stream) {
     fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
     if (s != FA_OK) return s;
-    if (d != 128 && d != 256) return FA_ERR_HEADDIM;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_HEADDIM;
     if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
     const float ds[3] = {q_descale, k_descale, v_descale};
     for (float x : ds)
@@ -345,7 +348,7 @@ fa_status fa_fwd_fp8_splitkv(const void* q, const void* k, const void* v, float 
                              cudaStream_t stream) {
     fa_status s = fa::check_common(q, k, v, B, H, Nq, Nk, d, scale);
     if (s != FA_OK) return s;
-    if (d != 128 && d != 256) return FA_ERR_HEADDIM;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_HEADDIM;
     if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
     const float ds[3] = {q_descale, k_descale, v_descale};
     for (float x : ds)

@@ -1,7 +1,13 @@
-// Forward kernel instantiations for e4m3 Q, K, V at head dims 128 and 256.
+// Forward kernel instantiations for e4m3 Q, K, V at head dims 64, 128 and 256.
 #include "fa_fwd_kernel.cuh"
 
 namespace fa {
+cudaError_t launch_fwd_f8_d64(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+    return launch_fwd<64, true>(p, grid, stream);
+}
+cudaError_t launch_fwd_f8_d64_dual(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+    return launch_fwd<64, true, true>(p, grid, stream);
+}
 cudaError_t launch_fwd_f8_d128(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     return launch_fwd<128, true>(p, grid, stream);
 }

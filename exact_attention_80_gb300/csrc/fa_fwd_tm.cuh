@@ -68,6 +68,10 @@ struct TmCfg<128> {
 template <int D>
 struct TmCfg8;
 template <>
+struct TmCfg8<64> {
+    static constexpr int STAGES = 10, CTRL_REGS = 88, SOFTMAX_REGS = 208;
+};
+template <>
 struct TmCfg8<128> {
     static constexpr int STAGES = 8, CTRL_REGS = 88, SOFTMAX_REGS = 208;
 };
@@ -82,9 +86,13 @@ struct LayoutTM {
     static constexpr int STAGES = Cfg::STAGES;
     static constexpr int THREADS = (4 + 4 * Q_TILES) * 32;
     static constexpr int EB = F8 ? 1 : 2;              // input bytes per element
-    static constexpr int CHUNK_ELEMS = 128 / EB;       // elements per 128-byte swizzle row
+    // Swizzle row width: 128 bytes, or 64 when a whole row is 64 bytes (e4m3,
+    // d = 64; 64-byte swizzle).
+    static constexpr int ROW_BYTES = D * EB < 128 ? D * EB : 128;
+    static constexpr int CHUNK_ELEMS = ROW_BYTES / EB; // elements per swizzle row
     static constexpr int CHUNKS = D / CHUNK_ELEMS;     // column chunks of a Q/K/V row
     static constexpr int K_MMA = 32 / EB;              // K elements per MMA instruction
+    static constexpr int KSTEPS_ROW = ROW_BYTES / 32;  // MMA K steps per swizzle row
 
     // shared memory (offsets from a 1024-aligned base)
     static constexpr uint32_t Q_TILE_BYTES = kBM * D * EB;
@@ -119,6 +127,7 @@ struct LayoutTM {
     static_assert(ALLOC_BYTES <= 232448, "shared memory over the 227 KB per-CTA limit");
     static_assert(ALLOC_BYTES > 232448 / 2, "two CTAs per SM would contend for TMEM");
     static_assert(D % 64 == 0 && STAGES >= 3, "tile shape");
+    static_assert(ROW_BYTES == 128 || ROW_BYTES == 64, "swizzle rows of 128 or 64 bytes");
 
     // Register split: the sum is the launch allocation (THREADS x LAUNCH_REGS),
     // checked on the host.
@@ -154,7 +163,7 @@ __device__ __forceinline__ void tm_dual_control(const FwdParams& p, uint32_t sba
             mbar_arrive_expect_tx(bar(L::BAR_QFULL + 0), L::Q_TILE_BYTES);
 #pragma unroll
             for (int c = 0; c < L::CHUNKS; ++c)
-                tma_load_3d(sbase + L::Q_OFF + c * (kBM * 128), &p.tm_q, bar(L::BAR_QFULL + 0),
+                tma_load_3d(sbase + L::Q_OFF + c * (kBM * L::ROW_BYTES), &p.tm_q, bar(L::BAR_QFULL + 0),
                             L::CHUNK_ELEMS * c, w.q0, w.zq);
         }
         RingPos<ST> pos;
@@ -172,7 +181,7 @@ __device__ __forceinline__ void tm_dual_control(const FwdParams& p, uint32_t sba
                 const int row = ((t ? w.kv_tile0[1] : w.kv_tile0[0]) + kv) * BN;
 #pragma unroll
                 for (int c = 0; c < L::CHUNKS; ++c)
-                    tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
+                    tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * L::ROW_BYTES), map,
                                 bar(L::BAR_KVFULL + pos.slot), L::CHUNK_ELEMS * c, row, w.zq);
             }
             ++issued;
@@ -211,8 +220,8 @@ __device__ __forceinline__ void tm_dual_control(const FwdParams& p, uint32_t sba
             F8 ? make_idesc_e4m3(kBM, BN, false, false) : make_idesc_bf16(kBM, BN, false, false);
         constexpr uint32_t IDESC_O =
             F8 ? make_idesc_e4m3(kBM, D, false, true) : make_idesc_bf16(kBM, D, false, true);
-        const uint64_t kmaj0 = make_sdesc_sw128(sbase, 16, 1024);
-        const uint64_t vmn0 = make_sdesc_sw128(sbase, BN * 128, 1024);
+        const uint64_t kmaj0 = make_sdesc_rows<L::ROW_BYTES>(sbase, 16, 8 * L::ROW_BYTES);
+        const uint64_t vmn0 = make_sdesc_rows<L::ROW_BYTES>(sbase, BN * L::ROW_BYTES, 8 * L::ROW_BYTES);
         const uint32_t kmaj_lo = static_cast<uint32_t>(kmaj0);
         const uint32_t kmaj_hi = static_cast<uint32_t>(kmaj0 >> 32);
         const uint32_t vmn_lo = static_cast<uint32_t>(vmn0);
@@ -225,9 +234,10 @@ __device__ __forceinline__ void tm_dual_control(const FwdParams& p, uint32_t sba
             const uint32_t kb = L::SLOT_OFF + slot * L::SLOT_BYTES;
 #pragma unroll
             for (int kk = 0; kk < D / L::K_MMA; ++kk) {
-                const uint32_t in_row = (kk & 3) * 32;
-                const uint64_t a = desc(kmaj_lo, kmaj_hi, L::Q_OFF + (kk >> 2) * (kBM * 128) + in_row);
-                const uint64_t b = desc(kmaj_lo, kmaj_hi, kb + (kk >> 2) * (BN * 128) + in_row);
+                const uint32_t in_row = (kk % L::KSTEPS_ROW) * 32;
+                const int ch = kk / L::KSTEPS_ROW;
+                const uint64_t a = desc(kmaj_lo, kmaj_hi, L::Q_OFF + ch * (kBM * L::ROW_BYTES) + in_row);
+                const uint64_t b = desc(kmaj_lo, kmaj_hi, kb + ch * (BN * L::ROW_BYTES) + in_row);
                 if (leader) {
                     if constexpr (F8) umma_ss_f8(tmem + L::S_COL(t), a, b, IDESC_S, kk > 0 ? 1u : 0u);
                     else umma_ss(tmem + L::S_COL(t), a, b, IDESC_S, kk > 0 ? 1u : 0u);
@@ -238,7 +248,7 @@ __device__ __forceinline__ void tm_dual_control(const FwdParams& p, uint32_t sba
             const uint32_t vb = L::SLOT_OFF + slot * L::SLOT_BYTES;
 #pragma unroll
             for (int kk = 0; kk < BN / L::K_MMA; ++kk) {
-                const uint64_t b = desc(vmn_lo, vmn_hi, vb + kk * (L::K_MMA * 128));
+                const uint64_t b = desc(vmn_lo, vmn_hi, vb + kk * (L::K_MMA * L::ROW_BYTES));
                 if (leader) {
                     if constexpr (F8)
                         umma_ts_f8(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8, b, IDESC_O,
@@ -369,7 +379,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
                     mbar_arrive_expect_tx(bar(L::BAR_QFULL + t), L::Q_TILE_BYTES);
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
-                        tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128),
+                        tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * L::ROW_BYTES),
                                     &p.tm_q, bar(L::BAR_QFULL + t), L::CHUNK_ELEMS * c, w.qbase + w.q0 + t * kBM,
                                     w.zq);
                 }
@@ -396,7 +406,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
                     const int row = w.kbase + (w.kv_tile0 + kv) * BN;
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
-                        tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
+                        tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * L::ROW_BYTES), map,
                                     bar(L::BAR_KVFULL + pos.slot), L::CHUNK_ELEMS * c, row, w.zq);
                 }
                 issued = e + 1;
@@ -440,8 +450,9 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             // Descriptors are built once; an operand at byte offset `off` from a
             // base adds off >> 4 to the low word (the 14-bit start field never
             // carries: shared addresses stay below 2^18).
-            const uint64_t kmaj0 = make_sdesc_sw128(sbase, 16, 1024);          // Q, K: K-major
-            const uint64_t vmn0 = make_sdesc_sw128(sbase, BN * 128, 1024);     // V: MN-major
+            // Q, K: K-major; V: MN-major (8-row groups 8 swizzle rows apart).
+            const uint64_t kmaj0 = make_sdesc_rows<L::ROW_BYTES>(sbase, 16, 8 * L::ROW_BYTES);
+            const uint64_t vmn0 = make_sdesc_rows<L::ROW_BYTES>(sbase, BN * L::ROW_BYTES, 8 * L::ROW_BYTES);
             const uint32_t kmaj_lo = static_cast<uint32_t>(kmaj0);
             const uint32_t kmaj_hi = static_cast<uint32_t>(kmaj0 >> 32);
             const uint32_t vmn_lo = static_cast<uint32_t>(vmn0);
@@ -452,15 +463,16 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             auto issue_s = [&](int t, int slot) {
                 const uint32_t qa = L::Q_OFF + t * L::Q_TILE_BYTES;
                 const uint32_t kb = L::SLOT_OFF + slot * L::SLOT_BYTES;
-                // One MMA takes 32 bytes of K (16 bf16 or 32 e4m3) of a 128-byte row.
+                // One MMA takes 32 bytes of K (16 bf16 or 32 e4m3) of a swizzle row.
                 if constexpr (F8) {
 #pragma unroll
                     for (int kk = 0; kk < D / L::K_MMA; ++kk) {
-                        const uint32_t in_row = (kk & 3) * 32;
+                        const uint32_t in_row = (kk % L::KSTEPS_ROW) * 32;
+                        const int ch = kk / L::KSTEPS_ROW;
                         if (leader)
                             umma_ss_f8(tmem + L::S_COL(t),
-                                       desc(kmaj_lo, kmaj_hi, qa + (kk >> 2) * (kBM * 128) + in_row),
-                                       desc(kmaj_lo, kmaj_hi, kb + (kk >> 2) * (BN * 128) + in_row), IDESC_S,
+                                       desc(kmaj_lo, kmaj_hi, qa + ch * (kBM * L::ROW_BYTES) + in_row),
+                                       desc(kmaj_lo, kmaj_hi, kb + ch * (BN * L::ROW_BYTES) + in_row), IDESC_S,
                                        kk > 0 ? 1u : 0u);
                     }
                 } else {
@@ -476,8 +488,8 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             };
             // O_t += P_t V: A = P_t packed two bf16 (four e4m3) per TMEM column,
             // so one MMA's K keys (16 bf16 or 32 e4m3) are 8 columns; B = V
-            // MN-major (K key rows of 128 bytes, K/8 swizzle atoms of 1024 bytes;
-            // 128-byte column chunks of d BN*128 bytes apart).
+            // MN-major (K key rows of one swizzle row each, K/8 swizzle atoms;
+            // column chunks of d BN swizzle rows apart).
             auto issue_pv = [&](int t, int slot, bool accumulate) {
                 const uint32_t vb = L::SLOT_OFF + slot * L::SLOT_BYTES;
                 if constexpr (F8) {
@@ -485,7 +497,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
                     for (int kk = 0; kk < BN / L::K_MMA; ++kk)
                         if (leader)
                             umma_ts_f8(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8,
-                                       desc(vmn_lo, vmn_hi, vb + kk * (L::K_MMA * 128)), IDESC_O,
+                                       desc(vmn_lo, vmn_hi, vb + kk * (L::K_MMA * L::ROW_BYTES)), IDESC_O,
                                        (accumulate || kk > 0) ? 1u : 0u);
                 } else {
 #pragma unroll

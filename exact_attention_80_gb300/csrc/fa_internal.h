@@ -81,12 +81,15 @@ FwdConfig fwd_config(int d);
 cudaError_t launch_fwd_d64(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d256(const FwdParams& p, unsigned grid, cudaStream_t stream);
-// e4m3 Q, K, V (tm_q/tm_k/tm_v are byte maps, box {128, rows, 1}); d = 128, 256.
+// e4m3 Q, K, V (tm_q/tm_k/tm_v are byte maps, box {128, rows, 1}, or {64,
+// rows, 1} with the 64-byte swizzle at d = 64); d = 64, 128, 256.
+cudaError_t launch_fwd_f8_d64(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_f8_d128(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_f8_d256(const FwdParams& p, unsigned grid, cudaStream_t stream);
 // Dual-range split-KV CTAs (p.dual = 1): grid B*H*ceil(num_splits / 2).
 cudaError_t launch_fwd_d64_dual(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128_dual(const FwdParams& p, unsigned grid, cudaStream_t stream);
+cudaError_t launch_fwd_f8_d64_dual(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_f8_d128_dual(const FwdParams& p, unsigned grid, cudaStream_t stream);
 
 // Split-KV launches with one query tile per head (Nq <= 128, d <= 128, dense)

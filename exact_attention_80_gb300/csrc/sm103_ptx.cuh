@@ -237,19 +237,30 @@ __host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N, bool a_mn_m
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle.
+// Shared-memory matrix descriptor, swizzled layouts.
 // [0,14) start>>4, [16,30) leading byte offset>>4, [32,46) stride byte
-// offset>>4, [46,48) version = 1, [49,52) base offset = 0 (atoms 1024-aligned),
-// [61,64) layout = 2 (SWIZZLE_128B).
-__device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                     uint32_t sbo_bytes) {
+// offset>>4, [46,48) version = 1, [49,52) base offset = 0 (atoms aligned to
+// their own size), [61,64) layout: 2 = SWIZZLE_128B (atom 8 rows x 128 bytes),
+// 4 = SWIZZLE_64B (8 rows x 64 bytes).
+__device__ __forceinline__ uint64_t make_sdesc_layout(uint32_t saddr, uint32_t lbo_bytes,
+                                                      uint32_t sbo_bytes, uint32_t layout) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
     d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
+    d |= static_cast<uint64_t>(layout & 7u) << 61;
     return d;
+}
+__device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes,
+                                                     uint32_t sbo_bytes) {
+    return make_sdesc_layout(saddr, lbo_bytes, sbo_bytes, 2u);
+}
+// The descriptor of a swizzled tile whose rows are ROW_BYTES (128 or 64) wide.
+template <int ROW_BYTES>
+__device__ __forceinline__ uint64_t make_sdesc_rows(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    static_assert(ROW_BYTES == 128 || ROW_BYTES == 64, "128- or 64-byte swizzle rows");
+    return make_sdesc_layout(saddr, lbo_bytes, sbo_bytes, ROW_BYTES == 128 ? 2u : 4u);
 }
 
 // 32 lanes x 32 consecutive 32-bit columns; thread i of the warp gets lane

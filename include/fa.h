@@ -172,7 +172,7 @@ fa_status fa_fwd_varlen(const void* q, const void* k, const void* v, void* o, fl
  * is taken before the rounding. So O carries a rounding error of relative
  * size about 2^-4 / sqrt(3) per term, which averages over the keys. The LSE
  * does not carry it.
- * d = 128 or 256 (else FA_ERR_HEADDIM). No varlen; the split-KV form is
+ * d = 64, 128 or 256 (else FA_ERR_HEADDIM). No varlen; the split-KV form is
  * fa_fwd_fp8_splitkv. causal as fa_fwd. FA_ERR_SCALE if a descale is not finite and > 0,
  * or if scale * q_descale * k_descale is not.
  */

@@ -140,7 +140,7 @@ def _fp8(lib, q=FAKE, k=FAKE, v=FAKE, qd=0.03125, kd=0.03125, vd=0.03125, o=FAKE
 @pytest.mark.parametrize("kw,code", [
     (dict(q=0), 1), (dict(v=0), 1), (dict(o=0), 1), (dict(lse=0), 1),
     (dict(Nq=0), 3), (dict(B=0), 3),
-    (dict(d=64), 4), (dict(d=96), 4), (dict(d=512), 4),
+    (dict(d=32), 4), (dict(d=96), 4), (dict(d=512), 4),
     (dict(qd=0.0), 9), (dict(kd=-1.0), 9), (dict(vd=float("nan")), 9), (dict(vd=float("inf")), 9),
     (dict(scale=0.0), 9), (dict(qd=1e-30, kd=1e-30), 9), (dict(qd=1e30, kd=1e30), 9),
     (dict(q=FAKE + 8), 2), (dict(o=FAKE + 8), 2), (dict(lse=FAKE + 2), 2),
@@ -151,7 +151,7 @@ def test_fp8_rejects(lib, kw, code):
 
 
 @pytest.mark.parametrize("kw,code", [
-    (dict(ws=0), 6), (dict(ws=FAKE + 4), 6), (dict(S=0), 5), (dict(S=257), 5), (dict(d=64), 4),
+    (dict(ws=0), 6), (dict(ws=FAKE + 4), 6), (dict(S=0), 5), (dict(S=257), 5), (dict(d=96), 4),
     (dict(q=0), 1), (dict(vd=0.0), 9), (dict(causal=5), 11), (dict(Nk=0), 3),
 ])
 def test_fp8_splitkv_rejects(lib, kw, code):

@@ -69,13 +69,16 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("d", [128, 64])
 @pytest.mark.parametrize("B,H,Nq,Nk,causal", CASES)
-def test_fp8_parity(B, H, Nq, Nk, causal):
+def test_fp8_parity(B, H, Nq, Nk, causal, d):
+    """d = 128 (128-byte swizzle rows) and d = 64 (64-byte rows, 64-byte
+    swizzle)."""
     descales = (2.0 ** -5, 2.0 ** -5, 2.0 ** -5)
-    q8, k8, v8, scale, o, lse = run_fp8(B, H, Nq, Nk, causal, 5100 + Nq + Nk, descales)
+    q8, k8, v8, scale, o, lse = run_fp8(B, H, Nq, Nk, causal, 5100 + Nq + Nk + d, descales, d=d)
     o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, causal)
     sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, causal)
-    check_fp8(o, lse, o_ref, lse_ref, sigma, f"B{B} H{H} Nq{Nq} Nk{Nk} {causal}")
+    check_fp8(o, lse, o_ref, lse_ref, sigma, f"d{d} B{B} H{H} Nq{Nq} Nk{Nk} {causal}")
 
 
 def test_fp8_descales():
@@ -153,6 +156,32 @@ def test_fp8_dual_range_split(S, Nq):
     o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, "bottom_right")
     sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, "bottom_right")
     check_fp8(o, lse, o_ref, lse_ref, sigma, f"dual S={S} Nq={Nq}")
+
+
+@pytest.mark.parametrize("S,Nq", [(3, 200), (2, 128), (7, 100), (40, 1)])
+def test_fp8_splitkv_d64(S, Nq):
+    """d = 64 e4m3 through split-KV + merge: two query tiles per CTA (Nq = 200)
+    and dual-range CTAs (Nq <= 128), odd split counts and splits without keys."""
+    descales = (0.0123, 0.0071, 0.3)
+    q8, k8, v8, scale, o, lse = run_fp8(2, 2, Nq, 4000, "bottom_right", 5800 + S + Nq, descales, d=64,
+                                        num_splits=S)
+    o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, "bottom_right")
+    sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, "bottom_right")
+    check_fp8(o, lse, o_ref, lse_ref, sigma, f"d64 S={S} Nq={Nq}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_full_size_d64_sampled_heads(causal):
+    """The batched shape at d = 64 (B=8, H=32, N=2048) in e4m3, as the bench
+    times it: every row of three heads, spread over the grid, against the
+    oracle."""
+    B, H, N, d = 8, 32, 2048, 64
+    descales = (2.0 ** -5, 2.0 ** -5, 2.0 ** -5)
+    q8, k8, v8, scale, o, lse = run_fp8(B, H, N, N, causal, 5901, descales, d)
+    for b, h in ((0, 0), (3, 17), (7, 31)):
+        o_ref, lse_ref = ofp8.attention_fp8_f64(q8[b, h], k8[b, h], v8[b, h], *descales, scale, causal)
+        sigma = ofp8.p_rounding_sigma(q8[b, h], k8[b, h], v8[b, h], *descales, scale, causal)
+        check_fp8(o[b, h], lse[b, h], o_ref, lse_ref, sigma, f"d64 head {b},{h} causal={causal}")
 
 
 D256_CASES = [
