@@ -211,9 +211,15 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
-def kernel_name(d: int) -> str:
-    """The forward kernel the library launches for head dim d."""
-    return f"fa_fwd_tp_kernel<{d}>" if d == 256 else f"fa_fwd_tm_kernel<{d}>"
+def kernel_name(fa, B: int, H: int, Nq: int, d: int, sms: int) -> str:
+    """The forward kernel fa_fwd launches for this shape: the one-tile kernel at
+    d = 256; at d = 64 and 128 the two-tile kernel, with persistent CTAs when its
+    work units fill four waves of one CTA per SM (include/fa.h, fa_fwd)."""
+    if d == 256:
+        return f"fa_fwd_tp_kernel<{d}>"
+    if fa.fa_fwd_grid_ctas(B, H, Nq, d, 1) >= 4 * sms:
+        return f"fa_fwd_tmp_kernel<{d}>"
+    return f"fa_fwd_tm_kernel<{d}>"
 
 
 def cpu_threads() -> int:
@@ -537,6 +543,7 @@ def run_case(args) -> None:
     capture, which then sees only these launches. Cases:
 
     ``fwd:<workload>``        fa_fwd on a benchmark workload (c1 .. c4)
+    ``rows:<workload>:<R>``   fa_fwd_rows with R query rows per CTA (one unit per CTA)
     ``split:<S>``             fa_fwd_splitkv + fa_combine on c5 with S splits
     ``fp8[:<d>]``             fa_fwd_fp8 on the c2 shape at head dim d (default 128;
                               e4m3, descales 2^-5)
@@ -559,6 +566,12 @@ def run_case(args) -> None:
         q, k, v = device_qkv(c, gen, device)
         o, lse = torch.empty_like(q), torch.empty(q.shape[:3], device=device)
         fns["fa_fwd"] = lambda: fa.fa_fwd(q, k, v, o, lse, c["causal"], stream=stream)
+    elif kind == "rows":
+        wl, _, rows = arg.partition(":")
+        c = CONFIGS[wl]
+        q, k, v = device_qkv(c, gen, device)
+        o, lse = torch.empty_like(q), torch.empty(q.shape[:3], device=device)
+        fns["fa_fwd_rows"] = lambda: fa.fa_fwd_rows(q, k, v, o, lse, int(rows), c["causal"], stream=stream)
     elif kind == "split":
         c = CONFIGS["c5"]
         S = int(arg)
@@ -726,6 +739,7 @@ def run_ours(args):
                "sample": f"{heads} passes of the float64 NumPy oracle over one seeded "
                          f"{c['Nq']}x{c['Nk']} d={d} head of {wl} (the same synthetic head each "
                          f"time, all its queries against all its keys), {secs:.1f} s"}
+    kname = kernel_name(fa, B, H, Nq, d, torch.cuda.get_device_properties(device).multi_processor_count)
     line = {
         "metric": "attention fwd TFLOPS (bf16, 4*B*H*Nq*Nk*d, halved for causal)",
         "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
@@ -733,11 +747,11 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16)",
         "config": workload_config(wl, world),
-        "roofline": {"bound": "tensor", "kernel": kernel_name(d),
+        "roofline": {"bound": "tensor", "kernel": kname,
                      "achieved": round(achieved, 1), "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": round(achieved / peak_tf, 4),
                      "peak_kind": f"{peak_kind} bf16 burst (kernel timed alone)",
-                     "traffic": recorded_traffic(kernel_name(d), wl),
+                     "traffic": recorded_traffic(kname, wl),
                      "flops_per_launch": flops},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),

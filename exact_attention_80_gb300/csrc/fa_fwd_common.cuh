@@ -417,4 +417,54 @@ __device__ __forceinline__ void store_rows_tma(const FwdParams& p, const RowMap&
     __syncwarp();
 }
 
+// store_rows_tma for persistent CTAs: the warp stages its 32 rows one
+// 64-column chunk at a time in its own 4 KB buffer `buf` (32 rows x 128 bytes,
+// the layout of one 32-row box of the O tensor map). Before each chunk it waits
+// until its earlier TMA stores (this unit's previous chunk, or the previous
+// unit's last) have read the buffer; the wait for the last chunk is left to
+// the next call, or to the end of the kernel.
+template <int D>
+__device__ __forceinline__ void store_rows_tma_buf(const FwdParams& p, const RowMap& rm, int bh, int q_row0,
+                                                   int r, int q_row, float m, float m_true, float l,
+                                                   float l_o, uint32_t tO, uint32_t buf) {
+    const int lane = r & 31;
+    const int quarter = r >> 5;
+    const RowOut<D> out(p, rm, bh, 0, q_row, m, m_true, l, l_o);
+    const uint32_t swz = static_cast<uint32_t>(r & 7);
+    const int wrow0 = q_row0 + quarter * 32;
+    const bool any_row = wrow0 < rm.len_q;
+    const uint32_t line = buf + lane * 128;
+#pragma unroll 1
+    for (int c = 0; c < D / 64; ++c) {
+        uint32_t a[32], b[32];
+        tmem_ld32(tO + c * 64, a);
+        tmem_ld32(tO + c * 64 + 32, b);
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+        tmem_wait_ld();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t x0 = hh ? b[2 * i] : a[2 * i];
+                const uint32_t x1 = hh ? b[2 * i + 1] : a[2 * i + 1];
+                pk[i] = pack_bf16x2(__uint_as_float(x0) * out.f, __uint_as_float(x1) * out.f);
+            }
+#pragma unroll
+            for (int uu = 0; uu < 4; ++uu) {
+                const uint32_t u = static_cast<uint32_t>(hh * 4 + uu);
+                st_shared_v4(line + ((u ^ swz) << 4), pk[4 * uu], pk[4 * uu + 1], pk[4 * uu + 2], pk[4 * uu + 3]);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && any_row) {
+            tma_store_3d(&p.tm_o, buf, 64 * c, wrow0, bh);
+            bulk_commit_group();
+        }
+    }
+    out.finish(p);
+}
+
 }  // namespace fa

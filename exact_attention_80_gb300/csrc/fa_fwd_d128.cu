@@ -9,4 +9,7 @@ cudaError_t launch_fwd_d128(const FwdParams& p, unsigned grid, cudaStream_t stre
 cudaError_t launch_fwd_d128_dual(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     return launch_fwd<128, false, true>(p, grid, stream);
 }
+cudaError_t launch_fwd_d128_persist(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+    return launch_fwd<128, false, false, true>(p, grid, stream);
+}
 }  // namespace fa

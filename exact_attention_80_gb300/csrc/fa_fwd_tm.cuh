@@ -64,6 +64,13 @@ template <>
 struct TmCfg<128> {
     static constexpr int STAGES = 5, CTRL_REGS = 88, SOFTMAX_REGS = 208;
 };
+// Persistent CTAs stage O in buffers of their own (the next unit's Q loads
+// into the Q tiles meanwhile), which takes one K/V slot at d = 128.
+template <int D>
+struct TmPersistCfg {
+    static constexpr int STAGES = D == 128 ? 4 : 8;
+    static constexpr int CTRL_REGS = D == 128 ? 88 : 104, SOFTMAX_REGS = D == 128 ? 208 : 200;
+};
 // 8-bit (e4m3) inputs: K/V slots are half the size, so the ring is deeper.
 template <int D>
 struct TmCfg8;
@@ -77,13 +84,14 @@ struct TmCfg8<128> {
 };
 
 // F8: Q, K, V are e4m3 (one byte per element) and both MMAs are
-// kind::f8f6f4; otherwise bf16 and kind::f16.
-template <int D, bool F8 = false>
+// kind::f8f6f4; otherwise bf16 and kind::f16. PERSIST: persistent CTAs
+// (bf16, plain mode), each walking several query units.
+template <int D, bool F8 = false, bool PERSIST = false>
 struct LayoutTM {
     using Cfg = std::conditional_t<F8, TmCfg8<D>, TmCfg<D>>;
     static constexpr int Q_TILES = 2;
     static constexpr int BN = 128;
-    static constexpr int STAGES = Cfg::STAGES;
+    static constexpr int STAGES = PERSIST ? TmPersistCfg<D>::STAGES : Cfg::STAGES;
     static constexpr int THREADS = (4 + 4 * Q_TILES) * 32;
     static constexpr int EB = F8 ? 1 : 2;              // input bytes per element
     // Swizzle row width: 128 bytes, or 64 when a whole row is 64 bytes (e4m3,
@@ -100,9 +108,12 @@ struct LayoutTM {
     static constexpr uint32_t Q_OFF = 0;
     static constexpr uint32_t SLOT_OFF = Q_OFF + Q_TILES * Q_TILE_BYTES;
     // bf16 O is staged for its TMA store in the tile's Q memory when that holds
-    // a bf16 tile; 8-bit Q tiles are half that size, so F8 has buffers of its own.
+    // a bf16 tile; 8-bit Q tiles are half that size, so F8 has buffers of its
+    // own. Persistent CTAs stage each warp's 32 rows, 64 columns at a time, in
+    // a 4 KB buffer per warp (the next unit's Q may be loading).
     static constexpr uint32_t OST_OFF = SLOT_OFF + STAGES * SLOT_BYTES;
-    static constexpr uint32_t OST_TILE_BYTES = F8 ? kBM * D * 2 : 0;
+    static constexpr uint32_t OST_WARP_BYTES = 32 * 128;
+    static constexpr uint32_t OST_TILE_BYTES = F8 ? kBM * D * 2 : (PERSIST ? 4 * OST_WARP_BYTES : 0);
     static constexpr uint32_t BAR_OFF = OST_OFF + Q_TILES * OST_TILE_BYTES;
     static constexpr int BAR_QFULL = 0;                       // [tile] Q_t landed
     static constexpr int BAR_KVFULL = BAR_QFULL + Q_TILES;
@@ -110,7 +121,10 @@ struct LayoutTM {
     static constexpr int BAR_SFULL = BAR_KVEMPTY + STAGES;  // [tile] S_t(j) (and PV_t(j-1)) done
     static constexpr int BAR_PFULL = BAR_SFULL + Q_TILES;   // [tile] P_t(j) in TMEM (one arrival per warp)
     static constexpr int BAR_OFULL = BAR_PFULL + Q_TILES;   // [tile] last PV_t finished
-    static constexpr int BAR_DRAIN = BAR_OFULL + Q_TILES;
+    // [tile] persistent CTAs: the unit's last S_t MMA finished, Q_t free (one
+    // completion per unit in which the tile has keys)
+    static constexpr int BAR_QEMPTY = BAR_OFULL + Q_TILES;
+    static constexpr int BAR_DRAIN = BAR_QEMPTY + Q_TILES;
     static constexpr int NUM_BARS = BAR_DRAIN + 1;
     static constexpr uint32_t MISC_OFF = BAR_OFF + NUM_BARS * 8;  // [0] tmem base, [1] abort
     static constexpr uint32_t BYTES = MISC_OFF + 16;
@@ -128,13 +142,14 @@ struct LayoutTM {
     static_assert(ALLOC_BYTES > 232448 / 2, "two CTAs per SM would contend for TMEM");
     static_assert(D % 64 == 0 && STAGES >= 3, "tile shape");
     static_assert(ROW_BYTES == 128 || ROW_BYTES == 64, "swizzle rows of 128 or 64 bytes");
+    static_assert(!(PERSIST && F8), "persistent CTAs: bf16 inputs");
 
     // Register split: the sum is the launch allocation (THREADS x LAUNCH_REGS),
     // checked on the host.
     static constexpr bool REG_SPLIT = true;
     static constexpr int LAUNCH_REGS = 168;
-    static constexpr int CTRL_REGS = Cfg::CTRL_REGS;
-    static constexpr int SOFTMAX_REGS = Cfg::SOFTMAX_REGS;
+    static constexpr int CTRL_REGS = PERSIST ? TmPersistCfg<D>::CTRL_REGS : Cfg::CTRL_REGS;
+    static constexpr int SOFTMAX_REGS = PERSIST ? TmPersistCfg<D>::SOFTMAX_REGS : Cfg::SOFTMAX_REGS;
     static_assert(128 * CTRL_REGS + 256 * SOFTMAX_REGS == THREADS * LAUNCH_REGS,
                   "register split must equal the launch allocation");
 };
@@ -305,11 +320,249 @@ __device__ __forceinline__ void tm_dual_control(const FwdParams& p, uint32_t sba
     }
 }
 
+// Unit of a persistent CTA's round k, or -1 when the round has none for it.
+// A round walks gridDim.x consecutive units (one wave's worth, sharing heads in
+// L2, the order compute_work gives them), forwards on even rounds and backwards
+// on odd ones: under a causal mask a round's heaviest units come first, so a
+// CTA that took one of them takes one of the lightest next.
+__device__ __forceinline__ long long persist_unit(const FwdParams& p, int k) {
+    const long long g = gridDim.x;
+    const long long c = (k & 1) ? g - 1 - blockIdx.x : blockIdx.x;
+    const long long lin = static_cast<long long>(k) * g + c;
+    return lin < p.total_units ? lin : -1;
+}
+
+// Control warps of a persistent CTA (bf16, plain mode, dense): the producer and
+// the issuer of tm_forward's one-unit CTA, run over the CTA's units with the
+// K/V ring and every barrier's phase carried from unit to unit. Phases count
+// per tile: SFULL_t and PFULL_t complete once per key step of the tile,
+// QFULL_t, QEMPTY_t and OFULL_t once per unit in which the tile has keys.
+//   Q_t of the next unit loads as soon as the last S_t MMA of the unit before
+//   it has completed: the issuer commits QEMPTY_t right after that MMA. Each
+//   waiter of a barrier sees every one of its phases in turn (an mbarrier
+//   wait tells phases apart by parity alone, so a waiter must never be two
+//   phases away from the one it waits for): the producer has waited for the
+//   previous QEMPTY_t phase before it issued the load that the next one
+//   releases. O_t of the next
+//   unit is first written by its PV_t(0), which waits for P_t(0); the softmax
+//   threads hand that P over only after their epilogue has read O_t out of TMEM.
+template <int D>
+__device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t sbase, uint32_t tmem,
+                                                   volatile uint32_t* abort_flag, int warp) {
+    using L = LayoutTM<D, false, true>;
+    constexpr int QT = L::Q_TILES;
+    constexpr int BN = L::BN;
+    constexpr int ST = L::STAGES;
+    auto bar = [&](int i) -> uint32_t { return sbase + L::BAR_OFF + 8u * i; };
+    const int rounds = static_cast<int>((p.total_units + gridDim.x - 1) / gridDim.x);
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        const bool leader = elect_one();
+        RingPos<ST> pos;
+        int issued = 0;           // ring entries issued, all units
+        int q_loads[QT] = {};     // Q_t loads issued
+        bool ok = true;
+        for (int k = 0; k < rounds && ok; ++k) {
+            const long long lin = persist_unit(p, k);
+            if (lin < 0) continue;
+            Work<QT> w;
+            compute_work<QT, BN>(p, lin, w);
+            if (w.nmax == 0) continue;
+            auto load_q = [&](int t) -> bool {
+                if (w.n[t] == 0) return true;
+                if (q_loads[t] > 0 &&
+                    !__all_sync(0xffffffffu, wait_phase(bar(L::BAR_QEMPTY + t), (q_loads[t] - 1) & 1, p,
+                                                        abort_flag, kStatusWaitQ)))
+                    return false;
+                if (leader && !p.test_withhold_q) {
+                    mbar_arrive_expect_tx(bar(L::BAR_QFULL + t), L::Q_TILE_BYTES);
+#pragma unroll
+                    for (int c = 0; c < L::CHUNKS; ++c)
+                        tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128), &p.tm_q,
+                                    bar(L::BAR_QFULL + t), L::CHUNK_ELEMS * c, w.q0 + t * kBM, w.zq);
+                }
+                ++q_loads[t];
+                return true;
+            };
+            // Q_0, K_0, then Q_1, as in the one-unit CTA.
+            ok = load_q(0);
+            const int total = 2 * w.nmax;
+            for (int e = 0; e < total && ok; ++e) {
+                const bool is_v = (e & 1) != 0;
+                const int kv = e >> 1;
+                if (issued >= ST) {
+                    ok = __all_sync(0xffffffffu, wait_phase(bar(L::BAR_KVEMPTY + pos.slot), pos.phase ^ 1u, p,
+                                                            abort_flag, kStatusWaitKvEmpty));
+                    if (!ok) break;
+                }
+                if (leader) {
+                    mbar_arrive_expect_tx(bar(L::BAR_KVFULL + pos.slot), L::SLOT_BYTES);
+                    const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
+                    const int row = (w.kv_tile0 + kv) * BN;
+#pragma unroll
+                    for (int c = 0; c < L::CHUNKS; ++c)
+                        tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
+                                    bar(L::BAR_KVFULL + pos.slot), L::CHUNK_ELEMS * c, row, w.zq);
+                }
+                ++issued;
+                pos.advance();
+                if (e == 0) ok = load_q(1);
+            }
+        }
+        if (ok) {
+            // Every slot's last use released: no commit arrival still in flight.
+            for (int e = max(0, issued - ST); e < issued && ok; ++e)
+                ok = __all_sync(0xffffffffu, wait_phase(bar(L::BAR_KVEMPTY + e % ST), (e / ST) & 1, p, abort_flag,
+                                                        kStatusWaitKvEmpty));
+        } else {
+            // Let every copy already issued land before the CTA goes away.
+#pragma unroll
+            for (int t = 0; t < QT; ++t)
+                if (q_loads[t] > 0 && !p.test_withhold_q)
+                    wait_phase(bar(L::BAR_QFULL + t), (q_loads[t] - 1) & 1, p, abort_flag, kStatusWaitDrain, false);
+            for (int e = max(0, issued - ST); e < issued; ++e)
+                wait_phase(bar(L::BAR_KVFULL + e % ST), (e / ST) & 1, p, abort_flag, kStatusWaitDrain, false);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        const bool leader = elect_one();
+        auto wait_all = [&](uint32_t b, uint32_t parity, unsigned what) {
+            return __all_sync(0xffffffffu, wait_phase(b, parity, p, abort_flag, what));
+        };
+        constexpr uint32_t IDESC_S = make_idesc_bf16(kBM, BN, false, false);
+        constexpr uint32_t IDESC_O = make_idesc_bf16(kBM, D, false, true);
+        const uint64_t kmaj0 = make_sdesc_sw128(sbase, 16, 1024);
+        const uint64_t vmn0 = make_sdesc_sw128(sbase, BN * 128, 1024);
+        const uint32_t kmaj_lo = static_cast<uint32_t>(kmaj0);
+        const uint32_t kmaj_hi = static_cast<uint32_t>(kmaj0 >> 32);
+        const uint32_t vmn_lo = static_cast<uint32_t>(vmn0);
+        const uint32_t vmn_hi = static_cast<uint32_t>(vmn0 >> 32);
+        auto desc = [](uint32_t lo, uint32_t hi, uint32_t off) -> uint64_t {
+            return (static_cast<uint64_t>(hi) << 32) | (lo + (off >> 4));
+        };
+        auto issue_s = [&](int t, int slot) {
+            const uint32_t qa = L::Q_OFF + t * L::Q_TILE_BYTES;
+            const uint32_t kb = L::SLOT_OFF + slot * L::SLOT_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+                const uint32_t in_row = (kk & 3) * 32;
+                if (leader)
+                    umma_ss(tmem + L::S_COL(t), desc(kmaj_lo, kmaj_hi, qa + (kk >> 2) * (kBM * 128) + in_row),
+                            desc(kmaj_lo, kmaj_hi, kb + (kk >> 2) * (BN * 128) + in_row), IDESC_S,
+                            kk > 0 ? 1u : 0u);
+            }
+        };
+        auto issue_pv = [&](int t, int slot, bool accumulate) {
+            const uint32_t vb = L::SLOT_OFF + slot * L::SLOT_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+                if (leader)
+                    umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8, desc(vmn_lo, vmn_hi, vb + kk * 2048),
+                            IDESC_O, (accumulate || kk > 0) ? 1u : 0u);
+        };
+        RingPos<ST> pos;
+        int slot_v = 0, slot_k = 0;
+        // Phase parities carried across units: bit t of sbits = parity of the
+        // tile's earlier key steps (PFULL_t), of qbits = parity of its earlier
+        // Q_t loads (QFULL_t).
+        uint32_t sbits = 0, qbits = 0;
+        bool ok = true;
+        constexpr bool kKvWaitMid1 = (D >= 128);
+        for (int k = 0; k < rounds && ok; ++k) {
+            const long long lin = persist_unit(p, k);
+            if (lin < 0) continue;
+            Work<QT> w;
+            compute_work<QT, BN>(p, lin, w);
+            if (w.nmax == 0) continue;
+            auto wait_kv = [&](int j) -> bool {
+                slot_v = pos.slot;
+                if (!wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull)) return false;
+                pos.advance();
+                if (j + 1 < w.nmax) {
+                    slot_k = pos.slot;
+                    if (!wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull)) return false;
+                    pos.advance();
+                }
+                return true;
+            };
+            ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
+            if (ok) {
+#pragma unroll
+                for (int t = 0; t < QT; ++t) {
+                    if (ok && w.n[t] > 0) {
+                        ok = wait_all(bar(L::BAR_QFULL + t), (qbits >> t) & 1u, kStatusWaitQ);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(t, pos.slot);
+                        if (leader) umma_commit(bar(L::BAR_SFULL + t));
+                        if (w.n[t] == 1 && leader) umma_commit(bar(L::BAR_QEMPTY + t));
+                    }
+                }
+            }
+            if (ok) {
+                if (leader) umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
+                pos.advance();
+                ok = wait_kv(0);
+            }
+            for (int j = 0; j < w.nmax && ok; ++j) {
+                const int sv = slot_v, sk = slot_k;
+                const bool k_next = (j + 1 < w.nmax);
+                if (j < w.n[0]) {
+                    ok = wait_all(bar(L::BAR_PFULL + 0), (sbits ^ static_cast<uint32_t>(j)) & 1u, kStatusWaitP);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(0, sv, j > 0);
+                    if (j + 1 < w.n[0]) {
+                        issue_s(0, sk);
+                        if (leader) umma_commit(bar(L::BAR_SFULL + 0));
+                        if (j + 2 == w.n[0] && leader) umma_commit(bar(L::BAR_QEMPTY + 0));
+                    } else {
+                        if (leader) umma_commit(bar(L::BAR_OFULL + 0));
+                    }
+                }
+                if (!kKvWaitMid1 && k_next) {
+                    ok = wait_kv(j + 1);
+                    if (!ok) break;
+                }
+                const bool act1 = j < w.n[1];
+                if (act1) {
+                    ok = wait_all(bar(L::BAR_PFULL + 1), ((sbits >> 1) ^ static_cast<uint32_t>(j)) & 1u, kStatusWaitP);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(1, sv, j > 0);
+                }
+                if (kKvWaitMid1 && k_next) {
+                    ok = wait_kv(j + 1);
+                    if (!ok) break;
+                }
+                if (act1) {
+                    if (j + 1 < w.n[1]) {
+                        issue_s(1, sk);
+                        if (leader) umma_commit(bar(L::BAR_SFULL + 1));
+                        if (j + 2 == w.n[1] && leader) umma_commit(bar(L::BAR_QEMPTY + 1));
+                    } else {
+                        if (leader) umma_commit(bar(L::BAR_OFULL + 1));
+                    }
+                }
+                if (leader) umma_commit(bar(L::BAR_KVEMPTY + sv));
+                if (k_next && leader) umma_commit(bar(L::BAR_KVEMPTY + sk));
+            }
+#pragma unroll
+            for (int t = 0; t < QT; ++t) {
+                sbits ^= static_cast<uint32_t>(w.n[t] & 1) << t;
+                qbits ^= static_cast<uint32_t>(w.n[t] > 0 ? 1 : 0) << t;
+            }
+        }
+        if (leader) umma_commit(bar(L::BAR_DRAIN));
+        wait_phase(bar(L::BAR_DRAIN), 0, p, abort_flag, kStatusWaitDrain, false);
+    }
+}
+
 // DUAL: split-KV with one query tile, both tiles on the same rows (see
 // tm_dual_control); the softmax groups then take their tile's own split.
-template <int D, bool F8, bool DUAL = false>
+template <int D, bool F8, bool DUAL = false, bool PERSIST = false>
 __device__ __forceinline__ void tm_forward(const FwdParams& p) {
-    using L = LayoutTM<D, F8>;
+    using L = LayoutTM<D, F8, PERSIST>;
     constexpr int QT = L::Q_TILES;
     constexpr int BN = L::BN;
     constexpr int ST = L::STAGES;
@@ -336,6 +589,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             mbar_init(bar(L::BAR_SFULL + t), 1);
             mbar_init(bar(L::BAR_PFULL + t), 4);  // one arrival per warp of the group
             mbar_init(bar(L::BAR_OFULL + t), 1);
+            mbar_init(bar(L::BAR_QEMPTY + t), 1);
         }
         mbar_init(bar(L::BAR_DRAIN), 1);
         *abort_flag = 0u;
@@ -361,7 +615,9 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
       if constexpr (L::REG_SPLIT) setmaxnreg_dec<L::CTRL_REGS>();
       // The work record is derived inside each role, after its register limit
       // is set, so that no role carries fields it does not use.
-      if constexpr (DUAL) {
+      if constexpr (PERSIST) {
+        tm_persist_control<D>(p, sbase, tmem, abort_flag, warp);
+      } else if constexpr (DUAL) {
         tm_dual_control<D, F8>(p, sbase, tmem, abort_flag, warp);
       } else {
       Work<QT> w;
@@ -602,12 +858,24 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
     } else {
         // ------------------------------------------------------------ softmax
         if constexpr (L::REG_SPLIT) setmaxnreg_inc<L::SOFTMAX_REGS>();
-        std::conditional_t<DUAL, WorkDual, Work<QT>> w;
-        if constexpr (DUAL) compute_work_dual<BN>(p, blockIdx.x, w);
-        else compute_work<QT, BN>(p, blockIdx.x, w);
         const int t = (warp - 4) >> 2;
         const int quarter = warp & 3;  // TMEM lane quarter this warp may access
         const int r = quarter * 32 + lane;
+        // Persistent CTAs walk their units (persist_unit); the phases of S_t
+        // and O_t carry over: s_phase counts the tile's earlier key steps,
+        // o_phase its earlier units with keys. A one-unit CTA runs the body once.
+        const int rounds = PERSIST ? static_cast<int>((p.total_units + gridDim.x - 1) / gridDim.x) : 1;
+        int s_phase = 0, o_phase = 0;
+        bool ok = true;
+        for (int k = 0; k < rounds && ok; ++k) {
+        long long lin = blockIdx.x;
+        if constexpr (PERSIST) {
+            lin = persist_unit(p, k);
+            if (lin < 0) continue;
+        }
+        std::conditional_t<DUAL, WorkDual, Work<QT>> w;
+        if constexpr (DUAL) compute_work_dual<BN>(p, lin, w);
+        else compute_work<QT, BN>(p, lin, w);
         const int q_row = w.q0 + (DUAL ? 0 : t * kBM) + r;
         // This tile's key split: the CTA's, or its own in a dual-range CTA.
         int kv_tile0_t, kv_end_t, split_t;
@@ -641,9 +909,8 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
         // bf16 P: the rounding error of each key tile's largest p, relative to m
         // like l. l + lc is the denominator of O (see RowOut).
         float lc = 0.f;
-        bool ok = true;
         for (int j = 0; j < n; ++j) {
-            ok = wait_phase(bar(L::BAR_SFULL + t), j & 1, p, abort_flag, kStatusWaitS);
+            ok = wait_phase(bar(L::BAR_SFULL + t), (s_phase + j) & 1, p, abort_flag, kStatusWaitS);
             // tcgen05.ld/st are warp-collective: the whole warp leaves together.
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
@@ -786,14 +1053,21 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
         }
 
         if (ok && n > 0) {
-            ok = wait_phase(bar(L::BAR_OFULL + t), 0, p, abort_flag, kStatusWaitO);
+            ok = wait_phase(bar(L::BAR_OFULL + t), o_phase & 1, p, abort_flag, kStatusWaitO);
             ok = __all_sync(0xffffffffu, ok);
             if (ok) tc_fence_after();
         }
         // A tile slot the CTA does not own (one tile per CTA, fa_fwd_rows) writes
         // nothing: its rows belong to another CTA.
-        if (!DUAL && t >= p.tiles_per_cta) ok = false;
-        if constexpr (F8) {
+        if (!DUAL && !PERSIST && t >= p.tiles_per_cta) ok = false;
+        if constexpr (PERSIST) {
+            // Plain mode, dense: bf16 O staged per warp in its own buffer.
+            if (ok && n > 0)
+                store_rows_tma_buf<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, l + lc, tO,
+                                      sbase + L::OST_OFF + t * L::OST_TILE_BYTES + quarter * L::OST_WARP_BYTES);
+            else if (ok)
+                write_row<D>(p, w.rm, w.bh, 0, q_row, n, m, m_true, l, l + lc, tO);
+        } else if constexpr (F8) {
             // Dense layouts only (the host rejects varlen). Plain mode: bf16
             // o_scale * O_t / l staged in the tile's own buffer and written with
             // TMA. Split mode: the partial state, O scaled by o_scale, per row.
@@ -811,6 +1085,16 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             } else if (ok && (!DUAL || split_t < p.num_splits)) {
                 write_row<D>(p, w.rm, w.bh, split_t, q_row, n, m, m_true, l, l + lc, tO);
             }
+        }
+        s_phase += n;
+        o_phase += n > 0 ? 1 : 0;
+        }  // units
+        // Persistent CTAs leave their last TMA stores' shared-memory reads for
+        // here (store_rows_tma_buf waits for a warp's earlier ones before it
+        // overwrites its buffer).
+        if constexpr (PERSIST) {
+            if (lane == 0) bulk_wait_group_read0();
+            __syncwarp();
         }
     }
 
@@ -834,6 +1118,14 @@ template <int D>
 __global__ void __launch_bounds__(LayoutTM<D, true>::THREADS, 1)
     fa_fwd_tm8_kernel(const __grid_constant__ FwdParams p) {
     tm_forward<D, true>(p);
+}
+
+// Persistent CTAs (bf16, plain mode, dense): grid min(units, SMs), each CTA
+// walking its units with persist_unit.
+template <int D>
+__global__ void __launch_bounds__(LayoutTM<D, false, true>::THREADS, 1)
+    fa_fwd_tmp_kernel(const __grid_constant__ FwdParams p) {
+    tm_forward<D, false, false, true>(p);
 }
 
 // Dual-range split-KV CTAs (one query tile), bf16 and e4m3 inputs.

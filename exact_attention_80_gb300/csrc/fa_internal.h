@@ -60,6 +60,7 @@ struct FwdParams {
     int kv_tiles_per_split;  // ceil(ceil(Nk/BN) / num_splits)
     int head_group;          // heads per scheduling group (CTA order)
     int dual;                // 1: dual-range split CTAs (split mode, Nq <= 128, d <= 128)
+    long long total_units;   // persistent launches: work units in the launch (CTAs walk them)
     float scale_log2;        // scale * log2(e) (8-bit inputs: times the Q and K descales)
     float o_scale;           // 8-bit inputs: the V descale, applied to O at the end
     long long wait_limit;    // cycles
@@ -80,6 +81,9 @@ FwdConfig fwd_config(int d);
 
 cudaError_t launch_fwd_d64(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FwdParams& p, unsigned grid, cudaStream_t stream);
+// Persistent two-tile kernels (plain mode, dense bf16): grid min(units, SMs).
+cudaError_t launch_fwd_d64_persist(const FwdParams& p, unsigned grid, cudaStream_t stream);
+cudaError_t launch_fwd_d128_persist(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d256(const FwdParams& p, unsigned grid, cudaStream_t stream);
 // e4m3 Q, K, V (tm_q/tm_k/tm_v are byte maps, box {128, rows, 1}, or {64,
 // rows, 1} with the 64-byte swizzle at d = 64); d = 64, 128, 256.

@@ -75,10 +75,15 @@ typedef enum {
  * fa_fwd — fused attention forward, one launch.
  *   q    [B][H][Nq][d] bf16 (read)        k, v [B][H][Nk][d] bf16 (read)
  *   o    [B][H][Nq][d] bf16 (written)     lse  [B][H][Nq] fp32 (written)
- * Work partition: each CTA owns query tiles of one (b, h) and sweeps all keys
- * it needs ("AI 大模型之 FlashAttention_02", section "从头级并行转向序列级并行":
- * query tiles of one head go to different CTAs, no cross-CTA reduction).
- * Causal tiles that lie wholly above the diagonal are skipped.
+ * Work partition: each work unit is the query tiles of one (b, h) that one CTA
+ * owns, swept over all keys they need ("AI 大模型之 FlashAttention_02", section
+ * "从头级并行转向序列级并行": query tiles of one head go to different CTAs, no
+ * cross-CTA reduction). Causal tiles that lie wholly above the diagonal are
+ * skipped. One CTA per unit, except at d = 64 and 128 when the units fill at
+ * least four waves of CTAs (four per SM): then one persistent CTA per SM walks
+ * its share of the units in order, so that a unit's Q load and start-up
+ * overlap the previous unit's last key steps. The result is the same bit for
+ * bit either way.
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int H, int Nq, int Nk, int d, float scale, int causal,
@@ -245,8 +250,10 @@ fa_status fa_fwd_rows(const void* q, const void* k, const void* v, void* o, floa
                       cudaStream_t stream);
 
 /*
- * fa_fwd_grid_ctas — number of CTAs fa_fwd (num_splits = 1) or
- * fa_fwd_splitkv would launch for this shape: B * H * ceil(Nq / BM) * num_splits,
+ * fa_fwd_grid_ctas — number of work units (CTAs of one unit each) fa_fwd
+ * (num_splits = 1) or fa_fwd_splitkv would run for this shape (fa_fwd launches
+ * one persistent CTA per SM instead when the units fill four waves, see
+ * fa_fwd): B * H * ceil(Nq / BM) * num_splits,
  * BM = 256 query rows per CTA for d <= 128 (two 128-row tiles) and 128 for
  * d = 256 ("AI 大模型之 FlashAttention_02", section "从头级并行转向序列级并行" and
  * the printed CTA counts of section "本册配套实验验证记录"). Split-KV launches

@@ -489,6 +489,24 @@ def whole_tensor_check(pool, c, inputs, splits=(1,), rows_per_cta=None):
     return {S: checks[S].finish(B * H) for S in splits}
 
 
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("causal", [False, True, "bottom_right"])
+def test_persistent_ctas_ragged(head_pool, d, causal):
+    """More query units than four waves of CTAs (B=2, H=160, Nq=300, Nk=333:
+    640 units of 256 rows, each head's last tile ragged), so fa_fwd runs
+    persistent CTAs that walk several units each: every head against the
+    oracle, and bit for bit the output of one unit per CTA (fa_fwd_rows with
+    256 rows)."""
+    B, H, Nq, Nk = 2, 160, 300, 333
+    c = dict(B=B, H=H, Nq=Nq, Nk=Nk, d=d, causal=causal, name="persistent")
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 7100 + d)
+    whole_tensor_check(head_pool, c, (q, k, v))
+    scale = f32(1.0 / math.sqrt(d))
+    o1, l1 = run_gpu(q, k, v, causal, scale)
+    o2, l2 = run_gpu_rows(q, k, v, causal, scale, 256)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 @pytest.mark.parametrize("name", ["c1", "c2", "c2_causal", "c3", "c3_causal", "c4"])
 def test_full_size_whole_tensor(head_pool, name):
     """Whole O and LSE of each benchmark workload against the oracle (C4 with its
