@@ -203,6 +203,30 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
     }
 }
 
+// wait_phase for a whole warp that waits together: every lane polls, and the
+// loop's exits are warp votes, so the warp runs it as one (no divergent exits
+// to reconverge from). True once every lane has seen the phase complete; false
+// as wait_phase returns false (abort raised elsewhere, or this warp's wait ran
+// past the limit, which raises it).
+__device__ __forceinline__ bool wait_phase_warp(uint32_t bar, uint32_t parity, const FwdParams& p,
+                                                volatile uint32_t* abort_flag, unsigned what,
+                                                bool honor_abort = true) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    const long long start = clock64();
+    while (true) {
+        if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+        if (honor_abort && __any_sync(0xffffffffu, *abort_flag != 0u)) return false;
+        if (__any_sync(0xffffffffu, clock64() - start > p.wait_limit)) {
+            if ((threadIdx.x & 31) == 0) {
+                *abort_flag = 1u;
+                atomicOr(p.status, what);
+            }
+            __syncwarp();
+            return false;
+        }
+    }
+}
+
 // One query row's output, written 32 fp32 columns at a time from the final
 // accumulator row: normalised O (bf16) and LSE in plain mode, or the
 // unnormalised partial state (O, m, l) in split mode. Deferred normalisation:

@@ -910,9 +910,8 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
         // like l. l + lc is the denominator of O (see RowOut).
         float lc = 0.f;
         for (int j = 0; j < n; ++j) {
-            ok = wait_phase(bar(L::BAR_SFULL + t), (s_phase + j) & 1, p, abort_flag, kStatusWaitS);
             // tcgen05.ld/st are warp-collective: the whole warp leaves together.
-            ok = __all_sync(0xffffffffu, ok);
+            ok = wait_phase_warp(bar(L::BAR_SFULL + t), (s_phase + j) & 1, p, abort_flag, kStatusWaitS);
             if (!ok) break;
             tc_fence_after();
 
@@ -1053,8 +1052,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
         }
 
         if (ok && n > 0) {
-            ok = wait_phase(bar(L::BAR_OFULL + t), o_phase & 1, p, abort_flag, kStatusWaitO);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = wait_phase_warp(bar(L::BAR_OFULL + t), o_phase & 1, p, abort_flag, kStatusWaitO);
             if (ok) tc_fence_after();
         }
         // A tile slot the CTA does not own (one tile per CTA, fa_fwd_rows) writes
