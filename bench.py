@@ -374,6 +374,7 @@ def extra_workloads(device, stream, reps: int = 20):
     out["c5_fp8"] = fp8_decode_workload(device, stream, reps)
     out["c2_bwd"] = bwd_workload(device, stream, reps)
     out["c2_bwd_d64"] = bwd_workload(device, stream, reps, d=64)
+    out["bwd_d256"] = bwd_workload(device, stream, reps, d=256, shape=(2, 16, 4096))
     return out
 
 
@@ -410,17 +411,17 @@ def tile_sweep(device, stream, reps):
     return res
 
 
-def bwd_workload(device, stream, reps, d=128):
-    """The backward (fa_bwd) on the C2 shape (B=8, H=32, N=2048) at head dim d
-    (128, or 64), both masks, on seeded device-side N(0,1) bf16 inputs and
-    upstream gradient; FLOPs 2.5x the forward's metric (five GEMMs against two).
-    The three launches of one call are timed together."""
+def bwd_workload(device, stream, reps, d=128, shape=(8, 32, 2048)):
+    """The backward (fa_bwd) on a (B, H, N) shape (default the C2 one) at head
+    dim d, both masks, on seeded device-side N(0,1) bf16 inputs and upstream
+    gradient; FLOPs 2.5x the forward's metric (five GEMMs against two). The
+    three launches of one call are timed together."""
     import torch
 
     import exact_attention_80_gb300 as fa
     from exact_attention_80_gb300.inputs import metric_flops
 
-    B, H, N = 8, 32, 2048
+    B, H, N = shape
     gen = torch.Generator(device=device).manual_seed(1010)
     q, k, v, do = (torch.randn((B, H, N, d), generator=gen, device=device).to(torch.bfloat16)
                    for _ in range(4))

@@ -1,4 +1,4 @@
-// fa_bwd.cu — attention backward for head dims 64 and 128: dQ, dK, dV. Holds the
+// fa_bwd.cu — attention backward for head dims 64, 128 and 256: dQ, dK, dV. Holds the
 // backward's kernels and its C entry points (fa_bwd_workspace_bytes, fa_bwd).
 //
 // What is computed (the plain definition of the forward differentiated; the
@@ -47,6 +47,15 @@
 // operand, K read MN-major, has a second 64-dim chunk of zeros that the CTA
 // writes once, so lanes 64-127 of dQ^T are zero and only the readout warps of
 // lanes 0-63 take it out.
+//
+// Head dim 256: dV and dK of 128 keys at d = 256 would take all 512 TMEM
+// columns, so each key tile has two CTAs, one per 128-column half of the head
+// dim. Both compute the whole S^T and dP^T (the contraction runs over all 256
+// columns); each accumulates its half of dV and dK in TMEM and adds its half
+// of dQ. K and V stay resident (64 KB each), which leaves shared memory for one
+// Q/dO stage: the issuer then runs the steps one after another (S^T and dP^T
+// of step h + 1 once step h's dV and dK have read the stage and its load has
+// landed) instead of in pairs.
 #include <cuda_bf16.h>
 
 #include <cstring>
@@ -82,24 +91,27 @@ namespace {
 
 constexpr int kBwdKeys = 128;   // keys per CTA (TMEM lanes of S^T, dP^T, dV, dK)
 constexpr int kBwdHalf = 64;    // queries per step
-constexpr int kBwdStages = 3;   // Q/dO (+ -LSE log2e, -D) ring slots
 constexpr float kLog2e = 1.4426950408889634f;
 
 template <int D>
 struct LayoutBwd {
-    static_assert(D == 64 || D == 128, "head dim 64 or 128");
+    static_assert(D == 64 || D == 128 || D == 256, "head dim 64, 128 or 256");
+    static constexpr int DH = D < 128 ? D : 128;        // head-dim columns of dV, dK, dQ a CTA owns
+    static constexpr int HALVES = D / DH;               // CTAs per key tile
+    static constexpr int STAGES = D == 256 ? 1 : 3;     // Q/dO (+ -LSE log2e, -D) ring slots
     // warp 0 producer, warp 1 issuer, warps 2-3 idle, warps 4-11 compute (two
     // per TMEM lane quarter, one per 32-query chunk of a step), warps 12-15
     // dQ readout (one per lane quarter; at D = 64 the first two only).
     static constexpr int COMPUTE_WARPS = 8;
     static constexpr int READOUT_WARPS = 4;
-    static constexpr int READOUT_ACTIVE = D / 32;                   // lane quarters holding dQ^T
+    static constexpr int READOUT_ACTIVE = DH / 32;                  // lane quarters holding dQ^T
     static constexpr int CHUNKS = D / 64;                           // 64-column chunks of a row
+    static constexpr int DH_CHUNKS = DH / 64;                       // chunks of the CTA's head-dim part
     static constexpr int THREADS = 128 + 32 * (COMPUTE_WARPS + READOUT_WARPS);
     static constexpr uint32_t KV_CHUNK = kBwdKeys * 128;            // 16 KB: 64 columns of K or V
-    // K always spans two chunks: dQ^T reads it as an M = 128 operand, and at
+    // K spans at least two chunks: dQ^T reads it as an M = 128 operand, and at
     // D = 64 the second chunk is zeros.
-    static constexpr uint32_t K_BYTES = 2 * KV_CHUNK;
+    static constexpr uint32_t K_BYTES = (CHUNKS < 2 ? 2 : CHUNKS) * KV_CHUNK;
     static constexpr uint32_t V_BYTES = CHUNKS * KV_CHUNK;
     static constexpr uint32_t QH_CHUNK = kBwdHalf * 128;            // 8 KB: 64 columns of a step's Q or dO
     static constexpr uint32_t QH_BYTES = CHUNKS * QH_CHUNK;
@@ -112,16 +124,16 @@ struct LayoutBwd {
     static constexpr uint32_t V_OFF = K_OFF + K_BYTES;
     static constexpr uint32_t STAGE_OFF = V_OFF + V_BYTES;           // [stage]: Q, dO
     static constexpr uint32_t Q_IN = 0, DO_IN = QH_BYTES;
-    static constexpr uint32_t DS_OFF = STAGE_OFF + kBwdStages * STAGE_BYTES;  // [buffer]
+    static constexpr uint32_t DS_OFF = STAGE_OFF + STAGES * STAGE_BYTES;  // [buffer]
     static constexpr uint32_t ROWS_OFF = DS_OFF + 2 * DS_BYTES;     // [stage]: -LSE log2e, -D
     static constexpr uint32_t NL_IN = 0, ND_IN = ROWS_BYTES;
-    static constexpr uint32_t BAR_OFF = ROWS_OFF + kBwdStages * 2 * ROWS_BYTES;
+    static constexpr uint32_t BAR_OFF = ROWS_OFF + STAGES * 2 * ROWS_BYTES;
     static_assert(STAGE_OFF % 1024 == 0 && STAGE_BYTES % 1024 == 0 && QH_CHUNK % 1024 == 0 &&
                       DS_OFF % 1024 == 0 && DS_BYTES % 1024 == 0, "swizzle atoms must be 1024-aligned");
     static constexpr int BAR_KV = 0;
     static constexpr int BAR_QFULL = 1;                    // [stage]
-    static constexpr int BAR_QEMPTY = BAR_QFULL + kBwdStages;   // [stage]
-    static constexpr int BAR_SFULL = BAR_QEMPTY + kBwdStages;   // [buffer] S^T, dP^T done
+    static constexpr int BAR_QEMPTY = BAR_QFULL + STAGES;   // [stage]
+    static constexpr int BAR_SFULL = BAR_QEMPTY + STAGES;   // [buffer] S^T, dP^T done
     static constexpr int BAR_PREADY = BAR_SFULL + 2;    // [buffer] P^T, dS^T written (one arrival per compute warp)
     static constexpr int BAR_DQFULL = BAR_PREADY + 2;   // [buffer] dQ^T done (and every earlier MMA)
     static constexpr int BAR_DQREAD = BAR_DQFULL + 2;   // [buffer] dQ^T read (one arrival per readout warp)
@@ -232,8 +244,11 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const int bh = blockIdx.x / p.k_tiles;
-    const int kt = blockIdx.x % p.k_tiles;
+    // CTA = (head, key tile, head-dim part), the part fastest.
+    const int hd = static_cast<int>(blockIdx.x % L::HALVES);
+    const int tile_lin = static_cast<int>(blockIdx.x / L::HALVES);
+    const int bh = tile_lin / p.k_tiles;
+    const int kt = tile_lin % p.k_tiles;
     const int k0 = kt * kBwdKeys;
     int h0, n;
     bwd_steps(p, kt, h0, n);
@@ -241,7 +256,7 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::BAR_KV), 1);
-        for (int st = 0; st < kBwdStages; ++st) {
+        for (int st = 0; st < L::STAGES; ++st) {
             mbar_init(bar(L::BAR_QFULL + st), 1);
             mbar_init(bar(L::BAR_QEMPTY + st), 1);
         }
@@ -292,9 +307,9 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
         bool ok = true;
         int issued = 0;
         for (int h = 0; h < n && ok; ++h) {
-            const int st = h % kBwdStages;
-            if (h >= kBwdStages)
-                ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_QEMPTY + st), ((h / kBwdStages) - 1) & 1, p,
+            const int st = h % L::STAGES;
+            if (h >= L::STAGES)
+                ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_QEMPTY + st), ((h / L::STAGES) - 1) & 1, p,
                                                       abort_flag, kStatusWaitKvEmpty));
             if (!ok) break;
             if (leader) {
@@ -314,13 +329,13 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
         if (ok) {
             // The issuer's last slot releases: no commit arrival may still be in
             // flight when the CTA exits.
-            for (int h = max(0, n - kBwdStages); h < n && ok; ++h)
-                ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_QEMPTY + h % kBwdStages), (h / kBwdStages) & 1, p,
+            for (int h = max(0, n - L::STAGES); h < n && ok; ++h)
+                ok = __all_sync(0xffffffffu, bwd_wait(bar(L::BAR_QEMPTY + h % L::STAGES), (h / L::STAGES) & 1, p,
                                                       abort_flag, kStatusWaitKvEmpty));
         } else {
             bwd_wait(bar(L::BAR_KV), 0, p, abort_flag, kStatusWaitDrain, false);
-            for (int h = max(0, issued - kBwdStages); h < issued; ++h)
-                bwd_wait(bar(L::BAR_QFULL + h % kBwdStages), (h / kBwdStages) & 1, p, abort_flag,
+            for (int h = max(0, issued - L::STAGES); h < issued; ++h)
+                bwd_wait(bar(L::BAR_QFULL + h % L::STAGES), (h / L::STAGES) & 1, p, abort_flag,
                          kStatusWaitDrain, false);
         }
     } else if (warp == 1 && n > 0) {
@@ -330,7 +345,7 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
             return __all_sync(0xffffffffu, bwd_wait(b, parity, p, abort_flag, what));
         };
         constexpr uint32_t IDESC_S = make_idesc_bf16(128, kBwdHalf, false, false);  // S^T, dP^T
-        constexpr uint32_t IDESC_ACC = make_idesc_bf16(128, D, false, true);        // dV, dK
+        constexpr uint32_t IDESC_ACC = make_idesc_bf16(128, L::DH, false, true);    // dV, dK (this CTA's part)
         constexpr uint32_t IDESC_DQ = make_idesc_bf16(128, kBwdHalf, true, true);   // dQ^T
         // K-major operands (8-row groups 1024 bytes apart); MN-major ones with
         // their 64-element chunks KV_CHUNK (K as A of dQ^T) or QH_CHUNK (Q, dO
@@ -347,8 +362,8 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
         // S^T_h = K Q_h^T and dP^T_h = V dO_h^T into buffer h & 1 (lanes = keys,
         // 64 query columns each), reading ring slot h % 3.
         auto issue_sdp = [&](int h) -> bool {
-            const int st = h % kBwdStages;
-            if (!wait_all(bar(L::BAR_QFULL + st), (h / kBwdStages) & 1, kStatusWaitQ)) return false;
+            const int st = h % L::STAGES;
+            if (!wait_all(bar(L::BAR_QFULL + st), (h / L::STAGES) & 1, kStatusWaitQ)) return false;
             tc_fence_after();
             const uint32_t sb = L::STAGE_OFF + st * L::STAGE_BYTES;
             const uint32_t col = L::BUF_COL(h & 1);
@@ -378,8 +393,9 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
             const int b = h & 1;
             if (!wait_all(bar(L::BAR_PREADY + b), (h >> 1) & 1, kStatusWaitP)) return false;
             tc_fence_after();
-            const int st = h % kBwdStages;
-            const uint32_t sb = L::STAGE_OFF + st * L::STAGE_BYTES;
+            const int st = h % L::STAGES;
+            // B of dV and dK: this CTA's head-dim part of dO_h and Q_h.
+            const uint32_t sb = L::STAGE_OFF + st * L::STAGE_BYTES + hd * L::DH_CHUNKS * L::QH_CHUNK;
             const uint32_t col = L::BUF_COL(b);
 #pragma unroll
             for (int kk = 0; kk < kBwdHalf / 16; ++kk) {
@@ -396,7 +412,8 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
             const uint32_t dsb = L::DS_OFF + b * L::DS_BYTES;
 #pragma unroll
             for (int kk = 0; kk < kBwdKeys / 16; ++kk) {
-                const uint64_t a = desc(kmn_lo, kmn_hi, L::K_OFF + kk * 2048);
+                // A: this CTA's head-dim part of K (M = 128 head dims).
+                const uint64_t a = desc(kmn_lo, kmn_hi, L::K_OFF + hd * L::DH_CHUNKS * L::KV_CHUNK + kk * 2048);
                 const uint64_t bds = desc(qmn_lo, qmn_hi, dsb + kk * 2048);
                 if (leader) umma_ss(tmem + col, a, bds, IDESC_DQ, kk > 0 ? 1u : 0u);
             }
@@ -404,18 +421,35 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
             return true;
         };
         bool ok = wait_all(bar(L::BAR_KV), 0, kStatusWaitKvFull);
-        if (ok) ok = issue_sdp(0);
-        if (ok && n > 1) ok = issue_sdp(1);
-        for (int a = 0; a < n && ok; a += 2) {
-            ok = issue_vkq(a, a == 0);
-            if (ok && a + 1 < n) ok = issue_vkq(a + 1, false);
-            // The next pair's S^T and dP^T, each once the readout group has taken
-            // the dQ^T of two steps back out of its buffer.
-            for (int h = a + 2; h < a + 4 && h < n && ok; ++h) {
-                ok = wait_all(bar(L::BAR_DQREAD + (h & 1)), ((h - 2) >> 1) & 1, kStatusWaitO);
-                if (ok) {
-                    tc_fence_after();
-                    ok = issue_sdp(h);
+        if constexpr (L::STAGES >= 3) {
+            if (ok) ok = issue_sdp(0);
+            if (ok && n > 1) ok = issue_sdp(1);
+            for (int a = 0; a < n && ok; a += 2) {
+                ok = issue_vkq(a, a == 0);
+                if (ok && a + 1 < n) ok = issue_vkq(a + 1, false);
+                // The next pair's S^T and dP^T, each once the readout group has
+                // taken the dQ^T of two steps back out of its buffer.
+                for (int h = a + 2; h < a + 4 && h < n && ok; ++h) {
+                    ok = wait_all(bar(L::BAR_DQREAD + (h & 1)), ((h - 2) >> 1) & 1, kStatusWaitO);
+                    if (ok) {
+                        tc_fence_after();
+                        ok = issue_sdp(h);
+                    }
+                }
+            }
+        } else {
+            // One stage: step h + 1's Q and dO load once step h's dV and dK MMAs
+            // have read the stage, so its S^T and dP^T follow step h's MMAs.
+            if (ok) ok = issue_sdp(0);
+            for (int h = 0; h < n && ok; ++h) {
+                ok = issue_vkq(h, h == 0);
+                if (ok && h + 1 < n) {
+                    if (h >= 1)
+                        ok = wait_all(bar(L::BAR_DQREAD + ((h + 1) & 1)), ((h - 1) >> 1) & 1, kStatusWaitO);
+                    if (ok) {
+                        tc_fence_after();
+                        ok = issue_sdp(h + 1);
+                    }
                 }
             }
         }
@@ -450,7 +484,7 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
             tmem_wait_ld();
             // The slot's -LSE log2e and -D for this chunk's 32 queries (the S^T
             // commit implies the slot's loads landed: the issuer waited for them).
-            const uint32_t rb = sbase + L::ROWS_OFF + (h % kBwdStages) * 2 * L::ROWS_BYTES;
+            const uint32_t rb = sbase + L::ROWS_OFF + (h % L::STAGES) * 2 * L::ROWS_BYTES;
             const uint32_t nl = rb + L::NL_IN + 128 * g;
             const uint32_t nd = rb + L::ND_IN + 128 * g;
             uint32_t pk[16], dk[16];
@@ -480,7 +514,8 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::BAR_PREADY + b));
         }
-        // dK (scaled) and dV of this key row, head-dim columns D/2 g .. D/2 g + D/2 - 1,
+        // dK (scaled) and dV of this key row, columns DH/2 g .. DH/2 g + DH/2 - 1 of
+        // the CTA's head-dim part,
         // once every MMA has finished (the last dQ^T commit covers them all);
         // zero when no query step sees the key tile. tcgen05.ld is
         // warp-collective: the loads run for the whole warp (`ok` is
@@ -491,11 +526,14 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
             if (ok) tc_fence_after();
         }
         if (ok) {
-            __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(p.dk) + (static_cast<size_t>(bh) * p.Nk + key) * D;
-            __nv_bfloat16* dvp = static_cast<__nv_bfloat16*>(p.dv) + (static_cast<size_t>(bh) * p.Nk + key) * D;
+            // This CTA's head-dim part of the key row's dK and dV.
+            __nv_bfloat16* dkp =
+                static_cast<__nv_bfloat16*>(p.dk) + (static_cast<size_t>(bh) * p.Nk + key) * D + hd * L::DH;
+            __nv_bfloat16* dvp =
+                static_cast<__nv_bfloat16*>(p.dv) + (static_cast<size_t>(bh) * p.Nk + key) * D + hd * L::DH;
 #pragma unroll 1
-            for (int j = 0; j < L::CHUNKS; ++j) {
-                const int cc = L::CHUNKS * g + j;
+            for (int j = 0; j < L::DH_CHUNKS; ++j) {
+                const int cc = L::DH_CHUNKS * g + j;
                 uint32_t kr[32], vr[32];
                 if (n > 0) {
                     tmem_ld32(tmem + lane_field + L::DK_COL + cc * 32, kr);
@@ -545,7 +583,7 @@ __global__ void __launch_bounds__(LayoutBwd<D>::THREADS, 1) fa_bwd_kernel(const 
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(L::BAR_DQREAD + b));
-            float* dst = p.dq_acc + (row0 + static_cast<size_t>(h0 + h) * kBwdHalf) * D + r;
+            float* dst = p.dq_acc + (row0 + static_cast<size_t>(h0 + h) * kBwdHalf) * D + hd * L::DH + r;
 #pragma unroll
             for (int e = 0; e < 32; ++e) atomicAdd(dst + e * D, __uint_as_float(lo[e]));
 #pragma unroll
@@ -597,10 +635,12 @@ __global__ void __launch_bounds__(256) fa_bwd_pre_kernel(const __nv_bfloat16* __
         nlse2[row] = nl;
     }
     float* z = dq_acc + static_cast<size_t>(row) * D + lane * (D / 32);
-    if constexpr (D == 128)
-        *reinterpret_cast<float4*>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
-    else
+    if constexpr (D >= 128) {
+#pragma unroll
+        for (int e = 0; e < D / 128; ++e) reinterpret_cast<float4*>(z)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
         *reinterpret_cast<float2*>(z) = make_float2(0.f, 0.f);
+    }
 }
 
 // dQ = scale * accumulator, to bf16: one warp per query row, D / 32 columns
@@ -616,14 +656,17 @@ __global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict_
     const long long arow = bh * Nq_pad + (row - bh * Nq);
     const float* src = acc + static_cast<size_t>(arow) * D + lane * (D / 32);
     __nv_bfloat16* dst = dq + static_cast<size_t>(row) * D + lane * (D / 32);
-    if constexpr (D == 128) {
-        const float4 a = *reinterpret_cast<const float4*>(src);
-        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
-        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
-        uint2 out;
-        out.x = *reinterpret_cast<uint32_t*>(&lo);
-        out.y = *reinterpret_cast<uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(dst) = out;
+    if constexpr (D >= 128) {
+#pragma unroll
+        for (int e = 0; e < D / 128; ++e) {
+            const float4 a = reinterpret_cast<const float4*>(src)[e];
+            __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * scale, a.y * scale);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * scale, a.w * scale);
+            uint2 out;
+            out.x = *reinterpret_cast<uint32_t*>(&lo);
+            out.y = *reinterpret_cast<uint32_t*>(&hi);
+            reinterpret_cast<uint2*>(dst)[e] = out;
+        }
     } else {
         const float2 a = *reinterpret_cast<const float2*>(src);
         *reinterpret_cast<__nv_bfloat162*>(dst) = __floats2bfloat162_rn(a.x * scale, a.y * scale);
@@ -656,7 +699,7 @@ cudaError_t launch_bwd_main(const BwdParams& p, cudaStream_t stream) {
                                     static_cast<int>(L::ALLOC_BYTES));
     });
     if (e != cudaSuccess) return e;
-    const long long ctas = static_cast<long long>(p.BH) * p.k_tiles;
+    const long long ctas = static_cast<long long>(p.BH) * p.k_tiles * L::HALVES;
     if (ctas < 1 || ctas > 0x7fffffffll) return cudaErrorInvalidConfiguration;
     fa_bwd_kernel<D><<<static_cast<unsigned>(ctas), L::THREADS, L::ALLOC_BYTES, stream>>>(p);
     return cudaGetLastError();
@@ -689,7 +732,7 @@ cudaError_t launch_bwd(const BwdParams& p, const void* o, const void* dout, cons
 extern "C" {
 
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d) {
-    if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128)) return 0;
+    if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128 && d != 256)) return 0;
     const size_t rows_pad = static_cast<size_t>(B) * H * ((static_cast<size_t>(Nq) + 127) / 128 * 128);
     return rows_pad * (static_cast<size_t>(d) + 2) * sizeof(float);
 }
@@ -702,7 +745,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     // Query rows are padded to whole 128-row tiles and key tiles counted in
     // int: both lengths must leave room for that rounding.
     if (Nq > 0x7fffffff - 127 || Nk > 0x7fffffff - 127) return FA_ERR_SHAPE;
-    if (d != 64 && d != 128) return FA_ERR_HEADDIM;
+    if (d != 64 && d != 128 && d != 256) return FA_ERR_HEADDIM;
     if (!fa::valid_causal(causal)) return FA_ERR_CAUSAL;
     if (!o || !dout || !lse || !dq || !dk || !dv) return FA_ERR_NULL;
     if (!fa::aligned(o, 16) || !fa::aligned(dout, 16) || !fa::aligned(lse, 4) ||
@@ -738,8 +781,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.scale_log2 = scale * 1.4426950408889634f;
     p.wait_limit = fa::kDefaultWaitLimit;
     if (fa::device_status_ptr(&p.status) != cudaSuccess) return FA_ERR_CUDA;
-    const cudaError_t e = d == 64 ? fa::launch_bwd<64>(p, o, dout, lse, dq, stream)
-                                  : fa::launch_bwd<128>(p, o, dout, lse, dq, stream);
+    const cudaError_t e = d == 64    ? fa::launch_bwd<64>(p, o, dout, lse, dq, stream)
+                          : d == 128 ? fa::launch_bwd<128>(p, o, dout, lse, dq, stream)
+                                     : fa::launch_bwd<256>(p, o, dout, lse, dq, stream);
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 

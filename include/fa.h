@@ -203,7 +203,7 @@ fa_status fa_fwd_fp8_splitkv(const void* q, const void* k, const void* v, float 
  * fa_bwd_workspace_bytes — bytes of the fp32 workspace fa_bwd needs, with the
  * query rows of each head padded to Nq_pad = 128 * ceil(Nq / 128): a dQ
  * accumulator [B][H][Nq_pad][d], then -LSE log2(e) and -D, each
- * [B][H][Nq_pad]. 0 when an argument is out of range (d must be 64 or 128).
+ * [B][H][Nq_pad]. 0 when an argument is out of range (d must be 64, 128 or 256).
  */
 size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d);
 
@@ -223,8 +223,9 @@ size_t fa_bwd_workspace_bytes(int B, int H, int Nq, int d);
  * fp32 dQ accumulator; the main launch runs one CTA per (head, 128-key tile),
  * which accumulates its keys' dK and dV over all query tiles in fp32 and adds
  * its dS K to the dQ accumulator (fp32 atomic adds, across key tiles); a last
- * launch writes dQ = scale times the accumulator in bf16. d = 64 or 128 (else
- * FA_ERR_HEADDIM); causal as fa_fwd.
+ * launch writes dQ = scale times the accumulator in bf16. d = 64, 128 or 256
+ * (else FA_ERR_HEADDIM; at 256 each key tile takes two CTAs, one per half of
+ * the head dim); causal as fa_fwd.
  * Three launches on `stream`, no synchronisation.
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,

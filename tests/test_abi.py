@@ -166,7 +166,7 @@ def test_fp8_splitkv_rejects(lib, kw, code):
 @pytest.mark.parametrize("kw,code", [
     (dict(q=0), 1), (dict(o=0), 1), (dict(do=0), 1), (dict(lse=0), 1), (dict(dq=0), 1),
     (dict(dk=0), 1), (dict(dv=0), 1), (dict(ws=0), 6), (dict(ws=FAKE + 4), 6),
-    (dict(d=96), 4), (dict(d=256), 4), (dict(Nq=0), 3), (dict(scale=0.0), 9), (dict(causal=3), 11),
+    (dict(d=96), 4), (dict(d=512), 4), (dict(Nq=0), 3), (dict(scale=0.0), 9), (dict(causal=3), 11),
     (dict(dq=FAKE + 8), 2), (dict(o=FAKE + 2), 2), (dict(lse=FAKE + 2), 2),
     (dict(Nq=2**31 - 100), 3), (dict(Nk=2**31 - 100), 3),  # no room to round up to 128-row tiles
 ])
@@ -180,7 +180,8 @@ def test_bwd_rejects(lib, kw, code):
     assert fa.fa_bwd_workspace_bytes(2, 3, 77, 128) == 2 * 3 * 128 * 130 * 4
     assert fa.fa_bwd_workspace_bytes(1, 1, 129, 128) == 256 * 130 * 4
     assert fa.fa_bwd_workspace_bytes(2, 3, 77, 64) == 2 * 3 * 128 * 66 * 4
-    assert fa.fa_bwd_workspace_bytes(2, 3, 77, 256) == 0
+    assert fa.fa_bwd_workspace_bytes(2, 3, 77, 256) == 2 * 3 * 128 * 258 * 4
+    assert fa.fa_bwd_workspace_bytes(2, 3, 77, 96) == 0
 
 
 def test_workspace_bytes(lib):

@@ -66,7 +66,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("B,H,Nq,Nk,causal", CASES)
 def test_backward_parity(B, H, Nq, Nk, causal, d):
     got, ref = run_bwd(B, H, Nq, Nk, causal, 8100 + Nq + Nk + d, d)
@@ -74,7 +74,7 @@ def test_backward_parity(B, H, Nq, Nk, causal, d):
         check_grad(g, r, f"{name} B{B} H{H} Nq{Nq} Nk{Nk} {causal} d{d}")
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_backward_negative_scores_key_tail(d):
     """Every score near -200 (Q along u, K against it): LSE is about -190, so an
     unmasked missing key of the ragged last key tile (its S reads 0) would give
@@ -145,3 +145,30 @@ def test_backward_full_size_every_head(head_pool, causal, d):
             check_grad(g[i], r, f"{name} head {i} causal={causal}")
         seen += 1
     assert seen == B * H
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_d256_sampled_heads(head_pool, causal):
+    """Head dim 256 at the bench's shape (B=2, H=16, N=4096): two CTAs per key
+    tile, one per half of the head dim, and one Q/dO stage. dQ, dK and dV of
+    three heads spread over the grid against the oracle."""
+    B, H, N, d = 2, 16, 4096, 256
+    q, k, v = make_qkv(B, H, N, N, d, 8401)
+    do = make_grad_output(B, H, N, d, 8402)
+    scale = f32(1.0 / math.sqrt(d))
+    qc, kc, vc, doc = q.cuda(), k.cuda(), v.cuda(), do.cuda()
+    o, lse = fa.attention(qc, kc, vc, causal=causal, scale=scale)
+    dq, dk, dv = fa.attention_backward(qc, kc, vc, o, lse, doc, causal=causal, scale=scale)
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(clear=True) == fa.FA_OK
+    got = [t.reshape(B * H, N, d).cpu() for t in (dq, dk, dv)]
+    qh, kh, vh, doh = (t.reshape(B * H, N, d) for t in (q, k, v, do))
+    heads = (0, 17, B * H - 1)
+    tasks = ((i, qh[i].float().numpy(), kh[i].float().numpy(), vh[i].float().numpy(),
+              doh[i].float().numpy(), scale, causal) for i in heads)
+    seen = 0
+    for i, *ref in head_pool.backward_heads(tasks):
+        for g, r, name in zip(got, ref, ("dq", "dk", "dv")):
+            check_grad(g[i], r, f"d256 {name} head {i} causal={causal}")
+        seen += 1
+    assert seen == len(heads)
