@@ -41,12 +41,20 @@ def test_hook_rejects_unbounded_or_tiny_limits():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("d", [128, 256])
-def test_bounded_wait_times_out_and_context_survives(d):
+@pytest.mark.parametrize("d,persistent", [(128, False), (256, False), (128, True), (64, True)])
+def test_bounded_wait_times_out_and_context_survives(d, persistent):
+    """persistent: enough query units (four per SM) that the launch runs
+    persistent CTAs, whose control warps carry the ring across units; their
+    abort path is the one exercised."""
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA device")
     fn = _hook()
     B, H, Nq, Nk = 1, 2, 256, 300
+    if persistent:
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        Nq = 300                      # two 256-row units per head, the second ragged
+        H = 2 * sms                   # 4 x SMs units
+        assert fa.fa_fwd_grid_ctas(B, H, Nq, d, 1) >= 4 * sms
     q, k, v = (t.cuda() for t in make_qkv(B, H, Nq, Nk, d, 5150 + d))
     o = torch.full((B, H, Nq, d), 7.0, dtype=torch.bfloat16, device="cuda")
     lse = torch.full((B, H, Nq), 7.0, dtype=torch.float32, device="cuda")
