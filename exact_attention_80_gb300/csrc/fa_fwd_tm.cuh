@@ -140,7 +140,9 @@ struct LayoutTM {
     static_assert(256 + Q_TILES * D <= 512, "O region overflows TMEM");
     static_assert(ALLOC_BYTES <= 232448, "shared memory over the 227 KB per-CTA limit");
     static_assert(ALLOC_BYTES > 232448 / 2, "two CTAs per SM would contend for TMEM");
-    static_assert(D % 64 == 0 && STAGES >= 3, "tile shape");
+    // A step holds V_j and K_{j+1} while it waits for V_{j+1} and K_{j+2}
+    // (before it releases the first two), so the ring needs four slots.
+    static_assert(D % 64 == 0 && STAGES >= 4, "tile shape and ring depth");
     static_assert(ROW_BYTES == 128 || ROW_BYTES == 64, "swizzle rows of 128 or 64 bytes");
     static_assert(!(PERSIST && F8), "persistent CTAs: bf16 inputs");
 
