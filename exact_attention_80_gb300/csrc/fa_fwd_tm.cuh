@@ -339,82 +339,129 @@ __device__ __forceinline__ long long persist_unit(const FwdParams& p, int k) {
 // K/V ring and every barrier's phase carried from unit to unit. Phases count
 // per tile: SFULL_t and PFULL_t complete once per key step of the tile,
 // QFULL_t, QEMPTY_t and OFULL_t once per unit in which the tile has keys.
-//   Q_t of the next unit loads as soon as the last S_t MMA of the unit before
-//   it has completed: the issuer commits QEMPTY_t right after that MMA. Each
-//   waiter of a barrier sees every one of its phases in turn (an mbarrier
-//   wait tells phases apart by parity alone, so a waiter must never be two
-//   phases away from the one it waits for): the producer has waited for the
-//   previous QEMPTY_t phase before it issued the load that the next one
-//   releases. O_t of the next
-//   unit is first written by its PV_t(0), which waits for P_t(0); the softmax
-//   threads hand that P over only after their epilogue has read O_t out of TMEM.
+//   The K/V ring holds pairs of slots: the entry of step j holds V_j and the K
+//   tile the step's S MMAs read, K_{j+1}, or, at a unit's last step, K_0 of the
+//   CTA's next unit (the CTA's first entry holds that unit's K_0 alone). The
+//   issuer then waits for one entry and releases one per step, and the next
+//   unit's first S MMAs read a K tile that is already resident.
+//   Q_t of the next unit loads as soon as the unit's last S_t MMA has
+//   completed: the issuer commits QEMPTY_t right after that MMA. Each waiter
+//   of a barrier sees every one of its phases in turn (an mbarrier wait tells
+//   phases apart by parity alone, so a waiter must never be two phases away
+//   from the one it waits for): the producer has waited for the previous
+//   QEMPTY_t phase before it issued the load that the next one releases. O_t of
+//   the next unit is first written by its PV_t(0), which waits for P_t(0); the
+//   softmax threads hand that P over only after their epilogue has read O_t out
+//   of TMEM.
 template <int D>
 __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t sbase, uint32_t tmem,
                                                    volatile uint32_t* abort_flag, int warp) {
     using L = LayoutTM<D, false, true>;
     constexpr int QT = L::Q_TILES;
     constexpr int BN = L::BN;
-    constexpr int ST = L::STAGES;
+    constexpr int NP = L::STAGES / 2;  // ring entries: slot pairs (V half, K half)
+    static_assert(L::STAGES % 2 == 0 && NP >= 2, "the ring holds pairs of K/V slots");
     auto bar = [&](int i) -> uint32_t { return sbase + L::BAR_OFF + 8u * i; };
+    auto v_half = [](int e) -> uint32_t { return L::SLOT_OFF + (2 * e) * L::SLOT_BYTES; };
+    auto k_half = [](int e) -> uint32_t { return L::SLOT_OFF + (2 * e + 1) * L::SLOT_BYTES; };
     const int rounds = static_cast<int>((p.total_units + gridDim.x - 1) / gridDim.x);
+    // The CTA's next unit with keys at round k or later: its work in w, its
+    // round in k; false when there is none.
+    auto next_unit = [&](int& k, Work<QT>& w) -> bool {
+        for (; k < rounds; ++k) {
+            const long long lin = persist_unit(p, k);
+            if (lin < 0) continue;
+            compute_work<QT, BN>(p, lin, w);
+            if (w.nmax > 0) return true;
+        }
+        return false;
+    };
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         const bool leader = elect_one();
-        RingPos<ST> pos;
+        RingPos<NP> pos;
         int issued = 0;           // ring entries issued, all units
         int q_loads[QT] = {};     // Q_t loads issued
         bool ok = true;
-        for (int k = 0; k < rounds && ok; ++k) {
-            const long long lin = persist_unit(p, k);
-            if (lin < 0) continue;
-            Work<QT> w;
-            compute_work<QT, BN>(p, lin, w);
-            if (w.nmax == 0) continue;
-            auto load_q = [&](int t) -> bool {
-                if (w.n[t] == 0) return true;
-                if (q_loads[t] > 0 &&
-                    !__all_sync(0xffffffffu, wait_phase(bar(L::BAR_QEMPTY + t), (q_loads[t] - 1) & 1, p,
-                                                        abort_flag, kStatusWaitQ)))
-                    return false;
-                if (leader && !p.test_withhold_q) {
-                    mbar_arrive_expect_tx(bar(L::BAR_QFULL + t), L::Q_TILE_BYTES);
+        auto load_q = [&](const Work<QT>& u, int t) -> bool {
+            if (u.n[t] == 0) return true;
+            if (q_loads[t] > 0 &&
+                !__all_sync(0xffffffffu, wait_phase(bar(L::BAR_QEMPTY + t), (q_loads[t] - 1) & 1, p,
+                                                    abort_flag, kStatusWaitQ)))
+                return false;
+            if (leader && !p.test_withhold_q) {
+                mbar_arrive_expect_tx(bar(L::BAR_QFULL + t), L::Q_TILE_BYTES);
 #pragma unroll
-                    for (int c = 0; c < L::CHUNKS; ++c)
-                        tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128), &p.tm_q,
-                                    bar(L::BAR_QFULL + t), L::CHUNK_ELEMS * c, w.q0 + t * kBM, w.zq);
-                }
-                ++q_loads[t];
-                return true;
-            };
-            // Q_0, K_0, then Q_1, as in the one-unit CTA.
-            ok = load_q(0);
-            const int total = 2 * w.nmax;
-            for (int e = 0; e < total && ok; ++e) {
-                const bool is_v = (e & 1) != 0;
-                const int kv = e >> 1;
-                if (issued >= ST) {
-                    ok = __all_sync(0xffffffffu, wait_phase(bar(L::BAR_KVEMPTY + pos.slot), pos.phase ^ 1u, p,
-                                                            abort_flag, kStatusWaitKvEmpty));
-                    if (!ok) break;
-                }
-                if (leader) {
-                    mbar_arrive_expect_tx(bar(L::BAR_KVFULL + pos.slot), L::SLOT_BYTES);
-                    const CUtensorMap* map = is_v ? &p.tm_v : &p.tm_k;
-                    const int row = (w.kv_tile0 + kv) * BN;
-#pragma unroll
-                    for (int c = 0; c < L::CHUNKS; ++c)
-                        tma_load_3d(sbase + L::SLOT_OFF + pos.slot * L::SLOT_BYTES + c * (BN * 128), map,
-                                    bar(L::BAR_KVFULL + pos.slot), L::CHUNK_ELEMS * c, row, w.zq);
-                }
-                ++issued;
-                pos.advance();
-                if (e == 0) ok = load_q(1);
+                for (int c = 0; c < L::CHUNKS; ++c)
+                    tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128), &p.tm_q,
+                                bar(L::BAR_QFULL + t), L::CHUNK_ELEMS * c, u.q0 + t * kBM, u.zq);
             }
+            ++q_loads[t];
+            return true;
+        };
+        // One ring entry: V rows from vrow and K rows from krow of heads vz, kz
+        // (a row < 0: that half stays empty).
+        auto load_pair = [&](int vrow, int vz, int krow, int kz) -> bool {
+            if (issued >= NP &&
+                !__all_sync(0xffffffffu, wait_phase(bar(L::BAR_KVEMPTY + pos.slot), pos.phase ^ 1u, p,
+                                                    abort_flag, kStatusWaitKvEmpty)))
+                return false;
+            if (leader) {
+                const uint32_t full = bar(L::BAR_KVFULL + pos.slot);
+                mbar_arrive_expect_tx(full, (vrow >= 0 ? L::SLOT_BYTES : 0u) + (krow >= 0 ? L::SLOT_BYTES : 0u));
+                if (vrow >= 0) {
+#pragma unroll
+                    for (int c = 0; c < L::CHUNKS; ++c)
+                        tma_load_3d(sbase + v_half(pos.slot) + c * (BN * 128), &p.tm_v, full, L::CHUNK_ELEMS * c,
+                                    vrow, vz);
+                }
+                if (krow >= 0) {
+#pragma unroll
+                    for (int c = 0; c < L::CHUNKS; ++c)
+                        tma_load_3d(sbase + k_half(pos.slot) + c * (BN * 128), &p.tm_k, full, L::CHUNK_ELEMS * c,
+                                    krow, kz);
+                }
+            }
+            ++issued;
+            pos.advance();
+            return true;
+        };
+        int k = 0;
+        Work<QT> w;
+        bool have = next_unit(k, w);
+        if (have) {
+            // Q_0, K_0 (the first entry), then Q_1, as in the one-unit CTA.
+            ok = load_q(w, 0);
+            if (ok) ok = load_pair(-1, 0, w.kv_tile0 * BN, w.zq);
+            if (ok) ok = load_q(w, 1);
+        }
+        while (have && ok) {
+            int kn = k + 1;
+            Work<QT> wn;
+            const bool have_next = next_unit(kn, wn);
+            for (int j = 0; j < w.nmax && ok; ++j) {
+                int krow = -1, kz = 0;
+                if (j + 1 < w.nmax) {
+                    krow = (w.kv_tile0 + j + 1) * BN;
+                    kz = w.zq;
+                } else if (have_next) {
+                    krow = wn.kv_tile0 * BN;
+                    kz = wn.zq;
+                }
+                ok = load_pair((w.kv_tile0 + j) * BN, w.zq, krow, kz);
+            }
+            if (ok && have_next) {
+                ok = load_q(wn, 0);
+                if (ok) ok = load_q(wn, 1);
+            }
+            w = wn;
+            k = kn;
+            have = have_next;
         }
         if (ok) {
-            // Every slot's last use released: no commit arrival still in flight.
-            for (int e = max(0, issued - ST); e < issued && ok; ++e)
-                ok = __all_sync(0xffffffffu, wait_phase(bar(L::BAR_KVEMPTY + e % ST), (e / ST) & 1, p, abort_flag,
+            // Every entry's last use released: no commit arrival still in flight.
+            for (int e = max(0, issued - NP); e < issued && ok; ++e)
+                ok = __all_sync(0xffffffffu, wait_phase(bar(L::BAR_KVEMPTY + e % NP), (e / NP) & 1, p, abort_flag,
                                                         kStatusWaitKvEmpty));
         } else {
             // Let every copy already issued land before the CTA goes away.
@@ -422,8 +469,8 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
             for (int t = 0; t < QT; ++t)
                 if (q_loads[t] > 0 && !p.test_withhold_q)
                     wait_phase(bar(L::BAR_QFULL + t), (q_loads[t] - 1) & 1, p, abort_flag, kStatusWaitDrain, false);
-            for (int e = max(0, issued - ST); e < issued; ++e)
-                wait_phase(bar(L::BAR_KVFULL + e % ST), (e / ST) & 1, p, abort_flag, kStatusWaitDrain, false);
+            for (int e = max(0, issued - NP); e < issued; ++e)
+                wait_phase(bar(L::BAR_KVFULL + e % NP), (e / NP) & 1, p, abort_flag, kStatusWaitDrain, false);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -442,9 +489,9 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
         auto desc = [](uint32_t lo, uint32_t hi, uint32_t off) -> uint64_t {
             return (static_cast<uint64_t>(hi) << 32) | (lo + (off >> 4));
         };
-        auto issue_s = [&](int t, int slot) {
+        // S_t = Q_t K^T from the K tile at shared offset kb; O_t += P_t V from vb.
+        auto issue_s = [&](int t, uint32_t kb) {
             const uint32_t qa = L::Q_OFF + t * L::Q_TILE_BYTES;
-            const uint32_t kb = L::SLOT_OFF + slot * L::SLOT_BYTES;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
                 const uint32_t in_row = (kk & 3) * 32;
@@ -454,40 +501,30 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
                             kk > 0 ? 1u : 0u);
             }
         };
-        auto issue_pv = [&](int t, int slot, bool accumulate) {
-            const uint32_t vb = L::SLOT_OFF + slot * L::SLOT_BYTES;
+        auto issue_pv = [&](int t, uint32_t vb, bool accumulate) {
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
                 if (leader)
                     umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8, desc(vmn_lo, vmn_hi, vb + kk * 2048),
                             IDESC_O, (accumulate || kk > 0) ? 1u : 0u);
         };
-        RingPos<ST> pos;
-        int slot_v = 0, slot_k = 0;
         // Phase parities carried across units: bit t of sbits = parity of the
         // tile's earlier key steps (PFULL_t), of qbits = parity of its earlier
         // Q_t loads (QFULL_t).
         uint32_t sbits = 0, qbits = 0;
+        RingPos<NP> pos;  // the entry in use
         bool ok = true;
+        bool first = true;
         constexpr bool kKvWaitMid1 = (D >= 128);
-        for (int k = 0; k < rounds && ok; ++k) {
-            const long long lin = persist_unit(p, k);
-            if (lin < 0) continue;
-            Work<QT> w;
-            compute_work<QT, BN>(p, lin, w);
-            if (w.nmax == 0) continue;
-            auto wait_kv = [&](int j) -> bool {
-                slot_v = pos.slot;
-                if (!wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull)) return false;
-                pos.advance();
-                if (j + 1 < w.nmax) {
-                    slot_k = pos.slot;
-                    if (!wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull)) return false;
-                    pos.advance();
-                }
-                return true;
-            };
-            ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
+        int k = 0;
+        Work<QT> w;
+        while (ok && next_unit(k, w)) {
+            // pos: the entry whose K half holds this unit's K_0 (the previous
+            // unit's last entry, already waited for; or the CTA's first).
+            if (first) {
+                ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
+                first = false;
+            }
             if (ok) {
 #pragma unroll
                 for (int t = 0; t < QT; ++t) {
@@ -495,27 +532,31 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
                         ok = wait_all(bar(L::BAR_QFULL + t), (qbits >> t) & 1u, kStatusWaitQ);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_s(t, pos.slot);
+                        issue_s(t, k_half(pos.slot));
                         if (leader) umma_commit(bar(L::BAR_SFULL + t));
                         if (w.n[t] == 1 && leader) umma_commit(bar(L::BAR_QEMPTY + t));
                     }
                 }
             }
             if (ok) {
+                // That entry's V half was read by the previous unit's last PVs,
+                // issued before these S MMAs.
                 if (leader) umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
                 pos.advance();
-                ok = wait_kv(0);
+                ok = wait_all(bar(L::BAR_KVFULL + pos.slot), pos.phase, kStatusWaitKvFull);
             }
             for (int j = 0; j < w.nmax && ok; ++j) {
-                const int sv = slot_v, sk = slot_k;
+                const uint32_t vb = v_half(pos.slot), kb = k_half(pos.slot);
                 const bool k_next = (j + 1 < w.nmax);
+                RingPos<NP> nxt = pos;
+                nxt.advance();
                 if (j < w.n[0]) {
                     ok = wait_all(bar(L::BAR_PFULL + 0), (sbits ^ static_cast<uint32_t>(j)) & 1u, kStatusWaitP);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv(0, sv, j > 0);
+                    issue_pv(0, vb, j > 0);
                     if (j + 1 < w.n[0]) {
-                        issue_s(0, sk);
+                        issue_s(0, kb);
                         if (leader) umma_commit(bar(L::BAR_SFULL + 0));
                         if (j + 2 == w.n[0] && leader) umma_commit(bar(L::BAR_QEMPTY + 0));
                     } else {
@@ -523,7 +564,7 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
                     }
                 }
                 if (!kKvWaitMid1 && k_next) {
-                    ok = wait_kv(j + 1);
+                    ok = wait_all(bar(L::BAR_KVFULL + nxt.slot), nxt.phase, kStatusWaitKvFull);
                     if (!ok) break;
                 }
                 const bool act1 = j < w.n[1];
@@ -531,30 +572,37 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
                     ok = wait_all(bar(L::BAR_PFULL + 1), ((sbits >> 1) ^ static_cast<uint32_t>(j)) & 1u, kStatusWaitP);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv(1, sv, j > 0);
+                    issue_pv(1, vb, j > 0);
                 }
                 if (kKvWaitMid1 && k_next) {
-                    ok = wait_kv(j + 1);
+                    ok = wait_all(bar(L::BAR_KVFULL + nxt.slot), nxt.phase, kStatusWaitKvFull);
                     if (!ok) break;
                 }
                 if (act1) {
                     if (j + 1 < w.n[1]) {
-                        issue_s(1, sk);
+                        issue_s(1, kb);
                         if (leader) umma_commit(bar(L::BAR_SFULL + 1));
                         if (j + 2 == w.n[1] && leader) umma_commit(bar(L::BAR_QEMPTY + 1));
                     } else {
                         if (leader) umma_commit(bar(L::BAR_OFULL + 1));
                     }
                 }
-                if (leader) umma_commit(bar(L::BAR_KVEMPTY + sv));
-                if (k_next && leader) umma_commit(bar(L::BAR_KVEMPTY + sk));
+                // A unit's last entry stays: its K half is the next unit's K_0.
+                if (k_next) {
+                    if (leader) umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
+                    pos = nxt;
+                }
             }
 #pragma unroll
             for (int t = 0; t < QT; ++t) {
                 sbits ^= static_cast<uint32_t>(w.n[t] & 1) << t;
                 qbits ^= static_cast<uint32_t>(w.n[t] > 0 ? 1 : 0) << t;
             }
+            ++k;
         }
+        // The last unit's last entry.
+        if (!first && leader) umma_commit(bar(L::BAR_KVEMPTY + pos.slot));
+        // Every MMA this thread issued must finish before TMEM can be freed.
         if (leader) umma_commit(bar(L::BAR_DRAIN));
         wait_phase(bar(L::BAR_DRAIN), 0, p, abort_flag, kStatusWaitDrain, false);
     }
