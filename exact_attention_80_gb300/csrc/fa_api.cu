@@ -206,7 +206,7 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
                          const Varlen* vl = nullptr, const float* f8_descale = nullptr,
                          int tiles_per_cta = 0) {
     const FwdConfig c = fwd_config(d);
-    // Persistent CTAs for the plain dense bf16 forward of the two-tile kernel
+    // Persistent CTAs for the plain dense forward of the two-tile kernel
     // when its units fill at least four waves of CTAs, where the saved CTA
     // start-up and Q latency outweigh the persistent control code's slower
     // key steps (fa_fwd_rows, which fixes the rows per CTA, keeps one unit per
@@ -283,13 +283,15 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
 
     cudaError_t e = cudaErrorInvalidValue;
     p.dual = dual ? 1 : 0;
-    const bool persist = !row_choice && !f8_descale && !vl && !split_mode && (d == 64 || d == 128) &&
-                         ctas >= 4ll * sms;
+    const bool persist = !row_choice && !vl && !split_mode && (d == 64 || d == 128) && ctas >= 4ll * sms;
     p.total_units = ctas;
     const unsigned grid = static_cast<unsigned>(
         dual ? static_cast<long long>(BH) * ((num_splits + 1) / 2) : (persist ? sms : ctas));
     if (persist) {
-        e = d == 64 ? launch_fwd_d64_persist(p, grid, stream) : launch_fwd_d128_persist(p, grid, stream);
+        if (f8_descale)
+            e = d == 64 ? launch_fwd_f8_d64_persist(p, grid, stream) : launch_fwd_f8_d128_persist(p, grid, stream);
+        else
+            e = d == 64 ? launch_fwd_d64_persist(p, grid, stream) : launch_fwd_d128_persist(p, grid, stream);
         return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
     }
     if (f8_descale) {

@@ -85,13 +85,14 @@ struct TmCfg8<128> {
 
 // F8: Q, K, V are e4m3 (one byte per element) and both MMAs are
 // kind::f8f6f4; otherwise bf16 and kind::f16. PERSIST: persistent CTAs
-// (bf16, plain mode), each walking several query units.
+// (plain mode), each walking several query units.
 template <int D, bool F8 = false, bool PERSIST = false>
 struct LayoutTM {
     using Cfg = std::conditional_t<F8, TmCfg8<D>, TmCfg<D>>;
     static constexpr int Q_TILES = 2;
     static constexpr int BN = 128;
-    static constexpr int STAGES = PERSIST ? TmPersistCfg<D>::STAGES : Cfg::STAGES;
+    static constexpr bool PERSIST_BF16 = PERSIST && !F8;
+    static constexpr int STAGES = PERSIST_BF16 ? TmPersistCfg<D>::STAGES : Cfg::STAGES;
     static constexpr int THREADS = (4 + 4 * Q_TILES) * 32;
     static constexpr int EB = F8 ? 1 : 2;              // input bytes per element
     // Swizzle row width: 128 bytes, or 64 when a whole row is 64 bytes (e4m3,
@@ -109,8 +110,8 @@ struct LayoutTM {
     static constexpr uint32_t SLOT_OFF = Q_OFF + Q_TILES * Q_TILE_BYTES;
     // bf16 O is staged for its TMA store in the tile's Q memory when that holds
     // a bf16 tile; 8-bit Q tiles are half that size, so F8 has buffers of its
-    // own. Persistent CTAs stage each warp's 32 rows, 64 columns at a time, in
-    // a 4 KB buffer per warp (the next unit's Q may be loading).
+    // own. Persistent bf16 CTAs stage each warp's 32 rows, 64 columns at a time,
+    // in a 4 KB buffer per warp (the next unit's Q may be loading).
     static constexpr uint32_t OST_OFF = SLOT_OFF + STAGES * SLOT_BYTES;
     static constexpr uint32_t OST_WARP_BYTES = 32 * 128;
     static constexpr uint32_t OST_TILE_BYTES = F8 ? kBM * D * 2 : (PERSIST ? 4 * OST_WARP_BYTES : 0);
@@ -144,14 +145,14 @@ struct LayoutTM {
     // (before it releases the first two), so the ring needs four slots.
     static_assert(D % 64 == 0 && STAGES >= 4, "tile shape and ring depth");
     static_assert(ROW_BYTES == 128 || ROW_BYTES == 64, "swizzle rows of 128 or 64 bytes");
-    static_assert(!(PERSIST && F8), "persistent CTAs: bf16 inputs");
+    static_assert(!PERSIST || STAGES % 2 == 0, "persistent CTAs pair their K/V slots");
 
     // Register split: the sum is the launch allocation (THREADS x LAUNCH_REGS),
     // checked on the host.
     static constexpr bool REG_SPLIT = true;
     static constexpr int LAUNCH_REGS = 168;
-    static constexpr int CTRL_REGS = PERSIST ? TmPersistCfg<D>::CTRL_REGS : Cfg::CTRL_REGS;
-    static constexpr int SOFTMAX_REGS = PERSIST ? TmPersistCfg<D>::SOFTMAX_REGS : Cfg::SOFTMAX_REGS;
+    static constexpr int CTRL_REGS = PERSIST_BF16 ? TmPersistCfg<D>::CTRL_REGS : Cfg::CTRL_REGS;
+    static constexpr int SOFTMAX_REGS = PERSIST_BF16 ? TmPersistCfg<D>::SOFTMAX_REGS : Cfg::SOFTMAX_REGS;
     static_assert(128 * CTRL_REGS + 256 * SOFTMAX_REGS == THREADS * LAUNCH_REGS,
                   "register split must equal the launch allocation");
 };
@@ -353,10 +354,11 @@ __device__ __forceinline__ long long persist_unit(const FwdParams& p, int k) {
 //   the next unit is first written by its PV_t(0), which waits for P_t(0); the
 //   softmax threads hand that P over only after their epilogue has read O_t out
 //   of TMEM.
-template <int D>
+template <int D, bool F8>
 __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t sbase, uint32_t tmem,
                                                    volatile uint32_t* abort_flag, int warp) {
-    using L = LayoutTM<D, false, true>;
+    using L = LayoutTM<D, F8, true>;
+    constexpr uint32_t RB = L::ROW_BYTES;  // swizzle row bytes
     constexpr int QT = L::Q_TILES;
     constexpr int BN = L::BN;
     constexpr int NP = L::STAGES / 2;  // ring entries: slot pairs (V half, K half)
@@ -393,7 +395,7 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
                 mbar_arrive_expect_tx(bar(L::BAR_QFULL + t), L::Q_TILE_BYTES);
 #pragma unroll
                 for (int c = 0; c < L::CHUNKS; ++c)
-                    tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * 128), &p.tm_q,
+                    tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * RB), &p.tm_q,
                                 bar(L::BAR_QFULL + t), L::CHUNK_ELEMS * c, u.q0 + t * kBM, u.zq);
             }
             ++q_loads[t];
@@ -412,13 +414,13 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
                 if (vrow >= 0) {
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
-                        tma_load_3d(sbase + v_half(pos.slot) + c * (BN * 128), &p.tm_v, full, L::CHUNK_ELEMS * c,
+                        tma_load_3d(sbase + v_half(pos.slot) + c * (BN * RB), &p.tm_v, full, L::CHUNK_ELEMS * c,
                                     vrow, vz);
                 }
                 if (krow >= 0) {
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
-                        tma_load_3d(sbase + k_half(pos.slot) + c * (BN * 128), &p.tm_k, full, L::CHUNK_ELEMS * c,
+                        tma_load_3d(sbase + k_half(pos.slot) + c * (BN * RB), &p.tm_k, full, L::CHUNK_ELEMS * c,
                                     krow, kz);
                 }
             }
@@ -478,10 +480,12 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
         auto wait_all = [&](uint32_t b, uint32_t parity, unsigned what) {
             return __all_sync(0xffffffffu, wait_phase(b, parity, p, abort_flag, what));
         };
-        constexpr uint32_t IDESC_S = make_idesc_bf16(kBM, BN, false, false);
-        constexpr uint32_t IDESC_O = make_idesc_bf16(kBM, D, false, true);
-        const uint64_t kmaj0 = make_sdesc_sw128(sbase, 16, 1024);
-        const uint64_t vmn0 = make_sdesc_sw128(sbase, BN * 128, 1024);
+        constexpr uint32_t IDESC_S =
+            F8 ? make_idesc_e4m3(kBM, BN, false, false) : make_idesc_bf16(kBM, BN, false, false);
+        constexpr uint32_t IDESC_O =
+            F8 ? make_idesc_e4m3(kBM, D, false, true) : make_idesc_bf16(kBM, D, false, true);
+        const uint64_t kmaj0 = make_sdesc_rows<L::ROW_BYTES>(sbase, 16, 8 * RB);
+        const uint64_t vmn0 = make_sdesc_rows<L::ROW_BYTES>(sbase, BN * RB, 8 * RB);
         const uint32_t kmaj_lo = static_cast<uint32_t>(kmaj0);
         const uint32_t kmaj_hi = static_cast<uint32_t>(kmaj0 >> 32);
         const uint32_t vmn_lo = static_cast<uint32_t>(vmn0);
@@ -490,23 +494,36 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
             return (static_cast<uint64_t>(hi) << 32) | (lo + (off >> 4));
         };
         // S_t = Q_t K^T from the K tile at shared offset kb; O_t += P_t V from vb.
+        // One MMA takes 32 bytes of K (16 bf16 or 32 e4m3) of a swizzle row; P is
+        // packed two bf16 or four e4m3 per TMEM column, so one MMA's keys are 8
+        // columns.
         auto issue_s = [&](int t, uint32_t kb) {
             const uint32_t qa = L::Q_OFF + t * L::Q_TILE_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-                const uint32_t in_row = (kk & 3) * 32;
-                if (leader)
-                    umma_ss(tmem + L::S_COL(t), desc(kmaj_lo, kmaj_hi, qa + (kk >> 2) * (kBM * 128) + in_row),
-                            desc(kmaj_lo, kmaj_hi, kb + (kk >> 2) * (BN * 128) + in_row), IDESC_S,
-                            kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / L::K_MMA; ++kk) {
+                const uint32_t in_row = (kk % L::KSTEPS_ROW) * 32;
+                const int ch = kk / L::KSTEPS_ROW;
+                const uint64_t a = desc(kmaj_lo, kmaj_hi, qa + ch * (kBM * RB) + in_row);
+                const uint64_t b = desc(kmaj_lo, kmaj_hi, kb + ch * (BN * RB) + in_row);
+                if (leader) {
+                    if constexpr (F8) umma_ss_f8(tmem + L::S_COL(t), a, b, IDESC_S, kk > 0 ? 1u : 0u);
+                    else umma_ss(tmem + L::S_COL(t), a, b, IDESC_S, kk > 0 ? 1u : 0u);
+                }
             }
         };
         auto issue_pv = [&](int t, uint32_t vb, bool accumulate) {
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-                if (leader)
-                    umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8, desc(vmn_lo, vmn_hi, vb + kk * 2048),
-                            IDESC_O, (accumulate || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < BN / L::K_MMA; ++kk) {
+                const uint64_t b = desc(vmn_lo, vmn_hi, vb + kk * (L::K_MMA * RB));
+                if (leader) {
+                    if constexpr (F8)
+                        umma_ts_f8(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8, b, IDESC_O,
+                                   (accumulate || kk > 0) ? 1u : 0u);
+                    else
+                        umma_ts(tmem + L::O_COL(t), tmem + L::S_COL(t) + kk * 8, b, IDESC_O,
+                                (accumulate || kk > 0) ? 1u : 0u);
+                }
+            }
         };
         // Phase parities carried across units: bit t of sbits = parity of the
         // tile's earlier key steps (PFULL_t), of qbits = parity of its earlier
@@ -666,7 +683,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
       // The work record is derived inside each role, after its register limit
       // is set, so that no role carries fields it does not use.
       if constexpr (PERSIST) {
-        tm_persist_control<D>(p, sbase, tmem, abort_flag, warp);
+        tm_persist_control<D, F8>(p, sbase, tmem, abort_flag, warp);
       } else if constexpr (DUAL) {
         tm_dual_control<D, F8>(p, sbase, tmem, abort_flag, warp);
       } else {
@@ -1108,7 +1125,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
         // A tile slot the CTA does not own (one tile per CTA, fa_fwd_rows) writes
         // nothing: its rows belong to another CTA.
         if (!DUAL && !PERSIST && t >= p.tiles_per_cta) ok = false;
-        if constexpr (PERSIST) {
+        if constexpr (PERSIST && !F8) {
             // Plain mode, dense: bf16 O staged per warp in its own buffer.
             if (ok && n > 0)
                 store_rows_tma_buf<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, l + lc, tO,
@@ -1168,12 +1185,17 @@ __global__ void __launch_bounds__(LayoutTM<D, true>::THREADS, 1)
     tm_forward<D, true>(p);
 }
 
-// Persistent CTAs (bf16, plain mode, dense): grid min(units, SMs), each CTA
-// walking its units with persist_unit.
+// Persistent CTAs (plain mode, dense): grid min(units, SMs), each CTA walking
+// its units with persist_unit; bf16 and e4m3 inputs.
 template <int D>
 __global__ void __launch_bounds__(LayoutTM<D, false, true>::THREADS, 1)
     fa_fwd_tmp_kernel(const __grid_constant__ FwdParams p) {
     tm_forward<D, false, false, true>(p);
+}
+template <int D>
+__global__ void __launch_bounds__(LayoutTM<D, true, true>::THREADS, 1)
+    fa_fwd_tmp8_kernel(const __grid_constant__ FwdParams p) {
+    tm_forward<D, true, false, true>(p);
 }
 
 // Dual-range split-KV CTAs (one query tile), bf16 and e4m3 inputs.

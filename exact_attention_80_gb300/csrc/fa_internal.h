@@ -81,9 +81,11 @@ FwdConfig fwd_config(int d);
 
 cudaError_t launch_fwd_d64(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FwdParams& p, unsigned grid, cudaStream_t stream);
-// Persistent two-tile kernels (plain mode, dense bf16): grid min(units, SMs).
+// Persistent two-tile kernels (plain mode, dense bf16 or e4m3): grid min(units, SMs).
 cudaError_t launch_fwd_d64_persist(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128_persist(const FwdParams& p, unsigned grid, cudaStream_t stream);
+cudaError_t launch_fwd_f8_d64_persist(const FwdParams& p, unsigned grid, cudaStream_t stream);
+cudaError_t launch_fwd_f8_d128_persist(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d256(const FwdParams& p, unsigned grid, cudaStream_t stream);
 // e4m3 Q, K, V (tm_q/tm_k/tm_v are byte maps, box {128, rows, 1}, or {64,
 // rows, 1} with the 64-byte swizzle at d = 64); d = 64, 128, 256.

@@ -158,6 +158,21 @@ def test_fp8_dual_range_split(S, Nq):
     check_fp8(o, lse, o_ref, lse_ref, sigma, f"dual S={S} Nq={Nq}")
 
 
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("causal", [False, True, "bottom_right"])
+def test_fp8_persistent_ctas(d, causal):
+    """More query units than four waves of CTAs (B=2, H=160, Nq=300, Nk=333:
+    640 units, each head's last tile ragged), so fa_fwd_fp8 runs persistent
+    CTAs that walk several units each; every element against the oracle."""
+    B, H, Nq, Nk = 2, 160, 300, 333
+    assert fa.fa_fwd_grid_ctas(B, H, Nq, d, 1) >= 4 * torch.cuda.get_device_properties(0).multi_processor_count
+    descales = (2.0 ** -5, 0.02, 0.3)
+    q8, k8, v8, scale, o, lse = run_fp8(B, H, Nq, Nk, causal, 5950 + d, descales, d=d)
+    o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, causal)
+    sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, causal)
+    check_fp8(o, lse, o_ref, lse_ref, sigma, f"persistent d{d} {causal}")
+
+
 @pytest.mark.parametrize("S,Nq", [(3, 200), (2, 128), (7, 100), (40, 1)])
 def test_fp8_splitkv_d64(S, Nq):
     """d = 64 e4m3 through split-KV + merge: two query tiles per CTA (Nq = 200)
