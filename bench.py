@@ -502,7 +502,8 @@ def fp8_workload(device, stream, reps, shape=(8, 32, 2048, 128), causal=False, s
     ms = statistics.median(time_launches(fn, reps, stream, queue_ahead=True))
     tflops = metric_flops(B, H, N, N, d, causal) / ms / 1e9
     peak_tf, _, kind = measured_peaks()
-    kernel = "fa_fwd_tp8_kernel<256>" if d == 256 else f"fa_fwd_tm8_kernel<{d}>"
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    kernel = kernel_name(fa, B, H, N, d, sms).replace("_kernel", "8_kernel")
     return {"tflops": round(tflops, 1), "us": round(ms * 1e3, 1), "kernel": kernel,
             "shape": f"B={B} H={H} N={N} d={d} {'causal' if causal else 'non-causal'}",
             "roofline_frac": round(tflops / (2.0 * peak_tf), 4),
