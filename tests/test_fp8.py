@@ -173,6 +173,17 @@ def test_fp8_persistent_ctas(d, causal):
     check_fp8(o, lse, o_ref, lse_ref, sigma, f"persistent d{d} {causal}")
 
 
+def test_fp8_persistent_rows_without_keys():
+    """e4m3 persistent CTAs over units with no key step, or keys in the
+    second tile only (bottom-right, Nq = 700 > Nk = 200, 960 units)."""
+    B, H, Nq, Nk, d = 1, 320, 700, 200, 128
+    descales = (2.0 ** -5, 2.0 ** -5, 2.0 ** -5)
+    q8, k8, v8, scale, o, lse = run_fp8(B, H, Nq, Nk, "bottom_right", 5960, descales, d=d)
+    o_ref, lse_ref = ofp8.attention_fp8_f64(q8, k8, v8, *descales, scale, "bottom_right")
+    sigma = ofp8.p_rounding_sigma(q8, k8, v8, *descales, scale, "bottom_right")
+    check_fp8(o, lse, o_ref, lse_ref, sigma, "persistent, rows without keys")
+
+
 @pytest.mark.parametrize("S,Nq", [(3, 200), (2, 128), (7, 100), (40, 1)])
 def test_fp8_splitkv_d64(S, Nq):
     """d = 64 e4m3 through split-KV + merge: two query tiles per CTA (Nq = 200)

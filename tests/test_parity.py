@@ -507,6 +507,23 @@ def test_persistent_ctas_ragged(head_pool, d, causal):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_persistent_ctas_rows_without_keys(head_pool, d):
+    """Persistent CTAs over units in which one or both tiles see no key
+    (bottom-right alignment with Nq = 700 > Nk = 200: rows 0-499 see none, so
+    the first unit of each head has no key step at all and the second has keys
+    only in its second tile): 960 units, every head against the oracle (O = 0
+    and LSE = -inf on rows that see no key) and bit for bit one unit per CTA."""
+    B, H, Nq, Nk = 1, 320, 700, 200
+    c = dict(B=B, H=H, Nq=Nq, Nk=Nk, d=d, causal="bottom_right", name="persistent, rows without keys")
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 7300 + d)
+    whole_tensor_check(head_pool, c, (q, k, v))
+    scale = f32(1.0 / math.sqrt(d))
+    o1, l1 = run_gpu(q, k, v, "bottom_right", scale)
+    o2, l2 = run_gpu_rows(q, k, v, "bottom_right", scale, 256)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
 @pytest.mark.parametrize("name", ["c1", "c2", "c2_causal", "c3", "c3_causal", "c4"])
 def test_full_size_whole_tensor(head_pool, name):
     """Whole O and LSE of each benchmark workload against the oracle (C4 with its
