@@ -508,6 +508,27 @@ def test_persistent_ctas_ragged(head_pool, d, causal):
 
 
 @pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("B,H,Nq,Nk,causal", [
+    (8, 80, 1, 1000, False),          # one query row per head: tile 1 of every unit idle
+    (2, 320, 129, 129, True),         # a one-row second tile
+    (4, 80, 512, 77, "bottom_right"),  # fewer keys than one key tile
+])
+def test_persistent_ctas_small_units(head_pool, B, H, Nq, Nk, causal, d):
+    """Persistent launches (at least four waves of units) whose units are
+    short or partly idle; every head against the oracle and bit for bit one
+    unit per CTA."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert fa.fa_fwd_grid_ctas(B, H, Nq, d, 1) >= 4 * sms
+    c = dict(B=B, H=H, Nq=Nq, Nk=Nk, d=d, causal=causal, name="persistent, short units")
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 7400 + Nq + d)
+    whole_tensor_check(head_pool, c, (q, k, v))
+    scale = f32(1.0 / math.sqrt(d))
+    o1, l1 = run_gpu(q, k, v, causal, scale)
+    o2, l2 = run_gpu_rows(q, k, v, causal, scale, 256)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("d", [128, 64])
 def test_persistent_ctas_rows_without_keys(head_pool, d):
     """Persistent CTAs over units in which one or both tiles see no key
     (bottom-right alignment with Nq = 700 > Nk = 200: rows 0-499 see none, so
