@@ -5,8 +5,10 @@
 //                tiles alternating on the tensor core.
 //   d = 256:     fa_fwd_tp.cuh — one query tile per CTA (O takes half of TMEM),
 //                BN = 96, S double-buffered in TMEM with P packed over it.
-//   e4m3 inputs: the same kernels instantiated for 8-bit operands (d = 128:
-//                fa_fwd_tm.cuh; d = 256: fa_fwd_tp.cuh).
+//   e4m3 inputs: the same kernels instantiated for 8-bit operands (d = 64,
+//                128: fa_fwd_tm.cuh; d = 256: fa_fwd_tp.cuh).
+//   Plain launches of at least four waves of units at d = 64, 128 run the
+//   two-tile kernel's persistent form (one CTA per SM).
 #pragma once
 
 #include <type_traits>

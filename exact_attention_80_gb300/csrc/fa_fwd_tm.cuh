@@ -38,12 +38,15 @@
 // leave at their next wait, in-flight TMA copies and MMAs are waited for
 // (again bounded), TMEM is freed and the CTA exits.
 //
-// Compile-time forms of the one body (tm_forward<D, F8, DUAL>):
-//   F8    e4m3 Q, K, V: kind::f8f6f4 MMAs, P packed four e4m3 per TMEM column,
-//         bf16 O staged in buffers of its own (fa_fwd_tm8_kernel).
-//   DUAL  split-KV with one query tile: both tile slots on the same rows, each
-//         with its own key split (tm_dual_control; fa_fwd_tmd_kernel,
-//         fa_fwd_tm8d_kernel).
+// Compile-time forms of the one body (tm_forward<D, F8, DUAL, PERSIST>):
+//   F8       e4m3 Q, K, V: kind::f8f6f4 MMAs, P packed four e4m3 per TMEM
+//            column, bf16 O staged in buffers of its own (fa_fwd_tm8_kernel).
+//   DUAL     split-KV with one query tile: both tile slots on the same rows,
+//            each with its own key split (tm_dual_control; fa_fwd_tmd_kernel,
+//            fa_fwd_tm8d_kernel).
+//   PERSIST  one CTA per SM walking several query units, the ring and the
+//            barrier phases carried across them (tm_persist_control;
+//            fa_fwd_tmp_kernel, fa_fwd_tmp8_kernel).
 #pragma once
 
 #include <type_traits>
