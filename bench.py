@@ -355,6 +355,10 @@ def extra_workloads(device, stream, reps: int = 20):
                     f_comb()
                 ms_s = statistics.median(time_launches(f_split, reps, stream, queue_ahead=True))
                 ms_c = statistics.median(time_launches(f_comb, reps, stream, queue_ahead=True))
+                # The decode step as a caller runs it: split, then merge, back to
+                # back (the merge's launch overlaps the split's tail).
+                ms_sc = statistics.median(time_launches(lambda: (f_split(), f_comb()), reps, stream,
+                                                        queue_ahead=True))
                 kv_bytes = 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2
                 part = S * B * H * Nq * (d + 2) * 4
                 comb_bytes = part + B * H * Nq * (d * 2 + 4)
@@ -362,7 +366,10 @@ def extra_workloads(device, stream, reps: int = 20):
                     "tflops": round(flops / (ms_s + ms_c) / 1e9, 1),
                     "split_us": round(ms_s * 1e3, 1), "combine_us": round(ms_c * 1e3, 1),
                     "split_gbs": round((kv_bytes + part) / ms_s / 1e6, 1),
-                    "combine_gbs": round(comb_bytes / ms_c / 1e6, 1)}
+                    "combine_gbs": round(comb_bytes / ms_c / 1e6, 1),
+                    "split_then_combine_us": round(ms_sc * 1e3, 1),
+                    "combine_in_sequence_us": round((ms_sc - ms_s) * 1e3, 1),
+                    "tflops_in_sequence": round(flops / ms_sc / 1e9, 1)}
             out[name] = sweep
         del q, k, v, o, lse
     out["c3_tile_sweep"] = tile_sweep(device, stream, reps)

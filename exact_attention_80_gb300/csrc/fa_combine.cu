@@ -22,6 +22,7 @@
 #include <cuda_bf16.h>
 
 #include "fa_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace fa {
 
@@ -74,6 +75,9 @@ __global__ void __launch_bounds__(256)
     __shared__ float part[Sh::MAX_WARPS][D];
     __shared__ float wsh[Sh::MAX_WARPS][FA_MAX_SPLITS];
 
+    // Launched with programmatic stream serialization after the split-KV
+    // kernel: nothing here reads the workspace before that grid has completed.
+    griddep_wait();
     const int S = num_splits;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows_per_block = (blockDim.x >> 5) / W;
@@ -223,6 +227,14 @@ cudaError_t launch_combine_d(const float* ws_o, const float* ws_m, const float* 
     cfg.blockDim = dim3(static_cast<unsigned>(warps * 32), 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
+    // Programmatic dependent launch: the merge may be scheduled while the
+    // split-KV grid before it in the stream finishes (the kernel waits for that
+    // grid's completion before its first read), which hides the launch gap.
+    cudaLaunchAttribute attr = {};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, fa_combine_kernel<D>, ws_o, ws_m, ws_l, o, lse, rows,
                               num_splits, W);
 }
