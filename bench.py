@@ -278,6 +278,17 @@ def time_launches(fn, steps: int, stream, queue_ahead: bool = False):
     return [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
 
 
+def spread_us(times_ms) -> dict:
+    """Median, 10th and 90th percentile of per-launch times, in microseconds."""
+    xs = sorted(times_ms)
+    n = len(xs)
+
+    def q(f):
+        return round(xs[min(n - 1, int(f * (n - 1) + 0.5))] * 1e3, 1)
+
+    return {"median_us": round(statistics.median(xs) * 1e3, 1), "p10_us": q(0.1), "p90_us": q(0.9)}
+
+
 def fill_splits(fa, B, H, Nq, d, sms):
     """The largest split count whose split-KV grid still fits one CTA per SM."""
     best = 1
@@ -335,8 +346,11 @@ def extra_workloads(device, stream, reps: int = 20):
             fn = lambda: fa.fa_fwd(q, k, v, o, lse, causal, stream=stream)  # noqa: E731
             for _ in range(3):
                 fn()
-            ms = statistics.median(time_launches(fn, reps, stream, queue_ahead=True))
-            out[name] = {"tflops": round(flops / ms / 1e9, 1), "us": round(ms * 1e3, 1)}
+            times = time_launches(fn, reps, stream, queue_ahead=True)
+            ms = statistics.median(times)
+            sp = spread_us(times)
+            out[name] = {"tflops": round(flops / ms / 1e9, 1), "us": round(ms * 1e3, 1),
+                         "p10_us": sp["p10_us"], "p90_us": sp["p90_us"]}
             if c.get("outlier_frac"):
                 out[name]["inputs"] = (f"N(0,1) bf16, {c['outlier_frac']:.0%} of K rows per head "
                                        "scaled x8 (seeded permutation)")
@@ -353,12 +367,13 @@ def extra_workloads(device, stream, reps: int = 20):
                 for _ in range(3):
                     f_split()
                     f_comb()
-                ms_s = statistics.median(time_launches(f_split, reps, stream, queue_ahead=True))
-                ms_c = statistics.median(time_launches(f_comb, reps, stream, queue_ahead=True))
+                t_s = time_launches(f_split, reps, stream, queue_ahead=True)
+                t_c = time_launches(f_comb, reps, stream, queue_ahead=True)
                 # The decode step as a caller runs it: split, then merge, back to
                 # back (the merge's launch overlaps the split's tail).
-                ms_sc = statistics.median(time_launches(lambda: (f_split(), f_comb()), reps, stream,
-                                                        queue_ahead=True))
+                t_sc = time_launches(lambda: (f_split(), f_comb()), reps, stream, queue_ahead=True)
+                ms_s, ms_c, ms_sc = (statistics.median(t) for t in (t_s, t_c, t_sc))
+                sp_sc = spread_us(t_sc)
                 kv_bytes = 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2
                 part = S * B * H * Nq * (d + 2) * 4
                 comb_bytes = part + B * H * Nq * (d * 2 + 4)
@@ -368,6 +383,7 @@ def extra_workloads(device, stream, reps: int = 20):
                     "split_gbs": round((kv_bytes + part) / ms_s / 1e6, 1),
                     "combine_gbs": round(comb_bytes / ms_c / 1e6, 1),
                     "split_then_combine_us": round(ms_sc * 1e3, 1),
+                    "split_then_combine_p10_p90_us": [sp_sc["p10_us"], sp_sc["p90_us"]],
                     "combine_in_sequence_us": round((ms_sc - ms_s) * 1e3, 1),
                     "tflops_in_sequence": round(flops / ms_sc / 1e9, 1)}
             out[name] = sweep
@@ -693,6 +709,9 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = dist_sum(flops, world, device) * args.steps / (total_ms / 1e3) / 1e12
     avg_launch_ms = statistics.mean(per_step)
+    # Spread of this rank's per-launch times (median, p10, p90), from the same
+    # events as avg_launch_ms.
+    launch_spread = spread_us(per_step)
 
     # ---- numeric check outside the timed window: one whole (b, h) head, chosen
     # by the seed, element by element against the oracle
@@ -767,6 +786,7 @@ def run_ours(args):
                 "how": f"fa_fwd_from_host: the batch in {e2e_launches} slices along B, host-to-device "
                        "copies, kernels and device-to-host copies on three streams"},
         "gpu_launches": args.steps,
+        "per_launch": launch_spread,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "parity_whole_head": {"head": [b, h], "max_abs": worst, "rel_l2": rel, "lse_abs": lse_err},
