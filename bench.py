@@ -211,13 +211,17 @@ def recorded_traffic(kernel: str, workload: str):
     return None
 
 
-def kernel_name(fa, B: int, H: int, Nq: int, d: int, sms: int) -> str:
+def kernel_name(fa, B: int, H: int, Nq: int, d: int, sms: int, Nk: int | None = None,
+                causal: bool = False) -> str:
     """The forward kernel fa_fwd launches for this shape: the one-tile kernel at
     d = 256; at d = 64 and 128 the two-tile kernel, with persistent CTAs when its
-    work units fill four waves of one CTA per SM (include/fa.h, fa_fwd)."""
+    work units fill four waves of one CTA per SM and span at most 16 key tiles of
+    128 (32 for non-causal d = 128) (include/fa.h, fa_fwd)."""
     if d == 256:
         return f"fa_fwd_tp_kernel<{d}>"
-    if fa.fa_fwd_grid_ctas(B, H, Nq, d, 1) >= 4 * sms:
+    key_tiles = -(-(Nq if Nk is None else Nk) // 128)
+    short_units = key_tiles <= 16 or (d == 128 and not causal and key_tiles <= 32)
+    if short_units and fa.fa_fwd_grid_ctas(B, H, Nq, d, 1) >= 4 * sms:
         return f"fa_fwd_tmp_kernel<{d}>"
     return f"fa_fwd_tm_kernel<{d}>"
 
@@ -526,7 +530,7 @@ def fp8_workload(device, stream, reps, shape=(8, 32, 2048, 128), causal=False, s
     tflops = metric_flops(B, H, N, N, d, causal) / ms / 1e9
     peak_tf, _, kind = measured_peaks()
     sms = torch.cuda.get_device_properties(device).multi_processor_count
-    kernel = kernel_name(fa, B, H, N, d, sms).replace("_kernel", "8_kernel")
+    kernel = kernel_name(fa, B, H, N, d, sms, N, causal).replace("_kernel", "8_kernel")
     return {"tflops": round(tflops, 1), "us": round(ms * 1e3, 1), "kernel": kernel,
             "shape": f"B={B} H={H} N={N} d={d} {'causal' if causal else 'non-causal'}",
             "roofline_frac": round(tflops / (2.0 * peak_tf), 4),
@@ -767,7 +771,8 @@ def run_ours(args):
                "sample": f"{heads} passes of the float64 NumPy oracle over one seeded "
                          f"{c['Nq']}x{c['Nk']} d={d} head of {wl} (the same synthetic head each "
                          f"time, all its queries against all its keys), {secs:.1f} s"}
-    kname = kernel_name(fa, B, H, Nq, d, torch.cuda.get_device_properties(device).multi_processor_count)
+    kname = kernel_name(fa, B, H, Nq, d, torch.cuda.get_device_properties(device).multi_processor_count,
+                        Nk, bool(causal))
     line = {
         "metric": "attention fwd TFLOPS (bf16, 4*B*H*Nq*Nk*d, halved for causal)",
         "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,

@@ -207,10 +207,14 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
                          int tiles_per_cta = 0) {
     const FwdConfig c = fwd_config(d);
     // Persistent CTAs for the plain dense forward of the two-tile kernel
-    // when its units fill at least four waves of CTAs, where the saved CTA
-    // start-up and Q latency outweigh the persistent control code's slower
-    // key steps (fa_fwd_rows, which fixes the rows per CTA, keeps one unit per
-    // CTA).
+    // when its units fill at least four waves of CTAs and are short: the saved
+    // CTA start-up and Q latency are per unit, the persistent control code's
+    // slower key steps per step, and its static schedule balances long causal
+    // units worse than the hardware does. Measured crossover (one unit per CTA
+    // against persistent): persistent wins up to 16 key tiles of 128 (Nk <=
+    // 2048), and non-causal d = 128 up to 32; beyond, one unit per CTA is as
+    // fast or faster (up to 24 % on long causal sequences). fa_fwd_rows, which
+    // fixes the rows per CTA, keeps one unit per CTA.
     const bool row_choice = tiles_per_cta > 0;
     if (tiles_per_cta <= 0) tiles_per_cta = c.q_tiles;
     const long long ctas = grid_ctas(B, H, Nq, d, num_splits, tiles_per_cta);
@@ -283,7 +287,10 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
 
     cudaError_t e = cudaErrorInvalidValue;
     p.dual = dual ? 1 : 0;
-    const bool persist = !row_choice && !vl && !split_mode && (d == 64 || d == 128) && ctas >= 4ll * sms;
+    const int key_tiles = (Nk + 127) / 128;
+    const bool short_units = key_tiles <= 16 || (d == 128 && !causal && key_tiles <= 32);
+    const bool persist =
+        !row_choice && !vl && !split_mode && (d == 64 || d == 128) && short_units && ctas >= 4ll * sms;
     p.total_units = ctas;
     const unsigned grid = static_cast<unsigned>(
         dual ? static_cast<long long>(BH) * ((num_splits + 1) / 2) : (persist ? sms : ctas));

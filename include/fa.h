@@ -80,7 +80,8 @@ typedef enum {
  * "从头级并行转向序列级并行": query tiles of one head go to different CTAs, no
  * cross-CTA reduction). Causal tiles that lie wholly above the diagonal are
  * skipped. One CTA per unit, except at d = 64 and 128 when the units fill at
- * least four waves of CTAs (four per SM): then one persistent CTA per SM walks
+ * least four waves of CTAs (four per SM) and are short (Nk within 16 key tiles
+ * of 128, or 32 for non-causal d = 128): then one persistent CTA per SM walks
  * its share of the units in order, so that a unit's Q load and start-up
  * overlap the previous unit's last key steps. The result is the same bit for
  * bit either way.
@@ -253,8 +254,8 @@ fa_status fa_fwd_rows(const void* q, const void* k, const void* v, void* o, floa
 /*
  * fa_fwd_grid_ctas — number of work units (CTAs of one unit each) fa_fwd
  * (num_splits = 1) or fa_fwd_splitkv would run for this shape (fa_fwd launches
- * one persistent CTA per SM instead when the units fill four waves, see
- * fa_fwd): B * H * ceil(Nq / BM) * num_splits,
+ * one persistent CTA per SM instead when the units fill four waves and are
+ * short, see fa_fwd): B * H * ceil(Nq / BM) * num_splits,
  * BM = 256 query rows per CTA for d <= 128 (two 128-row tiles) and 128 for
  * d = 256 ("AI 大模型之 FlashAttention_02", section "从头级并行转向序列级并行" and
  * the printed CTA counts of section "本册配套实验验证记录"). Split-KV launches
