@@ -77,7 +77,9 @@ __global__ void __launch_bounds__(256)
 
     // Launched with programmatic stream serialization after the split-KV
     // kernel: nothing here reads the workspace before that grid has completed.
+    // A forward launched next may be scheduled once every CTA here has started.
     griddep_wait();
+    if (threadIdx.x == 0) griddep_launch_dependents();
     const int S = num_splits;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows_per_block = (blockDim.x >> 5) / W;

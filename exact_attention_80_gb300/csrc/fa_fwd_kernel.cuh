@@ -60,8 +60,14 @@ cudaError_t launch_fwd(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     cfg.blockDim = dim3(L::THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::ALLOC_BYTES;
     cfg.stream = stream;
-    cfg.attrs = nullptr;
-    cfg.numAttrs = 0;
+    // Programmatic dependent launch: the kernels wait for the previous grid in
+    // the stream before touching global memory, so their launch and start-up
+    // may overlap its end.
+    cudaLaunchAttribute attr = {};
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kernel, p);
 }
 

@@ -647,10 +647,13 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Split-KV partials are merged by fa_combine, launched with programmatic
-    // stream serialization: it may be scheduled once every CTA here has started
-    // (it waits for this grid's completion before reading the workspace).
-    if (p.split_mode && threadIdx.x == 0) griddep_launch_dependents();
+    // Launched with programmatic stream serialization: nothing here reads or
+    // writes global memory before the grid before it in the stream has
+    // completed (griddep_wait), and a grid launched the same way after this one
+    // (the next forward, or fa_combine's merge of these partial states) may be
+    // scheduled once every CTA here has started; it waits in turn.
+    griddep_wait();
+    if (threadIdx.x == 0) griddep_launch_dependents();
 
 
     if (threadIdx.x == 0) {

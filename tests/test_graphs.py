@@ -66,6 +66,7 @@ def test_graph_replay_matches_eager(B, H, Nq, Nk, splits, causal):
     ws = torch.empty(fa.fa_splitkv_workspace_bytes(B, H, Nq, d, splits) // 4, device=dev)
 
     stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize()  # inputs and outputs made on the default stream
     with torch.cuda.stream(stream):
         _calls(q, k, v, outs, ws, splits, causal, scale, stream)  # warm-up (kernel attributes, scratch)
     stream.synchronize()
@@ -83,13 +84,18 @@ def test_graph_replay_matches_eager(B, H, Nq, Nk, splits, causal):
     torch.cuda.synchronize()
     assert fa.fa_device_status(clear=True) == fa.FA_OK
     replayed = [t.clone() for t in outs]
+    torch.cuda.synchronize()  # the clones are read before the eager calls overwrite the outputs
 
     # The same calls made eagerly on the new inputs.
     with torch.cuda.stream(stream):
         _calls(q, k, v, outs, ws, splits, causal, scale, stream)
     stream.synchronize()
     assert fa.fa_device_status(clear=True) == fa.FA_OK
-    for a, b in zip(replayed, outs):
+    # Outputs the calls wrote (the allocation-free call runs only where its
+    # partial states fit the library's scratch; unwritten buffers hold stale
+    # bits, NaN patterns included).
+    written = 6 if _static_fits(B, H, Nq, d) else 4
+    for a, b in zip(replayed[:written], outs[:written]):
         assert torch.equal(a, b)
 
     qc, kc, vc = q.cpu(), k.cpu(), v.cpu()
