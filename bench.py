@@ -282,6 +282,22 @@ def time_launches(fn, steps: int, stream, queue_ahead: bool = False):
     return [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
 
 
+def time_back_to_back(fn, steps: int, stream) -> float:
+    """Mean ms per call of `steps` calls queued behind a device sleep and
+    bracketed by one pair of CUDA events (nothing between the calls)."""
+    import torch
+
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(200_000 * steps)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
 def spread_us(times_ms) -> dict:
     """Median, 10th and 90th percentile of per-launch times, in microseconds."""
     xs = sorted(times_ms)
@@ -355,6 +371,11 @@ def extra_workloads(device, stream, reps: int = 20):
             sp = spread_us(times)
             out[name] = {"tflops": round(flops / ms / 1e9, 1), "us": round(ms * 1e3, 1),
                          "p10_us": sp["p10_us"], "p90_us": sp["p90_us"]}
+            if name == "c1":
+                # A launch-bound call: also the mean over calls issued back to back
+                # with no event between them (as a loop of small attention calls
+                # runs), where one call's launch overlaps the previous one's end.
+                out[name]["us_back_to_back"] = round(time_back_to_back(fn, 200, stream) * 1e3, 2)
             if c.get("outlier_frac"):
                 out[name]["inputs"] = (f"N(0,1) bf16, {c['outlier_frac']:.0%} of K rows per head "
                                        "scaled x8 (seeded permutation)")
