@@ -722,21 +722,25 @@ def run_ours(args):
         sampler.start()
     dist_barrier(world, device)
     torch.cuda.synchronize()
-    per_step = time_launches(step, args.steps, stream)
+    # The K steps back to back between one pair of CUDA events (queued behind a
+    # device sleep so that the host's launch rate does not show): an event
+    # between launches would serialise each launch against the previous one's
+    # end.
+    local_ms = time_back_to_back(step, args.steps, stream) * args.steps
     torch.cuda.synchronize()
     dist_barrier(world, device)
     if sampler:
         sampler.stop()
-    total_ms = dist_max(sum(per_step), world, device)
+    total_ms = dist_max(local_ms, world, device)
     status = fa.fa_device_status(clear=True, stream=stream)
     if status != fa.FA_OK:
         raise RuntimeError(f"device status {fa.fa_status_string(status)}")
     ms_per_step = total_ms / args.steps
     value = dist_sum(flops, world, device) * args.steps / (total_ms / 1e3) / 1e12
-    avg_launch_ms = statistics.mean(per_step)
-    # Spread of this rank's per-launch times (median, p10, p90), from the same
-    # events as avg_launch_ms.
-    launch_spread = spread_us(per_step)
+    avg_launch_ms = local_ms / args.steps
+    # Spread of the per-launch time (median, p10, p90): a separate pass with an
+    # event after every launch, outside the timed region.
+    launch_spread = spread_us(time_launches(step, min(args.steps, 200), stream, queue_ahead=True))
 
     # ---- numeric check outside the timed window: one whole (b, h) head, chosen
     # by the seed, element by element against the oracle
