@@ -923,8 +923,9 @@ def main(argv=None):
                     help="seconds of float64 oracle work for cpu_baseline")
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-chunks", type=int, default=4,
-                    help="slices of the batch whose copies overlap the kernels end to end")
+    ap.add_argument("--e2e-chunks", type=int, default=8,
+                    help="slices of the batch (along B) whose copies overlap the kernels end to "
+                         "end: 8 gave 239 TFLOPS on C2 against 232 with 4, 16 the same as 8")
     ap.add_argument("--case", default=None,
                     help="run one workload's kernels only, for an ncu capture (see run_case)")
     args = ap.parse_args(argv)
