@@ -794,7 +794,7 @@ def run_ours(args):
     dist_barrier(world, device)
     e2e_ms = dist_max(sum(time_launches(e2e_step, e2e_steps, stream)), world, device) / e2e_steps
     e2e_value = dist_sum(flops, world, device) / (e2e_ms / 1e3) / 1e12
-    e2e_launches = min(args.e2e_chunks, B)
+    e2e_launches = min(args.e2e_chunks, B * H)
     h2d = (qp.numel() + kp.numel() + vp.numel()) * 2
     d2h = op.numel() * 2 + lp.numel() * 4
 
@@ -835,7 +835,7 @@ def run_ours(args):
                      "flops_per_launch": flops},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "how": f"fa_fwd_from_host: the batch in {e2e_launches} slices along B, host-to-device "
+                "how": f"fa_fwd_from_host: the heads in {e2e_launches} slices, host-to-device "
                        "copies, kernels and device-to-host copies on three streams"},
         "gpu_launches": args.steps,
         "per_launch": launch_spread,
@@ -924,8 +924,8 @@ def main(argv=None):
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-chunks", type=int, default=8,
-                    help="slices of the batch (along B) whose copies overlap the kernels end to "
-                         "end: 8 gave 239 TFLOPS on C2 against 232 with 4, 16 the same as 8")
+                    help="slices of consecutive (b, h) heads whose copies overlap the kernels end "
+                         "to end")
     ap.add_argument("--case", default=None,
                     help="run one workload's kernels only, for an ncu capture (see run_case)")
     args = ap.parse_args(argv)

@@ -454,11 +454,13 @@ def fa_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse, 
     ``q_host``, ``k_host``, ``v_host`` (bf16 [B,H,N,d]) are copied into the
     device tensors ``q``, ``k``, ``v`` of the same shapes, the forward writes the
     device ``o``, ``lse``, and they are copied back into ``o_host``, ``lse_host``.
-    The batch is cut into ``chunks`` slices along B so that the copies of one
-    slice overlap the kernel of another: host-to-device copies on one side
-    stream, the kernels on ``stream``, device-to-host copies on another. Every
-    call starts after the work already queued on ``stream`` and ``stream`` waits
-    for the last copy back, so a caller synchronises on ``stream`` alone.
+    The (b, h) heads are cut into ``chunks`` slices of consecutive heads
+    (contiguous in every tensor; each slice runs as one forward over its heads)
+    so that the copies of one slice overlap the kernel of another:
+    host-to-device copies on one side stream, the kernels on ``stream``,
+    device-to-host copies on another. Every call starts after the work already
+    queued on ``stream`` and ``stream`` waits for the last copy back, so a caller
+    synchronises on ``stream`` alone.
     """
     import torch
 
@@ -470,27 +472,32 @@ def fa_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse, 
         _need(t, name, tuple(dev_t.shape), dev_t.dtype, cpu)
         if not t.is_pinned():
             raise ValueError(f"{name} must be in pinned host memory")
-    chunks = max(1, min(int(chunks), B))
+    BH = B * H
+    chunks = max(1, min(int(chunks), BH))
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     s_in, s_out = _side_streams(q.device)
     s_in.wait_stream(stream)
-    bounds = [(B * i // chunks, B * (i + 1) // chunks) for i in range(chunks)]
+    # Heads flattened: [1, B*H, N, d] views (contiguous tensors, checked above).
+    flat = lambda t: t.view(1, BH, *t.shape[2:])  # noqa: E731
+    qh, kh, vh, oh, lh = (flat(t) for t in (q_host, k_host, v_host, o_host, lse_host))
+    qd, kd, vd, od, ld = (flat(t) for t in (q, k, v, o, lse))
+    bounds = [(BH * i // chunks, BH * (i + 1) // chunks) for i in range(chunks)]
     done_out = None
-    for b0, b1 in bounds:
+    for h0, h1 in bounds:
         with torch.cuda.stream(s_in):
-            for src, dst in ((q_host, q), (k_host, k), (v_host, v)):
-                dst[b0:b1].copy_(src[b0:b1], non_blocking=True)
+            for src, dst in ((qh, qd), (kh, kd), (vh, vd)):
+                dst[:, h0:h1].copy_(src[:, h0:h1], non_blocking=True)
             ev_in = torch.cuda.Event()
             ev_in.record(s_in)
         stream.wait_event(ev_in)
-        fa_fwd(q[b0:b1], k[b0:b1], v[b0:b1], o[b0:b1], lse[b0:b1], causal, scale, stream)
+        fa_fwd(qd[:, h0:h1], kd[:, h0:h1], vd[:, h0:h1], od[:, h0:h1], ld[:, h0:h1], causal, scale, stream)
         ev_c = torch.cuda.Event()
         ev_c.record(stream)
         s_out.wait_event(ev_c)
         with torch.cuda.stream(s_out):
-            o_host[b0:b1].copy_(o[b0:b1], non_blocking=True)
-            lse_host[b0:b1].copy_(lse[b0:b1], non_blocking=True)
+            oh[:, h0:h1].copy_(od[:, h0:h1], non_blocking=True)
+            lh[:, h0:h1].copy_(ld[:, h0:h1], non_blocking=True)
             done_out = torch.cuda.Event()
             done_out.record(s_out)
     stream.wait_event(done_out)
