@@ -383,12 +383,13 @@ def test_shift_invariance_on_gpu():
     assert (o1.float() - o2.float()).abs().max().item() <= 2 * MAX_ABS
 
 
-@pytest.mark.parametrize("chunks", [1, 3, 4])
+@pytest.mark.parametrize("chunks", [1, 3, 4, 5, 12])
 def test_forward_from_pinned_host_buffers(chunks):
-    """fa_fwd_from_host (copies of one batch slice overlapping the kernel of
-    another, on three streams) gives bit for bit what fa_fwd gives on
-    device-resident inputs, and matches the oracle; a second call reuses the
-    staging buffers."""
+    """fa_fwd_from_host (copies of one slice of consecutive (b, h) heads
+    overlapping the kernel of another, on three streams; slices that cross
+    batch entries, uneven ones, one head each) gives bit for bit what fa_fwd
+    gives on device-resident inputs, and matches the oracle; a second call
+    reuses the staging buffers."""
     B, H, Nq, Nk, d = 4, 3, 300, 333, 128
     q, k, v = make_qkv(B, H, Nq, Nk, d, 4040 + chunks)
     scale = f32(1.0 / math.sqrt(d))
