@@ -72,7 +72,9 @@ struct TmCfg<128> {
 template <int D>
 struct TmPersistCfg {
     static constexpr int STAGES = D == 128 ? 4 : 8;
-    static constexpr int CTRL_REGS = D == 128 ? 88 : 104, SOFTMAX_REGS = D == 128 ? 208 : 200;
+    // Spill-free at both head dims (104 / 200 spilled at d = 64 once the kernels
+    // wait for the previous grid; 88 / 208 is also 2 % faster there).
+    static constexpr int CTRL_REGS = 88, SOFTMAX_REGS = 208;
 };
 // 8-bit (e4m3) inputs: K/V slots are half the size, so the ring is deeper.
 template <int D>
