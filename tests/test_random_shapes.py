@@ -28,6 +28,7 @@ def _needs_cuda():
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA device")
 
+
 MAX_ABS = 2e-2
 REL_L2 = 5e-3
 LSE_ABS = 1e-3
