@@ -79,6 +79,36 @@ def make_grad_output(B: int, H: int, Nq: int, d: int, seed: int):
     return torch.randn((B, H, Nq, d), generator=g, dtype=torch.float32).to(torch.bfloat16)
 
 
+def make_device_normal(shape, seed: int, device, dtype=None, chunk: int = 1 << 28):
+    """A tensor of i.i.d. N(0, 1) draws made on ``device`` by a seeded device
+    generator, in float32 and rounded to ``dtype`` (bf16 by default), filled
+    ``chunk`` elements at a time so that no float32 copy of the whole tensor is
+    held. For sizes too large to draw on the host; only the rows a test checks
+    are copied back for the oracle."""
+    dtype = torch.bfloat16 if dtype is None else dtype
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    t = torch.empty(shape, dtype=dtype, device=device)
+    flat = t.view(-1)
+    for i in range(0, flat.numel(), chunk):
+        n = min(chunk, flat.numel() - i)
+        flat[i:i + n] = torch.randn(n, generator=g, dtype=torch.float32, device=device).to(dtype)
+    return t
+
+
+def make_device_e4m3(shape, seed: int, device, descale: float, chunk: int = 1 << 28):
+    """e4m3 codes (uint8) made on ``device`` by the recipe of
+    :func:`make_qkv_fp8` (N(0, 1) / descale, clamped to +-448, rounded by
+    torch), from a seeded device generator, ``chunk`` elements at a time."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    t = torch.empty(shape, dtype=torch.uint8, device=device)
+    flat = t.view(-1)
+    for i in range(0, flat.numel(), chunk):
+        n = min(chunk, flat.numel() - i)
+        x = (torch.randn(n, generator=g, dtype=torch.float32, device=device) / float(descale)).clamp(-448.0, 448.0)
+        flat[i:i + n] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+    return t
+
+
 def to_f64(t):
     """Exact upcast of a (bf16) torch tensor to a float64 numpy array."""
     return t.to(torch.float64).numpy()
