@@ -794,7 +794,7 @@ def run_ours(args):
     dist_barrier(world, device)
     e2e_ms = dist_max(sum(time_launches(e2e_step, e2e_steps, stream)), world, device) / e2e_steps
     e2e_value = dist_sum(flops, world, device) / (e2e_ms / 1e3) / 1e12
-    e2e_launches = min(args.e2e_chunks, B * H)
+    e2e_launches = len(fa.head_slices(B * H, args.e2e_chunks))
     h2d = (qp.numel() + kp.numel() + vp.numel()) * 2
     d2h = op.numel() * 2 + lp.numel() * 4
 
@@ -835,8 +835,9 @@ def run_ours(args):
                      "flops_per_launch": flops},
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                "how": f"fa_fwd_from_host: the heads in {e2e_launches} slices, host-to-device "
-                       "copies, kernels and device-to-host copies on three streams"},
+                "how": f"fa_fwd_from_host: the heads in {e2e_launches} slices (the last two a half "
+                       "and a quarter of the others), host-to-device copies, kernels and "
+                       "device-to-host copies on three streams"},
         "gpu_launches": args.steps,
         "per_launch": launch_spread,
         "clocks": clocks,

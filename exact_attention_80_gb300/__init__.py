@@ -447,6 +447,28 @@ def _side_streams(device):
     return _SIDE_STREAMS[key]
 
 
+def head_slices(BH: int, chunks: int):
+    """The ``(h0, h1)`` bounds :func:`fa_fwd_from_host` cuts ``BH`` heads into:
+    at most ``chunks`` non-empty slices of consecutive heads covering
+    ``[0, BH)``. With three or more, the last two slices get a half and a
+    quarter of the others' share: the last slice's kernel and copy back run
+    after every copy in has finished, so a smaller last slice leaves less of
+    the call uncovered."""
+    chunks = max(1, min(int(chunks), BH))
+    weights = [1.0] * (chunks - 2) + [0.5, 0.25] if chunks >= 3 else [1.0] * chunks
+    total = sum(weights)
+    bounds, acc, prev = [], 0.0, 0
+    for w in weights:
+        acc += w
+        cur = min(BH, int(round(BH * acc / total)))
+        if cur > prev:
+            bounds.append((prev, cur))
+            prev = cur
+    if prev < BH:
+        bounds.append((prev, BH))
+    return bounds
+
+
 def fa_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse, causal=False,
                      scale: float | None = None, chunks: int = 4, stream=None):
     """The forward of :func:`fa_fwd` on inputs and outputs in pinned host memory.
@@ -454,9 +476,10 @@ def fa_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse, 
     ``q_host``, ``k_host``, ``v_host`` (bf16 [B,H,N,d]) are copied into the
     device tensors ``q``, ``k``, ``v`` of the same shapes, the forward writes the
     device ``o``, ``lse``, and they are copied back into ``o_host``, ``lse_host``.
-    The (b, h) heads are cut into ``chunks`` slices of consecutive heads
-    (contiguous in every tensor; each slice runs as one forward over its heads)
-    so that the copies of one slice overlap the kernel of another:
+    The (b, h) heads are cut into at most ``chunks`` slices of consecutive heads
+    (:func:`head_slices`; contiguous in every tensor, each slice runs as one
+    forward over its heads) so that the copies of one slice overlap the kernel
+    of another:
     host-to-device copies on one side stream, the kernels on ``stream``,
     device-to-host copies on another. Every call starts after the work already
     queued on ``stream`` and ``stream`` waits for the last copy back, so a caller
@@ -473,7 +496,6 @@ def fa_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse, 
         if not t.is_pinned():
             raise ValueError(f"{name} must be in pinned host memory")
     BH = B * H
-    chunks = max(1, min(int(chunks), BH))
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     s_in, s_out = _side_streams(q.device)
@@ -482,7 +504,7 @@ def fa_fwd_from_host(q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse, 
     flat = lambda t: t.view(1, BH, *t.shape[2:])  # noqa: E731
     qh, kh, vh, oh, lh = (flat(t) for t in (q_host, k_host, v_host, o_host, lse_host))
     qd, kd, vd, od, ld = (flat(t) for t in (q, k, v, o, lse))
-    bounds = [(BH * i // chunks, BH * (i + 1) // chunks) for i in range(chunks)]
+    bounds = head_slices(BH, chunks)
     done_out = None
     for h0, h1 in bounds:
         with torch.cuda.stream(s_in):

@@ -150,3 +150,20 @@ def test_static_scratch_outputs_checked(stub):
     with pytest.raises(ValueError):
         fa.fa_fwd_splitkv_static(q, k, k, bf16(1, 2, 64, 128), f32(1, 2, 63), 4, stream=0)
     assert stub.calls == ["fa_fwd_splitkv_static"]
+
+
+@pytest.mark.parametrize("BH,chunks", [(256, 8), (256, 1), (256, 2), (256, 3), (256, 12), (3, 8),
+                                       (1, 8), (7, 5), (5, 5), (1000, 64)])
+def test_head_slices_cover_the_heads(BH, chunks):
+    """fa_fwd_from_host's slices: consecutive, non-empty, covering [0, BH), at
+    most `chunks` of them; with three or more, the last two are no larger than
+    the ones before them."""
+    b = fa.head_slices(BH, chunks)
+    assert 1 <= len(b) <= min(chunks, BH)
+    assert b[0][0] == 0 and b[-1][1] == BH
+    assert all(h0 < h1 for h0, h1 in b)
+    assert all(b[i][1] == b[i + 1][0] for i in range(len(b) - 1))
+    sizes = [h1 - h0 for h0, h1 in b]
+    if min(chunks, BH) >= 3 and BH >= 4 * chunks:
+        assert sizes[-1] <= sizes[-2] <= min(sizes[:-2])
+        assert sizes[-1] < max(sizes)
