@@ -299,6 +299,28 @@ def time_launches(fn, steps: int, stream, queue_ahead: bool = False):
     return [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
 
 
+def time_alternating(fa_fn, fb_fn, steps: int, stream):
+    """Per-launch ms of `fa_fn` and `fb_fn` run alternately (a, b, a, b, ...) in
+    one sequence queued behind a device sleep, an event between every two
+    launches; returns the two lists. A drift of the clock over the run then
+    moves both alike, so their per-pair differences stay meaningful."""
+    import torch
+
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps + 1)]
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(400_000 * steps)
+    evs[0].record(stream)
+    for i in range(steps):
+        fa_fn()
+        evs[2 * i + 1].record(stream)
+        fb_fn()
+        evs[2 * i + 2].record(stream)
+    torch.cuda.synchronize()
+    ta = [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(steps)]
+    tb = [evs[2 * i + 1].elapsed_time(evs[2 * i + 2]) for i in range(steps)]
+    return ta, tb
+
+
 def time_back_to_back(fn, steps: int, stream) -> float:
     """Mean ms per call of `steps` calls queued behind a device sleep and
     bracketed by one pair of CUDA events (nothing between the calls)."""
@@ -409,12 +431,13 @@ def extra_workloads(device, stream, reps: int = 20):
                 for _ in range(3):
                     f_split()
                     f_comb()
-                t_s = time_launches(f_split, reps, stream, queue_ahead=True)
                 t_c = time_launches(f_comb, reps, stream, queue_ahead=True)
                 # The decode step as a caller runs it: split, then merge, back to
-                # back (the merge's launch overlaps the split's tail).
-                t_sc = time_launches(lambda: (f_split(), f_comb()), reps, stream, queue_ahead=True)
+                # back (the merge's launch overlaps the split's tail), timed
+                # alternately with the split alone.
+                t_s, t_sc = time_alternating(f_split, lambda: (f_split(), f_comb()), reps, stream)
                 ms_s, ms_c, ms_sc = (statistics.median(t) for t in (t_s, t_c, t_sc))
+                ms_in_seq = statistics.median([b - a for a, b in zip(t_s, t_sc)])
                 sp_sc = spread_us(t_sc)
                 kv_bytes = 2 * B * H * Nk * d * 2 + 2 * B * H * Nq * d * 2
                 part = S * B * H * Nq * (d + 2) * 4
@@ -426,7 +449,7 @@ def extra_workloads(device, stream, reps: int = 20):
                     "combine_gbs": round(comb_bytes / ms_c / 1e6, 1),
                     "split_then_combine_us": round(ms_sc * 1e3, 1),
                     "split_then_combine_p10_p90_us": [sp_sc["p10_us"], sp_sc["p90_us"]],
-                    "combine_in_sequence_us": round((ms_sc - ms_s) * 1e3, 1),
+                    "combine_in_sequence_us": round(ms_in_seq * 1e3, 1),
                     "tflops_in_sequence": round(flops / ms_sc / 1e9, 1)}
             out[name] = sweep
         del q, k, v, o, lse
