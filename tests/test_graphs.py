@@ -102,3 +102,67 @@ def test_graph_replay_matches_eager(B, H, Nq, Nk, splits, causal):
     heads = [(0, 0), (B - 1, H - 1)]
     for i in range(3 if _static_fits(B, H, Nq, d) else 2):
         _check_heads(qc, kc, vc, replayed[2 * i].cpu(), replayed[2 * i + 1].cpu(), scale, causal, heads)
+
+
+def test_graph_replay_backward_fp8_varlen():
+    """The backward, the e4m3 forward and the variable-length forward captured
+    in one graph (caller-owned outputs and workspaces), replayed on new inputs
+    and compared bit for bit with the same calls made eagerly."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from exact_attention_80_gb300.inputs import make_grad_output, make_qkv_fp8, make_varlen
+
+    dev = torch.device("cuda", 0)
+    B, H, N, d = 2, 4, 300, 128
+    scale = f32(1.0 / math.sqrt(d))
+    ds = 2.0 ** -5
+    lq, lk = [100, 0, 257, 33], [90, 5, 300, 200]
+    # Captured buffers: inputs are refilled in place before the replay.
+    q, k, v = (t.to(dev) for t in make_qkv(B, H, N, N, d, 8300))
+    do = make_grad_output(B, H, N, d, 8301).to(dev)
+    q8, k8, v8 = (t.to(dev) for t in make_qkv_fp8(B, H, N, N, d, 8302))
+    qv, kv, vv, cu_q, cu_k = make_varlen(lq, lk, H, d, 8303)
+    qv, kv, vv, cu_q, cu_k = (t.to(dev) for t in (qv, kv, vv, cu_q, cu_k))
+    o, lse = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_bytes(B, H, N, d) // 4, dtype=torch.float32, device=dev)
+    o8, lse8 = torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    ov = torch.empty_like(qv)
+    lsev = torch.empty((H, qv.shape[0]), dtype=torch.float32, device=dev)
+    outs = (o, lse, dq, dk, dv, o8, lse8, ov, lsev)
+
+    def calls(st):
+        fa.fa_fwd(q, k, v, o, lse, True, scale, stream=st)
+        fa.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, True, scale, stream=st)
+        fa.fa_fwd_fp8(q8, k8, v8, ds, ds, ds, o8, lse8, False, scale, stream=st)
+        fa.fa_fwd_varlen(qv, kv, vv, ov, lsev, cu_q, cu_k, max(lq), "bottom_right", scale, stream=st)
+
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        calls(stream)  # warm-up
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        calls(torch.cuda.current_stream(dev))
+
+    q.copy_(make_qkv(B, H, N, N, d, 8400)[0].to(dev))
+    do.copy_(make_grad_output(B, H, N, d, 8401).to(dev))
+    q8.copy_(make_qkv_fp8(B, H, N, N, d, 8402)[0].to(dev))
+    vv.copy_(make_varlen(lq, lk, H, d, 8403)[2].to(dev))
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert fa.fa_device_status(clear=True) == fa.FA_OK
+    replayed = [t.clone() for t in outs]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        calls(stream)
+    stream.synchronize()
+    assert fa.fa_device_status(clear=True) == fa.FA_OK
+    for name, a, b in zip(("o", "lse", "dq", "dk", "dv", "o8", "lse8", "ov", "lsev"), replayed, outs):
+        assert torch.equal(a, b), name
+    # The replay ran on the new inputs: its output differs from the warm-up's.
+    o_ref, _ = oracle.attention_f64(to_f64(q[0, 0].cpu()), to_f64(k[0, 0].cpu()), to_f64(v[0, 0].cpu()),
+                                    scale, True)
+    assert np.abs(replayed[0][0, 0].float().cpu().numpy() - o_ref).max() <= MAX_ABS
