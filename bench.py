@@ -243,7 +243,9 @@ def kernel_name(fa, B: int, H: int, Nq: int, d: int, sms: int, Nk: int | None = 
     return f"fa_fwd_tm_kernel<{d}>"
 
 
-def cpu_threads() -> int:
+def blas_threads():
+    """The BLAS pool's thread count as threadpoolctl reports it, or None where
+    threadpoolctl is not installed."""
     try:
         from threadpoolctl import threadpool_info
 
@@ -252,7 +254,11 @@ def cpu_threads() -> int:
             return int(n[0])
     except Exception:
         pass
-    return os.cpu_count() or 1
+    return None
+
+
+def cpu_threads() -> int:
+    return blas_threads() or os.cpu_count() or 1
 
 
 def oracle_sample(cfg: dict, budget_s: float, seed: int, max_heads: int | None = None):
@@ -833,6 +839,7 @@ def run_ours(args):
     if world == 1 and not args.no_cpu_baseline:
         tf, heads, secs = oracle_sample(c, args.cpu_budget, seed)
         cpu = {"value": round(tf, 6), "unit": "TFLOPS", "cores": cpu_threads(), "kind": "oracle",
+               "os_cpu_count": os.cpu_count(), "blas_threads": blas_threads(),
                "sample": f"{heads} passes of the float64 NumPy oracle over one seeded "
                          f"{c['Nq']}x{c['Nk']} d={d} head of {wl} (the same synthetic head each "
                          f"time, all its queries against all its keys), {secs:.1f} s"}
@@ -914,7 +921,7 @@ def run_reference(args):
         "data": "synthetic (seeded N(0,1) bf16, upcast to float64)",
         "config": workload_config(wl, world),
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOPS", "cores": cpu_threads(),
-                         "kind": "oracle",
+                         "kind": "oracle", "os_cpu_count": os.cpu_count(), "blas_threads": blas_threads(),
                          "sample": f"each step = {rows_per_step} query rows of one (b,h) head "
                                    f"of {wl} against all {Nk} keys (float64 NumPy oracle)"},
         "e2e": {"value": round(value, 6), "unit": "TFLOPS", "h2d_bytes_per_step": 0,
