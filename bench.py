@@ -475,8 +475,8 @@ def extra_workloads(device, stream, reps: int = 20):
 def tile_sweep(device, stream, reps):
     """The long-sequence workload (B=1, H=8, N=8192, d=128), both masks, at each
     query-tile size a CTA can own: 256 rows (two 128-row tiles, fa_fwd's
-    choice) and 128 rows (one tile, fa_fwd_rows). Tiles of 64 rows are not
-    offered (a 128-row tile is the MMA height with one TMEM lane per row)."""
+    choice), 128 rows (one tile, fa_fwd_rows) and 64 rows (one tile of M = 64
+    MMAs, fa_fwd_rows)."""
     import torch
 
     import exact_attention_80_gb300 as fa
@@ -492,14 +492,13 @@ def tile_sweep(device, stream, reps):
         lse = torch.empty((B, H, Nq), device=device)
         flops = metric_flops(B, H, Nq, Nk, d, causal)
         line = {}
-        for rows in (256, 128):
+        for rows in (256, 128, 64):
             fn = lambda: fa.fa_fwd_rows(q, k, v, o, lse, rows, causal, stream=stream)  # noqa: E731
             for _ in range(3):
                 fn()
             ms = statistics.median(time_launches(fn, reps, stream, queue_ahead=True))
             line[f"rows_{rows}"] = {"tflops": round(flops / ms / 1e9, 1), "us": round(ms * 1e3, 1),
                                     "ctas": B * H * -(-Nq // rows)}
-        line["rows_64"] = "not offered"
         res[name] = line
         del q, k, v, o, lse
     return res

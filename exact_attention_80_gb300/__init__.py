@@ -192,7 +192,7 @@ def fa_fwd(q, k, v, o, lse, causal=False, scale: float | None = None, stream=Non
 def fa_fwd_rows(q, k, v, o, lse, rows_per_cta: int, causal=False, scale: float | None = None,
                 stream=None):
     """:func:`fa_fwd` with ``rows_per_cta`` query rows per CTA (include/fa.h,
-    fa_fwd_rows: 128 or 256 at d <= 128, 128 at d = 256)."""
+    fa_fwd_rows: 64, 128 or 256 at d <= 128, 128 at d = 256)."""
     B, H, Nq, Nk, d = _bhnd(q, k, v)
     _need_o_lse(o, lse, B, H, Nq, d, q.device)
     scale = default_scale(d) if scale is None else float(scale)

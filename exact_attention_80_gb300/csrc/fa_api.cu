@@ -183,9 +183,10 @@ fa_status check_common(const void* q, const void* k, const void* v, int B, int H
 
 namespace {
 
-long long grid_ctas(int B, int H, int Nq, int d, int num_splits, int tiles_per_cta = 0) {
+long long grid_ctas(int B, int H, int Nq, int d, int num_splits, int tiles_per_cta = 0,
+                    bool bm64 = false) {
     const FwdConfig c = fwd_config(d);
-    const long long rows_per_cta = 128ll * (tiles_per_cta > 0 ? tiles_per_cta : c.q_tiles);
+    const long long rows_per_cta = bm64 ? 64ll : 128ll * (tiles_per_cta > 0 ? tiles_per_cta : c.q_tiles);
     const long long units = (Nq + rows_per_cta - 1) / rows_per_cta;
     return static_cast<long long>(B) * H * units * num_splits;
 }
@@ -204,7 +205,7 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
                          int num_splits, int split_mode, cudaStream_t stream,
                          long long wait_limit = kDefaultWaitLimit, int withhold_q = 0,
                          const Varlen* vl = nullptr, const float* f8_descale = nullptr,
-                         int tiles_per_cta = 0) {
+                         int tiles_per_cta = 0, bool bm64 = false) {
     const FwdConfig c = fwd_config(d);
     // Persistent CTAs for the plain dense forward of the two-tile kernel
     // when its units fill at least four waves of CTAs and are short: the saved
@@ -217,7 +218,7 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     // fixes the rows per CTA, keeps one unit per CTA.
     const bool row_choice = tiles_per_cta > 0;
     if (tiles_per_cta <= 0) tiles_per_cta = c.q_tiles;
-    const long long ctas = grid_ctas(B, H, Nq, d, num_splits, tiles_per_cta);
+    const long long ctas = grid_ctas(B, H, Nq, d, num_splits, tiles_per_cta, bm64);
     if (ctas < 1 || ctas > 0x7fffffffll) return FA_ERR_SHAPE;
     const bool dual = use_dual(Nq, d, num_splits, split_mode, vl != nullptr);
 
@@ -267,6 +268,7 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
     p.split_mode = split_mode;
     p.n_units = static_cast<int>(ctas / (static_cast<long long>(BH) * num_splits));
     p.tiles_per_cta = tiles_per_cta;
+    p.bm64 = bm64 ? 1 : 0;
     const int kv_tiles = (Nk + c.bn - 1) / c.bn;
     // (Varlen: one split; every sequence's key tiles fit in ceil(total_k / BN).)
     p.kv_tiles_per_split = (kv_tiles + num_splits - 1) / num_splits;
@@ -307,6 +309,10 @@ fa_status launch_forward(const void* q, const void* k, const void* v, void* o, f
         else if (d == 256) e = launch_fwd_f8_d256(p, grid, stream);
         return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
     }
+    if (bm64) {
+        e = d == 64 ? launch_fwd_d64_rows64(p, grid, stream) : launch_fwd_d128_rows64(p, grid, stream);
+        return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+    }
     switch (d) {
         case 64: e = dual ? launch_fwd_d64_dual(p, grid, stream) : launch_fwd_d64(p, grid, stream); break;
         case 128: e = dual ? launch_fwd_d128_dual(p, grid, stream) : launch_fwd_d128(p, grid, stream); break;
@@ -341,6 +347,10 @@ fa_status fa_fwd_rows(const void* q, const void* k, const void* v, void* o, floa
     if (!o || !lse) return FA_ERR_NULL;
     if (!fa::aligned(o, 16) || !fa::aligned(lse, 4)) return FA_ERR_ALIGN;
     const int slots = fa::fwd_config(d).q_tiles;
+    // 64 rows: one M = 64 tile per CTA, at d = 64 and 128 (the two-tile kernel).
+    if (rows_per_cta == 64 && slots >= 2)
+        return fa::launch_forward(q, k, v, o, lse, nullptr, B, H, Nq, Nk, d, scale, causal, 1, 0,
+                                  stream, fa::kDefaultWaitLimit, 0, nullptr, nullptr, 1, true);
     if (rows_per_cta % 128 != 0 || rows_per_cta < 128 || rows_per_cta / 128 > slots) return FA_ERR_TILE;
     return fa::launch_forward(q, k, v, o, lse, nullptr, B, H, Nq, Nk, d, scale, causal, 1, 0,
                               stream, fa::kDefaultWaitLimit, 0, nullptr, nullptr, rows_per_cta / 128);

@@ -77,7 +77,9 @@ __device__ __forceinline__ void compute_work(const FwdParams& p, long long lin, 
     const int heads_here = min(p.head_group, p.BH - group * p.head_group);
     const int unit = p.n_units - 1 - r / heads_here;
     w.bh = group * p.head_group + r % heads_here;
-    w.q0 = unit * p.tiles_per_cta * kBM;
+    // Query rows per tile: 128, or 64 for the 64-row tiles of fa_fwd_rows.
+    const int bm = p.bm64 ? 64 : kBM;
+    w.q0 = unit * p.tiles_per_cta * bm;
     // The sequence's rows and keys: the whole head (dense), or the packed
     // sequence b of a variable-length batch.
     int len_q = p.Nq, len_k = p.Nk;
@@ -119,13 +121,13 @@ __device__ __forceinline__ void compute_work(const FwdParams& p, long long lin, 
     w.nmax = 0;
 #pragma unroll
     for (int t = 0; t < QT; ++t) {
-        const int row0 = w.q0 + t * kBM;
+        const int row0 = w.q0 + t * bm;
         int n = 0;
         if (t < p.tiles_per_cta && row0 < len_q) {
             int end = t1;
             if (p.causal) {
                 // Keys up to the tile's last row + causal_off; none if that is < 0.
-                const int last_key = min(row0 + kBM - 1, len_q - 1) + w.causal_off;
+                const int last_key = min(row0 + bm - 1, len_q - 1) + w.causal_off;
                 end = min(end, last_key < 0 ? 0 : last_key / BN + 1);
             }
             n = max(0, end - t0);

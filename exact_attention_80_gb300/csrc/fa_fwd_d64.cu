@@ -9,6 +9,9 @@ cudaError_t launch_fwd_d64(const FwdParams& p, unsigned grid, cudaStream_t strea
 cudaError_t launch_fwd_d64_dual(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     return launch_fwd<64, false, true>(p, grid, stream);
 }
+cudaError_t launch_fwd_d64_rows64(const FwdParams& p, unsigned grid, cudaStream_t stream) {
+    return launch_fwd<64, false, false, false, true>(p, grid, stream);
+}
 cudaError_t launch_fwd_d64_persist(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     return launch_fwd<64, false, false, true>(p, grid, stream);
 }

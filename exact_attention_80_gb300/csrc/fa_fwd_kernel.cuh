@@ -24,13 +24,15 @@ using FwdLayout = std::conditional_t<D == 256, LayoutTP<D>, LayoutTM<D>>;
 // F8: e4m3 inputs. DUAL: dual-range split-KV CTAs (one query tile). PERSIST:
 // persistent CTAs (plain mode). All are forms of the two-tile kernel
 // (d = 64 or 128), but for e4m3 at d = 256.
-template <int D, bool F8 = false, bool DUAL = false, bool PERSIST = false>
+// M64: one 64-row query tile per CTA (bf16, d = 64 or 128).
+template <int D, bool F8 = false, bool DUAL = false, bool PERSIST = false, bool M64 = false>
 cudaError_t launch_fwd(const FwdParams& p, unsigned grid, cudaStream_t stream) {
     using L = std::conditional_t<
         PERSIST, LayoutTM<D, F8, true>,
         std::conditional_t<F8, std::conditional_t<D == 256, LayoutTP<D, true>, LayoutTM<D, true>>, FwdLayout<D>>>;
     constexpr auto kernel = [] {
-        if constexpr (PERSIST && F8) return fa_fwd_tmp8_kernel<D>;
+        if constexpr (M64) return fa_fwd_tm64_kernel<D>;
+        else if constexpr (PERSIST && F8) return fa_fwd_tmp8_kernel<D>;
         else if constexpr (PERSIST) return fa_fwd_tmp_kernel<D>;
         else if constexpr (F8 && DUAL) return fa_fwd_tm8d_kernel<D>;
         else if constexpr (F8 && D == 256) return fa_fwd_tp8_kernel<D>;

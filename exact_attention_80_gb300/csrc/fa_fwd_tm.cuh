@@ -632,7 +632,10 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
 
 // DUAL: split-KV with one query tile, both tiles on the same rows (see
 // tm_dual_control); the softmax groups then take their tile's own split.
-template <int D, bool F8, bool DUAL = false, bool PERSIST = false>
+// M64: one 64-row query tile per CTA (fa_fwd_rows with 64 rows): M = 64 MMAs,
+// whose accumulator rows 16 q + i sit in TMEM lanes 32 q + i (i < 16) of lane
+// quarter q; lanes 16-31 of each quarter hold no row.
+template <int D, bool F8, bool DUAL = false, bool PERSIST = false, bool M64 = false>
 __device__ __forceinline__ void tm_forward(const FwdParams& p) {
     using L = LayoutTM<D, F8, PERSIST>;
     constexpr int QT = L::Q_TILES;
@@ -778,10 +781,11 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             auto wait_all = [&](uint32_t b, uint32_t parity, unsigned what) {
                 return __all_sync(0xffffffffu, wait_phase(b, parity, p, abort_flag, what));
             };
+            constexpr int MMA_M = M64 ? 64 : kBM;
             constexpr uint32_t IDESC_S =
-                F8 ? make_idesc_e4m3(kBM, BN, false, false) : make_idesc_bf16(kBM, BN, false, false);
+                F8 ? make_idesc_e4m3(MMA_M, BN, false, false) : make_idesc_bf16(MMA_M, BN, false, false);
             constexpr uint32_t IDESC_O =
-                F8 ? make_idesc_e4m3(kBM, D, false, true) : make_idesc_bf16(kBM, D, false, true);
+                F8 ? make_idesc_e4m3(MMA_M, D, false, true) : make_idesc_bf16(MMA_M, D, false, true);
             // Descriptors are built once; an operand at byte offset `off` from a
             // base adds off >> 4 to the low word (the 14-bit start field never
             // carries: shared addresses stay below 2^18).
@@ -939,7 +943,10 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
         if constexpr (L::REG_SPLIT) setmaxnreg_inc<L::SOFTMAX_REGS>();
         const int t = (warp - 4) >> 2;
         const int quarter = warp & 3;  // TMEM lane quarter this warp may access
-        const int r = quarter * 32 + lane;
+        // The query row of this thread's TMEM lane; with 64-row tiles only
+        // lanes 0-15 of each quarter hold one (the others run along for the
+        // warp-collective TMEM accesses and write nothing).
+        const int r = M64 ? quarter * 16 + (lane & 15) : quarter * 32 + lane;
         // Persistent CTAs walk their units (persist_unit); the phases of S_t
         // and O_t carry over: s_phase counts the tile's earlier key steps,
         // o_phase its earlier units with keys. A one-unit CTA runs the body once.
@@ -955,7 +962,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
         std::conditional_t<DUAL, WorkDual, Work<QT>> w;
         if constexpr (DUAL) compute_work_dual<BN>(p, lin, w);
         else compute_work<QT, BN>(p, lin, w);
-        const int q_row = w.q0 + (DUAL ? 0 : t * kBM) + r;
+        const int q_row = (M64 && lane >= 16) ? (1 << 30) : w.q0 + (DUAL ? 0 : t * kBM) + r;
         // This tile's key split: the CTA's, or its own in a dual-range CTA.
         int kv_tile0_t, kv_end_t, split_t;
         if constexpr (DUAL) {
@@ -1154,9 +1161,9 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             else if (ok && (!DUAL || split_t < p.num_splits))
                 write_row<D>(p, w.rm, w.bh, split_t, q_row, n, m - kP8Shift, m_true, l, l, tO, p.o_scale);
         } else {
-            if (ok && !p.split_mode && !p.varlen && n > 0) {
+            if (ok && !M64 && !p.split_mode && !p.varlen && n > 0) {
                 // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA
-                // stores per warp.
+                // stores per warp (128-row tiles; 64-row tiles write per row).
                 store_rows_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, l + lc, tO,
                                   sbase + L::Q_OFF + t * L::Q_TILE_BYTES);
             } else if (ok && (!DUAL || split_t < p.num_splits)) {
@@ -1187,6 +1194,13 @@ template <int D>
 __global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
     fa_fwd_tm_kernel(const __grid_constant__ FwdParams p) {
     tm_forward<D, false>(p);
+}
+
+// bf16, one 64-row query tile per CTA (fa_fwd_rows with 64 rows).
+template <int D>
+__global__ void __launch_bounds__(LayoutTM<D>::THREADS, 1)
+    fa_fwd_tm64_kernel(const __grid_constant__ FwdParams p) {
+    tm_forward<D, false, false, false, true>(p);
 }
 
 // e4m3 Q, K, V with per-tensor descales (FA-3 page, section 7.3: 8-bit inputs

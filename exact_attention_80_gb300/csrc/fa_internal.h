@@ -57,6 +57,7 @@ struct FwdParams {
     int split_mode;          // 0: write O/LSE, 1: write partial (O, m, l)
     int n_units;             // query units of (tiles_per_cta * 128) rows per head
     int tiles_per_cta;       // 128-row query tiles a CTA owns (up to the kernel's tile slots)
+    int bm64;                // 1: one 64-row query tile per CTA (M = 64 MMAs; fa_fwd_rows)
     int kv_tiles_per_split;  // ceil(ceil(Nk/BN) / num_splits)
     int head_group;          // heads per scheduling group (CTA order)
     int dual;                // 1: dual-range split CTAs (split mode, Nq <= 128, d <= 128)
@@ -80,7 +81,9 @@ struct FwdConfig {
 FwdConfig fwd_config(int d);
 
 cudaError_t launch_fwd_d64(const FwdParams& p, unsigned grid, cudaStream_t stream);
+cudaError_t launch_fwd_d64_rows64(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128(const FwdParams& p, unsigned grid, cudaStream_t stream);
+cudaError_t launch_fwd_d128_rows64(const FwdParams& p, unsigned grid, cudaStream_t stream);
 // Persistent two-tile kernels (plain mode, dense bf16 or e4m3): grid min(units, SMs).
 cudaError_t launch_fwd_d64_persist(const FwdParams& p, unsigned grid, cudaStream_t stream);
 cudaError_t launch_fwd_d128_persist(const FwdParams& p, unsigned grid, cudaStream_t stream);

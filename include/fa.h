@@ -241,11 +241,12 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  * of section "本册配套实验验证记录"). rows_per_cta = 256 is fa_fwd's own
  * choice at d <= 128: two 128-row tiles that alternate on the tensor core.
  * rows_per_cta = 128 gives each CTA one 128-row tile (the other tile slot
- * idles), so twice as many CTAs share the GPU and each computes alone. At
- * d = 256 only 128 is offered (fa_fwd's choice there). A 128-row tile is the
- * tcgen05 MMA height with one TMEM lane per query row; tiles of 64 rows are
- * not offered. Other values: FA_ERR_TILE. Arguments, layouts and the other
- * status codes are those of fa_fwd; the result equals fa_fwd's bit for bit.
+ * idles), so twice as many CTAs share the GPU and each computes alone.
+ * rows_per_cta = 64 (d <= 128) gives each CTA one 64-row tile computed with
+ * M = 64 MMAs, whose accumulator rows take 16 of each 32-lane TMEM quarter.
+ * At d = 256 only 128 is offered (fa_fwd's choice there). Other values:
+ * FA_ERR_TILE. Arguments, layouts and the other status codes are those of
+ * fa_fwd; the result equals fa_fwd's bit for bit.
  */
 fa_status fa_fwd_rows(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                       int H, int Nq, int Nk, int d, float scale, int causal, int rows_per_cta,

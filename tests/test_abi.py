@@ -246,15 +246,15 @@ def test_bench_fill_splits(lib):
 
 
 def test_rows_per_cta_refused_before_any_cuda_call(lib):
-    """fa_fwd_rows offers 128 or 256 query rows per CTA at d <= 128 and 128 at
-    d = 256; anything else is FA_ERR_TILE (13), checked on the host (fake
+    """fa_fwd_rows offers 64, 128 or 256 query rows per CTA at d <= 128 and 128
+    at d = 256; anything else is FA_ERR_TILE (13), checked on the host (fake
     pointers are never used)."""
     fn = lib.fa_fwd_rows
     i, f = ctypes.c_int, ctypes.c_float
     fn.argtypes = [P, P, P, P, P, i, i, i, i, i, f, i, i, P]
     fn.restype = i
     fake = P(0x10000)
-    for d, rows in ((128, 64), (128, 384), (64, 192), (256, 256), (128, 0), (256, 64)):
+    for d, rows in ((128, 32), (128, 384), (64, 192), (256, 256), (128, 0), (256, 64), (64, -64)):
         assert fn(fake, fake, fake, fake, fake, 1, 8, 1024, 1024, d, 0.1, 0, rows, P(0)) == 13, (d, rows)
     assert lib.fa_status_string(13).decode().startswith("FA_ERR_TILE")
     # A head dim outside the set is still FA_ERR_HEADDIM, and bad pointers keep their codes.

@@ -580,6 +580,32 @@ def test_full_size_one_tile_per_cta(head_pool, name):
     whole_tensor_check(head_pool, c, config_inputs(name), rows_per_cta=128)
 
 
+@pytest.mark.parametrize("name", ["c3", "c3_causal"])
+def test_full_size_64_row_tiles(head_pool, name):
+    """The sweep point of 64 rows per CTA (fa_fwd_rows; M = 64 MMAs): whole O
+    and LSE of the long-sequence workload against the oracle."""
+    c = dict(CONFIGS[name], name=name + " rows=64")
+    whole_tensor_check(head_pool, c, config_inputs(name), rows_per_cta=64)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True, "bottom_right"])
+@pytest.mark.parametrize("Nq,Nk", [(389, 457), (1, 300), (63, 64), (700, 200), (200, 1)])
+def test_64_row_tiles(d, causal, Nq, Nk):
+    """64 query rows per CTA: ragged shapes (a tail in the 64-row tile and in
+    the key tile, one query row, rows that see no key) against the oracle, and
+    bit for bit fa_fwd's output (a row's arithmetic does not depend on the
+    MMA height that computes it)."""
+    B, H = 2, 3
+    q, k, v = make_qkv(B, H, Nq, Nk, d, 970 + d + Nq)
+    scale = f32(1.0 / math.sqrt(d))
+    o, lse = run_gpu_rows(q, k, v, causal, scale, 64)
+    oo, ll = oracle.attention_f64(to_f64(q), to_f64(k), to_f64(v), scale, causal)
+    check(o, lse, oo, ll, f"rows=64 d={d} {causal} Nq={Nq} Nk={Nk}")
+    o_ref, lse_ref = run_gpu(q, k, v, causal, scale)
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)
+
+
 @pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True, "bottom_right"])
 def test_rows_per_cta_equal_fa_fwd(d, causal):
