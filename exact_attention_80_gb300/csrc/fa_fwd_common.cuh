@@ -60,6 +60,16 @@ struct Work {
     int nmax;
 };
 
+// First query row of tile slot t (0 or 1) of a unit that starts at row q0.
+// Under a causal mask, with two slots, the slots are reversed: slot 0 takes
+// the unit's later rows, whose tile sees one more key tile. The MMA issuer
+// serves slot 0 first in every key step, so the tile that ends last, and sets
+// when the unit's epilogue and the next unit can run, is served first.
+__device__ __forceinline__ int tile_row0(const FwdParams& p, int q0, int t) {
+    const int bm = p.bm64 ? 64 : kBM;
+    return q0 + ((p.causal && p.tiles_per_cta == 2) ? 1 - t : t) * bm;
+}
+
 // Unit `lin` (blockIdx.x for a one-unit CTA; a persistent CTA walks lin =
 // blockIdx.x + k * gridDim.x).
 template <int QT, int BN>
@@ -121,7 +131,7 @@ __device__ __forceinline__ void compute_work(const FwdParams& p, long long lin, 
     w.nmax = 0;
 #pragma unroll
     for (int t = 0; t < QT; ++t) {
-        const int row0 = w.q0 + t * bm;
+        const int row0 = tile_row0(p, w.q0, t);
         int n = 0;
         if (t < p.tiles_per_cta && row0 < len_q) {
             int end = t1;

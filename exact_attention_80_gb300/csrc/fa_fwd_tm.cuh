@@ -401,7 +401,7 @@ __device__ __forceinline__ void tm_persist_control(const FwdParams& p, uint32_t 
 #pragma unroll
                 for (int c = 0; c < L::CHUNKS; ++c)
                     tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * RB), &p.tm_q,
-                                bar(L::BAR_QFULL + t), L::CHUNK_ELEMS * c, u.q0 + t * kBM, u.zq);
+                                bar(L::BAR_QFULL + t), L::CHUNK_ELEMS * c, tile_row0(p, u.q0, t), u.zq);
             }
             ++q_loads[t];
             return true;
@@ -718,7 +718,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
 #pragma unroll
                     for (int c = 0; c < L::CHUNKS; ++c)
                         tma_load_3d(sbase + L::Q_OFF + t * L::Q_TILE_BYTES + c * (kBM * L::ROW_BYTES),
-                                    &p.tm_q, bar(L::BAR_QFULL + t), L::CHUNK_ELEMS * c, w.qbase + w.q0 + t * kBM,
+                                    &p.tm_q, bar(L::BAR_QFULL + t), L::CHUNK_ELEMS * c, w.qbase + tile_row0(p, w.q0, t),
                                     w.zq);
                 }
             };
@@ -962,7 +962,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
         std::conditional_t<DUAL, WorkDual, Work<QT>> w;
         if constexpr (DUAL) compute_work_dual<BN>(p, lin, w);
         else compute_work<QT, BN>(p, lin, w);
-        const int q_row = (M64 && lane >= 16) ? (1 << 30) : w.q0 + (DUAL ? 0 : t * kBM) + r;
+        const int q_row = (M64 && lane >= 16) ? (1 << 30) : (DUAL ? w.q0 : tile_row0(p, w.q0, t)) + r;
         // This tile's key split: the CTA's, or its own in a dual-range CTA.
         int kv_tile0_t, kv_end_t, split_t;
         if constexpr (DUAL) {
@@ -1147,7 +1147,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
         if constexpr (PERSIST && !F8) {
             // Plain mode, dense: bf16 O staged per warp in its own buffer.
             if (ok && n > 0)
-                store_rows_tma_buf<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, l + lc, tO,
+                store_rows_tma_buf<D>(p, w.rm, w.zq, q_row - r, r, q_row, m, m_true, l, l + lc, tO,
                                       sbase + L::OST_OFF + t * L::OST_TILE_BYTES + quarter * L::OST_WARP_BYTES);
             else if (ok)
                 write_row<D>(p, w.rm, w.bh, 0, q_row, n, m, m_true, l, l + lc, tO);
@@ -1156,7 +1156,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             // o_scale * O_t / l staged in the tile's own buffer and written with
             // TMA. Split mode: the partial state, O scaled by o_scale, per row.
             if (ok && !p.split_mode && n > 0)
-                store_rows_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m - kP8Shift, m_true, l, l, tO,
+                store_rows_tma<D>(p, w.rm, w.zq, q_row - r, r, q_row, m - kP8Shift, m_true, l, l, tO,
                                   sbase + L::OST_OFF + t * L::OST_TILE_BYTES, p.o_scale);
             else if (ok && (!DUAL || split_t < p.num_splits))
                 write_row<D>(p, w.rm, w.bh, split_t, q_row, n, m - kP8Shift, m_true, l, l, tO, p.o_scale);
@@ -1164,7 +1164,7 @@ __device__ __forceinline__ void tm_forward(const FwdParams& p) {
             if (ok && !M64 && !p.split_mode && !p.varlen && n > 0) {
                 // Plain mode: bf16 O_t staged in Q_t's shared memory, written with TMA
                 // stores per warp (128-row tiles; 64-row tiles write per row).
-                store_rows_tma<D>(p, w.rm, w.zq, w.q0 + t * kBM, r, q_row, m, m_true, l, l + lc, tO,
+                store_rows_tma<D>(p, w.rm, w.zq, q_row - r, r, q_row, m, m_true, l, l + lc, tO,
                                   sbase + L::Q_OFF + t * L::Q_TILE_BYTES);
             } else if (ok && (!DUAL || split_t < p.num_splits)) {
                 write_row<D>(p, w.rm, w.bh, split_t, q_row, n, m, m_true, l, l + lc, tO);
